@@ -1,0 +1,352 @@
+"""Pins for the fp64 oracle: checks against what the definition itself fixes.
+
+None of these recompute the recurrence the way the oracle does; each one uses
+a special case, an invariant, an independent library routine or a hand-derived
+example (tests/golden), so that a dropped term, a wrong sign or index, or a
+transposed operand in the oracle fails at least one of them.
+"""
+from fractions import Fraction
+from pathlib import Path
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import workloads
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+def _rand_inputs(rng, T, H, dk, dv, unit_k=True):
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    beta = rng.standard_normal((T, H))
+    gate = rng.standard_normal((T, H, dk))
+    return q, k, v, beta, gate
+
+
+# --------------------------------------------------------------------------
+# activations
+
+
+def test_gate_and_beta_activation_against_scipy():
+    x = np.array([-np.inf, -50.0, -3.0, -1e-3, 0.0, 1e-3, 2.5, 40.0, 700.0])
+    g = oracle.gate_log(x)
+    np.testing.assert_allclose(g, -np.logaddexp(0.0, x), rtol=1e-15, atol=0)
+    assert g[0] == 0.0 and g[4] == -np.log(2.0)
+    b = oracle.beta_act(x)
+    np.testing.assert_allclose(b, scipy.special.expit(x), rtol=1e-15, atol=0)
+    assert b[0] == 0.0 and b[4] == 0.5
+
+
+# --------------------------------------------------------------------------
+# hand-derived example
+
+
+def _read_golden(name):
+    vals = {}
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, rhs = (s.strip() for s in line.split("=", 1))
+        items = []
+        for tok in rhs.split():
+            items.append(float(tok) if "inf" in tok else float(Fraction(tok)))
+        vals[key] = np.array(items)
+    return vals
+
+
+def test_golden_dyadic_two_tokens_prefill_verify_commit():
+    g = _read_golden("dyadic_two_token.txt")
+    dk, dv = int(g["dk"][0]), int(g["dv"][0])
+    q = g["q"].reshape(2, 1, dk)
+    k = g["k"].reshape(2, 1, dk)
+    v = g["v"].reshape(2, 1, dv)
+    gate = g["gate_raw"].reshape(2, 1, dk)
+    beta = g["beta_raw"].reshape(2, 1)
+    S0 = g["S0_T"].reshape(1, 1, dv, dk)
+    out, S_fin, snap, st = oracle.prefill(q, k, v, beta, gate, [0, 2], S0=S0, chunk=1,
+                                          track=[[1]])
+    assert st == 0
+    np.testing.assert_array_equal(out.reshape(-1), g["o"])
+    np.testing.assert_array_equal(S_fin.reshape(-1), g["S2_T"])
+    np.testing.assert_array_equal(snap.reshape(-1), g["S1_T"])
+    # verify: two speculative steps from the same checkpoint, records u and (k, raw gate)
+    o2, ru, rkg, st = oracle.verify(q, k, v, beta, gate, S0.reshape(1, 1, dv, dk), [0], 2)
+    assert st == 0
+    np.testing.assert_array_equal(o2.reshape(-1), g["o"])
+    np.testing.assert_array_equal(ru.reshape(-1), g["u"])
+    np.testing.assert_array_equal(rkg[0, 0, :, :dk], k[:, 0])
+    np.testing.assert_array_equal(rkg[0, 0, :, dk:], gate[:, 0])
+    for a, want in ((0, g["S0_T"]), (1, g["S1_T"]), (2, g["S2_T"])):
+        pool, plan, st = oracle.commit(S0.reshape(1, 1, dv, dk), [0], [a], ru, rkg, 2)
+        np.testing.assert_array_equal(pool.reshape(-1), want)
+        assert list(plan[0]) == [a, 0, 0]
+        cf = oracle.commit_closed_form(S0[0, 0], rkg[0, 0, :, :dk], rkg[0, 0, :, dk:],
+                                       ru[0, 0], a)
+        np.testing.assert_array_equal(cf.reshape(-1), want)
+
+
+# --------------------------------------------------------------------------
+# special cases of the recurrence
+
+
+def test_beta_zero_state_only_decays():
+    rng = np.random.default_rng(11)
+    T, H, dk, dv = 37, 2, 8, 5
+    q, k, v, _, _ = _rand_inputs(rng, T, H, dk, dv)
+    g = -np.abs(rng.standard_normal((T, H, dk))) * 0.3
+    beta = np.zeros((T, H))
+    S0 = rng.standard_normal((1, H, dv, dk))
+    out, S_fin, _, _ = oracle.prefill(q, k, v, beta, g, [0, T], S0=S0,
+                                      flags=oracle.GATE_LOG | oracle.BETA_ACT)
+    G = np.cumsum(g, axis=0)  # [T,H,dk]
+    want_final = S0[0] * np.exp(G[-1])[:, None, :]
+    np.testing.assert_allclose(S_fin[0], want_final, rtol=1e-13, atol=1e-15)
+    # o_t = S_t^T q_t with S_t = Diag(exp G_t) S0
+    want_o = np.einsum("hvk,thk->thv", S0[0], np.exp(G) * q)
+    np.testing.assert_allclose(out, want_o, rtol=1e-12, atol=1e-14)
+
+
+def test_alpha_one_beta_zero_is_identity():
+    rng = np.random.default_rng(12)
+    T, H, dk, dv = 20, 3, 6, 7
+    q, k, v, _, _ = _rand_inputs(rng, T, H, dk, dv)
+    gate = np.full((T, H, dk), -np.inf)  # g = -softplus(-inf) = 0 -> alpha = 1
+    beta = np.full((T, H), -np.inf)      # sigmoid(-inf) = 0
+    S0 = rng.standard_normal((1, H, dv, dk))
+    out, S_fin, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0)
+    np.testing.assert_array_equal(S_fin, S0)
+    np.testing.assert_allclose(out, np.einsum("hvk,thk->thv", S0[0], q), rtol=1e-14,
+                               atol=1e-15)
+
+
+def test_orthonormal_keys_give_outer_product_sum():
+    rng = np.random.default_rng(13)
+    dk, dv, T = 16, 9, 12
+    Qm, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+    k = Qm[:T].reshape(T, 1, dk)          # orthonormal rows
+    v = rng.standard_normal((T, 1, dv))
+    q = rng.standard_normal((T, 1, dk))
+    g = np.zeros((T, 1, dk))
+    beta = np.ones((T, 1))
+    out, S_fin, _, _ = oracle.prefill(q, k, v, beta, g, [0, T],
+                                      flags=oracle.GATE_LOG | oracle.BETA_ACT)
+    KtV = k[:, 0].T @ v[:, 0]             # S_T = K^T V (d_k x d_v)
+    np.testing.assert_allclose(S_fin[0, 0], KtV.T, atol=1e-13)
+    # o_t = sum_{s<=t} v_s (k_s . q_t)
+    Pm = np.tril(q[:, 0] @ k[:, 0].T)
+    np.testing.assert_allclose(out[:, 0], Pm @ v[:, 0], atol=1e-13)
+
+
+def test_delta_rule_reads_back_the_written_value():
+    # beta = 1, |k| = 1, q = k: o_t = S_t^T k_t = v_t for any decay and any S0
+    rng = np.random.default_rng(14)
+    T, H, dk, dv = 50, 2, 12, 10
+    _, k, v, _, gate = _rand_inputs(rng, T, H, dk, dv)
+    beta = np.ones((T, H))
+    S0 = rng.standard_normal((1, H, dv, dk))
+    out, _, _, _ = oracle.prefill(k, k, v, beta, gate, [0, T], S0=S0, flags=oracle.BETA_ACT)
+    np.testing.assert_allclose(out, v, rtol=1e-12, atol=1e-12)
+
+
+def test_scalar_state_is_a_first_order_linear_recurrence():
+    # d_k = d_v = 1: s_t = alpha (1 - beta k^2) s + beta k v, o_t = s_t q_t
+    rng = np.random.default_rng(15)
+    T = 64
+    q, k, v, beta, gate = (rng.standard_normal((T, 1, 1)) for _ in range(5))
+    beta = beta[:, :, 0]
+    out, S_fin, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=np.array([[[[0.7]]]]))
+    a = np.exp(-np.logaddexp(0.0, gate[:, 0, 0]))
+    b = scipy.special.expit(beta[:, 0])
+    s = 0.7
+    want = []
+    for t in range(T):
+        kk, vv = k[t, 0, 0], v[t, 0, 0]
+        s = a[t] * (1.0 - b[t] * kk * kk) * s + b[t] * kk * vv
+        want.append(s * q[t, 0, 0])
+    np.testing.assert_allclose(out[:, 0, 0], want, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S_fin[0, 0, 0, 0], s, rtol=1e-12)
+
+
+def test_linear_in_initial_state_and_values():
+    rng = np.random.default_rng(16)
+    T, H, dk, dv = 40, 2, 8, 6
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((1, H, dv, dk))
+    o_full, s_full, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0)
+    o_a, s_a, _, _ = oracle.prefill(q, k, np.zeros_like(v), beta, gate, [0, T], S0=S0)
+    o_b, s_b, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=np.zeros_like(S0))
+    np.testing.assert_allclose(o_full, o_a + o_b, atol=1e-12)
+    np.testing.assert_allclose(s_full, s_a + s_b, atol=1e-12)
+
+
+def test_value_channels_are_independent():
+    rng = np.random.default_rng(17)
+    T, H, dk, dv = 30, 1, 8, 9
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((1, H, dv, dk))
+    perm = rng.permutation(dv)
+    o1, s1, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0)
+    o2, s2, _, _ = oracle.prefill(q, k, v[:, :, perm], beta, gate, [0, T],
+                                  S0=S0[:, :, perm, :])
+    np.testing.assert_allclose(o2, o1[:, :, perm], atol=1e-13)
+    np.testing.assert_allclose(s2, s1[:, :, perm, :], atol=1e-13)
+
+
+def test_state_norm_bound_with_unit_keys():
+    # |k|=1, beta in (0,1), alpha <= 1: ||S_t||_2 <= ||S_{t-1}||_2 + beta_t ||v_t||
+    rng = np.random.default_rng(18)
+    T, dk, dv = 200, 16, 16
+    q, k, v, beta, gate = _rand_inputs(rng, T, 1, dk, dv)
+    S0 = rng.standard_normal((1, 1, dv, dk))
+    bound = np.linalg.norm(S0[0, 0], 2)
+    cu = [0]
+    # check the bound at several prefixes via snapshots at every token (chunk=1)
+    track = np.arange(T, dtype=np.int32)[None, :]
+    _, S_fin, snap, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0, chunk=1,
+                                       track=track)
+    b = scipy.special.expit(beta[:, 0])
+    for t in range(1, T):
+        bound += b[t - 1] * np.linalg.norm(v[t - 1, 0])
+        assert np.linalg.norm(snap[0, t, 0], 2) <= bound * (1 + 1e-12)
+    del cu, S_fin
+
+
+# --------------------------------------------------------------------------
+# chunk form, snapshots, verify/commit
+
+
+@pytest.mark.parametrize("chunk", [4, 64])
+def test_chunked_form_agrees_with_recurrence(chunk):
+    rng = np.random.default_rng(19 + chunk)
+    lengths = [1, chunk - 1, chunk, chunk + 1, 2 * chunk + 5, 0, 3]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T, H, dk, dv = int(cu[-1]), 2, 16, 8
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((len(lengths), H, dv, dk)) * 0.1
+    o_r, s_r, _, _ = oracle.prefill(q, k, v, beta, gate, cu, S0=S0, scale=0.5)
+    o_c, s_c = oracle.chunked_prefill(q, k, v, beta, gate, cu, chunk=chunk, S0=S0, scale=0.5)
+    assert np.max(np.abs(o_r - o_c)) <= 1e-12
+    assert np.max(np.abs(s_r - s_c)) <= 1e-12
+
+
+def test_snapshot_equals_truncated_run():
+    rng = np.random.default_rng(21)
+    C, T, H, dk, dv = 8, 45, 2, 8, 8
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((1, H, dv, dk))
+    track = np.array([[0, 2, 5, -1]], np.int32)  # n_chunks = 6
+    _, _, snap, st = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0, chunk=C, track=track)
+    assert st == 0
+    for m, j in enumerate(track[0]):
+        if j < 0:
+            assert np.isnan(snap[0, m]).all()
+            continue
+        L = j * C
+        _, s_trunc, _, _ = oracle.prefill(q[:L], k[:L], v[:L], beta[:L], gate[:L], [0, L],
+                                          S0=S0)
+        np.testing.assert_array_equal(snap[0, m], s_trunc[0])
+    bad = np.array([[6]], np.int32)
+    _, _, snap, st = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0, chunk=C, track=bad)
+    assert st & oracle.BAD_TRACK and np.isnan(snap).all()
+
+
+def test_verify_then_commit_equals_repeated_decode():
+    rng = np.random.default_rng(22)
+    R, K, H, dk, dv = 3, 5, 2, 8, 6
+    q, k, v, beta, gate = _rand_inputs(rng, R * K, H, dk, dv)
+    pool = rng.standard_normal((4, H, dv, dk))
+    ckpt = np.array([2, 0, 3], np.int32)
+    out, ru, rkg, st = oracle.verify(q, k, v, beta, gate, pool, ckpt, K)
+    assert st == 0
+    for r in range(R):
+        p = pool.copy()
+        for t in range(K):
+            row = r * K + t
+            o1, p, _ = oracle.decode(q[row:row + 1], k[row:row + 1], v[row:row + 1],
+                                     beta[row:row + 1], gate[row:row + 1], p, [ckpt[r]])
+            np.testing.assert_array_equal(out[row], o1[0])
+            for a in (t + 1,):
+                pc, plan, _ = oracle.commit(pool, ckpt[r:r + 1], [a], ru[r:r + 1],
+                                            rkg[r:r + 1], K)
+                np.testing.assert_allclose(pc[ckpt[r]], p[ckpt[r]], rtol=1e-13, atol=1e-14)
+                cf = np.stack([oracle.commit_closed_form(pool[ckpt[r], h], rkg[r, h, :, :dk],
+                                                         rkg[r, h, :, dk:], ru[r, h], a)
+                               for h in range(H)])
+                np.testing.assert_allclose(cf, p[ckpt[r]], rtol=1e-12, atol=1e-13)
+
+
+def test_commit_closed_form_matches_bruteforce_every_accept_length():
+    rng = np.random.default_rng(23)
+    K, dk, dv = 7, 5, 4
+    S0 = rng.standard_normal((dv, dk))
+    rk = rng.standard_normal((K, dk))
+    rgate = rng.standard_normal((K, dk)) * 2
+    ru = rng.standard_normal((K, dv))
+    for a in range(K + 1):
+        pool, _, _ = oracle.commit(S0[None, None], [0], [a], ru[None, None],
+                                   np.concatenate([rk, rgate], 1)[None, None], K)
+        cf = oracle.commit_closed_form(S0, rk, rgate, ru, a)
+        np.testing.assert_allclose(cf, pool[0, 0], rtol=1e-13, atol=1e-14)
+
+
+def test_commit_plan_and_invalid_requests():
+    P, K = 8, 4
+    ckpt = np.array([0, 1, 2, 9, 3], np.int32)
+    acc = np.array([0, 4, 5, 1, -1], np.int32)
+    dst = np.array([5, 1, 2, 3, 4], np.int32)
+    plan = oracle.commit_plan(ckpt, acc, P, K, dst=dst)
+    assert plan.tolist() == [[0, 0, 5], [4, 1, 1], [-1, 2, 2], [-1, 9, 3], [-1, 3, 4]]
+    rng = np.random.default_rng(24)
+    pool = rng.standard_normal((P, 1, 2, 2))
+    ru = rng.standard_normal((5, 1, K, 2))
+    rkg = rng.standard_normal((5, 1, K, 4))
+    newp, plan2, st = oracle.commit(pool, ckpt, acc, ru, rkg, K, dst=dst)
+    assert plan2.tolist() == plan.tolist()
+    assert st & oracle.BAD_SLOT and st & oracle.BAD_ACCEPT
+    np.testing.assert_array_equal(newp[5], pool[0])   # a = 0, dst != src: copy
+    np.testing.assert_array_equal(newp[[2, 3, 4]], pool[[2, 3, 4]])  # skipped
+
+
+def test_decode_skips_negative_slots():
+    rng = np.random.default_rng(25)
+    q, k, v, beta, gate = _rand_inputs(rng, 2, 1, 4, 4)
+    pool = rng.standard_normal((3, 1, 4, 4))
+    out, newp, st = oracle.decode(q, k, v, beta, gate, pool, [-1, 2])
+    assert st == 0
+    assert (out[0] == 0).all()
+    np.testing.assert_array_equal(newp[:2], pool[:2])
+    out, newp, st = oracle.decode(q, k, v, beta, gate, pool, [3, 2])
+    assert st & oracle.BAD_SLOT
+
+
+def test_slot_copy_semantics():
+    rng = np.random.default_rng(26)
+    pool = rng.standard_normal((10, 3))
+    case = workloads.slot_copy_case(5, 10, 2, 3, 2)
+    (new,) = oracle.slot_copy([pool], case["clear"], case["src"], case["dst_offsets"],
+                              case["dst"])
+    for i, s in enumerate(case["src"]):
+        for d in case["dst"][i * 3:(i + 1) * 3]:
+            np.testing.assert_array_equal(new[d], pool[s])
+    for c in case["clear"]:
+        assert (new[c] == 0).all()
+    untouched = set(range(10)) - set(case["dst"]) - set(case["clear"])
+    for u in untouched:
+        np.testing.assert_array_equal(new[u], pool[u])
+
+
+def test_bf16_storage_round_trip():
+    x = np.array([0.0, 1.0, -2.5, 1.00390625, 1.005859375, 3.4e38, np.inf], np.float32)
+    bits = workloads.f32_to_bf16_bits(x)
+    y = workloads.bf16_bits_to_f32(bits)
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: nearest-even keeps 1
+    assert y[3] == 1.0 and y[4] == np.float32(1.0078125)
+    assert y[0] == 0 and y[1] == 1 and y[2] == -2.5 and np.isinf(y[5]) and np.isinf(y[6])
