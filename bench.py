@@ -1,0 +1,527 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA recurrent-state serving path on one GB300 (or N replicas).
+
+One step = one pass of every entry point over one batch of synthetic input:
+  * kda_chunk_prefill    : 8 packed sequences, lengths ~U[1024, 8192] (seed 1), H=32,
+                           d=128, chunk 64, bf16 in/out, fp32 state pool (64 slots,
+                           in-place init/final) and one fp32 snapshot per sequence.
+  * kda_recurrent_decode : 256 requests x 1 token, H=32, 1024-slot fp32 pool.
+  * kda_spec_verify + kda_spec_commit : 64 requests, K=7, H=32, in-place commit.
+  * kda_slot_copy        : 256 parents x 8 children + 512 clears, 4096-slot pool
+                           of 1 MiB fp32 states (H=16).
+`value` is the prefill throughput in tokens/s (device time of the prefill call,
+inputs resident in HBM); the other calls are reported in microseconds per
+call.  L2 is flushed (256 MiB write) before every timed call.
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+prefill workload on the host cores (the method has no runnable reference
+implementation; the oracle is the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "KDA prefill tokens/s and decode/verify+commit µs/step; % of HBM/TC roofline"
+D, C = 128, 64
+STATE_BYTES = D * D * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# algorithmic work per call
+
+
+def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
+    """Bytes and flops of one prefill call (per (token, head): q, k, v, raw gate,
+    raw beta, o; per (sequence, head): initial + final state and M snapshots)."""
+    T = sum(lengths)
+    per_tok = 4 * D * in_bytes + in_bytes + D * out_bytes
+    n_states = len(lengths) * H * (2 + M)
+    byts = T * H * per_tok + n_states * STATE_BYTES
+    flops = T * H * (10 * C * D + 6 * D * D + C * C / 3)
+    return byts, flops
+
+
+def decode_work(R, H):
+    return R * H * (2 * STATE_BYTES + 4 * D * 2 + 2 + D * 2)
+
+
+def verify_work(R, K, H):
+    return R * H * (STATE_BYTES + K * (4 * D * 2 + 2 + D * 2 + D * 4 + 2 * D * 2))
+
+
+def commit_work(acc, H):
+    return sum(H * (2 * STATE_BYTES + a * (D * 4 + 2 * D * 2)) for a in acc if a > 0)
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        load = [s for s, p in zip(sm, pw) if p is not None] or sm
+        hi = sorted(load)[len(load) // 2:] or load  # samples under load: upper half by clock
+        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# workloads on the device
+
+
+def to_dev(a, dtype, dev):
+    import torch
+
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+
+def i32(a, dev):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+
+
+class Step:
+    """All five entry points on resident device buffers."""
+
+    def __init__(self, dev):
+        import torch
+
+        import serving_kda_chunk_gb300 as kda
+
+        self.kda = kda
+        self.dev = dev
+        t0 = time.time()
+        c1 = W.cfg1()
+        self.c1 = c1
+        self.pre = {n: to_dev(c1[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+        self.pre_host = {n: torch.from_numpy(c1[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+                         for n in ("q", "k", "v", "beta", "gate")}
+        self.cu = i32(c1["cu_seqlens"], dev)
+        self.pool1 = torch.from_numpy(c1["pool"]).to(dev)
+        self.slots1 = i32(c1["init_slot"], dev)
+        self.track1 = i32(c1["track"], dev)
+        self.snap1 = torch.empty(c1["N"], 1, 32, D, D, device=dev)
+        self.out1 = torch.empty(c1["T"], 32, D, dtype=torch.bfloat16, device=dev)
+        self.out1_host = torch.empty(c1["T"], 32, D, dtype=torch.bfloat16).pin_memory()
+        ws = kda.kda_chunk_prefill_workspace_size(c1["T"], c1["N"], 32)
+        self.ws1 = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        c2 = W.cfg2()
+        self.dec = {n: to_dev(c2[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+        self.pool2 = torch.from_numpy(c2["pool"]).to(dev)
+        self.slot2 = i32(c2["slot"], dev)
+        self.out2 = torch.empty(256, 32, D, dtype=torch.bfloat16, device=dev)
+        c3 = W.cfg3()
+        self.c3 = c3
+        self.spec = {n: to_dev(c3[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+        self.pool3 = torch.from_numpy(c3["pool"]).to(dev)
+        self.ckpt3 = i32(c3["ckpt"], dev)
+        self.acc3 = i32(c3["num_accepted"], dev)
+        self.rec_u = torch.empty(64, 32, 7, D, device=dev)
+        self.rec_kg = torch.empty(64, 32, 7, 2 * D, dtype=torch.bfloat16, device=dev)
+        self.out3 = torch.empty(64 * 7, 32, D, dtype=torch.bfloat16, device=dev)
+        c4 = W.cfg4_slot_copy()
+        g = torch.Generator(device=dev).manual_seed(4)
+        self.pool4 = torch.empty(4096, 16, D, D, device=dev)
+        for i in range(0, 4096, 512):
+            self.pool4[i:i + 512].normal_(0.0, 0.1, generator=g)
+        self.c4 = {n: i32(c4[n], dev) for n in ("clear", "src", "dst_offsets", "dst")}
+        self.n4 = (len(c4["src"]), len(c4["dst"]), len(c4["clear"]))
+        self.ws4 = torch.empty(kda.kda_slot_copy_workspace_size(4096), dtype=torch.uint8,
+                               device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.setup_s = time.time() - t0
+        torch.cuda.synchronize()
+
+    def prefill(self, pre=None):
+        p = pre or self.pre
+        self.kda.kda_chunk_prefill(p["q"], p["k"], p["v"], p["beta"], p["gate"], self.cu,
+                                   self.out1, state_pool=self.pool1, init_slot=self.slots1,
+                                   final_slot=self.slots1, track_chunk_idx=self.track1,
+                                   track_state=self.snap1, workspace=self.ws1,
+                                   dev_status=self.status)
+
+    def decode(self):
+        d = self.dec
+        self.kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["beta"], d["gate"], self.pool2,
+                                      self.slot2, self.out2, dev_status=self.status)
+
+    def verify(self):
+        s = self.spec
+        self.kda.kda_spec_verify(s["q"], s["k"], s["v"], s["beta"], s["gate"], self.pool3,
+                                 self.ckpt3, self.rec_u, self.rec_kg, self.out3, K=7,
+                                 dev_status=self.status)
+
+    def commit(self):
+        self.kda.kda_spec_commit(self.pool3, self.ckpt3, self.acc3, self.rec_u, self.rec_kg, K=7,
+                                 dev_status=self.status)
+
+    def slot_copy(self):
+        c = self.c4
+        self.kda.kda_slot_copy([self.pool4], c["clear"], c["src"], c["dst_offsets"], c["dst"],
+                               self.ws4, dev_status=self.status)
+
+    # name -> (callable, kernel launches)
+    def calls(self):
+        return [("prefill", self.prefill, 1), ("decode", self.decode, 1),
+                ("verify", self.verify, 1), ("commit", self.commit, 1),
+                ("slot_copy", self.slot_copy, 2)]
+
+
+def run_device(step, steps, warmup, rank, world):
+    import torch
+
+    calls = step.calls()
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for _, fn, _ in calls:
+            step.flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    times = {name: [] for name, _, _ in calls}
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    evs = []
+    for _ in range(steps):
+        row = []
+        for name, fn, _ in calls:
+            step.flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            row.append((name, a, b))
+        evs.append(row)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    for row in evs:
+        for name, a, b in row:
+            times[name].append(a.elapsed_time(b) * 1e-3)
+    launches = steps * sum(n for _, _, n in calls)
+    return times, wall, clocks, launches
+
+
+def run_e2e(step, steps, warmup):
+    """Prefill through the public call with host buffers: pinned H2D of the inputs,
+    the call, D2H of the output, all inside the timed region."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    dev_in = step.pre
+    h2d = sum(t.numel() * t.element_size() for t in step.pre_host.values())
+    h2d += step.c1["cu_seqlens"].nbytes
+    d2h = step.out1.numel() * step.out1.element_size()
+    cu_host = torch.from_numpy(step.c1["cu_seqlens"]).pin_memory()
+
+    def once():
+        for n, t in step.pre_host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        step.cu.copy_(cu_host, non_blocking=True)
+        step.prefill(dev_in)
+        step.out1_host.copy_(step.out1, non_blocking=True)
+
+    for _ in range(warmup):
+        step.flush.zero_()
+        once()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        step.flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        once()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    return statistics.mean(ts), h2d, d2h
+
+
+# --------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the prefill workload
+
+
+def cpu_oracle_sample(heads=(0, 1, 2, 3), threads=None):
+    import oracle
+
+    c = W.cfg1()
+    H = c["H"]
+    hs = list(heads)
+    wid = lambda n: W.widen(c[n], "bf16")[:, hs]  # noqa: E731
+    S0 = c["pool"][c["init_slot"]][:, hs].astype(np.float64)
+    cores = threads or (os.cpu_count() or 1)
+    args = (wid("q"), wid("k"), wid("v"), W.widen(c["beta"], "bf16")[:, hs], wid("gate"))
+    t0 = time.perf_counter()
+    oracle.prefill(*args, c["cu_seqlens"], S0=S0, track=c["track"], n_threads=cores)
+    dt = time.perf_counter() - t0
+    tok_heads = c["T"] * len(hs)
+    value = tok_heads / H / dt  # full-width (all H heads) tokens per second
+    sample = (f"fp64 oracle prefill on heads {hs} of {H} for all {c['N']} sequences "
+              f"({c['T']} tokens), {dt:.2f} s wall; value scaled to all heads")
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas: no collective on the data path)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+
+
+def config_block():
+    lengths = W.cfg1_lengths()
+    return {"workload": (f"batched chunk prefill: 8 packed seqs, lengths {lengths} "
+                         f"(sum {sum(lengths)}), H=32, d_k=d_v=128, chunk=64, bf16 in/out, "
+                         "fp32 state; step also runs decode 256xH32, spec verify+commit "
+                         "64xK7xH32, slot copy 256x8 + 512 clears of 1 MiB states"),
+            "global_batch": 8, "seq_len": max(lengths), "tokens": sum(lengths),
+            "l2": "flushed (256 MiB write) before every timed call",
+            "parallelism": "replicas (one independent copy per GPU)"}
+
+
+def main_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    steps = max(1, min(args.steps, 3))
+    vals = []
+    for _ in range(max(0, min(args.warmup, 1))):
+        cpu_oracle_sample(heads=(0,))
+    cb = None
+    for _ in range(steps):
+        cb = cpu_oracle_sample(heads=(0,))
+        vals.append(cb["value"])
+    value = statistics.mean(vals)
+    cb["value"] = value
+    toks = sum(W.cfg1_lengths())
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": 1, "steps": steps, "warmup": min(args.warmup, 1),
+            "ms_per_step": toks / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_block(),
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        rc = main_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    step = Step(dev)
+    times, wall, clocks, launches = run_device(step, args.steps, args.warmup, rank, world)
+    e2e_t, h2d, d2h = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
+
+    hbm, tc, peak_kind = load_peaks()
+    mean = {k: statistics.mean(v) for k, v in times.items()}
+    lengths = step.c1["lengths"]
+    toks = sum(lengths)
+    t_pre = max_over_ranks(mean["prefill"], world)
+    value = sum_over_ranks(toks, world) / t_pre
+    e2e_val = sum_over_ranks(toks, world) / max_over_ranks(e2e_t, world)
+    pb, pf = prefill_work(lengths, 32, 1)
+    achieved = pb / mean["prefill"] / 1e9
+    t_hbm, t_tc = pb / (hbm * 1e9), pf / (tc * 1e12)
+    dec_b = decode_work(256, 32)
+    ver_b = verify_work(64, 7, 32)
+    com_b = commit_work(step.c3["num_accepted"].tolist(), 32)
+    cp_b = STATE_BYTES * 16 * (sum(step.n4))
+    parts = {
+        "prefill": {"us": mean["prefill"] * 1e6, "tokens_per_s": toks / mean["prefill"],
+                    "bytes": pb, "flops": pf, "hbm_frac": t_hbm / mean["prefill"],
+                    "tensor_frac": t_tc / mean["prefill"]},
+        "decode": {"us": mean["decode"] * 1e6, "bytes": dec_b,
+                   "hbm_frac": dec_b / (hbm * 1e9) / mean["decode"]},
+        "verify": {"us": mean["verify"] * 1e6, "bytes": ver_b,
+                   "hbm_frac": ver_b / (hbm * 1e9) / mean["verify"]},
+        "commit": {"us": mean["commit"] * 1e6, "bytes": com_b,
+                   "hbm_frac": com_b / (hbm * 1e9) / mean["commit"]},
+        "verify_commit_us_per_step": (mean["verify"] + mean["commit"]) * 1e6,
+        "slot_copy": {"us": mean["slot_copy"] * 1e6, "bytes": cp_b,
+                      "hbm_frac": cp_b / (hbm * 1e9) / mean["slot_copy"]},
+    }
+    step_s = sum(mean.values())
+    status = int(step.status.item())
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_sample()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; bf16 inputs, fp32 state)", "config": config_block(),
+        "roofline": {"bound": "hbm", "kernel": "kda_chunk_prefill", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "parts": parts,
+        "dev_status": status,
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,230 @@
+/*
+ * kda.h -- C ABI of libkda, the GB300 (sm_103a) library for the Kimi Delta
+ * Attention (KDA) recurrent-state hot path of a serving engine.
+ *
+ * The method.  Every attention head keeps a d_k x d_v state S (128 x 128)
+ * updated per token as
+ *     alpha_t = exp(g_t),  g_t = -softplus(raw gate_t)      (per key channel)
+ *     beta_t  = sigmoid(raw beta_t)                         (per token and head)
+ *     u_t = beta_t (v_t - (Diag(alpha_t) S_{t-1})^T k_t)
+ *     S_t = Diag(alpha_t) S_{t-1} + k_t u_t^T,      o_t = S_t^T (scale q_t).
+ * The serving pages that motivate each call:
+ *   - "State semantics" page (rollback, fork, replay, TP): rollback is an
+ *     exact block copy (section 2), a fork copies the whole state per
+ *     candidate (section 3), decode and verify activate gates inside the
+ *     kernel (section 4).
+ *   - SGLang PR 34820 page: chunk prefill writes the fp32 accumulator at a
+ *     per-sequence chunk index as the prefix-cache snapshot (implementation
+ *     breakdown, items 1-2, and the Helion kernel listing).
+ *   - vLLM PR 51855 page (RecoverSSM): verify keeps one checkpoint per request
+ *     and records fp32 u and activation-dtype key / raw gate (implementation
+ *     breakdown, items 1 and 3); commit rebuilds the state at the accepted
+ *     length in closed form after sampling (item 4).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *     owns all memory.  The library allocates nothing.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and never synchronises with the host.
+ *   - Activations are packed [rows, H, 128] with the channel contiguous, raw
+ *     beta is [rows, H].  `in_dtype` gives their element type (bf16 or fp32).
+ *     Outputs are [rows, H, d_v] of `out_dtype`; bf16 outputs are rounded to
+ *     nearest-even from the fp32 result.
+ *   - States are fp32 and stored transposed: pool[slot][h][v][k] = S[k][v]
+ *     (d_v rows of d_k contiguous floats, 64 KiB per head).
+ *   - d_k = d_v = 128 and chunk = 64 are the supported shapes; others return
+ *     KDA_ERR_UNSUPPORTED.  Every device pointer must be 16-byte aligned.
+ *   - Host-checkable errors (null pointer, bad size, misalignment) return a
+ *     kda_status and launch nothing.  Data-dependent errors found on the GPU
+ *     (a bad slot, track index, accepted length or cu_seqlens entry, an
+ *     overlap in a copy set) are OR-ed into *dev_status (device int32, may be
+ *     NULL) and the offending unit is skipped; kernels never trap.
+ *   - flags: KDA_GATE_LOG = the gate input already holds g (log decay);
+ *     KDA_BETA_ACT = the beta input already holds beta.  Default: both raw.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment   */
+    KDA_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set    */
+    KDA_ERR_CUDA = 3         /* a CUDA launch or runtime call failed         */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+#define KDA_GATE_LOG 1u
+#define KDA_BETA_ACT 2u
+
+/* bits OR-ed into *dev_status by the kernels */
+#define KDA_DEV_BAD_SLOT 1     /* slot index >= pool size (or required and < 0) */
+#define KDA_DEV_BAD_TRACK 2    /* track_chunk_idx outside [-1, n_chunks-1]      */
+#define KDA_DEV_BAD_ACCEPT 4   /* accepted length outside [0, q_len], bad q_len */
+#define KDA_DEV_BAD_SEQLEN 8   /* cu_seqlens not monotone or past T_tot         */
+#define KDA_DEV_OVERLAP 16     /* slot-copy sets not disjoint                    */
+
+#define KDA_MAX_POOLS 16
+
+/*
+ * kda_chunk_prefill -- chunked prefill over variable-length packed sequences
+ * (SGLang PR 34820 page, the fp32 track-state snapshot in chunk prefill).
+ *
+ *   q, k, gate_raw : [T_tot, H, d_k] in_dtype;  v : [T_tot, H, d_v] in_dtype
+ *   beta_raw       : [T_tot, H] in_dtype
+ *   cu_seqlens     : [N+1] int32 (device), cu_seqlens[0] = 0, non-decreasing,
+ *                    cu_seqlens[N] <= T_tot.  Sequence n is rows
+ *                    [cu_seqlens[n], cu_seqlens[n+1]); chunks restart at each
+ *                    sequence start and the last chunk may be partial.
+ *   state_pool     : [P, H, d_v, d_k] fp32.  init_slot[n] >= 0 reads the
+ *                    initial state from that slot (< 0: zero state);
+ *                    final_slot[n] >= 0 receives the state after the whole
+ *                    sequence (< 0: not written).  init and final may be the
+ *                    same slot (in-place continuation).  init_slot / final_slot
+ *                    may be NULL (= all -1).
+ *   track_chunk_idx: [N, M] int32 (device) or NULL when M = 0.  Entry j >= 0
+ *                    asks for the fp32 state after exactly j*chunk tokens of the
+ *                    sequence (j = 0 is the initial state), j in
+ *                    [0, n_chunks-1]; -1 = unused.
+ *   track_state    : [N, M, H, d_v, d_k] fp32 snapshots (written only for
+ *                    valid entries; the fp32 accumulator itself, never a
+ *                    rounded copy).
+ *   out            : [T_tot, H, d_v] out_dtype.
+ *   workspace      : ws_bytes of device scratch, at least
+ *                    kda_chunk_prefill_workspace_size(...) bytes (may be NULL
+ *                    when that size is 0).
+ * Units of work are (sequence, head); sequences must not share a final slot.
+ */
+kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* beta_raw,
+                             const void* gate_raw, kda_dtype in_dtype, const int32_t* cu_seqlens,
+                             int32_t N, int32_t T_tot, int32_t H, int32_t dk, int32_t dv,
+                             int32_t chunk, float scale, uint32_t flags, float* state_pool,
+                             int64_t P, const int32_t* init_slot, const int32_t* final_slot,
+                             const int32_t* track_chunk_idx, int32_t M, float* track_state,
+                             void* out, kda_dtype out_dtype, void* workspace, size_t ws_bytes,
+                             int32_t* dev_status, void* stream);
+
+size_t kda_chunk_prefill_workspace_size(int32_t T_tot, int32_t N, int32_t H, int32_t dk,
+                                        int32_t dv, int32_t chunk);
+
+/*
+ * kda_recurrent_decode -- one token per request, state updated in place in a
+ * slot-indexed fp32 pool ("state semantics" page, section 4: decode applies
+ * the gate activation inside the kernel).
+ *
+ *   q, k, gate_raw : [R, H, d_k];  v : [R, H, d_v];  beta_raw : [R, H]
+ *   slot           : [R] int32.  slot < 0: padding request, skipped, its
+ *                    output row is written as zeros.  slot >= P: skipped,
+ *                    zero output, KDA_DEV_BAD_SLOT.  Slots of one call must be
+ *                    distinct.
+ *   out            : [R, H, d_v] out_dtype.
+ */
+kda_status kda_recurrent_decode(const void* q, const void* k, const void* v, const void* beta_raw,
+                                const void* gate_raw, kda_dtype in_dtype, int32_t R, int32_t H,
+                                int32_t dk, int32_t dv, float scale, uint32_t flags,
+                                float* state_pool, int64_t P, const int32_t* slot, void* out,
+                                kda_dtype out_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * kda_spec_verify -- speculative verify from one checkpoint per request
+ * (vLLM PR 51855 page, implementation breakdown item 3: read the checkpoint
+ * only, compute the output at every speculative position, record u and the
+ * key / raw gate).
+ *
+ *   q, k, gate_raw : [R*K, H, d_k];  v : [R*K, H, d_v];  beta_raw : [R*K, H]
+ *                    (request r's position t is row r*K + t).
+ *   q_len          : [R] int32 in [0, K] or NULL (= K for all).
+ *   ckpt_slot      : [R] int32: the checkpoint read from state_pool (never
+ *                    written).  < 0: request skipped; >= P: skipped +
+ *                    KDA_DEV_BAD_SLOT.
+ *   rec_u          : [R, H, K, d_v] fp32, u_t as computed here.
+ *   rec_kg         : [R, H, K, 2*d_k] of in_dtype: k_t followed by the raw
+ *                    gate exactly as given.
+ *   out            : [R*K, H, d_v] out_dtype.
+ * Positions t >= q_len and skipped requests get zero outputs and records.
+ */
+kda_status kda_spec_verify(const void* q, const void* k, const void* v, const void* beta_raw,
+                           const void* gate_raw, kda_dtype in_dtype, int32_t R, int32_t K,
+                           const int32_t* q_len, int32_t H, int32_t dk, int32_t dv, float scale,
+                           uint32_t flags, const float* state_pool, int64_t P,
+                           const int32_t* ckpt_slot, float* rec_u, void* rec_kg, void* out,
+                           kda_dtype out_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * kda_spec_commit -- rebuild the state at the accepted length a_r in closed
+ * form (vLLM PR 51855 page, implementation breakdown item 4: the commit plan
+ * computes accepted lengths on the GPU, the commit kernel rebuilds the state
+ * in reverse order in one shot, without re-running the recursion):
+ *     S_a = Diag(exp sum_{t<=a} g_t) S_0 + sum_{t<=a} Diag(exp sum_{t<s<=a} g_s) k_t u_t^T
+ * with g_t recomputed from the recorded raw gate.
+ *
+ *   ckpt_slot    : [R] checkpoint slot (S_0).   dst_slot: [R] or NULL (= ckpt,
+ *                  in place).  num_accepted: [R] in [0, q_len_r].
+ *   q_len        : [R] or NULL (= K).   rec_u, rec_kg: as written by verify;
+ *                  rec_dtype is rec_kg's element type.
+ *   plan_out     : [R, 3] int32 (a, src, dst) or NULL; a = -1 marks a request
+ *                  that was skipped (bad slot or bad accepted length, with the
+ *                  matching dev_status bit).
+ * a = 0 writes nothing when dst == src and copies S_0 otherwise.  Destinations
+ * must be distinct and must not be another request's checkpoint.
+ */
+kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+                           const int32_t* dst_slot, const int32_t* num_accepted,
+                           const int32_t* q_len, int32_t R, int32_t K, int32_t H, int32_t dk,
+                           int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
+                           kda_dtype rec_dtype, int32_t* plan_out, int32_t* dev_status,
+                           void* stream);
+
+/*
+ * kda_slot_copy -- one fused launch that clears, copies and fans out state
+ * slots across several pools ("state semantics" page, section 2: rollback is
+ * an exact block copy, replayed on every pool in one launch; section 3: a
+ * fork copies the parent state to each candidate).
+ *
+ *   pools       : HOST array of n_pools (<= KDA_MAX_POOLS) descriptors; slot s
+ *                 of pool i is slot_bytes bytes at base + s*slot_stride_bytes.
+ *                 base, slot_stride_bytes and slot_bytes must be multiples of 16.
+ *   clear_slots : [n_clear] slots zeroed in every pool.
+ *   src_slots   : [n_src]; dst_offsets: [n_src+1] (CSR, dst_offsets[0] = 0,
+ *                 dst_offsets[n_src] = n_dst); dst_slots: [n_dst].  Source i
+ *                 is copied byte for byte to dst_slots[dst_offsets[i] ..
+ *                 dst_offsets[i+1]-1] in every pool.
+ *   workspace   : >= kda_slot_copy_workspace_size(max slots over the pools)
+ *                 bytes of device scratch (the disjointness check's bitmap).
+ * Precondition, checked on the GPU: destinations pairwise distinct and
+ * disjoint from sources and clears; clears distinct and disjoint from sources;
+ * every slot < num_slots of every pool.  On a violation nothing is copied and
+ * KDA_DEV_OVERLAP / KDA_DEV_BAD_SLOT is set.  Under the precondition the
+ * result is exact and independent of ordering.
+ */
+typedef struct {
+    void* base;
+    int64_t slot_stride_bytes;
+    int64_t slot_bytes;
+    int64_t num_slots;
+} kda_pool_desc;
+
+kda_status kda_slot_copy(const kda_pool_desc* pools, int32_t n_pools, const int32_t* clear_slots,
+                         int32_t n_clear, const int32_t* src_slots, const int32_t* dst_offsets,
+                         const int32_t* dst_slots, int32_t n_src, int32_t n_dst, void* workspace,
+                         size_t ws_bytes, int32_t* dev_status, void* stream);
+
+size_t kda_slot_copy_workspace_size(int64_t max_slots);
+
+const char* kda_status_string(kda_status s);
+
+/* Version of the library ABI (major * 100 + minor). */
+int32_t kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

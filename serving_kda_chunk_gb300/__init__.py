@@ -1,0 +1,209 @@
+"""Python binding of libkda, the sm_103a library for the KDA recurrent-state path.
+
+Argument marshalling only: every function below turns torch tensors into
+device pointers and sizes and calls the C ABI declared in include/kda.h; all
+arithmetic runs in the library's CUDA kernels.  There is no CPU fallback: if
+libkda.so is missing the import of the library raises.
+
+Entry points (same names as the C ABI):
+  kda_chunk_prefill, kda_recurrent_decode, kda_spec_verify, kda_spec_commit,
+  kda_slot_copy, kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+__all__ = [
+    "KDA_BF16", "KDA_F32", "KDA_GATE_LOG", "KDA_BETA_ACT", "KdaError", "lib",
+    "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_commit",
+    "kda_slot_copy", "kda_chunk_prefill_workspace_size", "kda_slot_copy_workspace_size",
+    "kda_status_string", "kda_abi_version", "PoolDesc",
+]
+
+KDA_BF16, KDA_F32 = 0, 1
+KDA_GATE_LOG, KDA_BETA_ACT = 1, 2
+KDA_DEV_BAD_SLOT, KDA_DEV_BAD_TRACK, KDA_DEV_BAD_ACCEPT = 1, 2, 4
+KDA_DEV_BAD_SEQLEN, KDA_DEV_OVERLAP = 8, 16
+KDA_MAX_POOLS = 16
+
+LIB_PATH = Path(__file__).resolve().parent / "libkda.so"
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {kda_status_string(status)} (status {status})")
+        self.status = status
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("slot_stride_bytes", ctypes.c_int64),
+                ("slot_bytes", ctypes.c_int64), ("num_slots", ctypes.c_int64)]
+
+
+def lib():
+    """The loaded C library with argument types set (raises if not built)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback path)")
+        L = ctypes.CDLL(str(LIB_PATH))
+        vp, i32, i64, f32, u32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                      ctypes.c_float, ctypes.c_uint32, ctypes.c_size_t)
+        L.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i32, i32, i32, i32,
+                                        i32, i32, f32, u32, vp, i64, vp, vp, vp, i32, vp, vp,
+                                        ctypes.c_int, vp, sz, vp, vp]
+        L.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32,
+                                           f32, u32, vp, i64, vp, vp, ctypes.c_int, vp, vp]
+        L.kda_spec_verify.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, vp, i32, i32,
+                                      i32, f32, u32, vp, i64, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+        L.kda_spec_commit.argtypes = [vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, i32, u32, vp,
+                                      vp, ctypes.c_int, vp, vp, vp]
+        L.kda_slot_copy.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp, i32, i32,
+                                    vp, sz, vp, vp]
+        L.kda_chunk_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.kda_chunk_prefill_workspace_size.restype = sz
+        L.kda_slot_copy_workspace_size.argtypes = [i64]
+        L.kda_slot_copy_workspace_size.restype = sz
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_abi_version.restype = i32
+        for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify",
+                  "kda_spec_commit", "kda_slot_copy"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def kda_abi_version() -> int:
+    return int(lib().kda_abi_version())
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return int(t)
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("libkda takes contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _dt(t) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise KdaError(status, where)
+
+
+# --------------------------------------------------------------------------
+# entry points
+
+
+def kda_chunk_prefill_workspace_size(T_tot, N, H, dk=128, dv=128, chunk=64) -> int:
+    return int(lib().kda_chunk_prefill_workspace_size(T_tot, N, H, dk, dv, chunk))
+
+
+def kda_slot_copy_workspace_size(max_slots) -> int:
+    return int(lib().kda_slot_copy_workspace_size(max_slots))
+
+
+def kda_chunk_prefill(q, k, v, beta_raw, gate_raw, cu_seqlens, out, *, state_pool=None,
+                      init_slot=None, final_slot=None, track_chunk_idx=None, track_state=None,
+                      scale=1.0, flags=0, chunk=64, workspace=None, dev_status=None, stream=None):
+    """Chunked prefill over packed sequences (see include/kda.h)."""
+    T_tot, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    M = 0 if track_chunk_idx is None else int(track_chunk_idx.shape[-1])
+    P = 0 if state_pool is None else int(state_pool.shape[0])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().kda_chunk_prefill(
+        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), _p(cu_seqlens), N, T_tot, H, dk,
+        dv, chunk, float(scale), int(flags), _p(state_pool), P, _p(init_slot), _p(final_slot),
+        _p(track_chunk_idx), M, _p(track_state), _p(out), _dt(out), _p(workspace), ws_bytes,
+        _p(dev_status), _stream(stream))
+    _check(st, "kda_chunk_prefill")
+
+
+def kda_recurrent_decode(q, k, v, beta_raw, gate_raw, state_pool, slot, out, *, scale=1.0,
+                         flags=0, dev_status=None, stream=None):
+    """One token per request, in place on state_pool[slot] (see include/kda.h)."""
+    R, H, dk = q.shape
+    dv = v.shape[2]
+    st = lib().kda_recurrent_decode(
+        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), R, H, dk, dv, float(scale),
+        int(flags), _p(state_pool), int(state_pool.shape[0]), _p(slot), _p(out), _dt(out),
+        _p(dev_status), _stream(stream))
+    _check(st, "kda_recurrent_decode")
+
+
+def kda_spec_verify(q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, rec_kg, out, *,
+                    K, q_len=None, scale=1.0, flags=0, dev_status=None, stream=None):
+    """K speculative positions per request from one checkpoint (see include/kda.h)."""
+    RK, H, dk = q.shape
+    dv = v.shape[2]
+    R = RK // K
+    st = lib().kda_spec_verify(
+        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), R, K, _p(q_len), H, dk, dv,
+        float(scale), int(flags), _p(state_pool), int(state_pool.shape[0]), _p(ckpt_slot),
+        _p(rec_u), _p(rec_kg), _p(out), _dt(out), _p(dev_status), _stream(stream))
+    _check(st, "kda_spec_verify")
+
+
+def kda_spec_commit(state_pool, ckpt_slot, num_accepted, rec_u, rec_kg, *, K, dst_slot=None,
+                    q_len=None, flags=0, plan_out=None, dev_status=None, stream=None):
+    """Closed-form rebuild at the accepted length (see include/kda.h)."""
+    P, H, dv, dk = state_pool.shape
+    R = ckpt_slot.shape[0]
+    st = lib().kda_spec_commit(
+        _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(num_accepted), _p(q_len), R, K, H,
+        dk, dv, int(flags), _p(rec_u), _p(rec_kg), _dt(rec_kg), _p(plan_out), _p(dev_status),
+        _stream(stream))
+    _check(st, "kda_spec_commit")
+
+
+def kda_slot_copy(pools, clear_slots, src_slots, dst_offsets, dst_slots, workspace, *,
+                  dev_status=None, stream=None):
+    """Clear / copy / fan out slots on every pool in one launch (see include/kda.h).
+
+    pools: list of CUDA tensors [num_slots, ...] (slot = first dimension)."""
+    n = len(pools)
+    descs = (PoolDesc * max(n, 1))()
+    for i, t in enumerate(pools):
+        descs[i] = PoolDesc(_p(t), t.stride(0) * t.element_size(),
+                            t[0].numel() * t.element_size(), t.shape[0])
+    n_clear = 0 if clear_slots is None else int(clear_slots.numel())
+    n_src = 0 if src_slots is None else int(src_slots.numel())
+    n_dst = 0 if dst_slots is None else int(dst_slots.numel())
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().kda_slot_copy(descs, n, _p(clear_slots), n_clear, _p(src_slots), _p(dst_offsets),
+                             _p(dst_slots), n_src, n_dst, _p(workspace), ws_bytes,
+                             _p(dev_status), _stream(stream))
+    _check(st, "kda_slot_copy")

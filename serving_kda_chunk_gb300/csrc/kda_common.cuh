@@ -1,0 +1,236 @@
+// kda_common.cuh -- device helpers shared by the libkda kernels (sm_103a).
+//
+// Gate and beta activations are applied inside every kernel with the same
+// code, in fp32: g = -softplus(raw gate) per key channel, beta = sigmoid(raw
+// beta).  The "state semantics" page (section 4) records that prefill and
+// decode/verify activated the gate in different places in the engines it
+// read; using one device function everywhere removes that difference here.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kD = 128;  // d_k = d_v
+constexpr int kChunk = 64;
+
+// ----------------------------------------------------------------------------
+// activations (fp32; CUDA's expf / log1pf)
+
+__device__ __forceinline__ float gate_log(float raw, uint32_t flags) {
+    if (flags & KDA_GATE_LOG) return raw;
+    // -softplus(x), split at 0 so exp never overflows
+    return raw > 0.f ? -(raw + log1pf(expf(-raw))) : -log1pf(expf(raw));
+}
+
+__device__ __forceinline__ float beta_act(float raw, uint32_t flags) {
+    if (flags & KDA_BETA_ACT) return raw;
+    return 1.f / (1.f + expf(-raw));
+}
+
+// ----------------------------------------------------------------------------
+// element access for bf16 / fp32 activations
+
+template <bool kBf16>
+struct Act;
+
+template <>
+struct Act<true> {
+    using T = __nv_bfloat16;
+    // four consecutive elements starting at element index i (i % 4 == 0)
+    static __device__ __forceinline__ float4 load4(const void* p, size_t i) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const T*>(p) + i));
+        float4 r;
+        r.x = __uint_as_float(w.x << 16);
+        r.y = __uint_as_float(w.x & 0xffff0000u);
+        r.z = __uint_as_float(w.y << 16);
+        r.w = __uint_as_float(w.y & 0xffff0000u);
+        return r;
+    }
+    static __device__ __forceinline__ float load1(const void* p, size_t i) {
+        return __bfloat162float(static_cast<const T*>(p)[i]);
+    }
+    // raw 8-byte copy of four elements (records keep the input bits)
+    static __device__ __forceinline__ void copy4(void* dst, size_t di, const void* src, size_t si) {
+        *reinterpret_cast<uint2*>(static_cast<T*>(dst) + di) =
+            __ldg(reinterpret_cast<const uint2*>(static_cast<const T*>(src) + si));
+    }
+    static __device__ __forceinline__ void zero4(void* dst, size_t di) {
+        *reinterpret_cast<uint2*>(static_cast<T*>(dst) + di) = make_uint2(0u, 0u);
+    }
+};
+
+template <>
+struct Act<false> {
+    static __device__ __forceinline__ float4 load4(const void* p, size_t i) {
+        return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+    }
+    static __device__ __forceinline__ float load1(const void* p, size_t i) {
+        return static_cast<const float*>(p)[i];
+    }
+    static __device__ __forceinline__ void copy4(void* dst, size_t di, const void* src, size_t si) {
+        *reinterpret_cast<float4*>(static_cast<float*>(dst) + di) =
+            __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(src) + si));
+    }
+    static __device__ __forceinline__ void zero4(void* dst, size_t di) {
+        *reinterpret_cast<float4*>(static_cast<float*>(dst) + di) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool kBf16Out>
+__device__ __forceinline__ void store1(void* out, size_t i, float x) {
+    if constexpr (kBf16Out)
+        static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(x);
+    else
+        static_cast<float*>(out)[i] = x;
+}
+
+template <bool kBf16Out>
+__device__ __forceinline__ void store4(void* out, size_t i, float4 x) {
+    if constexpr (kBf16Out) {
+        uint2 w = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + i) = w;
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = x;
+    }
+}
+
+__device__ __forceinline__ void report(int32_t* dev_status, int32_t bits) {
+    if (dev_status) atomicOr(dev_status, bits);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Sum two values across the warp with interleaved shuffles.
+__device__ __forceinline__ void warp_sum2(float& a, float& b) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+}
+
+__device__ __forceinline__ float4 f4_mul(float4 a, float4 b) {
+    return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+__device__ __forceinline__ float f4_dot(float4 a, float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+__device__ __forceinline__ float4 f4_fma(float s, float4 k, float4 x) {
+    return make_float4(fmaf(s, k.x, x.x), fmaf(s, k.y, x.y), fmaf(s, k.z, x.z), fmaf(s, k.w, x.w));
+}
+
+// ----------------------------------------------------------------------------
+// One recurrence step for 16 state rows held by a warp.
+//
+// The warp holds S^T rows [row0, row0+16) (a row = one value channel, 128 key
+// channels); lane l owns key channels [4l, 4l+4).  For each row c:
+//   x = alpha (.) S^T[c]              (X = Diag(alpha) S, by key channel)
+//   u = beta (v[c] - x . k)
+//   S^T[c] = x + u k
+//   o[c] = scale (x . q + u (k . q))  (= S_t^T (scale q))
+// Returns u and o of row c in lane (c - row0) (other lanes get garbage).
+struct StepIn {
+    float4 a;   // alpha for this lane's 4 key channels
+    float4 k;
+    float4 q;   // already multiplied by scale
+    float kq;   // full k . q (scaled)
+    float beta;
+};
+
+__device__ __forceinline__ void step_rows16(float4 (&s)[16], const StepIn& in, const float (&vrow)[16],
+                                            float& u_mine, float& o_mine, int lane) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float4 x = f4_mul(s[r], in.a);
+        float d1 = f4_dot(x, in.k);
+        float d2 = f4_dot(x, in.q);
+        warp_sum2(d1, d2);
+        const float u = in.beta * (vrow[r] - d1);
+        s[r] = f4_fma(u, in.k, x);
+        const float o = fmaf(u, in.kq, d2);
+        if (lane == r) {
+            u_mine = u;
+            o_mine = o;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// A tile of consecutive token rows staged in shared memory with the
+// activations applied: alpha = exp(g), q scaled, beta activated, k . q.
+template <int kTile>
+struct TokenTile {
+    float a[kTile][kD];
+    float k[kTile][kD];
+    float q[kTile][kD];
+    float v[kTile][kD];
+    float beta[kTile];
+    float kq[kTile];
+};
+
+// Rows row_base .. row_base+n_tok-1 of head h; 8 warps, a warp per row.
+template <bool kBf16, int kTile>
+__device__ __forceinline__ void stage_tokens(TokenTile<kTile>& tt, const void* q, const void* k,
+                                             const void* v, const void* beta_raw,
+                                             const void* gate_raw, size_t row_base, int n_tok,
+                                             int H, int h, float scale, uint32_t flags) {
+    using A = Act<kBf16>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < n_tok; t += (int)(blockDim.x >> 5)) {
+        const size_t th = (row_base + t) * (size_t)H + h;
+        const float4 g = A::load4(gate_raw, th * kD + 4 * lane);
+        const float4 kk = A::load4(k, th * kD + 4 * lane);
+        const float4 qq = A::load4(q, th * kD + 4 * lane);
+        const float4 vv = A::load4(v, th * kD + 4 * lane);
+        const float4 a = make_float4(expf(gate_log(g.x, flags)), expf(gate_log(g.y, flags)),
+                                     expf(gate_log(g.z, flags)), expf(gate_log(g.w, flags)));
+        const float4 qs = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);
+        *reinterpret_cast<float4*>(&tt.a[t][4 * lane]) = a;
+        *reinterpret_cast<float4*>(&tt.k[t][4 * lane]) = kk;
+        *reinterpret_cast<float4*>(&tt.q[t][4 * lane]) = qs;
+        *reinterpret_cast<float4*>(&tt.v[t][4 * lane]) = vv;
+        const float kq = warp_sum(f4_dot(kk, qs));
+        if (lane == 0) {
+            tt.kq[t] = kq;
+            tt.beta[t] = beta_act(A::load1(beta_raw, th), flags);
+        }
+    }
+}
+
+// Recurrence step for token t of a staged tile on the warp's 16 rows.
+template <int kTile>
+__device__ __forceinline__ void step_from_tile(float4 (&s)[16], const TokenTile<kTile>& tt, int t,
+                                               int row0, int lane, float& u_m, float& o_m) {
+    StepIn in;
+    in.a = *reinterpret_cast<const float4*>(&tt.a[t][4 * lane]);
+    in.k = *reinterpret_cast<const float4*>(&tt.k[t][4 * lane]);
+    in.q = *reinterpret_cast<const float4*>(&tt.q[t][4 * lane]);
+    in.kq = tt.kq[t];
+    in.beta = tt.beta[t];
+    float vrow[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(&tt.v[t][row0 + 4 * i]);
+        vrow[4 * i] = x.x;
+        vrow[4 * i + 1] = x.y;
+        vrow[4 * i + 2] = x.z;
+        vrow[4 * i + 3] = x.w;
+    }
+    step_rows16(s, in, vrow, u_m, o_m, lane);
+}
+
+}  // namespace kda

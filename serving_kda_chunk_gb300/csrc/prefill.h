@@ -1,0 +1,34 @@
+// prefill.h -- arguments shared by the kda_chunk_prefill kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kMaxTrack = 1024;  // snapshot requests per sequence
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* beta_raw;
+    const void* gate_raw;
+    const int32_t* cu_seqlens;
+    int32_t N, T_tot, H;
+    float scale;
+    uint32_t flags;
+    float* pool;
+    int64_t P;
+    const int32_t* init_slot;
+    const int32_t* final_slot;
+    const int32_t* track;
+    int32_t M;
+    float* track_state;
+    void* out;
+    int32_t* dev_status;
+};
+
+void launch_prefill_serial(const PrefillArgs& p, bool bf16_in, bool bf16_out, cudaStream_t s);
+
+}  // namespace kda

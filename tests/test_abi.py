@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad host-side arguments before launching anything."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "kda.h"
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import serving_kda_chunk_gb300 as kda
+
+    return kda
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_commit",
+              "kda_slot_copy"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(kda):
+    L = ctypes.CDLL(str(kda.LIB_PATH))
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(kda):
+    assert kda.kda_status_string(0) == "KDA_OK"
+    assert "INVALID_ARG" in kda.kda_status_string(1)
+    assert "UNSUPPORTED" in kda.kda_status_string(2)
+    assert kda.kda_abi_version() >= 100
+
+
+def test_workspace_sizes(kda):
+    assert kda.kda_slot_copy_workspace_size(0) == 16
+    assert kda.kda_slot_copy_workspace_size(4096) == 16 + 4096 // 8
+    assert kda.kda_slot_copy_workspace_size(129) % 16 == 0
+    assert kda.kda_chunk_prefill_workspace_size(1 << 20, 8, 32) >= 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced (checks fail first)
+
+
+def test_host_checks_reject_bad_arguments(kda):
+    L = kda.lib()
+    # unsupported head dimension
+    st = L.kda_recurrent_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 2, 64, 64, 1.0, 0, FAKE, 8,
+                                FAKE, FAKE, 0, None, None)
+    assert st == 2
+    # null input pointer
+    st = L.kda_recurrent_decode(None, FAKE, FAKE, FAKE, FAKE, 0, 4, 2, 128, 128, 1.0, 0, FAKE, 8,
+                                FAKE, FAKE, 0, None, None)
+    assert st == 1
+    # misaligned output
+    st = L.kda_recurrent_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 2, 128, 128, 1.0, 0, FAKE, 8,
+                                FAKE, FAKE + 2, 0, None, None)
+    assert st == 1
+    # bad dtype enum
+    st = L.kda_spec_verify(FAKE, FAKE, FAKE, FAKE, FAKE, 7, 4, 3, None, 2, 128, 128, 1.0, 0, FAKE,
+                           8, FAKE, FAKE, FAKE, FAKE, 0, None, None)
+    assert st == 2
+    # commit: K above the supported maximum
+    st = L.kda_spec_commit(FAKE, 8, FAKE, None, FAKE, None, 4, 1000, 2, 128, 128, 0, FAKE, FAKE,
+                           0, None, None, None)
+    assert st == 2
+    # prefill: chunk other than 64
+    st = L.kda_chunk_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 64, 2, 128, 128, 32, 1.0,
+                             0, None, 0, None, None, None, 0, None, FAKE, 0, None, 0, None, None)
+    assert st == 2
+    # prefill: snapshots requested without a snapshot buffer
+    st = L.kda_chunk_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 64, 2, 128, 128, 64, 1.0,
+                             0, None, 0, None, None, FAKE, 1, None, FAKE, 0, None, 0, None, None)
+    assert st == 1
+    # zero-sized work launches nothing and succeeds
+    assert L.kda_recurrent_decode(None, None, None, None, None, 0, 0, 2, 128, 128, 1.0, 0, None,
+                                  0, None, None, 0, None, None) == 0
+
+
+def test_slot_copy_host_checks(kda):
+    L = kda.lib()
+    descs = (kda.PoolDesc * 1)()
+    descs[0] = kda.PoolDesc(FAKE, 64, 64, 8)
+    # too many pools
+    assert L.kda_slot_copy(descs, 17, None, 0, None, FAKE, None, 0, 0, FAKE, 4096, None,
+                           None) == 1
+    # slot_bytes not a multiple of 16
+    descs[0] = kda.PoolDesc(FAKE, 64, 60, 8)
+    assert L.kda_slot_copy(descs, 1, None, 0, None, FAKE, None, 0, 0, FAKE, 4096, None,
+                           None) == 1
+    # workspace too small
+    descs[0] = kda.PoolDesc(FAKE, 64, 64, 1 << 20)
+    assert L.kda_slot_copy(descs, 1, None, 0, None, FAKE, None, 0, 0, FAKE, 16, None,
+                           None) == 1
+
+
+def test_product_path_has_no_cpu_fallback():
+    # the binding imports nothing from the oracle and no torch CPU op computes a result
+    src = (ROOT / "serving_kda_chunk_gb300" / "__init__.py").read_text()
+    assert "oracle" not in src.replace("no oracle", "")
+    for f in (ROOT / "serving_kda_chunk_gb300" / "csrc").glob("*"):
+        assert "oracle" not in f.read_text().lower(), f
