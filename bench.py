@@ -173,7 +173,7 @@ class Step:
         self.kda = kda
         self.dev = dev
         t0 = time.time()
-        c1 = W.cfg1()
+        c1 = _cfg1()
         self.c1 = c1
         self.pre = {n: to_dev(c1[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
         self.pre_host = {n: torch.from_numpy(c1[n].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -330,10 +330,20 @@ def run_e2e(step, steps, warmup):
 # CPU oracle on a bounded sample of the prefill workload
 
 
+_CFG1 = None
+
+
+def _cfg1():
+    global _CFG1
+    if _CFG1 is None:
+        _CFG1 = W.cfg1()
+    return _CFG1
+
+
 def cpu_oracle_sample(heads=(0, 1, 2, 3), threads=None):
     import oracle
 
-    c = W.cfg1()
+    c = _cfg1()
     H = c["H"]
     hs = list(heads)
     wid = lambda n: W.widen(c[n], "bf16")[:, hs]  # noqa: E731
@@ -422,7 +432,7 @@ def main_reference(args, rank, world):
         cpu_oracle_sample(heads=(0,))
     cb = None
     for _ in range(steps):
-        cb = cpu_oracle_sample(heads=(0,))
+        cb = cpu_oracle_sample()
         vals.append(cb["value"])
     value = statistics.mean(vals)
     cb["value"] = value

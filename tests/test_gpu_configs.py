@@ -1,0 +1,177 @@
+"""GPU parity at the full sizes of the serving workloads, in the launch
+configuration the benchmark times.  Where the fp64 oracle cannot cover the
+whole workload in seconds it checks sampled heads (all sequences / requests
+of those heads, every output, snapshot and final state of them)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import TOL_STATE, dev_tensor, i32, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import serving_kda_chunk_gb300 as kda
+
+    return kda
+
+
+def _prefill_gpu(kda, c, pool_np):
+    dt = c["dtype"]
+    pool = torch.from_numpy(pool_np).cuda() if pool_np is not None else None
+    odt = torch.bfloat16 if dt == "bf16" else torch.float32
+    out = torch.empty(c["T"], c["H"], 128, dtype=odt, device="cuda")
+    M = c["track"].shape[1]
+    snap = torch.full((c["N"], M, c["H"], 128, 128), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_chunk_prefill(dev_tensor(c["q"], dt), dev_tensor(c["k"], dt), dev_tensor(c["v"], dt),
+                          dev_tensor(c["beta"], dt), dev_tensor(c["gate"], dt),
+                          i32(c["cu_seqlens"]), out, state_pool=pool,
+                          init_slot=i32(c["init_slot"]), final_slot=i32(c["final_slot"]),
+                          track_chunk_idx=i32(c["track"]), track_state=snap, dev_status=st)
+    torch.cuda.synchronize()
+    return out, pool, snap, int(st.item())
+
+
+def _oracle_heads(c, heads, S0_all=None):
+    dt = c["dtype"]
+    sl = lambda n: W.widen(c[n], dt)[:, heads]  # noqa: E731
+    S0 = None if S0_all is None else S0_all[:, heads]
+    return oracle.prefill(sl("q"), sl("k"), sl("v"), sl("beta"), sl("gate"), c["cu_seqlens"],
+                          S0=S0, track=c["track"])
+
+
+def test_cfg0_tiny_prefill_fp32(kda):
+    c = W.cfg0()
+    c["final_slot"] = np.array([0], np.int32)  # also read back the final state
+    pool = np.zeros((1, 4, 128, 128), np.float32)
+    out, pool_d, snap, st = _prefill_gpu(kda, c, pool)
+    o_ref, s_ref, snap_ref, _ = _oracle_heads(c, list(range(4)))
+    assert st == 0
+    assert rel_l2(to_np(out), o_ref) < 1e-4
+    assert rel_l2(snap.cpu().numpy(), snap_ref) < TOL_STATE
+    assert rel_l2(pool_d.cpu().numpy(), s_ref) < TOL_STATE
+
+
+def test_cfg1_batched_prefill_sampled_heads(kda):
+    c = W.cfg1()
+    S0_all = c["pool"][c["init_slot"]].astype(np.float64)
+    out, pool, snap, st = _prefill_gpu(kda, c, c["pool"])
+    assert st == 0
+    heads = [0, 17, 31]
+    o_ref, s_ref, snap_ref, _ = _oracle_heads(c, heads, S0_all)
+    assert rel_l2(to_np(out[:, heads]), o_ref) < 5e-3
+    fin = pool.cpu().numpy()[c["final_slot"]][:, heads]
+    assert rel_l2(fin, s_ref) < TOL_STATE
+    assert rel_l2(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
+    # every head was written: final states differ from the initial ones
+    assert not np.array_equal(pool.cpu().numpy()[c["final_slot"]], c["pool"][c["init_slot"]])
+    assert not torch.isnan(snap).any()
+
+
+def test_cfg2_decode_full(kda):
+    d = W.cfg2()
+    pool = torch.from_numpy(d["pool"]).cuda()
+    out = torch.empty(256, 32, 128, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_recurrent_decode(*(dev_tensor(d[n], "bf16") for n in ("q", "k", "v", "beta", "gate")),
+                             pool, i32(d["slot"]), out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    wid = lambda n: W.widen(d[n], "bf16")  # noqa: E731
+    slots = d["slot"]
+    o_ref, p_ref, _ = oracle.decode(wid("q"), wid("k"), wid("v"), wid("beta"), wid("gate"),
+                                    d["pool"][slots], np.arange(256, dtype=np.int32))
+    assert rel_l2(to_np(out), o_ref) < 5e-3
+    assert rel_l2(pool[torch.from_numpy(slots).long().cuda()].cpu().numpy(), p_ref) < TOL_STATE
+    untouched = np.setdiff1d(np.arange(1024), slots)[:64]
+    assert np.array_equal(pool[torch.from_numpy(untouched).cuda()].cpu().numpy(),
+                          d["pool"][untouched])
+
+
+def test_cfg3_spec_verify_commit_full(kda):
+    s = W.cfg3()
+    pool = torch.from_numpy(s["pool"]).cuda()
+    rec_u = torch.empty(64, 32, 7, 128, device="cuda")
+    rec_kg = torch.empty(64, 32, 7, 256, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(448, 32, 128, dtype=torch.bfloat16, device="cuda")
+    plan = torch.empty(64, 3, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_spec_verify(*(dev_tensor(s[n], "bf16") for n in ("q", "k", "v", "beta", "gate")),
+                        pool, i32(s["ckpt"]), rec_u, rec_kg, out, K=7, dev_status=st)
+    kda.kda_spec_commit(pool, i32(s["ckpt"]), i32(s["num_accepted"]), rec_u, rec_kg, K=7,
+                        plan_out=plan, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    wid = lambda n: W.widen(s[n], "bf16")  # noqa: E731
+    o_ref, ru_ref, rkg_ref, _ = oracle.verify(wid("q"), wid("k"), wid("v"), wid("beta"),
+                                              wid("gate"), s["pool"], s["ckpt"], 7)
+    assert rel_l2(to_np(out), o_ref) < 5e-3
+    assert rel_l2(rec_u.cpu().numpy(), ru_ref) < TOL_STATE
+    assert np.array_equal(to_np(rec_kg), rkg_ref)
+    p_ref, plan_ref, _ = oracle.commit(s["pool"], s["ckpt"], s["num_accepted"], ru_ref, rkg_ref,
+                                       7)
+    assert np.array_equal(plan.cpu().numpy(), plan_ref)
+    assert rel_l2(pool.cpu().numpy(), p_ref) < TOL_STATE
+    # a = 0 in place leaves the checkpoint bit-identical
+    zero = s["ckpt"][s["num_accepted"] == 0]
+    assert np.array_equal(pool.cpu().numpy()[zero], s["pool"][zero])
+
+
+def test_cfg4_long_prefill_sampled_heads(kda):
+    c = W.cfg4_prefill()
+    c["final_slot"] = np.array([0], np.int32)
+    c["init_slot"] = np.array([-1], np.int32)
+    pool = np.zeros((1, 16, 128, 128), np.float32)
+    out, pool_d, snap, st = _prefill_gpu(kda, c, pool)
+    assert st == 0
+    heads = [5]
+    o_ref, s_ref, snap_ref, _ = _oracle_heads(c, heads)
+    assert rel_l2(to_np(out[:, heads]), o_ref) < 5e-3
+    assert rel_l2(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
+    assert rel_l2(pool_d.cpu().numpy()[:, heads], s_ref) < TOL_STATE
+    assert not torch.isnan(snap).any()
+
+
+def test_cfg4_slot_copy_sampled(kda):
+    sc = W.cfg4_slot_copy()
+    g = torch.Generator(device="cuda").manual_seed(4)
+    pool = torch.empty(4096, 16, 128, 128, device="cuda")
+    for i in range(0, 4096, 512):
+        pool[i:i + 512].normal_(0.0, 0.1, generator=g)
+    pick_src = np.arange(0, 256, 17)
+    sample = set(sc["src"][pick_src].tolist())
+    for i in pick_src:
+        sample |= set(sc["dst"][sc["dst_offsets"][i]:sc["dst_offsets"][i + 1]].tolist())
+    sample |= set(sc["clear"][::37].tolist())
+    touched = set(sc["src"].tolist()) | set(sc["dst"].tolist()) | set(sc["clear"].tolist())
+    sample |= set(sorted(set(range(4096)) - touched)[:16])
+    sample = np.array(sorted(sample))
+    idx = torch.from_numpy(sample).cuda()
+    before = {int(s): a for s, a in zip(sample, pool[idx].cpu().numpy())}
+    ws = torch.empty(kda.kda_slot_copy_workspace_size(4096), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_slot_copy([pool], i32(sc["clear"]), i32(sc["src"]), i32(sc["dst_offsets"]),
+                      i32(sc["dst"]), ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    after = {int(s): a for s, a in zip(sample, pool[idx].cpu().numpy())}
+    for i in pick_src:
+        s = int(sc["src"][i])
+        assert np.array_equal(after[s], before[s])
+        for d in sc["dst"][sc["dst_offsets"][i]:sc["dst_offsets"][i + 1]]:
+            assert np.array_equal(after[int(d)], before[s])
+    for cl in sc["clear"][::37]:
+        assert not after[int(cl)].any()
+    for u in sorted(set(range(4096)) - touched)[:16]:
+        assert np.array_equal(after[u], before[u])
