@@ -218,6 +218,35 @@ kda_status kda_slot_copy(const kda_pool_desc* pools, int32_t n_pools, const int3
 
 size_t kda_slot_copy_workspace_size(int64_t max_slots);
 
+/*
+ * kda_slot_copy_noalloc -- kda_slot_copy without a caller-provided workspace.
+ * The serving pages have no counterpart; this entry point exists for callers
+ * that cannot allocate device memory on demand (an engine whose allocator owns
+ * all device memory after start-up, or a path where a cudaMalloc and the
+ * device synchronisation it may cause are not acceptable).
+ *
+ * The disjointness check uses a fixed scratch array inside the library's own
+ * device memory, sized for KDA_SLOT_COPY_NOALLOC_MAX_SLOTS slots (about
+ * 128 KiB, held on every GPU that loads the library until the process exits).
+ *   - Arguments and results are those of kda_slot_copy minus the workspace.
+ *   - Returns KDA_ERR_UNSUPPORTED when the smallest pool has more than
+ *     KDA_SLOT_COPY_NOALLOC_MAX_SLOTS slots; nothing is launched then.
+ *   - Allocates nothing: no cudaMalloc / cudaFree and no allocating library
+ *     call.  The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array; the kernel clears the part it uses on
+ *     every call, but calls that may overlap on the GPU (different streams
+ *     without ordering between them) race on it and must be serialised.
+ */
+#define KDA_SLOT_COPY_NOALLOC_MAX_SLOTS (1 << 20)
+
+kda_status kda_slot_copy_noalloc(const kda_pool_desc* pools, int32_t n_pools,
+                                 const int32_t* clear_slots, int32_t n_clear,
+                                 const int32_t* src_slots, const int32_t* dst_offsets,
+                                 const int32_t* dst_slots, int32_t n_src, int32_t n_dst,
+                                 int32_t* dev_status, void* stream);
+
 const char* kda_status_string(kda_status s);
 
 /* Version of the library ABI (major * 100 + minor). */

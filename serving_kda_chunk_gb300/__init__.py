@@ -65,6 +65,9 @@ def lib():
                                       vp, ctypes.c_int, vp, vp, vp]
         L.kda_slot_copy.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp, i32, i32,
                                     vp, sz, vp, vp]
+        L.kda_slot_copy_noalloc.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp,
+                                            i32, i32, vp, vp]
+        L.kda_slot_copy_noalloc.restype = ctypes.c_int
         L.kda_chunk_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.kda_chunk_prefill_workspace_size.restype = sz
         L.kda_slot_copy_workspace_size.argtypes = [i64]

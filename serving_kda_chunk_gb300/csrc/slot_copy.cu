@@ -12,6 +12,8 @@
 // with 16-byte vector loads and stores.  A fan-out source piece is read once
 // into registers and written to each of its destinations.  The copy kernel
 // reads the verdict first and does nothing if the check failed.
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "kda_host.h"
 
@@ -189,3 +191,60 @@ extern "C" const char* kda_status_string(kda_status st) {
 }
 
 extern "C" int32_t kda_abi_version(void) { return 100; }
+
+// ----------------------------------------------------------------------------
+// Allocation-free variant.
+//
+// Some callers cannot hand the library a workspace: an engine that gives all
+// device memory to its own pool allocator when it starts and forbids any other
+// allocation afterwards, or a latency-critical path where a cudaMalloc (which
+// may synchronise the device) is not acceptable.  kda_slot_copy_noalloc uses a
+// fixed scratch array that lives in the library's own device memory instead.
+// The array is sized for KDA_SLOT_COPY_NOALLOC_MAX_SLOTS slots; every GPU that
+// loads the library holds it until the process exits.
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 16 + ((size_t)KDA_SLOT_COPY_NOALLOC_MAX_SLOTS + 127) / 128 * 16;
+
+static __device__ __align__(256) unsigned char g_slot_copy_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per
+// device; the name alone is only a host-side stand-in).
+kda_status scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_slot_copy_scratch) != cudaSuccess || p == nullptr)
+            return KDA_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" kda_status kda_slot_copy_noalloc(const kda_pool_desc* pools, int32_t n_pools,
+                                            const int32_t* clear_slots, int32_t n_clear,
+                                            const int32_t* src_slots, const int32_t* dst_offsets,
+                                            const int32_t* dst_slots, int32_t n_src, int32_t n_dst,
+                                            int32_t* dev_status, void* stream) {
+    KDA_REQUIRE(pools != nullptr && n_pools > 0 && n_pools <= KDA_MAX_POOLS, KDA_ERR_INVALID_ARG);
+    int64_t min_slots = INT64_MAX;
+    for (int i = 0; i < n_pools; ++i)
+        min_slots = pools[i].num_slots < min_slots ? pools[i].num_slots : min_slots;
+    // the disjointness bitmap covers slot ids below the smallest pool's size
+    KDA_REQUIRE(min_slots <= KDA_SLOT_COPY_NOALLOC_MAX_SLOTS, KDA_ERR_UNSUPPORTED);
+    void* scratch = nullptr;
+    const kda_status st = scratch_address(&scratch);
+    if (st != KDA_OK) return st;
+    return kda_slot_copy(pools, n_pools, clear_slots, n_clear, src_slots, dst_offsets, dst_slots,
+                         n_src, n_dst, scratch, kNoallocScratchBytes, dev_status, stream);
+}
