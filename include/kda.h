@@ -63,6 +63,10 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 
 #define KDA_GATE_LOG 1u
 #define KDA_BETA_ACT 2u
+/* kda_chunk_prefill only: evaluate token by token (the recurrent form) instead
+ * of chunk by chunk on the tensor cores; used to measure the chunk-vs-recurrent
+ * numerical gap ("state semantics" page, section 4 and its open item). */
+#define KDA_PREFILL_RECURRENT 4u
 
 /* bits OR-ed into *dev_status by the kernels */
 #define KDA_DEV_BAD_SLOT 1     /* slot index >= pool size (or required and < 0) */
@@ -70,6 +74,7 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 #define KDA_DEV_BAD_ACCEPT 4   /* accepted length outside [0, q_len], bad q_len */
 #define KDA_DEV_BAD_SEQLEN 8   /* cu_seqlens not monotone or past T_tot         */
 #define KDA_DEV_OVERLAP 16     /* slot-copy sets not disjoint                    */
+#define KDA_DEV_TIMEOUT 32     /* a bounded wait inside a kernel gave up         */
 
 #define KDA_MAX_POOLS 16
 
@@ -97,9 +102,12 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *                    valid entries; the fp32 accumulator itself, never a
  *                    rounded copy).
  *   out            : [T_tot, H, d_v] out_dtype.
- *   workspace      : ws_bytes of device scratch, at least
- *                    kda_chunk_prefill_workspace_size(...) bytes (may be NULL
- *                    when that size is 0).
+ *   workspace      : optional device scratch of ws_bytes >=
+ *                    kda_chunk_prefill_workspace_size(...) bytes.  With it the
+ *                    kernel schedules the longest sequences first; with NULL
+ *                    it runs them in input order (same results).
+ * bf16 activations run on the tensor-core chunk kernel; fp32 activations and
+ * KDA_PREFILL_RECURRENT run the token-serial kernel.
  * Units of work are (sequence, head); sequences must not share a final slot.
  */
 kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* beta_raw,

@@ -24,9 +24,9 @@ __all__ = [
 ]
 
 KDA_BF16, KDA_F32 = 0, 1
-KDA_GATE_LOG, KDA_BETA_ACT = 1, 2
+KDA_GATE_LOG, KDA_BETA_ACT, KDA_PREFILL_RECURRENT = 1, 2, 4
 KDA_DEV_BAD_SLOT, KDA_DEV_BAD_TRACK, KDA_DEV_BAD_ACCEPT = 1, 2, 4
-KDA_DEV_BAD_SEQLEN, KDA_DEV_OVERLAP = 8, 16
+KDA_DEV_BAD_SEQLEN, KDA_DEV_OVERLAP, KDA_DEV_TIMEOUT = 8, 16, 32
 KDA_MAX_POOLS = 16
 
 LIB_PATH = Path(__file__).resolve().parent / "libkda.so"

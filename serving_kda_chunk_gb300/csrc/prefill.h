@@ -7,6 +7,7 @@
 namespace kda {
 
 constexpr int kMaxTrack = 1024;  // snapshot requests per sequence
+constexpr int kMaxOrderN = 4096; // sequences ordered longest-first by the tensor-core prefill
 
 struct PrefillArgs {
     const void* q;
@@ -30,5 +31,10 @@ struct PrefillArgs {
 };
 
 void launch_prefill_serial(const PrefillArgs& p, bool bf16_in, bool bf16_out, cudaStream_t s);
+
+bool prefill_tc_supported(const PrefillArgs& p, bool bf16_in);
+size_t prefill_tc_workspace(int32_t N);
+void launch_prefill_tc(const PrefillArgs& p, bool bf16_out, void* workspace, size_t ws_bytes,
+                       cudaStream_t s);
 
 }  // namespace kda

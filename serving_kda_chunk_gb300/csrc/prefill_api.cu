@@ -9,12 +9,11 @@ using namespace kda;
 extern "C" size_t kda_chunk_prefill_workspace_size(int32_t T_tot, int32_t N, int32_t H,
                                                    int32_t dk, int32_t dv, int32_t chunk) {
     (void)T_tot;
-    (void)N;
     (void)H;
     (void)dk;
     (void)dv;
     (void)chunk;
-    return 0;
+    return prefill_tc_workspace(N);
 }
 
 extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void* v,
@@ -43,12 +42,14 @@ extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void
         KDA_REQUIRE(track_chunk_idx != nullptr && track_state != nullptr, KDA_ERR_INVALID_ARG);
         KDA_REQUIRE(aligned16(track_chunk_idx) && aligned16(track_state), KDA_ERR_INVALID_ARG);
     }
-    KDA_REQUIRE(ws_bytes >= kda_chunk_prefill_workspace_size(T_tot, N, H, dk, dv, chunk),
-                KDA_ERR_INVALID_ARG);
-    (void)workspace;
+    if (workspace) KDA_REQUIRE(aligned16(workspace), KDA_ERR_INVALID_ARG);
     PrefillArgs p{q,     k,         v,         beta_raw,   gate_raw,        cu_seqlens, N,
                   T_tot, H,         scale,     flags,      state_pool,      P,          init_slot,
                   final_slot, track_chunk_idx, M, track_state, out, dev_status};
-    launch_prefill_serial(p, in_dtype == KDA_BF16, out_dtype == KDA_BF16, as_stream(stream));
+    const bool bf16_in = in_dtype == KDA_BF16, bf16_out = out_dtype == KDA_BF16;
+    if (!(flags & KDA_PREFILL_RECURRENT) && prefill_tc_supported(p, bf16_in))
+        launch_prefill_tc(p, bf16_out, workspace, ws_bytes, as_stream(stream));
+    else
+        launch_prefill_serial(p, bf16_in, bf16_out, as_stream(stream));
     return launch_status();
 }
