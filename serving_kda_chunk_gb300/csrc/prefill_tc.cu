@@ -46,11 +46,10 @@ constexpr int kThreads = 256;
 constexpr int kTrackTc = 512;  // snapshot requests per sequence handled by this kernel
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_ST_HI = 0;  // A: S^T [c][i], K-major, 128 rows, K = 128
-constexpr uint32_t OFF_ST_LO = 32768;
+constexpr uint32_t OFF_ST_HI = 0;  // A: S^T [c][i], K-major, 128 rows, K = 128; before the
+constexpr uint32_t OFF_ST_LO = 32768;  // state pass the raw q, k, g tiles of the chunk (row-major)
 constexpr uint32_t OFF_X = 65536;  // 96 KiB reused by the chunk phases:
-//   raw q, k, g tiles (row-major [64][128] bf16)     X+0, X+16K, X+32K
-//   fallback alpha (fp32 [64][128])                  X+48K
+//   fallback alpha (fp32 [64][128]), dot scratch     X+0, X+32K
 //   L hi/lo (A, MN-major, M = 128, K = 128)          X+0,  X+32K
 //   R hi/lo (B, MN-major, N = 64,  K = 128)          X+64K, X+80K
 //   N, T (fp32 [64][68]) and solve temporaries       X+0 .. X+41K
@@ -67,11 +66,11 @@ constexpr uint32_t OFF_MISC = OFF_P_LO + 8192;
 constexpr uint32_t MISC_BYTES = 8192;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 
-constexpr uint32_t X_RAWQ = OFF_X, X_RAWK = OFF_X + 16384, X_RAWG = OFF_X + 32768;
-constexpr uint32_t X_ALPHA = OFF_X + 49152;
+constexpr uint32_t RAW_Q = OFF_ST_HI, RAW_K = OFF_ST_HI + 16384, RAW_G = OFF_ST_HI + 32768;
+constexpr uint32_t X_ALPHA = OFF_X, X_RED = OFF_X + 32768;
 constexpr uint32_t X_L_HI = OFF_X, X_L_LO = OFF_X + 32768, X_R_HI = OFF_X + 65536,
                    X_R_LO = OFF_X + 81920;
-constexpr uint32_t X_N = OFF_X, X_T = OFF_X + 17408, X_Y1 = OFF_X + 34816, X_Y2 = OFF_X + 36992;
+constexpr uint32_t X_N = OFF_X, X_T = OFF_X + 17408, X_Y1 = OFF_X + 34816, X_Y2 = OFF_X + 37376;
 constexpr uint32_t X_KG_HI = OFF_X, X_KG_LO = OFF_X + 16384, X_QG = OFF_X + 32768,
                    X_KT_HI = OFF_X + 49152, X_KT_LO = OFF_X + 65536, X_QG_LO = OFF_X + 81920;
 constexpr uint32_t X_W_HI = OFF_X, X_W_LO = OFF_X + 16384;
@@ -176,55 +175,75 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
     const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.gate_raw);
 
-    for (int j = 0; j < n_chunks && !timed_out; ++j) {
-        const int c0 = t0 + j * kChunk;
-        const int Lc = min(kChunk, t1 - c0);
-        fence_before();
-        __syncthreads();
-        // ---- stage raw q, k, g (row-major) and v (MN-major operand), beta
+    // Raw tiles of chunk jj arrive by cp.async: q, k, g row-major into the
+    // S-operand region (free from MMA 3 of the previous chunk until the state
+    // pass), v as the MN-major MMA operand (free after MMA 2).  Rows past the
+    // sequence are zero-filled.
+    auto prefetch_qkg = [&](int jj) {
+        const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
 #pragma unroll 4
         for (int it = tid; it < 64 * 16; it += kThreads) {
             const int t = it >> 4, ch = it & 15;
-            uint4 xq = make_uint4(0, 0, 0, 0), xk = xq, xg = xq, xv = xq;
-            if (t < Lc) {
-                const size_t e = ((size_t)(c0 + t) * H + h) * kD + ch * 8;
-                xq = __ldg(reinterpret_cast<const uint4*>(gq + e));
-                xk = __ldg(reinterpret_cast<const uint4*>(gk + e));
-                xg = __ldg(reinterpret_cast<const uint4*>(gg + e));
-                xv = __ldg(reinterpret_cast<const uint4*>(gv + e));
-            }
-            st16(sm, X_RAWQ + t * 256 + ch * 16, xq);
-            st16(sm, X_RAWK + t * 256 + ch * 16, xk);
-            st16(sm, X_RAWG + t * 256 + ch * 16, xg);
-            st16(sm, OFF_V + chunk_mn(ch * 8, t, 8192, 1024), xv);
+            const bool ok = t < ln;
+            const size_t e = ok ? ((size_t)(cn + t) * H + h) * kD + ch * 8 : 0;
+            const uint32_t nb = ok ? 16u : 0u;
+            cp_async16(sb + RAW_Q + t * 256 + ch * 16, gq + e, nb);
+            cp_async16(sb + RAW_K + t * 256 + ch * 16, gk + e, nb);
+            cp_async16(sb + RAW_G + t * 256 + ch * 16, gg + e, nb);
         }
-        if (tid < 64)
-            s_beta[tid] = tid < Lc ? beta_act(Act<true>::load1(p.beta_raw, (size_t)(c0 + tid) * H + h), p.flags)
-                                   : 0.f;
+    };
+    auto prefetch_v = [&](int jj) {
+        const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
+#pragma unroll 4
+        for (int it = tid; it < 64 * 16; it += kThreads) {
+            const int t = it >> 4, ch = it & 15;
+            const bool ok = t < ln;
+            const size_t e = ok ? ((size_t)(cn + t) * H + h) * kD + ch * 8 : 0;
+            cp_async16(sb + OFF_V + chunk_mn(ch * 8, t, 8192, 1024), gv + e, ok ? 16u : 0u);
+        }
+    };
+    // raw beta of chunk jj (activated when the chunk starts, so the load is never waited on
+    // early); -inf marks padding rows, whose beta is 0
+    auto load_beta = [&](int jj) {
+        const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
+        return tid < ln ? Act<true>::load1(p.beta_raw, (size_t)(cn + tid) * H + h) : -INFINITY;
+    };
+    float beta_next = 0.f;
+    if (n_chunks > 0) {
+        prefetch_qkg(0);
+        prefetch_v(0);
+        cp_async_commit();
+        if (tid < 64) beta_next = load_beta(0);
+    }
+
+    for (int j = 0; j < n_chunks && !timed_out; ++j) {
+        const int c0 = t0 + j * kChunk;
+        const int Lc = min(kChunk, t1 - c0);
+        const bool more = j + 1 < n_chunks;
+        cp_async_wait_all();
+        if (tid < 64) s_beta[tid] = tid < Lc ? beta_act(beta_next, p.flags) : 0.f;
+        fence_before();
         __syncthreads();
+        fence_after();
+        if (tid < 64 && more) beta_next = load_beta(j + 1);  // lands during this chunk
 
         // ---- channel pass: this thread's channel ci over tokens 32*hf .. 32*hf+31
-        float kv[32], qv[32], al[32], iv[32];
+        float al[32], iv[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = 32 * hf + u;
-            const float x = bf16_at(sm, X_RAWG + t * 256 + ci * 2);
+            const float x = bf16_at(sm, RAW_G + t * 256 + ci * 2);
             if (t < Lc) {
                 if (p.flags & KDA_GATE_LOG) {
-                    al[u] = expf(x);
-                    iv[u] = expf(-x);
+                    al[u] = __expf(x);
+                    iv[u] = __expf(-x);
                 } else {
-                    const float e = expf(x);
-                    iv[u] = 1.f + e;
-                    al[u] = 1.f / iv[u];
+                    iv[u] = 1.f + __expf(x);  // 1/alpha = 1 + e^x
+                    al[u] = __fdividef(1.f, iv[u]);
                 }
-                kv[u] = bf16_at(sm, X_RAWK + t * 256 + ci * 2);
-                qv[u] = bf16_at(sm, X_RAWQ + t * 256 + ci * 2) * p.scale;
             } else {
                 al[u] = 1.f;
                 iv[u] = 1.f;
-                kv[u] = 0.f;
-                qv[u] = 0.f;
             }
         }
         bool bad;
@@ -249,9 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int w = 7; w >= 0; --w) {
                         const int u = g8 * 8 + w;
-                        lk[w] = kv[u] * si;
-                        lq[w] = qv[u] * si;
-                        r[w] = kv[u] * sa;
+                        const float kk = bf16_at(sm, RAW_K + u * 256 + ci * 2);
+                        const float qq = bf16_at(sm, RAW_Q + u * 256 + ci * 2) * p.scale;
+                        lk[w] = kk * si;
+                        lq[w] = qq * si;
+                        r[w] = kk * sa;
                         sa *= al[u];
                         si *= iv[u];
                     }
@@ -276,11 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
                         const int u = g8 * 8 + w;
+                        const float kk = bf16_at(sm, RAW_K + (32 + u) * 256 + ci * 2);
+                        const float qq = bf16_at(sm, RAW_Q + (32 + u) * 256 + ci * 2) * p.scale;
                         fa *= al[u];
                         fi *= iv[u];
-                        lk[w] = kv[u] * fa;
-                        lq[w] = qv[u] * fa;
-                        r[w] = kv[u] * fi;
+                        lk[w] = kk * fa;
+                        lq[w] = qq * fa;
+                        r[w] = kk * fi;
                     }
                     uint4 hi, lo;
                     const int tt = 32 + g8 * 8;
@@ -315,34 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 commit(mbar);
             }
             if (hf == 0) s_gam[ci] = s_tot0[ci] * s_tot1[ci];
-            __syncthreads();
-            // ---- state pass: S_j -> snapshot, bf16 hi/lo operand, decay by e^{G_63}
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int col0 = colhalf * 64 + cc * 32;
-                float v[32];
-                ld32(tl + TM_S + col0, v);
-                for (int m = 0; m < p.M; ++m) {
-                    if (s_trk[m] != j) continue;
-                    float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
-                                  (size_t)row * kD + col0;
-#pragma unroll
-                    for (int q4 = 0; q4 < 32; q4 += 4)
-                        reinterpret_cast<float4*>(snap + q4)[0] =
-                            make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint4 hi, lo;
-                    split8(v + 8 * c8, hi, lo);
-                    st16(sm, OFF_ST_HI + chunk_k(row, col0 + 8 * c8, 128), hi);
-                    st16(sm, OFF_ST_LO + chunk_k(row, col0 + 8 * c8, 128), lo);
-                }
-#pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] *= s_gam[col0 + q];
-                st32(tl + TM_S + col0, v);
-            }
-            wait_st();
             const bool ok1 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
@@ -403,59 +398,64 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int r = 0; r < 16; ++r) Tm[(o + r) * NLD + o + jc] = x[r];
                 }
                 __syncthreads();
-                // level 1: T[a][a-1] = -D_a N[a][a-1] D_{a-1}, a in {1, 3}
-                float* Y1 = reinterpret_cast<float*>(sm + X_Y1);  // [2][16][17]
+                // level 1: T[a][a-1] = -D_a N[a][a-1] D_{a-1}, a in {1, 3}; a thread owns one
+                // row r and 2 adjacent columns of one 16x16 block
+                float* Y1 = reinterpret_cast<float*>(sm + X_Y1);  // [2][16][20]
                 {
-                    const int w = tid >> 7, e = tid & 127, r = e >> 3, cp = e & 7;
+                    const int w = tid >> 7, e = tid & 127, r = e >> 3, c = (e & 7) * 2;
                     const int a = 2 * w + 1, oa = 16 * a, ob = 16 * (a - 1);
+                    float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int c = cp + 8 * h2;
-                        float acc = 0.f;
-#pragma unroll
-                        for (int s = 0; s < 16; ++s)
-                            acc = fmaf(Nm[(oa + r) * NLD + ob + s], Tm[(ob + s) * NLD + ob + c], acc);
-                        Y1[(w * 16 + r) * 17 + c] = acc;
+                    for (int s = 0; s < 16; ++s) {
+                        const float nv = Nm[(oa + r) * NLD + ob + s];
+                        const float2 tv = *reinterpret_cast<const float2*>(&Tm[(ob + s) * NLD + ob + c]);
+                        y0 = fmaf(nv, tv.x, y0);
+                        y1 = fmaf(nv, tv.y, y1);
                     }
+                    *reinterpret_cast<float2*>(&Y1[(w * 16 + r) * 20 + c]) = make_float2(y0, y1);
+                    // T is lower triangular: the blocks above the diagonal pairs are zero
+                    Tm[(16 * (2 * w) + r) * NLD + 16 * (2 * w + 1) + c] = 0.f;
+                    Tm[(16 * (2 * w) + r) * NLD + 16 * (2 * w + 1) + c + 1] = 0.f;
                     __syncthreads();
+                    float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int c = cp + 8 * h2;
-                        float acc = 0.f;
-#pragma unroll
-                        for (int s = 0; s < 16; ++s)
-                            acc = fmaf(Tm[(oa + r) * NLD + oa + s], Y1[(w * 16 + s) * 17 + c], acc);
-                        Tm[(oa + r) * NLD + ob + c] = -acc;
+                    for (int s = 0; s < 16; ++s) {
+                        const float tv = Tm[(oa + r) * NLD + oa + s];
+                        const float2 yv = *reinterpret_cast<const float2*>(&Y1[(w * 16 + s) * 20 + c]);
+                        z0 = fmaf(tv, yv.x, z0);
+                        z1 = fmaf(tv, yv.y, z1);
                     }
+                    *reinterpret_cast<float2*>(&Tm[(oa + r) * NLD + ob + c]) = make_float2(-z0, -z1);
                 }
                 __syncthreads();
-                // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32])
-                float* Y2 = reinterpret_cast<float*>(sm + X_Y2);  // [32][33]
+                // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]);
+                // a thread owns one row r and 4 adjacent columns
+                float* Y2 = reinterpret_cast<float*>(sm + X_Y2);  // [32][36]
                 {
-                    const int r = tid >> 3, cb = tid & 7;
-#pragma unroll
-                    for (int m4 = 0; m4 < 4; ++m4) {
-                        const int c = cb + 8 * m4;
-                        float acc = 0.f;
+                    const int r = tid >> 3, c = (tid & 7) * 4;
+                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-                        for (int u = 0; u < 32; ++u) {
-                            const float tv = (u >= c) ? Tm[u * NLD + c] : 0.f;
-                            acc = fmaf(Nm[(32 + r) * NLD + u], tv, acc);
-                        }
-                        Y2[r * 33 + c] = acc;
+                    for (int u = 0; u < 32; ++u) {
+                        const float nv = Nm[(32 + r) * NLD + u];
+                        const float4 tv = *reinterpret_cast<const float4*>(&Tm[u * NLD + c]);
+                        y.x = fmaf(nv, tv.x, y.x);
+                        y.y = fmaf(nv, tv.y, y.y);
+                        y.z = fmaf(nv, tv.z, y.z);
+                        y.w = fmaf(nv, tv.w, y.w);
                     }
+                    *reinterpret_cast<float4*>(&Y2[r * 36 + c]) = y;
                     __syncthreads();
-#pragma unroll
-                    for (int m4 = 0; m4 < 4; ++m4) {
-                        const int c = cb + 8 * m4;
-                        float acc = 0.f;
+                    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-                        for (int s = 0; s < 32; ++s) {
-                            const float tv = (s <= r) ? Tm[(32 + r) * NLD + 32 + s] : 0.f;
-                            acc = fmaf(tv, Y2[s * 33 + c], acc);
-                        }
-                        Tm[(32 + r) * NLD + c] = -acc;
+                    for (int s = 0; s < 32; ++s) {
+                        const float tv = Tm[(32 + r) * NLD + 32 + s];
+                        const float4 yv = *reinterpret_cast<const float4*>(&Y2[s * 36 + c]);
+                        z.x = fmaf(tv, yv.x, z.x);
+                        z.y = fmaf(tv, yv.y, z.y);
+                        z.z = fmaf(tv, yv.z, z.z);
+                        z.w = fmaf(tv, yv.w, z.w);
                     }
+                    *reinterpret_cast<float4*>(&Tm[(32 + r) * NLD + c]) = make_float4(-z.x, -z.y, -z.z, -z.w);
                 }
                 __syncthreads();
                 // T_b = T Diag(beta) -> bf16 hi/lo operand [t][s] (lower triangle only)
@@ -479,37 +479,44 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             {
                 const float t0f = s_tot0[ci], t1f = s_tot1[ci];
                 float fw = (hf == 0) ? 1.f : t0f;  // e^{G_t}: running product from the chunk start
-                float kg[32], qg[32];
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    fw *= al[u];
-                    kg[u] = kv[u] * fw;
-                    qg[u] = qv[u] * fw;
-                }
-                float bw = (hf == 0) ? t1f : 1.f;  // e^{G_63 - G_t}: product over (t, 63]
-                float kt[32];
-#pragma unroll
-                for (int u = 31; u >= 0; --u) {
-                    kt[u] = kv[u] * bw;
-                    bw *= al[u];
-                }
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
+                    float kg[8], qg[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const int u = 8 * c8 + w, t = 32 * hf + u;
+                        fw *= al[u];
+                        kg[w] = bf16_at(sm, RAW_K + t * 256 + ci * 2) * fw;
+                        qg[w] = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale * fw;
+                    }
                     const int s0 = 32 * hf + 8 * c8;
                     uint4 hi, lo;
-                    split8(kg + 8 * c8, hi, lo);
+                    split8(kg, hi, lo);
                     st16(sm, X_KG_HI + chunk_k(ci, s0, 128), hi);
                     st16(sm, X_KG_LO + chunk_k(ci, s0, 128), lo);
-                    split8(kt + 8 * c8, hi, lo);
-                    st16(sm, X_KT_HI + chunk_k(ci, s0, 128), hi);
-                    st16(sm, X_KT_LO + chunk_k(ci, s0, 128), lo);
                     if constexpr (kBf16Out) {
-                        st16(sm, X_QG + chunk_mn(s0, ci, 1024, 1024), pack8(qg + 8 * c8));
+                        st16(sm, X_QG + chunk_mn(s0, ci, 1024, 1024), pack8(qg));
                     } else {
-                        split8(qg + 8 * c8, hi, lo);
+                        split8(qg, hi, lo);
                         st16(sm, X_QG + chunk_mn(s0, ci, 1024, 1024), hi);
                         st16(sm, X_QG_LO + chunk_mn(s0, ci, 1024, 1024), lo);
                     }
+                }
+                float bw = (hf == 0) ? t1f : 1.f;  // e^{G_63 - G_t}: product over (t, 63]
+#pragma unroll
+                for (int c8 = 3; c8 >= 0; --c8) {
+                    float kt[8];
+#pragma unroll
+                    for (int w = 7; w >= 0; --w) {
+                        const int u = 8 * c8 + w, t = 32 * hf + u;
+                        kt[w] = bf16_at(sm, RAW_K + t * 256 + ci * 2) * bw;
+                        bw *= al[u];
+                    }
+                    const int s0 = 32 * hf + 8 * c8;
+                    uint4 hi, lo;
+                    split8(kt, hi, lo);
+                    st16(sm, X_KT_HI + chunk_k(ci, s0, 128), hi);
+                    st16(sm, X_KT_LO + chunk_k(ci, s0, 128), lo);
                 }
             }
             fence_async_smem();
@@ -538,12 +545,44 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 }
                 commit(mbar);
             }
+            // ---- state pass (overlaps MMA 2): S_j -> snapshot, bf16 hi/lo operand (over the raw
+            //      tiles, all read by now), decay by e^{G_63}
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int col0 = colhalf * 64 + cc * 32;
+                float v[32];
+                ld32(tl + TM_S + col0, v);
+                for (int m = 0; m < p.M; ++m) {
+                    if (s_trk[m] != j) continue;
+                    float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
+                                  (size_t)row * kD + col0;
+#pragma unroll
+                    for (int q4 = 0; q4 < 32; q4 += 4)
+                        reinterpret_cast<float4*>(snap + q4)[0] =
+                            make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint4 hi, lo;
+                    split8(v + 8 * c8, hi, lo);
+                    st16(sm, OFF_ST_HI + chunk_k(row, col0 + 8 * c8, 128), hi);
+                    st16(sm, OFF_ST_LO + chunk_k(row, col0 + 8 * c8, 128), lo);
+                }
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] *= s_gam[col0 + q];
+                st32(tl + TM_S + col0, v);
+            }
+            wait_st();
             const bool ok2 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
             if (__syncthreads_or(!ok2)) {
                 timed_out = true;
                 break;
+            }
+            if (more) {
+                prefetch_v(j + 1);  // V is free once MMA 2 has completed
+                cp_async_commit();
             }
             // ---- W^T (lanes i, columns t) -> W operand (B, MN-major [i][t]) hi/lo
             {
@@ -592,6 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             if (__syncthreads_or(!ok3)) {
                 timed_out = true;
                 break;
+            }
+            if (more) {
+                prefetch_qkg(j + 1);  // the S operand region is free once MMA 3 has completed
+                cp_async_commit();
             }
             // ---- U^T (lanes c, columns s) -> UT operand (A, K-major [c][s]) hi/lo
             {
@@ -643,10 +686,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             {
                 float v[32];
                 ld32(tl + TM_OT + colhalf * 32, v);
+                if constexpr (kBf16Out) {
+                    // through shared memory (the T_b region, free now) for 16-byte row stores
+                    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TB_HI);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int t = colhalf * 32 + q;
-                    if (t < Lc) store1<kBf16Out>(p.out, ((size_t)(c0 + t) * H + h) * kD + row, v[q]);
+                    for (int q = 0; q < 32; ++q)
+                        ob[(colhalf * 32 + q) * kD + row] = __float2bfloat16_rn(v[q]);
+                    __syncthreads();
+#pragma unroll
+                    for (int it = tid; it < 64 * 16; it += kThreads) {
+                        const int t = it >> 4, ch = it & 15;
+                        if (t < Lc)
+                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                      ((size_t)(c0 + t) * H + h) * kD + ch * 8) =
+                                *reinterpret_cast<const uint4*>(sm + OFF_TB_HI + t * 256 + ch * 16);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int t = colhalf * 32 + q;
+                        if (t < Lc) store1<false>(p.out, ((size_t)(c0 + t) * H + h) * kD + row, v[q]);
+                    }
                 }
             }
         } else {
@@ -657,53 +717,74 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             fence_before();
             __syncthreads();
             fence_after();
-            if (warp < 4) {
+            {
+                // thread (row c, column half) keeps 64 state columns in registers; the two
+                // half-row dot products meet in shared memory
+                float* red = reinterpret_cast<float*>(sm + X_RED);  // [2 dots][2 halves][128]
                 const int c = row;
-                float s[kD];
+                float sv[64];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     float v[32];
-                    ld32(tl + TM_S + cc * 32, v);
+                    ld32(tl + TM_S + colhalf * 64 + cc * 32, v);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) s[cc * 32 + q] = v[q];
+                    for (int q = 0; q < 32; ++q) sv[cc * 32 + q] = v[q];
                 }
                 for (int m = 0; m < p.M; ++m) {
                     if (s_trk[m] != j) continue;
                     float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
-                                  (size_t)c * kD;
+                                  (size_t)c * kD + colhalf * 64;
 #pragma unroll
-                    for (int q4 = 0; q4 < kD; q4 += 4)
+                    for (int q4 = 0; q4 < 64; q4 += 4)
                         reinterpret_cast<float4*>(snap + q4)[0] =
-                            make_float4(s[q4], s[q4 + 1], s[q4 + 2], s[q4 + 3]);
+                            make_float4(sv[q4], sv[q4 + 1], sv[q4 + 2], sv[q4 + 3]);
                 }
                 for (int t = 0; t < Lc; ++t) {
-                    const float vt = bf16_at(sm, OFF_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
                     float d1 = 0.f;
 #pragma unroll
-                    for (int i = 0; i < kD; ++i) {
-                        s[i] *= alpha[t * kD + i];
-                        d1 = fmaf(s[i], bf16_at(sm, X_RAWK + t * 256 + i * 2), d1);
+                    for (int q = 0; q < 64; ++q) {
+                        const int i = colhalf * 64 + q;
+                        sv[q] *= alpha[t * kD + i];
+                        d1 = fmaf(sv[q], bf16_at(sm, RAW_K + t * 256 + i * 2), d1);
                     }
+                    red[colhalf * 128 + c] = d1;
+                    __syncthreads();
+                    d1 = red[c] + red[128 + c];
+                    const float vt = bf16_at(sm, OFF_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
                     const float uu = s_beta[t] * (vt - d1);
                     float o = 0.f;
 #pragma unroll
-                    for (int i = 0; i < kD; ++i) {
-                        s[i] = fmaf(uu, bf16_at(sm, X_RAWK + t * 256 + i * 2), s[i]);
-                        o = fmaf(s[i], bf16_at(sm, X_RAWQ + t * 256 + i * 2) * p.scale, o);
+                    for (int q = 0; q < 64; ++q) {
+                        const int i = colhalf * 64 + q;
+                        sv[q] = fmaf(uu, bf16_at(sm, RAW_K + t * 256 + i * 2), sv[q]);
+                        o = fmaf(sv[q], bf16_at(sm, RAW_Q + t * 256 + i * 2) * p.scale, o);
                     }
-                    store1<kBf16Out>(p.out, ((size_t)(c0 + t) * H + h) * kD + c, o);
+                    red[256 + colhalf * 128 + c] = o;
+                    __syncthreads();
+                    if (colhalf == 0)
+                        store1<kBf16Out>(p.out, ((size_t)(c0 + t) * H + h) * kD + c,
+                                         red[256 + c] + red[384 + c]);
                 }
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     float v[32];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = s[cc * 32 + q];
-                    st32(tl + TM_S + cc * 32, v);
+                    for (int q = 0; q < 32; ++q) v[q] = sv[cc * 32 + q];
+                    st32(tl + TM_S + colhalf * 64 + cc * 32, v);
                 }
                 wait_st();
             }
+            fence_before();
+            __syncthreads();
+            fence_after();
+            if (more) {
+                prefetch_qkg(j + 1);
+                prefetch_v(j + 1);
+                cp_async_commit();
+            }
         }
     }
+    cp_async_wait_all();
 
     fence_before();
     __syncthreads();

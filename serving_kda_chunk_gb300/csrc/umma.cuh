@@ -142,28 +142,38 @@ __device__ __forceinline__ void split(float x, __nv_bfloat16& hi, __nv_bfloat16&
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// Two fp32 values -> packed bf16x2 hi and lo (element a in the low half).
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Pack 8 fp32 values as bf16 hi and lo 16-byte chunks.
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        split(x[2 * j], h0, l0);
-        split(x[2 * j + 1], h1, l1);
-        h[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        l[j] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
+    split2(x[4], x[5], hi.z, lo.z);
+    split2(x[6], x[7], hi.w, lo.w);
 }
 __device__ __forceinline__ uint4 pack8(const float* x) {
-    uint32_t h[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        h[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[2 * j])) |
-               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[2 * j + 1])) << 16);
-    return make_uint4(h[0], h[1], h[2], h[3]);
+    return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
 }
+
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 }  // namespace umma
 }  // namespace kda
