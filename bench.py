@@ -66,6 +66,13 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
     return byts, flops
 
 
+# DRAM traffic of the chunked prefill kernel measured with ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum = 277.5 MB + 59.2 MB) on the `--profile prefill` case
+# (8 x 2048 tokens, 16 heads); traffic grows with the token-heads processed, so a
+# launch is charged this much per token-head.  Re-measure when the kernel changes.
+PREFILL_TRAFFIC_PER_TOKEN_HEAD = (277.5e6 + 59.2e6) / (8 * 2048 * 16)
+
+
 def decode_work(R, H):
     return R * H * (2 * STATE_BYTES + 4 * D * 2 + 2 + D * 2)
 
@@ -448,6 +455,48 @@ def main_reference(args, rank, world):
     return 0
 
 
+def run_profile_case(name, reps):
+    """One entry point on its workload, for an ncu capture (`--profile NAME`).
+
+    prefill runs a reduced batch (8 sequences x 2048 tokens, H=16: 168 MB of
+    activations, above L2) so that a full-set capture ends quickly; the other
+    entry points run their serving workloads."""
+    import torch
+
+    import serving_kda_chunk_gb300 as kda
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if name == "prefill":
+        c = W.prefill_case(11, [2048] * 8, 16, pool_slots=8)
+        t = {n: to_dev(c[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+        pool = torch.from_numpy(c["pool"]).to(dev)
+        sl, tr, cu = i32(c["init_slot"], dev), i32(c["track"], dev), i32(c["cu_seqlens"], dev)
+        snap = torch.empty(8, 1, 16, D, D, device=dev)
+        out = torch.empty(c["T"], 16, D, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(64, dtype=torch.uint8, device=dev)
+
+        def fn():
+            kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
+                                  state_pool=pool, init_slot=sl, final_slot=sl,
+                                  track_chunk_idx=tr, track_state=snap, workspace=ws)
+    else:
+        step = Step(dev)
+        fn = dict((n, f) for n, f, _ in step.calls())[name]
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    print(json.dumps({"profile": name, "us_per_call": times}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -455,7 +504,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode", "verify", "commit", "slot_copy"],
+                    help="run one entry point a few times (for an ncu capture) and exit")
     args = ap.parse_args()
+    if args.profile:
+        return run_profile_case(args.profile, max(args.steps, 1))
     rank, world, local = dist_setup()
     if args.impl == "reference":
         rc = main_reference(args, rank, world)
@@ -516,7 +569,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; bf16 inputs, fp32 state)", "config": config_block(),
         "roofline": {"bound": "hbm", "kernel": "kda_chunk_prefill", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": PREFILL_TRAFFIC_PER_TOKEN_HEAD * toks * 32,
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
