@@ -10,11 +10,12 @@
 //     c_t = sum_{t<s<=a} g_s  (c_0 = sum_{s<=a} g_s),
 // so every state element is one fused sum of a+1 terms.
 //
-// One CTA per (request, head).  Threads first walk the records backwards per
-// key channel to form F_t = exp(c_t) k_t and the total decay exp(c_0) in
-// shared memory, then each warp streams 16 rows of S^T: 64 KiB read from the
-// checkpoint and 64 KiB written to the destination slot (in place allowed:
-// each element is read and written by the same thread).
+// Four CTAs per (request, head), each owning 32 rows of S^T, so that more
+// independent load chains are resident per SM.  Threads first walk the records
+// backwards per key channel to form F_t = exp(c_t) k_t and the total decay
+// exp(c_0) in shared memory, then each warp streams 8 rows of S^T: 16 KiB per
+// CTA read from the checkpoint and written to the destination slot (in place
+// allowed: each element is read and written by the same thread).
 #include "kda_common.cuh"
 #include "kda_host.h"
 
@@ -23,8 +24,12 @@ namespace {
 
 constexpr int kMaxCommitK = 32;  // keeps the record staging under 48 KiB of shared memory
 
+constexpr int kCommitThreads = 128;  // 4 warps x 8 rows: a quarter of a state per CTA
+constexpr int kRowsPerWarp = 8;
+constexpr int kCtasPerUnit = kD / (4 * kRowsPerWarp);
+
 template <bool kBf16Rec>
-__global__ void __launch_bounds__(256) commit_kernel(
+__global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     float* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
     const int32_t* __restrict__ dst, const int32_t* __restrict__ acc,
     const int32_t* __restrict__ q_len, int32_t K, int32_t H, uint32_t flags,
@@ -35,17 +40,18 @@ __global__ void __launch_bounds__(256) commit_kernel(
     float* F = sm;                  // [a][128]
     float* U = sm + K * kD;         // [a][128]
     float* D = sm + 2 * K * kD;     // [128]
-    const int unit = blockIdx.x;
+    const int unit = blockIdx.x / kCtasPerUnit;  // (request, head); the rest picks the row block
+    const int part = blockIdx.x - unit * kCtasPerUnit;
     const int r = unit / H, h = unit - r * H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = warp * 16;
+    const int row0 = part * (4 * kRowsPerWarp) + warp * kRowsPerWarp;
     const int src = ckpt[r];
     const int d = dst ? dst[r] : src;
     const int ql = q_len ? q_len[r] : K;
     const int a = acc[r];
     const bool slot_ok = src >= 0 && src < P && d >= 0 && d < P;
     const bool ok = slot_ok && ql >= 0 && ql <= K && a >= 0 && a <= ql;
-    if (h == 0 && threadIdx.x == 0) {
+    if (h == 0 && part == 0 && threadIdx.x == 0) {
         if (plan_out) {
             plan_out[3 * r + 0] = ok ? a : -1;
             plan_out[3 * r + 1] = src;
@@ -59,19 +65,19 @@ __global__ void __launch_bounds__(256) commit_kernel(
     if (a == 0) {
         if (d == src) return;
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kRowsPerWarp; ++i) {
             const float4 x = __ldcs(reinterpret_cast<const float4*>(S0 + (size_t)(row0 + i) * kD) + lane);
             __stcs(reinterpret_cast<float4*>(SD + (size_t)(row0 + i) * kD) + lane, x);
         }
         return;
     }
     // issue the checkpoint loads early; they do not depend on the factors
-    float4 s[16];
+    float4 s[kRowsPerWarp];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kRowsPerWarp; ++i)
         s[i] = __ldcs(reinterpret_cast<const float4*>(S0 + (size_t)(row0 + i) * kD) + lane);
     const size_t rec0 = ((size_t)r * H + h) * K;
-    if (threadIdx.x < kD) {
+    {
         const int c = threadIdx.x;
         float suffix = 0.f;  // c_t, accumulated from t = a down to 1
         for (int t = a - 1; t >= 0; --t) {
@@ -82,16 +88,21 @@ __global__ void __launch_bounds__(256) commit_kernel(
         }
         D[c] = expf(suffix);
     }
-    for (int i = threadIdx.x; i < a * kD; i += blockDim.x) U[i] = rec_u[rec0 * kD + i];
+    // this CTA's 64 rows of u_t for every recorded step
+    for (int i = threadIdx.x; i < a * 4 * kRowsPerWarp; i += blockDim.x) {
+        const int t = i / (4 * kRowsPerWarp);
+        const int cc = part * (4 * kRowsPerWarp) + (i - t * 4 * kRowsPerWarp);
+        U[t * kD + cc] = rec_u[(rec0 + t) * kD + cc];
+    }
     __syncthreads();
     const float4 dec = *reinterpret_cast<const float4*>(&D[4 * lane]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = f4_mul(s[i], dec);
+    for (int i = 0; i < kRowsPerWarp; ++i) s[i] = f4_mul(s[i], dec);
     for (int t = 0; t < a; ++t) {
         const float4 f = *reinterpret_cast<const float4*>(&F[t * kD + 4 * lane]);
-        float urow[16];
+        float urow[kRowsPerWarp];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kRowsPerWarp / 4; ++j) {
             const float4 x = *reinterpret_cast<const float4*>(&U[t * kD + row0 + 4 * j]);
             urow[4 * j] = x.x;
             urow[4 * j + 1] = x.y;
@@ -99,10 +110,10 @@ __global__ void __launch_bounds__(256) commit_kernel(
             urow[4 * j + 3] = x.w;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = f4_fma(urow[i], f, s[i]);
+        for (int i = 0; i < kRowsPerWarp; ++i) s[i] = f4_fma(urow[i], f, s[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kRowsPerWarp; ++i)
         __stcs(reinterpret_cast<float4*>(SD + (size_t)(row0 + i) * kD) + lane, s[i]);
 }
 
@@ -122,17 +133,17 @@ extern "C" kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_
     KDA_REQUIRE(dtype_ok(rec_dtype), KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(K <= kMaxCommitK, KDA_ERR_UNSUPPORTED);
     if (R == 0) return KDA_OK;
-    KDA_REQUIRE((int64_t)R * H < (1ll << 31), KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE((int64_t)R * H < (1ll << 30), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {state_pool, ckpt_slot, num_accepted, rec_u, rec_kg};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
     cudaStream_t s = as_stream(stream);
     const size_t smem = (size_t)(2 * K + 1) * kD * sizeof(float);
     if (rec_dtype == KDA_BF16)
-        commit_kernel<true><<<(unsigned)(R * H), 256, smem, s>>>(
+        commit_kernel<true><<<(unsigned)(kCtasPerUnit * R * H), kCommitThreads, smem, s>>>(
             state_pool, P, ckpt_slot, dst_slot, num_accepted, q_len, K, H, flags, rec_u, rec_kg,
             plan_out, dev_status);
     else
-        commit_kernel<false><<<(unsigned)(R * H), 256, smem, s>>>(
+        commit_kernel<false><<<(unsigned)(kCtasPerUnit * R * H), kCommitThreads, smem, s>>>(
             state_pool, P, ckpt_slot, dst_slot, num_accepted, q_len, K, H, flags, rec_u, rec_kg,
             plan_out, dev_status);
     return launch_status();

@@ -4,11 +4,11 @@
 // "State semantics" page, section 4: decode applies the gate activation inside
 // the kernel and updates the per-head state in place.
 //
-// One CTA per (request, head); 8 warps each own 16 rows of S^T (a row = one
-// value channel, 128 contiguous key channels), a lane owns 4 key channels.
-// The whole 64 KiB state is loaded with 16-byte loads before any arithmetic
-// (16 loads in flight per lane), the row dot products are warp reductions,
-// and the updated rows are written back in place.  The kernel is bound by HBM
+// Four CTAs per (request, head); their 4 warps each own 8 rows of S^T (a row =
+// one value channel, 128 contiguous key channels), a lane owns 4 key channels.
+// A CTA's 16 KiB of state is loaded with 16-byte loads before any arithmetic,
+// the row dot products are warp reductions, and the updated rows are written
+// back in place; small CTAs keep many independent load chains resident.  The kernel is bound by HBM
 // traffic: 2 x 64 KiB of state per (request, head).
 #include "kda_common.cuh"
 #include "kda_host.h"
@@ -16,28 +16,35 @@
 namespace kda {
 namespace {
 
+constexpr int kDecThreads = 128;                   // 4 warps
+constexpr int kDecRows = 8;                        // state rows per warp
+constexpr int kDecCtas = kD / (4 * kDecRows);      // CTAs per (request, head)
+
 template <bool kBf16In, bool kBf16Out>
-__global__ void __launch_bounds__(256) decode_kernel(
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(
     const void* __restrict__ q, const void* __restrict__ k, const void* __restrict__ v,
     const void* __restrict__ beta_raw, const void* __restrict__ gate_raw, int32_t H, float scale,
     uint32_t flags, float* __restrict__ pool, int64_t P, const int32_t* __restrict__ slots,
     void* __restrict__ out, int32_t* __restrict__ dev_status) {
     using A = Act<kBf16In>;
-    const int unit = blockIdx.x;
+    const int unit = blockIdx.x / kDecCtas;
+    const int part = blockIdx.x - unit * kDecCtas;
     const int r = unit / H, h = unit - r * H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = warp * 16;
+    const int row0 = part * (4 * kDecRows) + warp * kDecRows;
     const size_t th = (size_t)r * H + h;
     const int slot = slots[r];
     if (slot < 0 || slot >= P) {
-        if (slot >= P && threadIdx.x == 0) report(dev_status, KDA_DEV_BAD_SLOT);
-        if (warp == 0) store4<kBf16Out>(out, th * kD + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
+        if (slot >= P && threadIdx.x == 0 && part == 0) report(dev_status, KDA_DEV_BAD_SLOT);
+        if (threadIdx.x < 4 * kDecRows / 4)
+            store4<kBf16Out>(out, th * kD + part * 4 * kDecRows + 4 * threadIdx.x,
+                             make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
     float* S = pool + ((size_t)slot * H + h) * (kD * kD);
-    float4 s[16];
+    float4 s[kDecRows];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kDecRows; ++i)
         s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(row0 + i) * kD) + lane);
 
     StepIn in;
@@ -49,26 +56,26 @@ __global__ void __launch_bounds__(256) decode_kernel(
     in.q = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);
     in.kq = warp_sum(f4_dot(in.k, in.q));
     in.beta = beta_act(A::load1(beta_raw, th), flags);
-    float vrow[16];
+    float vrow[kDecRows];
     {
-        const float vm = lane < 16 ? A::load1(v, th * kD + row0 + lane) : 0.f;
+        const float vm = lane < kDecRows ? A::load1(v, th * kD + row0 + lane) : 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) vrow[i] = __shfl_sync(0xffffffffu, vm, i);
+        for (int i = 0; i < kDecRows; ++i) vrow[i] = __shfl_sync(0xffffffffu, vm, i);
     }
     float u_m = 0.f, o_m = 0.f;
-    step_rows16(s, in, vrow, u_m, o_m, lane);
+    step_rows<kDecRows>(s, in, vrow, u_m, o_m, lane);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kDecRows; ++i)
         __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + i) * kD) + lane, s[i]);
-    if (lane < 16) store1<kBf16Out>(out, th * kD + row0 + lane, o_m);
+    if (lane < kDecRows) store1<kBf16Out>(out, th * kD + row0 + lane, o_m);
 }
 
 template <bool I, bool O>
 void launch(const void* q, const void* k, const void* v, const void* b, const void* g, int32_t R,
             int32_t H, float scale, uint32_t flags, float* pool, int64_t P, const int32_t* slot,
             void* out, int32_t* st, cudaStream_t s) {
-    decode_kernel<I, O><<<(unsigned)(R * H), 256, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P,
-                                                          slot, out, st);
+    decode_kernel<I, O><<<(unsigned)(kDecCtas * R * H), kDecThreads, 0, s>>>(
+        q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
 }
 
 }  // namespace
@@ -87,7 +94,7 @@ extern "C" kda_status kda_recurrent_decode(const void* q, const void* k, const v
     KDA_REQUIRE(dk == kD && dv == kD, KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(dtype_ok(in_dtype) && dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED);
     if (R == 0) return KDA_OK;
-    KDA_REQUIRE((int64_t)R * H < (1ll << 31), KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE((int64_t)R * H * kDecCtas < (1ll << 31), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {q, k, v, beta_raw, gate_raw, state_pool, slot, out};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
     cudaStream_t s = as_stream(stream);

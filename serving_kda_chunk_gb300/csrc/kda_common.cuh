@@ -151,10 +151,11 @@ struct StepIn {
     float beta;
 };
 
-__device__ __forceinline__ void step_rows16(float4 (&s)[16], const StepIn& in, const float (&vrow)[16],
-                                            float& u_mine, float& o_mine, int lane) {
+template <int RW>
+__device__ __forceinline__ void step_rows(float4 (&s)[RW], const StepIn& in, const float (&vrow)[RW],
+                                          float& u_mine, float& o_mine, int lane) {
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
+    for (int r = 0; r < RW; ++r) {
         float4 x = f4_mul(s[r], in.a);
         float d1 = f4_dot(x, in.k);
         float d2 = f4_dot(x, in.q);
@@ -230,7 +231,7 @@ __device__ __forceinline__ void step_from_tile(float4 (&s)[16], const TokenTile<
         vrow[4 * i + 2] = x.z;
         vrow[4 * i + 3] = x.w;
     }
-    step_rows16(s, in, vrow, u_m, o_m, lane);
+    step_rows<16>(s, in, vrow, u_m, o_m, lane);
 }
 
 }  // namespace kda
