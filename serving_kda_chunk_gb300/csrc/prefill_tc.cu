@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     float* s_tot0 = s_gam + 128;                              // 128
     float* s_tot1 = s_tot0 + 128;                             // 128
     int* s_trk = reinterpret_cast<int*>(s_tot1 + 128);        // kTrackTc
-    uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_trk + kTrackTc);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 1);
+    uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_trk + kTrackTc);  // [0]: MMA batches, [1]: state update
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;   // TMEM lane quarter this warp may access
@@ -138,14 +138,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 
     // ---- TMEM and the MMA completion barrier
     if (warp == 0) tmem_alloc(smem_u32(s_tmem), TM_COLS);
-    if (tid == 0) mbar_init(smem_u32(s_mbar), 1);
+    if (tid == 0) {
+        mbar_init(smem_u32(s_mbar), 1);
+        mbar_init(smem_u32(s_mbar + 1), 1);
+    }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lanes
-    const uint32_t mbar = smem_u32(s_mbar);
-    uint32_t phase = 0;
+    const uint32_t mbar = smem_u32(s_mbar);      // MMA batches whose results threads read
+    const uint32_t mbar_s = smem_u32(s_mbar + 1);  // the state update, waited one chunk later
+    uint32_t phase = 0, phase_s = 0;
+    bool pending_s = false;
 
     // ---- initial state into TMEM (row c = S^T row, this thread's 64 columns)
     {
@@ -221,9 +226,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         const int Lc = min(kChunk, t1 - c0);
         const bool more = j + 1 < n_chunks;
         cp_async_wait_all();
+        if (pending_s) {  // the previous state update still reads UT / KT and writes S
+            const bool ok = mbar_wait(mbar_s, phase_s, kWaitLimit);
+            phase_s ^= 1;
+            pending_s = false;
+            if (!ok) timed_out = true;
+        }
         if (tid < 64) s_beta[tid] = tid < Lc ? beta_act(beta_next, p.flags) : 0.f;
         fence_before();
-        __syncthreads();
+        if (__syncthreads_or(timed_out)) {
+            timed_out = true;
+            break;
+        }
         fence_after();
         if (tid < 64 && more) beta_next = load_beta(j + 1);  // lands during this chunk
 
@@ -535,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int s = 0; s < 4; ++s)
                         mma(tmem + TM_WT, desc_k(a, 128, s), desc_k(b, 64, s), idk, (pass | s) != 0);
                 }
+                commit(mbar);  // W^T only: U~^T (below) keeps running while W is extracted
 #pragma unroll
                 for (int pass = 0; pass < 2; ++pass) {
                     const uint32_t b = sb + (pass == 1 ? OFF_TB_LO : OFF_TB_HI);
@@ -543,7 +558,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                         mma(tmem + TM_UT, desc_mn(sb + OFF_V, 8192, 1024, s), desc_k(b, 64, s), idv,
                             (pass | s) != 0);
                 }
-                commit(mbar);
             }
             // ---- state pass (overlaps MMA 2): S_j -> snapshot, bf16 hi/lo operand (over the raw
             //      tiles, all read by now), decay by e^{G_63}
@@ -580,10 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 timed_out = true;
                 break;
             }
-            if (more) {
-                prefetch_v(j + 1);  // V is free once MMA 2 has completed
-                cp_async_commit();
-            }
             // ---- W^T (lanes i, columns t) -> W operand (B, MN-major [i][t]) hi/lo
             {
                 float v[32];
@@ -601,18 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             fence_before();
             __syncthreads();
             fence_after();
-            // ---- MMA 3: U^T = U~^T - S^T W^T ; O^T = S^T QG^T
+            // ---- MMA 3: O^T = S^T QG^T ; U^T = U~^T - S^T W^T (O first: one commit then frees the
+            //      S operand, the V tile and the W / QG tiles)
             if (tid == 0) {
                 const uint32_t idu = idesc_bf16(128, 64, false, true, true);
                 const uint32_t ido = idesc_bf16(128, 64, false, true, false);
-#pragma unroll
-                for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = sb + (pass == 2 ? OFF_ST_LO : OFF_ST_HI);
-                    const uint32_t b = sb + (pass == 1 ? X_W_LO : X_W_HI);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma(tmem + TM_UT, desc_k(a, 128, s), desc_mn(b, 1024, 1024, s), idu, 1u);
-                }
                 // bf16 outputs: S_hi QG_hi; fp32 outputs: + S_lo QG_hi + S_hi QG_lo
 #pragma unroll
                 for (int pass = 0; pass < (kBf16Out ? 1 : 3); ++pass) {
@@ -622,6 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int s = 0; s < 8; ++s)
                         mma(tmem + TM_OT, desc_k(a, 128, s), desc_mn(b, 1024, 1024, s), ido,
                             (pass | s) != 0);
+                }
+#pragma unroll
+                for (int pass = 0; pass < 3; ++pass) {
+                    const uint32_t a = sb + (pass == 2 ? OFF_ST_LO : OFF_ST_HI);
+                    const uint32_t b = sb + (pass == 1 ? X_W_LO : X_W_HI);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma(tmem + TM_UT, desc_k(a, 128, s), desc_mn(b, 1024, 1024, s), idu, 1u);
                 }
                 commit(mbar);
             }
@@ -633,7 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 break;
             }
             if (more) {
-                prefetch_qkg(j + 1);  // the S operand region is free once MMA 3 has completed
+                // every reader of the S operand region and of the V tile has completed
+                prefetch_qkg(j + 1);
+                prefetch_v(j + 1);
                 cp_async_commit();
             }
             // ---- U^T (lanes c, columns s) -> UT operand (A, K-major [c][s]) hi/lo
@@ -665,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int s = 0; s < 4; ++s)
                         mma(tmem + TM_OT, desc_k(a, 128, s), desc_k(b, 64, s), ido, 1u);
                 }
+                commit(mbar);  // the outputs; the state update below finishes in the background
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
                     const uint32_t a = sb + (pass == 2 ? X_UT_LO : X_UT_HI);
@@ -673,8 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int s = 0; s < 4; ++s)
                         mma(tmem + TM_S, desc_k(a, 128, s), desc_k(b, 128, s), ids, 1u);
                 }
-                commit(mbar);
+                commit(mbar_s);
             }
+            pending_s = true;
             const bool ok4 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
@@ -786,13 +801,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     }
     cp_async_wait_all();
 
+    if (pending_s && !timed_out) {
+        if (!mbar_wait(mbar_s, phase_s, kWaitLimit)) timed_out = true;
+        pending_s = false;
+    }
     fence_before();
-    __syncthreads();
+    timed_out = __syncthreads_or(timed_out);
     fence_after();
     if (timed_out) {
         if (tid == 0) report(p.dev_status, KDA_DEV_TIMEOUT);
         // give in-flight MMAs a bounded chance to drain before TMEM is released
         mbar_wait(mbar, phase, kWaitLimit);
+        if (pending_s) mbar_wait(mbar_s, phase_s, kWaitLimit);
     } else if (fin >= 0) {
         float* SD = p.pool + ((size_t)fin * H + h) * (kD * kD);
 #pragma unroll
