@@ -29,6 +29,12 @@
 // chunk's cumulative decay leaves the range those factors can carry (a factor
 // above 2^64), that chunk is evaluated token by token on CUDA cores instead.
 //
+// Work split: 512 threads.  TMEM passes: warp w reads lanes 32*(w%4)..+31 and
+// the column quarter w/4 of a tile.  Channel passes (gates, decayed operands):
+// thread (key channel tid%128, token quarter tid/128), 16 tokens each; the
+// running decay products start from the other quarters' totals, exchanged
+// through shared memory.
+//
 // The snapshot of chunk j (the state after j*64 tokens of the sequence, SGLang
 // PR 34820 page, the fp32 track-state snapshot) is written from the fp32 TMEM
 // accumulator when chunk j starts.
@@ -42,21 +48,19 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: four per TMEM lane quarter
 constexpr int kTrackTc = 512;  // snapshot requests per sequence handled by this kernel
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_ST_HI = 0;  // A: S^T [c][i], K-major, 128 rows, K = 128; before the
-constexpr uint32_t OFF_ST_LO = 32768;  // state pass the raw q, k, g tiles of the chunk (row-major)
-constexpr uint32_t OFF_X = 65536;  // 96 KiB reused by the chunk phases:
+constexpr uint32_t OFF_RAW = 0;      // raw q, k, g tiles of the chunk, row-major bf16 [t][128]
+constexpr uint32_t OFF_X = 49152;    // 96 KiB reused by the chunk phases:
 //   fallback alpha (fp32 [64][128]), dot scratch     X+0, X+32K
 //   L hi/lo (A, MN-major, M = 128, K = 128)          X+0,  X+32K
 //   R hi/lo (B, MN-major, N = 64,  K = 128)          X+64K, X+80K
-//   N, T (fp32 [64][68]) and solve temporaries       X+0 .. X+41K
-//   KG hi/lo (A, K-major [i][s]), QG (B, MN-major),
-//   KT hi/lo (B, K-major [i][s]), QG lo              X+0, X+16K, X+32K, X+48K, X+64K, X+80K
-//   W hi/lo (B, MN-major [i][t])                     X+0, X+16K
-//   UT hi/lo (A, K-major [c][s])                     X+0, X+16K
+//   N^T, T (fp32 [64][68]) and solve temporaries     X+0 .. X+41K
+//   QG (B, MN-major), KT hi/lo (B, K-major [i][s]),
+//   QG lo (fp32 outputs)                             X+32K, X+48K, X+64K, X+80K
+//   -W hi/lo (B, MN-major [i][t])                    X+0, X+16K
 constexpr uint32_t OFF_V = OFF_X + 98304;        // A: V, MN-major (c atoms 8 KiB apart, s groups 1 KiB)
 constexpr uint32_t OFF_TB_HI = OFF_V + 16384;    // B: T_b [t][s], K-major, 64 rows
 constexpr uint32_t OFF_TB_LO = OFF_TB_HI + 8192;
@@ -66,19 +70,22 @@ constexpr uint32_t OFF_MISC = OFF_P_LO + 8192;
 constexpr uint32_t MISC_BYTES = 8192;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 
-constexpr uint32_t RAW_Q = OFF_ST_HI, RAW_K = OFF_ST_HI + 16384, RAW_G = OFF_ST_HI + 32768;
+constexpr uint32_t RAW_Q = OFF_RAW, RAW_K = OFF_RAW + 16384, RAW_G = OFF_RAW + 32768;
 constexpr uint32_t X_ALPHA = OFF_X, X_RED = OFF_X + 32768;
 constexpr uint32_t X_L_HI = OFF_X, X_L_LO = OFF_X + 32768, X_R_HI = OFF_X + 65536,
                    X_R_LO = OFF_X + 81920;
 constexpr uint32_t X_N = OFF_X, X_T = OFF_X + 17408, X_Y1 = OFF_X + 34816, X_Y2 = OFF_X + 37376;
-constexpr uint32_t X_KG_HI = OFF_X, X_KG_LO = OFF_X + 16384, X_QG = OFF_X + 32768,
-                   X_KT_HI = OFF_X + 49152, X_KT_LO = OFF_X + 65536, X_QG_LO = OFF_X + 81920;
+constexpr uint32_t X_QG = OFF_X + 32768, X_KT_HI = OFF_X + 49152, X_KT_LO = OFF_X + 65536,
+                   X_QG_LO = OFF_X + 81920;
 constexpr uint32_t X_W_HI = OFF_X, X_W_LO = OFF_X + 16384;
-constexpr uint32_t X_UT_HI = OFF_X, X_UT_LO = OFF_X + 16384;
 constexpr int NLD = 68;  // fp32 row stride of the N / T matrices
 
-// TMEM columns
+// TMEM columns: fp32 accumulators, and bf16 hi/lo A operands (two per column) whose rows are
+// the TMEM lanes.  KG reuses the [A; P] columns once they are read, U^T those of W^T.
 constexpr uint32_t TM_S = 0, TM_AP = 128, TM_WT = 192, TM_UT = 256, TM_OT = 320;
+constexpr uint32_t TM_KG_HI = TM_AP, TM_KG_LO = TM_AP + 32;  // KG [i][s], K = 64
+constexpr uint32_t TM_U_HI = TM_WT, TM_U_LO = TM_WT + 32;    // U^T [c][s], K = 64
+constexpr uint32_t TM_SA_HI = 384, TM_SA_LO = 448;           // S^T [c][i], K = 128
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls; a healthy MMA batch completes in microseconds
@@ -100,17 +107,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                                              ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(sm);
     float* s_beta = reinterpret_cast<float*>(sm + OFF_MISC);  // 64
-    float* s_gam = s_beta + 64;                               // 128
-    float* s_tot0 = s_gam + 128;                              // 128
-    float* s_tot1 = s_tot0 + 128;                             // 128
-    int* s_trk = reinterpret_cast<int*>(s_tot1 + 128);        // kTrackTc
+    float* s_gam = s_beta + 64;                               // 128: e^{G_63}
+    float* s_seg_a = s_gam + 128;                             // [4][128]: prod of alpha per token quarter
+    float* s_seg_i = s_seg_a + 512;                           // [4][128]: prod of 1/alpha per quarter
+    int* s_trk = reinterpret_cast<int*>(s_seg_i + 512);       // kTrackTc
     uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_trk + kTrackTc);  // [0]: MMA batches, [1]: state update
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;   // TMEM lane quarter this warp may access
-    const int colhalf = warp >> 2;  // which column half this warp takes in TMEM passes
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int cq = warp >> 2;      // column quarter this warp takes in TMEM passes
     const int row = quarter * 32 + lane;
+    const int ci = tid & 127, tq = tid >> 7;  // channel passes: key channel, token quarter
     const int H = p.H;
     const int unit = blockIdx.x;
     const int n = order ? order[unit / H] : unit / H;
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         s_trk[m] = ok ? j : -1;
     }
 
-    // ---- TMEM and the MMA completion barrier
+    // ---- TMEM and the MMA completion barriers
     if (warp == 0) tmem_alloc(smem_u32(s_tmem), TM_COLS);
     if (tid == 0) {
         mbar_init(smem_u32(s_mbar), 1);
@@ -152,41 +160,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     uint32_t phase = 0, phase_s = 0;
     bool pending_s = false;
 
-    // ---- initial state into TMEM (row c = S^T row, this thread's 64 columns)
+    // ---- initial state into TMEM (row c = S^T row, this warp's 32 columns)
     {
         const float* S0 = init >= 0 ? p.pool + ((size_t)init * H + h) * (kD * kD) : nullptr;
+        const int col0 = cq * 32;
+        float v[32];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int col0 = colhalf * 64 + cc * 32;
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 x = S0 ? reinterpret_cast<const float4*>(S0 + (size_t)row * kD + col0 + j)[0]
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                v[j] = x.x;
-                v[j + 1] = x.y;
-                v[j + 2] = x.z;
-                v[j + 3] = x.w;
-            }
-            st32(tl + TM_S + col0, v);
+        for (int j = 0; j < 32; j += 4) {
+            float4 x = S0 ? reinterpret_cast<const float4*>(S0 + (size_t)row * kD + col0 + j)[0]
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j] = x.x;
+            v[j + 1] = x.y;
+            v[j + 2] = x.z;
+            v[j + 3] = x.w;
         }
+        st32(tl + TM_S + col0, v);
         wait_st();
     }
 
-    const int ci = tid & 127, hf = tid >> 7;  // channel-pass mapping: key channel, half chunk
     bool timed_out = false;
     const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
     const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
     const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
     const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.gate_raw);
 
-    // Raw tiles of chunk jj arrive by cp.async: q, k, g row-major into the
-    // S-operand region (free from MMA 3 of the previous chunk until the state
-    // pass), v as the MN-major MMA operand (free after MMA 2).  Rows past the
-    // sequence are zero-filled.
+    // Raw tiles of chunk jj arrive by cp.async: q, k, g row-major (free once the
+    // decayed operands of the previous chunk are written), v as the MN-major MMA
+    // operand (free after MMA 3).  Rows past the sequence are zero-filled.
     auto prefetch_qkg = [&](int jj) {
         const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
-#pragma unroll 4
+#pragma unroll
         for (int it = tid; it < 64 * 16; it += kThreads) {
             const int t = it >> 4, ch = it & 15;
             const bool ok = t < ln;
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     };
     auto prefetch_v = [&](int jj) {
         const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
-#pragma unroll 4
+#pragma unroll
         for (int it = tid; it < 64 * 16; it += kThreads) {
             const int t = it >> 4, ch = it & 15;
             const bool ok = t < ln;
@@ -241,49 +244,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         fence_after();
         if (tid < 64 && more) beta_next = load_beta(j + 1);  // lands during this chunk
 
-        // ---- channel pass: this thread's channel ci over tokens 32*hf .. 32*hf+31
-        float al[32], iv[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = 32 * hf + u;
-            const float x = bf16_at(sm, RAW_G + t * 256 + ci * 2);
-            if (t < Lc) {
-                if (p.flags & KDA_GATE_LOG) {
-                    al[u] = __expf(x);
-                    iv[u] = __expf(-x);
-                } else {
-                    iv[u] = 1.f + __expf(x);  // 1/alpha = 1 + e^x
-                    al[u] = __fdividef(1.f, iv[u]);
-                }
-            } else {
-                al[u] = 1.f;
-                iv[u] = 1.f;
-            }
-        }
-        bool bad;
+        // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
+        float al[16], iv[16];
+        float m_big = 1.f;  // product of the factors >= 1 this quarter contributes to its half
         {
-            // largest factor >= 1 this half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63]
-            float m = 1.f;
+            float pa = 1.f, pi = 1.f;
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-                if (hf == 1 || u > 0) m *= iv[u];
-            bad = !(m <= kFactorMax);
+            for (int u = 0; u < 16; ++u) {
+                const int t = 16 * tq + u;
+                const float x = bf16_at(sm, RAW_G + t * 256 + ci * 2);
+                if (t < Lc) {
+                    if (p.flags & KDA_GATE_LOG) {
+                        al[u] = __expf(x);
+                        iv[u] = __expf(-x);
+                    } else {
+                        iv[u] = 1.f + __expf(x);  // 1/alpha = 1 + e^x
+                        al[u] = __fdividef(1.f, iv[u]);
+                    }
+                } else {
+                    al[u] = 1.f;
+                    iv[u] = 1.f;
+                }
+                pa *= al[u];
+                pi *= iv[u];
+                if (tq != 0 || u > 0) m_big *= iv[u];
+            }
+            s_seg_a[tq * 128 + ci] = pa;
+            s_seg_i[tq * 128 + ci] = pi;
         }
+        __syncthreads();
+        bool bad = false;
+        // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
+        if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
+        if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
         const int fallback = __syncthreads_or(bad);
 
         if (!fallback) {
-            // ---- L = [k; q] e^{G_t - G_31}, R = k e^{G_31 - G_s} (half 0: backward from 31;
-            //      half 1: forward from 32), half totals for e^{G_31} and e^{G_63 - G_31}
-            if (hf == 0) {
+            // ---- L = [k; q] e^{G_t - G_31}, R = k e^{G_31 - G_s}: quarters 0, 1 backward
+            //      from token 31, quarters 2, 3 forward from token 32
+            if (tq < 2) {
                 float sa = 1.f, si = 1.f;  // prod over (u, 31] of alpha and of 1/alpha
+                if (tq == 0) {
+                    sa = s_seg_a[128 + ci];
+                    si = s_seg_i[128 + ci];
+                }
 #pragma unroll
-                for (int g8 = 3; g8 >= 0; --g8) {
+                for (int g8 = 1; g8 >= 0; --g8) {
                     float lk[8], lq[8], r[8];
 #pragma unroll
                     for (int w = 7; w >= 0; --w) {
-                        const int u = g8 * 8 + w;
-                        const float kk = bf16_at(sm, RAW_K + u * 256 + ci * 2);
-                        const float qq = bf16_at(sm, RAW_Q + u * 256 + ci * 2) * p.scale;
+                        const int u = g8 * 8 + w, t = 16 * tq + u;
+                        const float kk = bf16_at(sm, RAW_K + t * 256 + ci * 2);
+                        const float qq = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale;
                         lk[w] = kk * si;
                         lq[w] = qq * si;
                         r[w] = kk * sa;
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                         si *= iv[u];
                     }
                     uint4 hi, lo;
-                    const int tt = g8 * 8;
+                    const int tt = 16 * tq + g8 * 8;
                     split8(lk, hi, lo);
                     st16(sm, X_L_HI + chunk_mn(tt, ci, 1024, 2048), hi);
                     st16(sm, X_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
@@ -302,17 +314,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     st16(sm, X_R_HI + chunk_mn(tt, ci, 1024, 1024), hi);
                     st16(sm, X_R_LO + chunk_mn(tt, ci, 1024, 1024), lo);
                 }
-                s_tot0[ci] = sa;  // e^{G_31}
+                if (tq == 0) {
+                    const float a0 = s_seg_a[ci], a1 = s_seg_a[128 + ci], a2 = s_seg_a[256 + ci],
+                                a3 = s_seg_a[384 + ci];
+                    s_gam[ci] = (a0 * a1) * (a2 * a3);  // e^{G_63}
+                }
             } else {
-                float fa = 1.f, fi = 1.f;  // prod over [32, 32+u] of alpha and of 1/alpha
+                float fa = 1.f, fi = 1.f;  // prod over [32, t] of alpha and of 1/alpha
+                if (tq == 3) {
+                    fa = s_seg_a[256 + ci];
+                    fi = s_seg_i[256 + ci];
+                }
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
+                for (int g8 = 0; g8 < 2; ++g8) {
                     float lk[8], lq[8], r[8];
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
-                        const int u = g8 * 8 + w;
-                        const float kk = bf16_at(sm, RAW_K + (32 + u) * 256 + ci * 2);
-                        const float qq = bf16_at(sm, RAW_Q + (32 + u) * 256 + ci * 2) * p.scale;
+                        const int u = g8 * 8 + w, t = 16 * tq + u;
+                        const float kk = bf16_at(sm, RAW_K + t * 256 + ci * 2);
+                        const float qq = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale;
                         fa *= al[u];
                         fi *= iv[u];
                         lk[w] = kk * fa;
@@ -320,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                         r[w] = kk * fi;
                     }
                     uint4 hi, lo;
-                    const int tt = 32 + g8 * 8;
+                    const int tt = 16 * tq + g8 * 8;
                     split8(lk, hi, lo);
                     st16(sm, X_L_HI + chunk_mn(tt, ci, 1024, 2048), hi);
                     st16(sm, X_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
@@ -331,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     st16(sm, X_R_HI + chunk_mn(tt, ci, 1024, 1024), hi);
                     st16(sm, X_R_LO + chunk_mn(tt, ci, 1024, 1024), lo);
                 }
-                s_tot1[ci] = fa;  // e^{G_63 - G_31}
             }
             fence_async_smem();
             fence_before();
@@ -351,7 +370,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 }
                 commit(mbar);
             }
-            if (hf == 0) s_gam[ci] = s_tot0[ci] * s_tot1[ci];
             const bool ok1 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
@@ -360,105 +378,132 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 break;
             }
 
-            // ---- A -> N = Diag(beta) A (strict lower), P -> bf16 operand (lower incl. diagonal)
+            // ---- A -> N = Diag(beta) A (strict lower, stored transposed: Nt[s][t] = N[t][s]),
+            //      P -> bf16 operand (lower incl. diagonal)
             {
-                float v[32];
-                ld32(tl + TM_AP + colhalf * 32, v);
-                float* Nm = reinterpret_cast<float*>(sm + X_N);
+                float v[16];
+                ld16(tl + TM_AP + cq * 16, v);
+                float* Nt = reinterpret_cast<float*>(sm + X_N);
                 if (quarter < 2) {
                     const int t = row;
                     const float bt = s_beta[t];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int s = colhalf * 32 + q;
-                        Nm[t * NLD + s] = s < t ? bt * v[q] : 0.f;
+                    for (int q = 0; q < 16; ++q) {
+                        const int s = cq * 16 + q;
+                        Nt[s * NLD + t] = s < t ? bt * v[q] : 0.f;
                     }
                 } else {
                     const int t = row - 64;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int s = colhalf * 32 + q;
+                    for (int q = 0; q < 16; ++q) {
+                        const int s = cq * 16 + q;
                         if (s > t) v[q] = 0.f;
                     }
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
+                    for (int c8 = 0; c8 < 2; ++c8) {
                         if constexpr (kBf16Out) {
-                            st16(sm, OFF_P + chunk_k(t, colhalf * 32 + 8 * c8, 64), pack8(v + 8 * c8));
+                            st16(sm, OFF_P + chunk_k(t, cq * 16 + 8 * c8, 64), pack8(v + 8 * c8));
                         } else {
                             uint4 hi, lo;
                             split8(v + 8 * c8, hi, lo);
-                            st16(sm, OFF_P + chunk_k(t, colhalf * 32 + 8 * c8, 64), hi);
-                            st16(sm, OFF_P_LO + chunk_k(t, colhalf * 32 + 8 * c8, 64), lo);
+                            st16(sm, OFF_P + chunk_k(t, cq * 16 + 8 * c8, 64), hi);
+                            st16(sm, OFF_P_LO + chunk_k(t, cq * 16 + 8 * c8, 64), lo);
                         }
                     }
                 }
             }
             __syncthreads();
-            // ---- T = (I + N)^-1: 16x16 diagonal blocks, then block substitution
+            // ---- T = (I + N)^-1 (unit lower triangular): 16x16 diagonal blocks by forward
+            //      substitution, then the off-diagonal blocks by block substitution
             {
-                const float* Nm = reinterpret_cast<const float*>(sm + X_N);
+                const float* Nt = reinterpret_cast<const float*>(sm + X_N);
                 float* Tm = reinterpret_cast<float*>(sm + X_T);
                 if (tid < 64) {
+                    // column jc of the inverse of diagonal block b: x = e_jc, then for each s
+                    // (final from here on) x[r] -= N[r][s] x[s] for r > s
                     const int b = tid >> 4, jc = tid & 15, o = 16 * b;
                     float x[16];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        float acc = 0.f;
+                    for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
 #pragma unroll
-                        for (int s = 0; s < r; ++s) acc = fmaf(Nm[(o + r) * NLD + o + s], x[s], acc);
-                        x[r] = (r == jc) ? 1.f : -acc;
+                    for (int s = 0; s < 15; ++s) {
+                        float nr[16];
+#pragma unroll
+                        for (int r4 = (s + 1) / 4; r4 < 4; ++r4) {
+                            const float4 n4 = *reinterpret_cast<const float4*>(&Nt[(o + s) * NLD + o + 4 * r4]);
+                            nr[4 * r4] = n4.x;
+                            nr[4 * r4 + 1] = n4.y;
+                            nr[4 * r4 + 2] = n4.z;
+                            nr[4 * r4 + 3] = n4.w;
+                        }
+                        const float xs = x[s];
+#pragma unroll
+                        for (int r = s + 1; r < 16; ++r) x[r] = fmaf(-nr[r], xs, x[r]);
                     }
 #pragma unroll
                     for (int r = 0; r < 16; ++r) Tm[(o + r) * NLD + o + jc] = x[r];
+                } else if (tid < 64 + 256) {
+                    // the blocks above the diagonal pairs, (0,1) and (2,3), are zero
+                    const int e = tid - 64, r = e >> 4, c = e & 15;
+                    Tm[r * NLD + 16 + c] = 0.f;
+                    Tm[(32 + r) * NLD + 48 + c] = 0.f;
                 }
                 __syncthreads();
-                // level 1: T[a][a-1] = -D_a N[a][a-1] D_{a-1}, a in {1, 3}; a thread owns one
-                // row r and 2 adjacent columns of one 16x16 block
+                // level 1: T[a][a-1] = -T_aa N[a][a-1] T_{a-1,a-1}, a in {1, 3}; a thread owns
+                // row r and 4 adjacent columns of one 16x16 block
                 float* Y1 = reinterpret_cast<float*>(sm + X_Y1);  // [2][16][20]
-                {
-                    const int w = tid >> 7, e = tid & 127, r = e >> 3, c = (e & 7) * 2;
-                    const int a = 2 * w + 1, oa = 16 * a, ob = 16 * (a - 1);
-                    float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                    for (int s = 0; s < 16; ++s) {
-                        const float nv = Nm[(oa + r) * NLD + ob + s];
-                        const float2 tv = *reinterpret_cast<const float2*>(&Tm[(ob + s) * NLD + ob + c]);
-                        y0 = fmaf(nv, tv.x, y0);
-                        y1 = fmaf(nv, tv.y, y1);
-                    }
-                    *reinterpret_cast<float2*>(&Y1[(w * 16 + r) * 20 + c]) = make_float2(y0, y1);
-                    // T is lower triangular: the blocks above the diagonal pairs are zero
-                    Tm[(16 * (2 * w) + r) * NLD + 16 * (2 * w + 1) + c] = 0.f;
-                    Tm[(16 * (2 * w) + r) * NLD + 16 * (2 * w + 1) + c + 1] = 0.f;
-                    __syncthreads();
-                    float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-                    for (int s = 0; s < 16; ++s) {
-                        const float tv = Tm[(oa + r) * NLD + oa + s];
-                        const float2 yv = *reinterpret_cast<const float2*>(&Y1[(w * 16 + s) * 20 + c]);
-                        z0 = fmaf(tv, yv.x, z0);
-                        z1 = fmaf(tv, yv.y, z1);
-                    }
-                    *reinterpret_cast<float2*>(&Tm[(oa + r) * NLD + ob + c]) = make_float2(-z0, -z1);
-                }
-                __syncthreads();
-                // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]);
-                // a thread owns one row r and 4 adjacent columns
-                float* Y2 = reinterpret_cast<float*>(sm + X_Y2);  // [32][36]
-                {
-                    const int r = tid >> 3, c = (tid & 7) * 4;
+                const int w1 = tid >> 6, r1 = (tid & 63) >> 2, c1 = (tid & 3) * 4;
+                const int oa = 32 * w1 + 16, ob = 32 * w1;
+                if (tid < 128) {
                     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                    for (int u = 0; u < 32; ++u) {
-                        const float nv = Nm[(32 + r) * NLD + u];
-                        const float4 tv = *reinterpret_cast<const float4*>(&Tm[u * NLD + c]);
+#pragma unroll
+                    for (int s = 0; s < 16; ++s) {
+                        const float nv = Nt[(ob + s) * NLD + oa + r1];
+                        const float4 tv = *reinterpret_cast<const float4*>(&Tm[(ob + s) * NLD + ob + c1]);
                         y.x = fmaf(nv, tv.x, y.x);
                         y.y = fmaf(nv, tv.y, y.y);
                         y.z = fmaf(nv, tv.z, y.z);
                         y.w = fmaf(nv, tv.w, y.w);
                     }
-                    *reinterpret_cast<float4*>(&Y2[r * 36 + c]) = y;
-                    __syncthreads();
+                    *reinterpret_cast<float4*>(&Y1[(w1 * 16 + r1) * 20 + c1]) = y;
+                }
+                __syncthreads();
+                if (tid < 128) {
+                    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int s = 0; s < 16; ++s) {
+                        const float tv = Tm[(oa + r1) * NLD + oa + s];
+                        const float4 yv = *reinterpret_cast<const float4*>(&Y1[(w1 * 16 + s) * 20 + c1]);
+                        z.x = fmaf(tv, yv.x, z.x);
+                        z.y = fmaf(tv, yv.y, z.y);
+                        z.z = fmaf(tv, yv.z, z.z);
+                        z.w = fmaf(tv, yv.w, z.w);
+                    }
+                    *reinterpret_cast<float4*>(&Tm[(oa + r1) * NLD + ob + c1]) =
+                        make_float4(-z.x, -z.y, -z.z, -z.w);
+                }
+                __syncthreads();
+                // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]).
+                // First product: warp = 4-column group c2, lane = row; T[0:32, 0:32] is lower
+                // triangular, so the sum starts at u = c2.
+                float* Y2 = reinterpret_cast<float*>(sm + X_Y2);  // [32][36]
+                if (tid < 256) {
+                    const int c2 = 4 * warp;
+                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int u = c2; u < 32; ++u) {
+                        const float nv = Nt[u * NLD + 32 + lane];
+                        const float4 tv = *reinterpret_cast<const float4*>(&Tm[u * NLD + c2]);
+                        y.x = fmaf(nv, tv.x, y.x);
+                        y.y = fmaf(nv, tv.y, y.y);
+                        y.z = fmaf(nv, tv.z, y.z);
+                        y.w = fmaf(nv, tv.w, y.w);
+                    }
+                    *reinterpret_cast<float4*>(&Y2[lane * 36 + c2]) = y;
+                }
+                __syncthreads();
+                if (tid < 256) {
+                    const int r = tid >> 3, c = (tid & 7) * 4;
                     float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
                     for (int s = 0; s < 32; ++s) {
@@ -473,9 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 }
                 __syncthreads();
                 // T_b = T Diag(beta) -> bf16 hi/lo operand [t][s] (lower triangle only)
-#pragma unroll
-                for (int it = tid; it < 64 * 8; it += kThreads) {
-                    const int t = it >> 3, s0 = (it & 7) * 8;
+                {
+                    const int t = tid >> 3, s0 = (tid & 7) * 8;
                     float x[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -491,23 +535,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             __syncthreads();
             // ---- KG = k e^{G} (A, [i][s]), QG = q e^{G} (B, MN-major), KT = k e^{G_63 - G} ([i][s])
             {
-                const float t0f = s_tot0[ci], t1f = s_tot1[ci];
-                float fw = (hf == 0) ? 1.f : t0f;  // e^{G_t}: running product from the chunk start
+                const float a0 = s_seg_a[ci], a1 = s_seg_a[128 + ci], a2 = s_seg_a[256 + ci],
+                            a3 = s_seg_a[384 + ci];
+                // e^{G_t}: running product from the chunk start; e^{G_63 - G_t}: product over (t, 63]
+                float fw = tq == 0 ? 1.f : tq == 1 ? a0 : tq == 2 ? a0 * a1 : (a0 * a1) * a2;
+                float bw = tq == 3 ? 1.f : tq == 2 ? a3 : tq == 1 ? a2 * a3 : a1 * (a2 * a3);
+                uint32_t kgh[8], kgl[8];  // KG row ci, tokens 16*tq.., packed bf16 pairs
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int c8 = 0; c8 < 2; ++c8) {
                     float kg[8], qg[8];
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
-                        const int u = 8 * c8 + w, t = 32 * hf + u;
+                        const int u = 8 * c8 + w, t = 16 * tq + u;
                         fw *= al[u];
                         kg[w] = bf16_at(sm, RAW_K + t * 256 + ci * 2) * fw;
                         qg[w] = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale * fw;
                     }
-                    const int s0 = 32 * hf + 8 * c8;
+                    const int s0 = 16 * tq + 8 * c8;
                     uint4 hi, lo;
                     split8(kg, hi, lo);
-                    st16(sm, X_KG_HI + chunk_k(ci, s0, 128), hi);
-                    st16(sm, X_KG_LO + chunk_k(ci, s0, 128), lo);
+                    kgh[4 * c8] = hi.x; kgh[4 * c8 + 1] = hi.y; kgh[4 * c8 + 2] = hi.z; kgh[4 * c8 + 3] = hi.w;
+                    kgl[4 * c8] = lo.x; kgl[4 * c8 + 1] = lo.y; kgl[4 * c8 + 2] = lo.z; kgl[4 * c8 + 3] = lo.w;
                     if constexpr (kBf16Out) {
                         st16(sm, X_QG + chunk_mn(s0, ci, 1024, 1024), pack8(qg));
                     } else {
@@ -516,38 +564,44 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                         st16(sm, X_QG_LO + chunk_mn(s0, ci, 1024, 1024), lo);
                     }
                 }
-                float bw = (hf == 0) ? t1f : 1.f;  // e^{G_63 - G_t}: product over (t, 63]
 #pragma unroll
-                for (int c8 = 3; c8 >= 0; --c8) {
+                for (int c8 = 1; c8 >= 0; --c8) {
                     float kt[8];
 #pragma unroll
                     for (int w = 7; w >= 0; --w) {
-                        const int u = 8 * c8 + w, t = 32 * hf + u;
+                        const int u = 8 * c8 + w, t = 16 * tq + u;
                         kt[w] = bf16_at(sm, RAW_K + t * 256 + ci * 2) * bw;
                         bw *= al[u];
                     }
-                    const int s0 = 32 * hf + 8 * c8;
+                    const int s0 = 16 * tq + 8 * c8;
                     uint4 hi, lo;
                     split8(kt, hi, lo);
                     st16(sm, X_KT_HI + chunk_k(ci, s0, 128), hi);
                     st16(sm, X_KT_LO + chunk_k(ci, s0, 128), lo);
                 }
+                st8u(tl + TM_KG_HI + tq * 8, kgh);  // lane ci of this warp's quarter
+                st8u(tl + TM_KG_LO + tq * 8, kgl);
+                wait_st();
             }
             fence_async_smem();
             fence_before();
             __syncthreads();
             fence_after();
+            if (more) {
+                prefetch_qkg(j + 1);  // the raw q, k, g tiles of this chunk are consumed
+                cp_async_commit();
+            }
             // ---- MMA 2: W^T = KG T_b^T, U~^T = V^T T_b^T
             if (tid == 0) {
                 const uint32_t idk = idesc_bf16(128, 64, false, false, false);
                 const uint32_t idv = idesc_bf16(128, 64, true, false, false);
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = sb + (pass == 2 ? X_KG_LO : X_KG_HI);
+                    const uint32_t a = tmem + (pass == 2 ? TM_KG_LO : TM_KG_HI);
                     const uint32_t b = sb + (pass == 1 ? OFF_TB_LO : OFF_TB_HI);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma(tmem + TM_WT, desc_k(a, 128, s), desc_k(b, 64, s), idk, (pass | s) != 0);
+                        mma_ta(tmem + TM_WT, a + 8 * s, desc_k(b, 64, s), idk, (pass | s) != 0);
                 }
                 commit(mbar);  // W^T only: U~^T (below) keeps running while W is extracted
 #pragma unroll
@@ -559,11 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                             (pass | s) != 0);
                 }
             }
-            // ---- state pass (overlaps MMA 2): S_j -> snapshot, bf16 hi/lo operand (over the raw
-            //      tiles, all read by now), decay by e^{G_63}
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int col0 = colhalf * 64 + cc * 32;
+            // ---- state pass (overlaps MMA 2): S_j -> snapshot, bf16 hi/lo A operand in TMEM,
+            //      decay by e^{G_63}
+            {
+                const int col0 = cq * 32;
                 float v[32];
                 ld32(tl + TM_S + col0, v);
                 for (int m = 0; m < p.M; ++m) {
@@ -575,12 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                         reinterpret_cast<float4*>(snap + q4)[0] =
                             make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
                 }
+                {
+                    uint32_t sh[16], sl[16];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint4 hi, lo;
-                    split8(v + 8 * c8, hi, lo);
-                    st16(sm, OFF_ST_HI + chunk_k(row, col0 + 8 * c8, 128), hi);
-                    st16(sm, OFF_ST_LO + chunk_k(row, col0 + 8 * c8, 128), lo);
+                    for (int q2 = 0; q2 < 16; ++q2) split2(v[2 * q2], v[2 * q2 + 1], sh[q2], sl[q2]);
+                    st16u(tl + TM_SA_HI + cq * 16, sh);
+                    st16u(tl + TM_SA_LO + cq * 16, sl);
                 }
 #pragma unroll
                 for (int q = 0; q < 32; ++q) v[q] *= s_gam[col0 + q];
@@ -594,15 +647,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 timed_out = true;
                 break;
             }
-            // ---- W^T (lanes i, columns t) -> W operand (B, MN-major [i][t]) hi/lo
+            // ---- W^T (lanes i, columns t) -> -W operand (B, MN-major [i][t]) hi/lo
             {
-                float v[32];
-                ld32(tl + TM_WT + colhalf * 32, v);
+                float v[16];
+                ld16(tl + TM_WT + cq * 16, v);
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int q = 0; q < 16; ++q) v[q] = -v[q];
+#pragma unroll
+                for (int c8 = 0; c8 < 2; ++c8) {
                     uint4 hi, lo;
                     split8(v + 8 * c8, hi, lo);
-                    const int t = colhalf * 32 + 8 * c8;
+                    const int t = cq * 16 + 8 * c8;
                     st16(sm, X_W_HI + chunk_mn(t, row, 1024, 1024), hi);
                     st16(sm, X_W_LO + chunk_mn(t, row, 1024, 1024), lo);
                 }
@@ -611,28 +666,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             fence_before();
             __syncthreads();
             fence_after();
-            // ---- MMA 3: O^T = S^T QG^T ; U^T = U~^T - S^T W^T (O first: one commit then frees the
-            //      S operand, the V tile and the W / QG tiles)
+            // ---- MMA 3: O^T = S^T QG^T ; U^T = U~^T + S^T (-W)^T (one commit frees the V tile
+            //      and the W / QG tiles)
             if (tid == 0) {
-                const uint32_t idu = idesc_bf16(128, 64, false, true, true);
-                const uint32_t ido = idesc_bf16(128, 64, false, true, false);
+                const uint32_t idb = idesc_bf16(128, 64, false, true, false);
                 // bf16 outputs: S_hi QG_hi; fp32 outputs: + S_lo QG_hi + S_hi QG_lo
 #pragma unroll
                 for (int pass = 0; pass < (kBf16Out ? 1 : 3); ++pass) {
-                    const uint32_t a = sb + (pass == 1 ? OFF_ST_LO : OFF_ST_HI);
+                    const uint32_t a = tmem + (pass == 1 ? TM_SA_LO : TM_SA_HI);
                     const uint32_t b = sb + (pass == 2 ? X_QG_LO : X_QG);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        mma(tmem + TM_OT, desc_k(a, 128, s), desc_mn(b, 1024, 1024, s), ido,
-                            (pass | s) != 0);
+                        mma_ta(tmem + TM_OT, a + 8 * s, desc_mn(b, 1024, 1024, s), idb, (pass | s) != 0);
                 }
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = sb + (pass == 2 ? OFF_ST_LO : OFF_ST_HI);
+                    const uint32_t a = tmem + (pass == 2 ? TM_SA_LO : TM_SA_HI);
                     const uint32_t b = sb + (pass == 1 ? X_W_LO : X_W_HI);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        mma(tmem + TM_UT, desc_k(a, 128, s), desc_mn(b, 1024, 1024, s), idu, 1u);
+                        mma_ta(tmem + TM_UT, a + 8 * s, desc_mn(b, 1024, 1024, s), idb, 1u);
                 }
                 commit(mbar);
             }
@@ -644,25 +697,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 break;
             }
             if (more) {
-                // every reader of the S operand region and of the V tile has completed
-                prefetch_qkg(j + 1);
-                prefetch_v(j + 1);
+                prefetch_v(j + 1);  // MMA 2's reads of the V tile have completed
                 cp_async_commit();
             }
-            // ---- U^T (lanes c, columns s) -> UT operand (A, K-major [c][s]) hi/lo
+            // ---- U^T (lanes c, columns s) -> bf16 hi/lo A operand in TMEM
             {
-                float v[32];
-                ld32(tl + TM_UT + colhalf * 32, v);
+                float v[16];
+                ld16(tl + TM_UT + cq * 16, v);
+                uint32_t uh[8], ul[8];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint4 hi, lo;
-                    split8(v + 8 * c8, hi, lo);
-                    const int s0 = colhalf * 32 + 8 * c8;
-                    st16(sm, X_UT_HI + chunk_k(row, s0, 128), hi);
-                    st16(sm, X_UT_LO + chunk_k(row, s0, 128), lo);
-                }
+                for (int q2 = 0; q2 < 8; ++q2) split2(v[2 * q2], v[2 * q2 + 1], uh[q2], ul[q2]);
+                st8u(tl + TM_U_HI + cq * 8, uh);
+                st8u(tl + TM_U_LO + cq * 8, ul);
+                wait_st();
             }
-            fence_async_smem();
             fence_before();
             __syncthreads();
             fence_after();
@@ -672,20 +720,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 const uint32_t ids = idesc_bf16(128, 128, false, false, false);
 #pragma unroll
                 for (int pass = 0; pass < (kBf16Out ? 1 : 3); ++pass) {
-                    const uint32_t a = sb + (pass == 1 ? X_UT_LO : X_UT_HI);
+                    const uint32_t a = tmem + (pass == 1 ? TM_U_LO : TM_U_HI);
                     const uint32_t b = sb + (pass == 2 ? OFF_P_LO : OFF_P);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma(tmem + TM_OT, desc_k(a, 128, s), desc_k(b, 64, s), ido, 1u);
+                        mma_ta(tmem + TM_OT, a + 8 * s, desc_k(b, 64, s), ido, 1u);
                 }
                 commit(mbar);  // the outputs; the state update below finishes in the background
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = sb + (pass == 2 ? X_UT_LO : X_UT_HI);
+                    const uint32_t a = tmem + (pass == 2 ? TM_U_LO : TM_U_HI);
                     const uint32_t b = sb + (pass == 1 ? X_KT_LO : X_KT_HI);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma(tmem + TM_S, desc_k(a, 128, s), desc_k(b, 128, s), ids, 1u);
+                        mma_ta(tmem + TM_S, a + 8 * s, desc_k(b, 128, s), ids, 1u);
                 }
                 commit(mbar_s);
             }
@@ -699,14 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             }
             // ---- O^T (lanes c, columns t) -> out[t][h][c]
             {
-                float v[32];
-                ld32(tl + TM_OT + colhalf * 32, v);
+                float v[16];
+                ld16(tl + TM_OT + cq * 16, v);
                 if constexpr (kBf16Out) {
                     // through shared memory (the T_b region, free now) for 16-byte row stores
                     __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TB_HI);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        ob[(colhalf * 32 + q) * kD + row] = __float2bfloat16_rn(v[q]);
+                    for (int q = 0; q < 16; ++q)
+                        ob[(cq * 16 + q) * kD + row] = __float2bfloat16_rn(v[q]);
                     __syncthreads();
 #pragma unroll
                     for (int it = tid; it < 64 * 16; it += kThreads) {
@@ -718,75 +766,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int t = colhalf * 32 + q;
+                    for (int q = 0; q < 16; ++q) {
+                        const int t = cq * 16 + q;
                         if (t < Lc) store1<false>(p.out, ((size_t)(c0 + t) * H + h) * kD + row, v[q]);
                     }
                 }
             }
         } else {
-            // ---- fallback: this chunk token by token on CUDA cores (warps 0-3, a row each)
+            // ---- fallback: this chunk token by token on CUDA cores
             float* alpha = reinterpret_cast<float*>(sm + X_ALPHA);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) alpha[(32 * hf + u) * kD + ci] = al[u];
+            for (int u = 0; u < 16; ++u) alpha[(16 * tq + u) * kD + ci] = al[u];
             fence_before();
             __syncthreads();
             fence_after();
             {
-                // thread (row c, column half) keeps 64 state columns in registers; the two
-                // half-row dot products meet in shared memory
-                float* red = reinterpret_cast<float*>(sm + X_RED);  // [2 dots][2 halves][128]
+                // thread (row c, column quarter) keeps 32 state columns in registers; the four
+                // partial row dot products meet in shared memory
+                float* red = reinterpret_cast<float*>(sm + X_RED);  // [2 dots][4 quarters][128]
                 const int c = row;
-                float sv[64];
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-                    ld32(tl + TM_S + colhalf * 64 + cc * 32, v);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) sv[cc * 32 + q] = v[q];
-                }
+                float sv[32];
+                ld32(tl + TM_S + cq * 32, sv);
                 for (int m = 0; m < p.M; ++m) {
                     if (s_trk[m] != j) continue;
                     float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
-                                  (size_t)c * kD + colhalf * 64;
+                                  (size_t)c * kD + cq * 32;
 #pragma unroll
-                    for (int q4 = 0; q4 < 64; q4 += 4)
+                    for (int q4 = 0; q4 < 32; q4 += 4)
                         reinterpret_cast<float4*>(snap + q4)[0] =
                             make_float4(sv[q4], sv[q4 + 1], sv[q4 + 2], sv[q4 + 3]);
                 }
                 for (int t = 0; t < Lc; ++t) {
                     float d1 = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 64; ++q) {
-                        const int i = colhalf * 64 + q;
+                    for (int q = 0; q < 32; ++q) {
+                        const int i = cq * 32 + q;
                         sv[q] *= alpha[t * kD + i];
                         d1 = fmaf(sv[q], bf16_at(sm, RAW_K + t * 256 + i * 2), d1);
                     }
-                    red[colhalf * 128 + c] = d1;
+                    red[cq * 128 + c] = d1;
                     __syncthreads();
-                    d1 = red[c] + red[128 + c];
+                    d1 = (red[c] + red[128 + c]) + (red[256 + c] + red[384 + c]);
                     const float vt = bf16_at(sm, OFF_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
                     const float uu = s_beta[t] * (vt - d1);
                     float o = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 64; ++q) {
-                        const int i = colhalf * 64 + q;
+                    for (int q = 0; q < 32; ++q) {
+                        const int i = cq * 32 + q;
                         sv[q] = fmaf(uu, bf16_at(sm, RAW_K + t * 256 + i * 2), sv[q]);
                         o = fmaf(sv[q], bf16_at(sm, RAW_Q + t * 256 + i * 2) * p.scale, o);
                     }
-                    red[256 + colhalf * 128 + c] = o;
+                    red[512 + cq * 128 + c] = o;
                     __syncthreads();
-                    if (colhalf == 0)
+                    if (cq == 0)
                         store1<kBf16Out>(p.out, ((size_t)(c0 + t) * H + h) * kD + c,
-                                         red[256 + c] + red[384 + c]);
+                                         (red[512 + c] + red[640 + c]) + (red[768 + c] + red[896 + c]));
                 }
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = sv[cc * 32 + q];
-                    st32(tl + TM_S + colhalf * 64 + cc * 32, v);
-                }
+                st32(tl + TM_S + cq * 32, sv);
                 wait_st();
             }
             fence_before();
@@ -815,16 +851,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         if (pending_s) mbar_wait(mbar_s, phase_s, kWaitLimit);
     } else if (fin >= 0) {
         float* SD = p.pool + ((size_t)fin * H + h) * (kD * kD);
+        const int col0 = cq * 32;
+        float v[32];
+        ld32(tl + TM_S + col0, v);
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int col0 = colhalf * 64 + cc * 32;
-            float v[32];
-            ld32(tl + TM_S + col0, v);
-#pragma unroll
-            for (int q4 = 0; q4 < 32; q4 += 4)
-                reinterpret_cast<float4*>(SD + (size_t)row * kD + col0 + q4)[0] =
-                    make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
-        }
+        for (int q4 = 0; q4 < 32; q4 += 4)
+            reinterpret_cast<float4*>(SD + (size_t)row * kD + col0 + q4)[0] =
+                make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
     }
     fence_before();
     __syncthreads();
