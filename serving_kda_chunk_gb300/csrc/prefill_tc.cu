@@ -56,17 +56,17 @@ constexpr uint32_t OFF_RAW = 0;      // raw q, k, g tiles of the chunk, row-majo
 constexpr uint32_t OFF_X = 49152;    // 96 KiB reused by the chunk phases:
 //   fallback alpha (fp32 [64][128]), dot scratch     X+0, X+32K
 //   L hi/lo (A, MN-major, M = 128, K = 128)          X+0,  X+32K
-//   R hi/lo (B, MN-major, N = 64,  K = 128)          X+64K, X+80K
+//   [R hi; R lo] (B, MN-major, N = 2 x 64, K = 128)  X+64K, X+80K
 //   N^T, T (fp32 [64][68]) and solve temporaries     X+0 .. X+41K
-//   QG (B, MN-major), KT hi/lo (B, K-major [i][s]),
-//   QG lo (fp32 outputs)                             X+32K, X+48K, X+64K, X+80K
-//   -W hi/lo (B, MN-major [i][t])                    X+0, X+16K
-constexpr uint32_t OFF_V = OFF_X + 98304;        // A: V, MN-major (c atoms 8 KiB apart, s groups 1 KiB)
-constexpr uint32_t OFF_TB_HI = OFF_V + 16384;    // B: T_b [t][s], K-major, 64 rows
+//   [QG; -W hi; -W lo] (B, MN-major, N = 3 x 64)     X+0, X+16K, X+32K
+//   [KT hi; P] (B, K-major, 128 + 64 rows), KT lo    X+48K, X+64K, X+72K
+//   P lo (fp32 outputs)                              X+88K
+constexpr uint32_t OFF_V = OFF_X + 98304;  // A: V, MN-major (c atoms 8 KiB apart, s groups 1 KiB),
+                                           // two buffers (chunk parity) 16 KiB apart
+constexpr uint32_t OFF_TB_HI = OFF_V + 32768;    // B: [T_b hi; T_b lo] [t][s], K-major, 64 + 64 rows
 constexpr uint32_t OFF_TB_LO = OFF_TB_HI + 8192;
-constexpr uint32_t OFF_P = OFF_TB_LO + 8192;     // B: P [t][s], K-major, 64 rows
-constexpr uint32_t OFF_P_LO = OFF_P + 8192;      // P lo (fp32 outputs only)
-constexpr uint32_t OFF_MISC = OFF_P_LO + 8192;
+constexpr uint32_t OFF_QG_LO = OFF_TB_LO + 8192;  // QG lo (fp32 outputs), MN-major
+constexpr uint32_t OFF_MISC = OFF_QG_LO + 16384;
 constexpr uint32_t MISC_BYTES = 8192;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 
@@ -75,17 +75,22 @@ constexpr uint32_t X_ALPHA = OFF_X, X_RED = OFF_X + 32768;
 constexpr uint32_t X_L_HI = OFF_X, X_L_LO = OFF_X + 32768, X_R_HI = OFF_X + 65536,
                    X_R_LO = OFF_X + 81920;
 constexpr uint32_t X_N = OFF_X, X_T = OFF_X + 17408, X_Y1 = OFF_X + 34816, X_Y2 = OFF_X + 37376;
-constexpr uint32_t X_QG = OFF_X + 32768, X_KT_HI = OFF_X + 49152, X_KT_LO = OFF_X + 65536,
-                   X_QG_LO = OFF_X + 81920;
-constexpr uint32_t X_W_HI = OFF_X, X_W_LO = OFF_X + 16384;
+constexpr uint32_t X_QG = OFF_X, X_W_HI = OFF_X + 16384, X_W_LO = OFF_X + 32768;
+constexpr uint32_t X_KT_HI = OFF_X + 49152, X_P = OFF_X + 65536, X_KT_LO = OFF_X + 73728,
+                   X_P_LO = OFF_X + 90112;
 constexpr int NLD = 68;  // fp32 row stride of the N / T matrices
 
 // TMEM columns: fp32 accumulators, and bf16 hi/lo A operands (two per column) whose rows are
-// the TMEM lanes.  KG reuses the [A; P] columns once they are read, U^T those of W^T.
-constexpr uint32_t TM_S = 0, TM_AP = 128, TM_WT = 192, TM_UT = 256, TM_OT = 320;
-constexpr uint32_t TM_KG_HI = TM_AP, TM_KG_LO = TM_AP + 32;  // KG [i][s], K = 64
-constexpr uint32_t TM_U_HI = TM_WT, TM_U_LO = TM_WT + 32;    // U^T [c][s], K = 64
-constexpr uint32_t TM_SA_HI = 384, TM_SA_LO = 448;           // S^T [c][i], K = 128
+// the TMEM lanes.  A tcgen05.mma costs about the same for any N up to 256, so products that
+// share an A operand are issued as one MMA over B tiles laid side by side, into adjacent
+// accumulators: [S | O] takes U^T [KT; P], [O | U_a | U_b] takes S^T [QG; -W hi; -W lo].
+constexpr uint32_t TM_S = 0;                     // S^T, fp32, 128 columns
+constexpr uint32_t TM_O = 128;                   // O^T (W^T while MMA 2 runs)
+constexpr uint32_t TM_UA = 192, TM_UB = 256;     // U^T = U_a + U_b (hi and lo T_b parts)
+constexpr uint32_t TM_AP = 192;                  // [A; P] as hi + lo parts (MMA 1 only)
+constexpr uint32_t TM_SA_HI = 320, TM_SA_LO = 384;  // S^T [c][i], K = 128
+constexpr uint32_t TM_KG_HI = 448, TM_KG_LO = 480;  // KG [i][s], K = 64 (until MMA 2)
+constexpr uint32_t TM_U_HI = 448, TM_U_LO = 480;    // U^T [c][s], K = 64 (from MMA 3 on)
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls; a healthy MMA batch completes in microseconds
@@ -106,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(sm);
+    const uint32_t sb4 = sb >> 4;  // descriptor units
     float* s_beta = reinterpret_cast<float*>(sm + OFF_MISC);  // 64
     float* s_gam = s_beta + 64;                               // 128: e^{G_63}
     float* s_seg_a = s_gam + 128;                             // [4][128]: prod of alpha per token quarter
@@ -113,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     int* s_trk = reinterpret_cast<int*>(s_seg_i + 512);       // kTrackTc
     uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_trk + kTrackTc);  // [0]: MMA batches, [1]: state update
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 2);
+    int* s_abort = reinterpret_cast<int*>(s_tmem + 1);  // a wait that timed out inside a phase
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -149,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     if (tid == 0) {
         mbar_init(smem_u32(s_mbar), 1);
         mbar_init(smem_u32(s_mbar + 1), 1);
+        *s_abort = 0;
     }
     fence_before();
     __syncthreads();
@@ -186,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 
     // Raw tiles of chunk jj arrive by cp.async: q, k, g row-major (free once the
     // decayed operands of the previous chunk are written), v as the MN-major MMA
-    // operand (free after MMA 3).  Rows past the sequence are zero-filled.
+    // operand in the buffer of the chunk's parity (requested one chunk ahead).
+    // Rows past the sequence are zero-filled.
     auto prefetch_qkg = [&](int jj) {
         const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
 #pragma unroll
@@ -202,21 +211,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     };
     auto prefetch_v = [&](int jj) {
         const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
+        const uint32_t vb = OFF_V + (uint32_t)(jj & 1) * 16384;
 #pragma unroll
         for (int it = tid; it < 64 * 16; it += kThreads) {
             const int t = it >> 4, ch = it & 15;
             const bool ok = t < ln;
             const size_t e = ok ? ((size_t)(cn + t) * H + h) * kD + ch * 8 : 0;
-            cp_async16(sb + OFF_V + chunk_mn(ch * 8, t, 8192, 1024), gv + e, ok ? 16u : 0u);
+            cp_async16(sb + vb + chunk_mn(ch * 8, t, 8192, 1024), gv + e, ok ? 16u : 0u);
         }
     };
-    // raw beta of chunk jj (activated when the chunk starts, so the load is never waited on
-    // early); -inf marks padding rows, whose beta is 0
-    auto load_beta = [&](int jj) {
+    // raw beta of chunk jj, loaded one chunk ahead and activated when the chunk starts; rows
+    // past the sequence read its last token (never out of bounds) and get beta = 0 there.  No
+    // select on the loaded value, so nothing waits for the load before its use.
+    auto load_beta = [&](int jj) -> uint32_t {  // raw bf16 bits, widened when used
         const int cn = t0 + jj * kChunk, ln = min(kChunk, t1 - cn);
-        return tid < ln ? Act<true>::load1(p.beta_raw, (size_t)(cn + tid) * H + h) : -INFINITY;
+        return __ldg(static_cast<const unsigned short*>(p.beta_raw) + (size_t)(cn + min(tid, ln - 1)) * H + h);
     };
-    float beta_next = 0.f;
+    uint32_t beta_next = 0;
     if (n_chunks > 0) {
         prefetch_qkg(0);
         prefetch_v(0);
@@ -229,13 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         const int Lc = min(kChunk, t1 - c0);
         const bool more = j + 1 < n_chunks;
         cp_async_wait_all();
-        if (pending_s) {  // the previous state update still reads UT / KT and writes S
-            const bool ok = mbar_wait(mbar_s, phase_s, kWaitLimit);
-            phase_s ^= 1;
-            pending_s = false;
-            if (!ok) timed_out = true;
-        }
-        if (tid < 64) s_beta[tid] = tid < Lc ? beta_act(beta_next, p.flags) : 0.f;
+        if (tid < 64) s_beta[tid] = tid < Lc ? beta_act(__uint_as_float(beta_next << 16), p.flags) : 0.f;
         fence_before();
         if (__syncthreads_or(timed_out)) {
             timed_out = true;
@@ -243,6 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         }
         fence_after();
         if (tid < 64 && more) beta_next = load_beta(j + 1);  // lands during this chunk
+        const uint32_t v_cur = OFF_V + (uint32_t)(j & 1) * 16384;
+        if (more) {
+            prefetch_v(j + 1);  // the other buffer's last reader was chunk j - 1
+            cp_async_commit();
+        }
 
         // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
         float al[16], iv[16];
@@ -277,7 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
         if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
         if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
+        // the previous chunk's state update (U^T, KT operands; S) must be complete before the
+        // operand regions are rewritten and S is read: it ran behind this chunk's gate pass
+        if (pending_s) {
+            if (!mbar_wait(mbar_s, phase_s, kWaitLimit)) *s_abort = 1;
+            phase_s ^= 1;
+            pending_s = false;
+        }
+        fence_after();
         const int fallback = __syncthreads_or(bad);
+        if (*s_abort) {
+            timed_out = true;
+            break;
+        }
 
         if (!fallback) {
             // ---- L = [k; q] e^{G_t - G_31}, R = k e^{G_31 - G_s}: quarters 0, 1 backward
@@ -356,20 +378,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             fence_before();
             __syncthreads();
             fence_after();
-            // ---- MMA 1: [A; P] = [L_k; L_q] R^T
+            // ---- MMA 1: [A; P] = [L_k; L_q] R^T: L_hi [R_hi; R_lo]^T (N = 128) + L_lo R_hi^T
             if (tid == 0) {
-                const uint32_t id = idesc_bf16(128, 64, true, true, false);
+                const uint32_t id2 = idesc_bf16(128, 128, true, true, false);
+                const uint32_t id1 = idesc_bf16(128, 64, true, true, false);
 #pragma unroll
-                for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = sb + (pass == 2 ? X_L_LO : X_L_HI);
-                    const uint32_t b = sb + (pass == 1 ? X_R_LO : X_R_HI);
+                for (int s = 0; s < 8; ++s)
+                    mma(tmem + TM_AP, desc_mn4(sb4 + X_L_HI / 16, 1024, 2048, s),
+                        desc_mn4(sb4 + X_R_HI / 16, 16384, 1024, s), id2, s != 0);
 #pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma(tmem + TM_AP, desc_mn(a, 1024, 2048, s), desc_mn(b, 1024, 1024, s), id,
-                            (pass | s) != 0);
-                }
+                for (int s = 0; s < 8; ++s)
+                    mma(tmem + TM_AP, desc_mn4(sb4 + X_L_LO / 16, 1024, 2048, s),
+                        desc_mn4(sb4 + X_R_HI / 16, 16384, 1024, s), id1, 1u);
                 commit(mbar);
             }
+            // ---- state pass (overlaps MMA 1): S_j -> snapshot, bf16 hi/lo A operand in TMEM,
+            //      decay by e^{G_63}
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {  // 16 of this warp's 32 columns at a time
+                const int col0 = cq * 32 + 16 * hh;
+                float v[16];
+                ld16(tl + TM_S + col0, v);
+                for (int m = 0; m < p.M; ++m) {
+                    if (s_trk[m] != j) continue;
+                    float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
+                                  (size_t)row * kD + col0;
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; q4 += 4)
+                        reinterpret_cast<float4*>(snap + q4)[0] =
+                            make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
+                }
+                uint32_t sh[8], sl[8];
+#pragma unroll
+                for (int q2 = 0; q2 < 8; ++q2) split2(v[2 * q2], v[2 * q2 + 1], sh[q2], sl[q2]);
+                st8u(tl + TM_SA_HI + cq * 16 + 8 * hh, sh);
+                st8u(tl + TM_SA_LO + cq * 16 + 8 * hh, sl);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[q] *= s_gam[col0 + q];
+                st16f(tl + TM_S + col0, v);
+            }
+            wait_st();
             const bool ok1 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
@@ -381,8 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             // ---- A -> N = Diag(beta) A (strict lower, stored transposed: Nt[s][t] = N[t][s]),
             //      P -> bf16 operand (lower incl. diagonal)
             {
-                float v[16];
+                float v[16], v2[16];
                 ld16(tl + TM_AP + cq * 16, v);
+                ld16(tl + TM_AP + 64 + cq * 16, v2);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[q] += v2[q];
                 float* Nt = reinterpret_cast<float*>(sm + X_N);
                 if (quarter < 2) {
                     const int t = row;
@@ -402,12 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int c8 = 0; c8 < 2; ++c8) {
                         if constexpr (kBf16Out) {
-                            st16(sm, OFF_P + chunk_k(t, cq * 16 + 8 * c8, 64), pack8(v + 8 * c8));
+                            st16(sm, X_P + chunk_k(t, cq * 16 + 8 * c8, 64), pack8(v + 8 * c8));
                         } else {
                             uint4 hi, lo;
                             split8(v + 8 * c8, hi, lo);
-                            st16(sm, OFF_P + chunk_k(t, cq * 16 + 8 * c8, 64), hi);
-                            st16(sm, OFF_P_LO + chunk_k(t, cq * 16 + 8 * c8, 64), lo);
+                            st16(sm, X_P + chunk_k(t, cq * 16 + 8 * c8, 64), hi);
+                            st16(sm, X_P_LO + chunk_k(t, cq * 16 + 8 * c8, 64), lo);
                         }
                     }
                 }
@@ -561,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     } else {
                         split8(qg, hi, lo);
                         st16(sm, X_QG + chunk_mn(s0, ci, 1024, 1024), hi);
-                        st16(sm, X_QG_LO + chunk_mn(s0, ci, 1024, 1024), lo);
+                        st16(sm, OFF_QG_LO + chunk_mn(s0, ci, 1024, 1024), lo);
                     }
                 }
 #pragma unroll
@@ -591,55 +642,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 prefetch_qkg(j + 1);  // the raw q, k, g tiles of this chunk are consumed
                 cp_async_commit();
             }
-            // ---- MMA 2: W^T = KG T_b^T, U~^T = V^T T_b^T
+            // ---- MMA 2: W^T = KG T_b^T (into the O columns), U~^T = V^T [T_b hi; T_b lo]^T
+            //      (N = 128, into [U_a | U_b])
             if (tid == 0) {
                 const uint32_t idk = idesc_bf16(128, 64, false, false, false);
-                const uint32_t idv = idesc_bf16(128, 64, true, false, false);
+                const uint32_t idv = idesc_bf16(128, 128, true, false, false);
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
                     const uint32_t a = tmem + (pass == 2 ? TM_KG_LO : TM_KG_HI);
-                    const uint32_t b = sb + (pass == 1 ? OFF_TB_LO : OFF_TB_HI);
+                    const uint32_t b = sb4 + (pass == 1 ? OFF_TB_LO : OFF_TB_HI) / 16;
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma_ta(tmem + TM_WT, a + 8 * s, desc_k(b, 64, s), idk, (pass | s) != 0);
+                        mma_ta(tmem + TM_O, a + 8 * s, desc_k4(b, 64, s), idk, (pass | s) != 0);
                 }
                 commit(mbar);  // W^T only: U~^T (below) keeps running while W is extracted
 #pragma unroll
-                for (int pass = 0; pass < 2; ++pass) {
-                    const uint32_t b = sb + (pass == 1 ? OFF_TB_LO : OFF_TB_HI);
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma(tmem + TM_UT, desc_mn(sb + OFF_V, 8192, 1024, s), desc_k(b, 64, s), idv,
-                            (pass | s) != 0);
-                }
+                for (int s = 0; s < 4; ++s)
+                    mma(tmem + TM_UA, desc_mn4(sb4 + v_cur / 16, 8192, 1024, s),
+                        desc_k4(sb4 + OFF_TB_HI / 16, 128, s), idv, s != 0);
             }
-            // ---- state pass (overlaps MMA 2): S_j -> snapshot, bf16 hi/lo A operand in TMEM,
-            //      decay by e^{G_63}
-            {
-                const int col0 = cq * 32;
-                float v[32];
-                ld32(tl + TM_S + col0, v);
-                for (int m = 0; m < p.M; ++m) {
-                    if (s_trk[m] != j) continue;
-                    float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
-                                  (size_t)row * kD + col0;
-#pragma unroll
-                    for (int q4 = 0; q4 < 32; q4 += 4)
-                        reinterpret_cast<float4*>(snap + q4)[0] =
-                            make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
-                }
-                {
-                    uint32_t sh[16], sl[16];
-#pragma unroll
-                    for (int q2 = 0; q2 < 16; ++q2) split2(v[2 * q2], v[2 * q2 + 1], sh[q2], sl[q2]);
-                    st16u(tl + TM_SA_HI + cq * 16, sh);
-                    st16u(tl + TM_SA_LO + cq * 16, sl);
-                }
-#pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] *= s_gam[col0 + q];
-                st32(tl + TM_S + col0, v);
-            }
-            wait_st();
             const bool ok2 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
@@ -647,10 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 timed_out = true;
                 break;
             }
-            // ---- W^T (lanes i, columns t) -> -W operand (B, MN-major [i][t]) hi/lo
+            // ---- W^T (lanes i, columns t) -> -W operand (B, MN-major [i][t]) hi/lo; the O
+            //      columns are then cleared for MMA 3 to accumulate into
             {
                 float v[16];
-                ld16(tl + TM_WT + cq * 16, v);
+                ld16(tl + TM_O + cq * 16, v);
 #pragma unroll
                 for (int q = 0; q < 16; ++q) v[q] = -v[q];
 #pragma unroll
@@ -661,31 +683,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     st16(sm, X_W_HI + chunk_mn(t, row, 1024, 1024), hi);
                     st16(sm, X_W_LO + chunk_mn(t, row, 1024, 1024), lo);
                 }
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                st16f(tl + TM_O + cq * 16, v);
+                wait_st();
             }
             fence_async_smem();
             fence_before();
             __syncthreads();
             fence_after();
-            // ---- MMA 3: O^T = S^T QG^T ; U^T = U~^T + S^T (-W)^T (one commit frees the V tile
-            //      and the W / QG tiles)
+            // ---- MMA 3: [O | U_a | U_b] += S_hi^T [QG; -W_hi; -W_lo]^T (N = 192),
+            //      [O | U_a] += S_lo^T [QG; -W_hi]^T (N = 128); fp32 outputs also S_hi^T QG_lo^T.
+            //      U^T = U~^T - S^T W^T = U_a + U_b.  The commit also covers MMA 2's reads of V.
             if (tid == 0) {
-                const uint32_t idb = idesc_bf16(128, 64, false, true, false);
-                // bf16 outputs: S_hi QG_hi; fp32 outputs: + S_lo QG_hi + S_hi QG_lo
+                const uint32_t id3 = idesc_bf16(128, 192, false, true, false);
+                const uint32_t id2 = idesc_bf16(128, 128, false, true, false);
 #pragma unroll
-                for (int pass = 0; pass < (kBf16Out ? 1 : 3); ++pass) {
-                    const uint32_t a = tmem + (pass == 1 ? TM_SA_LO : TM_SA_HI);
-                    const uint32_t b = sb + (pass == 2 ? X_QG_LO : X_QG);
+                for (int s = 0; s < 8; ++s)
+                    mma_ta(tmem + TM_O, tmem + TM_SA_HI + 8 * s, desc_mn4(sb4 + X_QG / 16, 16384, 1024, s),
+                           id3, 1u);
 #pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma_ta(tmem + TM_OT, a + 8 * s, desc_mn(b, 1024, 1024, s), idb, (pass | s) != 0);
-                }
-#pragma unroll
-                for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = tmem + (pass == 2 ? TM_SA_LO : TM_SA_HI);
-                    const uint32_t b = sb + (pass == 1 ? X_W_LO : X_W_HI);
+                for (int s = 0; s < 8; ++s)
+                    mma_ta(tmem + TM_O, tmem + TM_SA_LO + 8 * s, desc_mn4(sb4 + X_QG / 16, 16384, 1024, s),
+                           id2, 1u);
+                if constexpr (!kBf16Out) {
+                    const uint32_t id1 = idesc_bf16(128, 64, false, true, false);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        mma_ta(tmem + TM_UT, a + 8 * s, desc_mn(b, 1024, 1024, s), idb, 1u);
+                        mma_ta(tmem + TM_O, tmem + TM_SA_HI + 8 * s,
+                               desc_mn4(sb4 + OFF_QG_LO / 16, 16384, 1024, s), id1, 1u);
                 }
                 commit(mbar);
             }
@@ -696,14 +722,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 timed_out = true;
                 break;
             }
-            if (more) {
-                prefetch_v(j + 1);  // MMA 2's reads of the V tile have completed
-                cp_async_commit();
-            }
             // ---- U^T (lanes c, columns s) -> bf16 hi/lo A operand in TMEM
             {
-                float v[16];
-                ld16(tl + TM_UT + cq * 16, v);
+                float v[16], v2[16];
+                ld16(tl + TM_UA + cq * 16, v);
+                ld16(tl + TM_UB + cq * 16, v2);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[q] += v2[q];
                 uint32_t uh[8], ul[8];
 #pragma unroll
                 for (int q2 = 0; q2 < 8; ++q2) split2(v[2 * q2], v[2 * q2 + 1], uh[q2], ul[q2]);
@@ -714,27 +739,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             fence_before();
             __syncthreads();
             fence_after();
-            // ---- MMA 4: O^T += U^T P^T ; S^T += U^T KT
+            // ---- MMA 4: [S | O] += U_hi^T [KT_hi; P]^T (N = 192); then the rest of the state
+            //      update, S^T += U_lo^T KT_hi + U_hi^T KT_lo, completes in the background
             if (tid == 0) {
-                const uint32_t ido = idesc_bf16(128, 64, false, false, false);
-                const uint32_t ids = idesc_bf16(128, 128, false, false, false);
+                const uint32_t id3 = idesc_bf16(128, 192, false, false, false);
+                const uint32_t id2 = idesc_bf16(128, 128, false, false, false);
 #pragma unroll
-                for (int pass = 0; pass < (kBf16Out ? 1 : 3); ++pass) {
-                    const uint32_t a = tmem + (pass == 1 ? TM_U_LO : TM_U_HI);
-                    const uint32_t b = sb + (pass == 2 ? OFF_P_LO : OFF_P);
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_ta(tmem + TM_OT, a + 8 * s, desc_k(b, 64, s), ido, 1u);
-                }
-                commit(mbar);  // the outputs; the state update below finishes in the background
-#pragma unroll
-                for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a = tmem + (pass == 2 ? TM_U_LO : TM_U_HI);
-                    const uint32_t b = sb + (pass == 1 ? X_KT_LO : X_KT_HI);
+                for (int s = 0; s < 4; ++s)
+                    mma_ta(tmem + TM_S, tmem + TM_U_HI + 8 * s, desc_k4(sb4 + X_KT_HI / 16, 192, s), id3, 1u);
+                if constexpr (!kBf16Out) {
+                    const uint32_t id1 = idesc_bf16(128, 64, false, false, false);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma_ta(tmem + TM_S, a + 8 * s, desc_k(b, 128, s), ids, 1u);
+                        mma_ta(tmem + TM_S, tmem + TM_U_LO + 8 * s, desc_k4(sb4 + X_KT_HI / 16, 192, s), id3,
+                               1u);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_ta(tmem + TM_O, tmem + TM_U_HI + 8 * s, desc_k4(sb4 + X_P_LO / 16, 64, s), id1, 1u);
                 }
+                commit(mbar);  // the outputs
+                if constexpr (kBf16Out) {
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_ta(tmem + TM_S, tmem + TM_U_LO + 8 * s, desc_k4(sb4 + X_KT_HI / 16, 128, s), id2,
+                               1u);
+                }
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ta(tmem + TM_S, tmem + TM_U_HI + 8 * s, desc_k4(sb4 + X_KT_LO / 16, 128, s), id2, 1u);
                 commit(mbar_s);
             }
             pending_s = true;
@@ -748,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             // ---- O^T (lanes c, columns t) -> out[t][h][c]
             {
                 float v[16];
-                ld16(tl + TM_OT + cq * 16, v);
+                ld16(tl + TM_O + cq * 16, v);
                 if constexpr (kBf16Out) {
                     // through shared memory (the T_b region, free now) for 16-byte row stores
                     __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TB_HI);
@@ -807,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     red[cq * 128 + c] = d1;
                     __syncthreads();
                     d1 = (red[c] + red[128 + c]) + (red[256 + c] + red[384 + c]);
-                    const float vt = bf16_at(sm, OFF_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
+                    const float vt = bf16_at(sm, v_cur + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
                     const float uu = s_beta[t] * (vt - d1);
                     float o = 0.f;
 #pragma unroll
@@ -830,7 +862,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             fence_after();
             if (more) {
                 prefetch_qkg(j + 1);
-                prefetch_v(j + 1);
                 cp_async_commit();
             }
         }

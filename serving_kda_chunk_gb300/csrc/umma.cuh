@@ -34,6 +34,22 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t base, uint32_t lbo, uint32_
     return desc(base + (uint32_t)(2 * s) * sbo, lbo, sbo);
 }
 
+// The same descriptors from a start address in 16-byte units (addr >> 4).  A
+// shared-memory address is below 2^18, so the field takes it without a mask and
+// a descriptor costs one add on top of fixed bits.
+__device__ __forceinline__ uint64_t desc4(uint32_t addr4, uint32_t lbo, uint32_t sbo) {
+    const uint32_t lo = addr4 + ((lbo >> 4) << 16);
+    const uint32_t hi = (sbo >> 4) | (1u << 14) | (2u << 29);
+    return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t desc_k4(uint32_t base4, int rows, int s) {
+    const int k0 = 16 * s;
+    return desc4(base4 + (uint32_t)(((k0 >> 6) * rows * 128 + (k0 & 63) * 2) >> 4), 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mn4(uint32_t base4, uint32_t lbo, uint32_t sbo, int s) {
+    return desc4(base4 + (uint32_t)(2 * s) * (sbo >> 4), lbo, sbo);
+}
+
 // Byte offset of the 16-byte chunk holding elements (r, k..k+7), k % 8 == 0,
 // of a K-major SW128 tile with `rows` rows.
 __device__ __forceinline__ uint32_t chunk_k(int r, int k, int rows) {
@@ -159,6 +175,18 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
 }
+__device__ __forceinline__ void st16f(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])));
+}
+
 // 8 / 16 consecutive 32-bit TMEM columns of this thread's lane (packed bf16 pairs).
 __device__ __forceinline__ void st8u(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
