@@ -237,8 +237,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, u
                  "r"(src_bytes)
                  : "memory");
 }
+// 4-byte asynchronous global -> shared copy (both addresses 4-byte aligned); src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async4(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// all but the most recently committed group
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 }  // namespace umma
 }  // namespace kda

@@ -11,16 +11,27 @@
 // (G_t = sum_{u<=t} g_u per key channel):
 //   u_t = beta_t (v_t - (k_t e^{G_t}) . S_0 - sum_{s<t} A_ts u_s),  A_ts = sum_i k_ti k_si e^{G_ti - G_si}
 //   o_t = (q_t e^{G_t}) . S_0 + sum_{s<=t} P_ts u_s,                P_ts = sum_i q_ti k_si e^{G_ti - G_si}
-// which is exactly K sequential steps of the recurrence.  One CTA per
-// (request, head), 128 threads.  The 2K dot products of every state row with
-// the gated keys and queries form one K S tile, D = S_0^T [K_G; Q_G]^T
-// (M = 128 value channels, N = 2K padded to 16, K = 128 key channels), run on
-// tcgen05 with the fp32 checkpoint split into bf16 hi + lo operands (three
-// passes, fp32 accumulation in TMEM).  The checkpoint is read once with
-// coalesced streaming loads straight into the swizzled operand tiles; the K x K
-// factors A and P are built from running products of alpha; each thread then
-// reads its row's 2K results from TMEM and solves the row's triangular system
-// in registers.  Loops are specialised on a compile-time bound of K.
+// which is exactly K sequential steps of the recurrence.
+//
+// The work is a stream of 64 KiB checkpoints, one per (request, head) unit, so
+// the kernel is persistent: one CTA per SM walks its units as a pipeline.
+//   - The checkpoint of unit j + 2 is requested by TMA (a two-dimensional
+//     tensor map over the pool, 128-byte swizzle, four [128 rows x 32 fp32]
+//     boxes) into a two-deep ring while unit j is worked on; the token rows
+//     arrive by cp.async one unit ahead.
+//   - Each thread converts 32 columns of one checkpoint row into bf16 hi + lo
+//     and stores them into TMEM, where they are the A operand (lane = value
+//     channel) of D = S_0^T [K_G; Q_G]^T (M = 128, N = 2K padded to 16,
+//     K = 128).  The hi / lo splits of the gated keys and queries lie side by
+//     side along N, so D takes 16 MMAs: S_hi [B_hi; B_lo]^T and S_lo B_hi^T.
+//   - The rows solve their triangular systems two units behind: while unit j
+//     is converted and its gated keys, queries and K x K factors are built
+//     (warps 4-15), warps 0-3 issue the MMAs of unit j - 1 and solve unit
+//     j - 2 from its 2K TMEM results.
+// TMEM holds two checkpoint operands and three accumulators.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kda_common.cuh"
 #include "kda_host.h"
 #include "umma.cuh"
@@ -28,291 +39,550 @@
 namespace kda {
 namespace {
 
-constexpr int kVThreads = 256;  // 128 rows / channels; the upper half helps stage the checkpoint
-constexpr int kMaxVerifyK = 16;
-
 using namespace umma;
 
-constexpr uint32_t kVWaitLimit = 1u << 22;  // polls; the MMA chain completes in microseconds
+constexpr int kVThreads = 512;          // 16 warps: four per TMEM lane quarter
+constexpr int kMaxVerifyK = 16;
+constexpr int kMaxUnitsPerCta = 512;    // per-CTA unit table in shared memory
+constexpr uint32_t kVWaitLimit = 1u << 22;  // polls; a checkpoint or an MMA batch lands in microseconds
 
-// KC: compile-time bound on K (2, 4, 8 or 16); NB = MMA N (K_G rows then Q_G rows).
+struct VerifyArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* beta_raw;
+    const void* gate_raw;
+    int32_t K;
+    const int32_t* q_len;
+    int32_t H;
+    float scale;
+    uint32_t flags;
+    int64_t P;
+    const int32_t* ckpt;
+    float* rec_u;
+    void* rec_kg;
+    void* out;
+    int32_t* dev_status;
+    int32_t n_units;
+};
+
+// Shared-memory plan for a compile-time bound KC on K and the activation element size ES.
+template <int KC, int ES>
+struct VLayout {
+    static constexpr int NB = 2 * KC < 16 ? 16 : 2 * KC;  // MMA N of one hi or lo half
+    static constexpr uint32_t RAW = 0;                      // 2 x 64 KiB checkpoint ring
+    static constexpr uint32_t BT = 131072;                  // 2 x [B_hi; B_lo] tiles, K-major
+    static constexpr uint32_t BT_BYTES = 2 * NB * 256;
+    static constexpr uint32_t KQG_BYTES = 3 * KC * 128 * ES;  // k, q, g rows [3][KC][128]
+    // two k, q, g buffers (rows requested two units ahead) where they fit, else one
+    static constexpr int NKQG = 131072 + 2 * BT_BYTES + 2 * KQG_BYTES + 3 * KC * 128 * ES + 28 * KC * KC +
+                                            20 * KC + kMaxUnitsPerCta * 8 + 64 + 1024 <= 232448 ? 2 : 1;
+    static constexpr uint32_t KQG = BT + 2 * BT_BYTES;
+    static constexpr uint32_t VB = KQG + NKQG * KQG_BYTES;  // 3 x v rows [KC][128]
+    static constexpr uint32_t VB_BYTES = KC * 128 * ES;
+    static constexpr uint32_t AP = VB + 3 * VB_BYTES;       // 3 x [KC][KC] fp32
+    static constexpr uint32_t RED = AP + 3 * KC * KC * 4;   // [4 warps][KC][KC]
+    static constexpr uint32_t BETA = RED + 4 * KC * KC * 4; // 3 x [KC] activated beta
+    static constexpr uint32_t BRAW = BETA + 3 * KC * 4;     // NKQG x [KC] 4-byte words holding raw beta
+    static constexpr uint32_t META = BRAW + 2 * KC * 4;     // [kMaxUnitsPerCta] (slot, q_len)
+    static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8;  // raw full [2], mma done [3]
+    static constexpr uint32_t END = MBAR + 5 * 8 + 24;
+    static constexpr size_t SMEM = END + 1024;  // + alignment slack
+};
+
+// TMEM columns: checkpoint operands [S hi (64) | S lo (64)] x 2, then three accumulators
+// [D_hi | D_lo] of 2 NB columns each.
+constexpr uint32_t TV_SA = 0, TV_D = 256;
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
+                 : "memory");
+}
+
+// One box of the tensor map at (x = column, y = row) into shared memory, completing on mbar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bar_named(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <bool kBf16>
+__device__ __forceinline__ float act_at(const uint8_t* p, int idx) {
+    if constexpr (kBf16)
+        return __uint_as_float((uint32_t)(reinterpret_cast<const uint16_t*>(p)[idx]) << 16);
+    else
+        return reinterpret_cast<const float*>(p)[idx];
+}
+
 template <int KC, bool kBf16In, bool kBf16Out>
-__global__ void __launch_bounds__(kVThreads) verify_kernel(
-    const void* __restrict__ q, const void* __restrict__ k, const void* __restrict__ v,
-    const void* __restrict__ beta_raw, const void* __restrict__ gate_raw, int32_t K,
-    const int32_t* __restrict__ q_len, int32_t H, float scale, uint32_t flags,
-    const float* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
-    float* __restrict__ rec_u, void* __restrict__ rec_kg, void* __restrict__ out,
-    int32_t* __restrict__ dev_status) {
-    using A = Act<kBf16In>;
-    constexpr int NB = 2 * KC < 16 ? 16 : 2 * KC;
-    constexpr uint32_t ST_HI = 0, ST_LO = 32768, KQ_HI = 65536, KQ_LO = 65536 + NB * 256;
-    constexpr uint32_t MISC = KQ_LO + NB * 256;
+__global__ void __launch_bounds__(kVThreads, 1)
+    verify_kernel(const __grid_constant__ CUtensorMap tmap, const VerifyArgs a) {
+    constexpr int ES = kBf16In ? 2 : 4;
+    using Lay = VLayout<KC, ES>;
+    constexpr int NB = Lay::NB;
+    constexpr int CPR = 128 * ES / 16;  // 16-byte chunks per token row
+    constexpr int NKQG = Lay::NKQG;     // k, q, g rows are requested NKQG units ahead
+    static_assert(TV_D + 3 * 2 * NB <= 512, "TMEM plan");
+
     extern __shared__ uint8_t vraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vraw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(sm);
-    float(*AP)[KC] = reinterpret_cast<float(*)[KC]>(sm + MISC);               // A at [t][s], P at [s][t]
-    float(*red)[KC][KC] = reinterpret_cast<float(*)[KC][KC]>(sm + MISC + KC * KC * 4);
-    float* sbeta = reinterpret_cast<float*>(sm + MISC + 5 * KC * KC * 4);
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + MISC + 5 * KC * KC * 4 + KC * 4 + 8 -
-                                                 ((5 * KC * KC * 4 + KC * 4) & 7));
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbar + 1);
+    const uint32_t sb4 = sb >> 4;
+    int2* meta = reinterpret_cast<int2*>(sm + Lay::META);
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sm + Lay::MBAR);  // raw full [2], mma done [3]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbars + 5);
+    float* sbeta = reinterpret_cast<float*>(sm + Lay::BETA);
 
-    const int unit = blockIdx.x;
-    const int r = unit / H, h = unit - r * H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot = ckpt[r];
-    int ql = q_len ? q_len[r] : K;
-    const bool slot_ok = slot >= 0 && slot < P;
-    const bool len_ok = ql >= 0 && ql <= K;
-    if (!(slot_ok && len_ok)) {
-        if (tid == 0 && h == 0) {
-            if (slot >= P) report(dev_status, KDA_DEV_BAD_SLOT);
-            if (!len_ok) report(dev_status, KDA_DEV_BAD_ACCEPT);
-        }
-        ql = 0;
-    }
-    const size_t rec0 = ((size_t)r * H + h) * K;
-    if (ql == 0) {
-        if (tid < kD) {
-            for (int t = 0; t < K; ++t) {
-                const size_t th = ((size_t)r * K + t) * H + h;
-                store1<kBf16Out>(out, th * kD + tid, 0.f);
-                rec_u[(rec0 + t) * kD + tid] = 0.f;
-                if (tid < 64) A::zero4(rec_kg, (rec0 + t) * 2 * kD + 4 * tid);
-            }
-        }
-        return;
-    }
-    // ---- every load of this unit goes out first: the token values of channel / row
-    //      i = tid (threads < 128) and the whole checkpoint (16 x 16 B per thread)
-    const int i = tid;
-    float kt[KC], qt[KC], gt[KC], vt[KC];
-    if (tid < kD) {
-#pragma unroll
-        for (int t = 0; t < KC; ++t) {
-            kt[t] = qt[t] = gt[t] = vt[t] = 0.f;
-            if (t < ql) {
-                const size_t th = ((size_t)r * K + t) * H + h;
-                kt[t] = A::load1(k, th * kD + i);
-                qt[t] = A::load1(q, th * kD + i);
-                gt[t] = A::load1(gate_raw, th * kD + i);
-                vt[t] = A::load1(v, th * kD + i);
-            }
-        }
-    }
-    const float braw = (tid >= kD && tid - kD < ql)
-                           ? A::load1(beta_raw, ((size_t)r * K + (tid - kD)) * H + h) : 0.f;
-    const float4* src = reinterpret_cast<const float4*>(pool + ((size_t)slot * H + h) * (kD * kD));
-    float4 x[16];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int u = tid + kVThreads * j;  // 8-float unit: row u >> 4, columns (u & 15) * 8
-        x[2 * j] = __ldcs(src + 2 * u);
-        x[2 * j + 1] = __ldcs(src + 2 * u + 1);
-    }
-    if (warp == 0) tmem_alloc(smem_u32(s_tmem), 32);
-    if (tid == 0) mbar_init(smem_u32(mbar), 1);
-    if (tid >= kD && tid - kD < ql) sbeta[tid - kD] = beta_act(braw, flags);
-    if (tid >= kD && tid < kD + 64) {
-        // records: key and raw gate exactly as given (upper threads, off the critical path)
-        const int e = tid - kD;
-        for (int t = 0; t < ql; ++t) {
-            const size_t th = ((size_t)r * K + t) * H + h;
-            if (e < 32)
-                A::copy4(rec_kg, (rec0 + t) * 2 * kD + 4 * e, k, th * kD + 4 * e);
-            else
-                A::copy4(rec_kg, (rec0 + t) * 2 * kD + kD + 4 * (e - 32), gate_raw, th * kD + 4 * (e - 32));
-        }
-    }
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int H = a.H, K = a.K;
+    const int G = gridDim.x;
+    const int nu = (a.n_units - (int)blockIdx.x + G - 1) / G;  // units of this CTA
 
-    // ---- checkpoint S_0^T (rows c, key channels i) -> bf16 hi/lo K-major operand tiles
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int u = tid + kVThreads * j;
-        const int c = u >> 4, g = (u & 15) * 8;
-        const float e[8] = {x[2 * j].x, x[2 * j].y, x[2 * j].z, x[2 * j].w,
-                            x[2 * j + 1].x, x[2 * j + 1].y, x[2 * j + 1].z, x[2 * j + 1].w};
-        uint4 hi, lo;
-        split8(e, hi, lo);
-        *reinterpret_cast<uint4*>(sm + ST_HI + chunk_k(c, g, 128)) = hi;
-        *reinterpret_cast<uint4*>(sm + ST_LO + chunk_k(c, g, 128)) = lo;
-    }
-
-    // ---- per key channel i: gated keys (rows 0..KC-1) and queries (rows KC..2KC-1) of the
-    //      B operand, the records, and the K x K pair factors
-    if (tid < kD) {
-        float at[KC];
-        float cum = 1.f;  // e^{G_t}
-        uint16_t* bh = reinterpret_cast<uint16_t*>(sm + KQ_HI);
-        uint16_t* bl = reinterpret_cast<uint16_t*>(sm + KQ_LO);
-        auto put = [&](int n, float val) {
-            const __nv_bfloat16 hh = __float2bfloat16_rn(val);
-            const __nv_bfloat16 ll = __float2bfloat16_rn(val - __bfloat162float(hh));
-            const uint32_t off = (chunk_k(n, i & ~7, NB) + (i & 7) * 2) >> 1;
-            bh[off] = __bfloat16_as_ushort(hh);
-            bl[off] = __bfloat16_as_ushort(ll);
-        };
-#pragma unroll
-        for (int t = 0; t < KC; ++t) {
-            qt[t] *= scale;
-            at[t] = 1.f;
-            if (t < ql) {
-                at[t] = expf(gate_log(gt[t], flags));
-                cum *= at[t];
-            }
-            put(t, kt[t] * cum);
-            put(KC + t, qt[t] * cum);
+    // ---- unit table: checkpoint slot and accepted length (0 = skipped)
+    for (int idx = tid; idx < nu; idx += kVThreads) {
+        const int unit = blockIdx.x + idx * G;
+        const int r = unit / H, h = unit - r * H;
+        const int slot = a.ckpt[r];
+        int ql = a.q_len ? a.q_len[r] : K;
+        const bool slot_ok = slot >= 0 && slot < a.P;
+        const bool len_ok = ql >= 0 && ql <= K;
+        if (h == 0) {
+            if (slot >= a.P) report(a.dev_status, KDA_DEV_BAD_SLOT);
+            if (!len_ok) report(a.dev_status, KDA_DEV_BAD_ACCEPT);
         }
-#pragma unroll
-        for (int n = 2 * KC; n < NB; ++n) put(n, 0.f);
-        // pair sums over channels, e^{G_t - G_s} as running products of alpha:
-        // value [a][b] = P_ab (a <= b) or A_ab (a > b), summed over the warp's 32 channels
-        if constexpr (KC <= 8) {
-            constexpr int NV = KC * KC < 32 ? 32 : KC * KC;
-            float vals[NV];
-#pragma unroll
-            for (int e = 0; e < NV; ++e) vals[e] = 0.f;
-#pragma unroll
-            for (int s0 = 0; s0 < KC; ++s0) {
-                float dec = 1.f;
-#pragma unroll
-                for (int t = s0; t < KC; ++t) {
-                    if (t > s0) dec *= at[t];
-                    const bool live = t < ql;
-                    vals[s0 * KC + t] = live ? qt[t] * kt[s0] * dec : 0.f;
-                    if (t > s0) vals[t * KC + s0] = live ? kt[t] * kt[s0] * dec : 0.f;
-                }
-            }
-            // butterfly reduce-scatter: lane l ends with the totals of entries l*M .. l*M+M-1
-            int n = NV;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const bool upper = (lane & off) != 0;
-                const int half = n / 2;
-#pragma unroll
-                for (int e = 0; e < NV / 2; ++e) {
-                    if (e < half) {
-                        const float send = upper ? vals[e] : vals[e + half];
-                        const float keep = upper ? vals[e + half] : vals[e];
-                        vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                    }
-                }
-                n = half;
-            }
-            constexpr int M = NV / 32;
-#pragma unroll
-            for (int e = 0; e < M; ++e) {
-                const int idx = lane * M + e;
-                if (idx < KC * KC) red[warp][idx / KC][idx % KC] = vals[e];
-            }
-        } else {
-#pragma unroll
-            for (int s0 = 0; s0 < KC; ++s0) {
-                if (s0 >= ql) continue;
-                float dec = 1.f;
-#pragma unroll
-                for (int t = s0; t < KC; ++t) {
-                    if (t >= ql) continue;
-                    if (t > s0) dec *= at[t];
-                    const float pp = warp_sum(qt[t] * kt[s0] * dec);
-                    if (lane == 0) red[warp][s0][t] = pp;
-                    if (t > s0) {
-                        const float pa = warp_sum(kt[t] * kt[s0] * dec);
-                        if (lane == 0) red[warp][t][s0] = pa;
-                    }
-                }
-            }
-        }
+        if (!(slot_ok && len_ok)) ql = 0;
+        meta[idx] = make_int2(slot, ql);
     }
-    fence_async_smem();
+    if (warp == 0) tmem_alloc(smem_u32(s_tmem), 512);
+    if (tid == 0) {
+        for (int b = 0; b < 5; ++b) mbar_init(smem_u32(mbars + b), 1);
+    }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_tmem;
-    // ---- D[c][n] = sum_i S_0^T[c][i] B[n][i]: hi*hi + lo*hi + hi*lo
-    if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, NB, false, false, false);
-#pragma unroll
-        for (int pass = 0; pass < 3; ++pass) {
-            const uint32_t a = sb + (pass == 1 ? ST_LO : ST_HI);
-            const uint32_t b = sb + (pass == 2 ? KQ_LO : KQ_HI);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma(tmem, desc_k(a, 128, s), desc_k(b, NB, s), id, (pass | s) != 0);
-        }
-        commit(smem_u32(mbar));
-    }
-    for (int e = tid; e < KC * KC; e += kVThreads) {
-        const int a = e / KC, b = e - a * KC;
-        AP[a][b] = red[0][a][b] + red[1][a][b] + red[2][a][b] + red[3][a][b];
-    }
-    __syncthreads();
-    const bool ok = mbar_wait(smem_u32(mbar), 0, kVWaitLimit);
-    fence_after();
-    const bool any_timeout = __syncthreads_or(!ok);
-    float d[32];
-    if (!any_timeout && warp < 4) ld32(tmem + ((uint32_t)(warp * 32) << 16), d);
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    // ---- triangular solve for row c, outputs and correction records
-    const int c = tid;
-    float u[KC];
+    auto unit_rh = [&](int idx, int& r, int& h) {
+        const int unit = blockIdx.x + idx * G;
+        r = unit / H;
+        h = unit - r * H;
+    };
+    // checkpoint of unit idx -> ring buffer idx & 1 (one thread; the unit must have q_len > 0)
+    auto request_ckpt = [&](int idx) {
+        int r, h;
+        unit_rh(idx, r, h);
+        const uint32_t mb = smem_u32(mbars + (idx & 1));
+        const uint32_t dst = sb + Lay::RAW + (uint32_t)(idx & 1) * 65536u;
+        const int y = (meta[idx].x * H + h) * 128;
+        mbar_expect_tx(mb, 65536u);
 #pragma unroll
-    for (int t = 0; t < KC; ++t) {
-        u[t] = 0.f;
-        if (t >= K || tid >= kD) continue;
-        const size_t th = ((size_t)r * K + t) * H + h;
-        if (t < ql && !any_timeout) {
-            float acc = d[t];
-#pragma unroll
-            for (int s0 = 0; s0 < t; ++s0) acc = fmaf(AP[t][s0], u[s0], acc);
-            u[t] = sbeta[t] * (vt[t] - acc);
-            float o = d[KC + t];
-#pragma unroll
-            for (int s0 = 0; s0 <= t; ++s0) o = fmaf(AP[s0][t], u[s0], o);
-            store1<kBf16Out>(out, th * kD + c, o);
-            rec_u[(rec0 + t) * kD + c] = u[t];
-        } else {
-            store1<kBf16Out>(out, th * kD + c, 0.f);
-            rec_u[(rec0 + t) * kD + c] = 0.f;
-            if (c < 64) A::zero4(rec_kg, (rec0 + t) * 2 * kD + 4 * c);
+        for (int p = 0; p < 4; ++p) tma_load_2d(dst + p * 16384, &tmap, 32 * p, y, mb);
+    };
+    // k, q, g rows and the raw beta words of unit idx -> KQG / BRAW [idx % NKQG] (all threads);
+    // v rows -> VB[idx % 3] (warps 0-3); rows past the accepted length are zero-filled
+    auto kqg_at = [&](int idx) { return Lay::KQG + (uint32_t)(idx % NKQG) * Lay::KQG_BYTES; };
+    auto prefetch_kqg = [&](int idx) {
+        const int ql = meta[idx].y;
+        int r, h;
+        unit_rh(idx, r, h);
+        for (int e2 = tid; e2 < 3 * KC * CPR; e2 += kVThreads) {
+            const int x = e2 / (KC * CPR), rem = e2 - x * KC * CPR, t = rem / CPR, ch = rem - t * CPR;
+            const void* src = x == 0 ? a.k : x == 1 ? a.q : a.gate_raw;
+            const bool ok = t < ql;
+            const size_t e = ok ? (((size_t)r * K + t) * H + h) * 128 : 0;
+            cp_async16(sb + kqg_at(idx) + (uint32_t)((x * KC + t) * 128 * ES + ch * 16),
+                       static_cast<const uint8_t*>(src) + e * ES + (ok ? ch * 16 : 0), ok ? 16u : 0u);
         }
+        if (tid < KC) {  // the aligned 4-byte word holding beta of position tid
+            const bool ok = tid < ql;
+            const size_t e = ok ? ((size_t)r * K + tid) * H + h : 0;
+            cp_async4(sb + Lay::BRAW + (uint32_t)((idx % NKQG) * KC + tid) * 4,
+                      static_cast<const uint8_t*>(a.beta_raw) + ((e * ES) & ~(size_t)3), ok ? 4u : 0u);
+        }
+    };
+    auto prefetch_v = [&](int idx) {
+        const int ql = meta[idx].y;
+        int r, h;
+        unit_rh(idx, r, h);
+        for (int e2 = tid; e2 < KC * CPR; e2 += 128) {
+            const int t = e2 / CPR, ch = e2 - t * CPR;
+            const bool ok = t < ql;
+            const size_t e = ok ? (((size_t)r * K + t) * H + h) * 128 : 0;
+            cp_async16(sb + Lay::VB + (uint32_t)(idx % 3) * Lay::VB_BYTES + (uint32_t)(t * 128 * ES + ch * 16),
+                       static_cast<const uint8_t*>(a.v) + e * ES + (ok ? ch * 16 : 0), ok ? 16u : 0u);
+        }
+    };
+    // checkpoint rows of ring buffer b, column quarter cq_ -> TMEM operand buffer b (hi | lo)
+    auto convert = [&](int b, int cq_) {
+        const uint8_t* raw = sm + Lay::RAW + (uint32_t)b * 65536u + (uint32_t)cq_ * 16384u;
+        float x[32];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float4 f = *reinterpret_cast<const float4*>(raw + row * 128 + ((m ^ (row & 7)) << 4));
+            x[4 * m] = f.x;
+            x[4 * m + 1] = f.y;
+            x[4 * m + 2] = f.z;
+            x[4 * m + 3] = f.w;
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t sh[8], sl[8];
+#pragma unroll
+            for (int q2 = 0; q2 < 8; ++q2) split2(x[16 * hh + 2 * q2], x[16 * hh + 2 * q2 + 1], sh[q2], sl[q2]);
+            const uint32_t col = TV_SA + (uint32_t)b * 128u + (uint32_t)cq_ * 16u + 8u * hh;
+            st8u(tl + col, sh);
+            st8u(tl + col + 64, sl);
+        }
+    };
+
+    // ---- prologue
+    uint32_t raw_pend = 0, mma_pend = 0;  // issued and not yet waited (raw: per ring buffer; mma: per unit % 3)
+    if (meta[0].y > 0) {
+        if (tid == 0) request_ckpt(0);
+        raw_pend |= 1u;
     }
-    if (any_timeout && tid == 0) report(dev_status, KDA_DEV_TIMEOUT);
+    if (nu > 1 && meta[1].y > 0) {
+        if (tid == 0) request_ckpt(1);
+        raw_pend |= 2u;
+    }
+    prefetch_kqg(0);
+    if (warp < 4) prefetch_v(0);
+    cp_async_commit();
+    if (NKQG == 2 && nu > 1) prefetch_kqg(1);
+    cp_async_commit();
+    uint32_t ph_raw = 0, ph_mma = 0;  // phase bits per barrier
+    bool timed_out = false;
+
+    for (int it = 0; it < nu + 2; ++it) {
+        const bool have = it < nu;
+        const int buf = it & 1;
+        const int ql = have ? meta[it].y : 0;
+        // ---- this unit's token rows (all but the most recent cp.async group when the k, q, g
+        //      rows run two units ahead) and its checkpoint
+        if (have) {
+            if constexpr (NKQG == 2)
+                cp_async_wait_1();
+            else
+                cp_async_wait_all();
+            if (raw_pend & (1u << buf)) {
+                if (!mbar_wait(smem_u32(mbars + buf), (ph_raw >> buf) & 1u, kVWaitLimit)) timed_out = true;
+                ph_raw ^= 1u << buf;
+                raw_pend &= ~(1u << buf);
+            }
+        } else {
+            cp_async_wait_all();
+        }
+        fence_before();
+        if (__syncthreads_or(timed_out)) {
+            timed_out = true;
+            break;
+        }
+        fence_after();
+        if (it >= 1 && it <= nu && meta[it - 1].y > 0) mma_pend |= 1u << ((it - 1) % 3);
+
+        if (warp < 4) {
+            // ---- MMAs of the previous unit: D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
+            if (tid == 0 && it >= 1 && it <= nu && meta[it - 1].y > 0) {
+                const int u = it - 1, ub = u & 1;
+                const uint32_t id2 = idesc_bf16(128, 2 * NB, false, false, false);
+                const uint32_t id1 = idesc_bf16(128, NB, false, false, false);
+                const uint32_t d = tmem + TV_D + (uint32_t)(u % 3) * (2 * NB);
+                const uint32_t sa = tmem + TV_SA + (uint32_t)ub * 128u;
+                const uint32_t b4 = sb4 + (Lay::BT + (uint32_t)ub * Lay::BT_BYTES) / 16;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) mma_ta(d, sa + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) mma_ta(d, sa + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
+                commit(smem_u32(mbars + 2 + u % 3));
+            }
+            // ---- rows of the unit two back: triangular solve, outputs, u records
+            if (it >= 2) {
+                const int pj = it - 2, pb = pj % 3;
+                const int pql = meta[pj].y;
+                int r, h;
+                unit_rh(pj, r, h);
+                const size_t rec0 = ((size_t)r * H + h) * K;
+                const int c = tid;
+                float d[2 * NB];
+                bool ok = true;
+                if (mma_pend & (1u << pb)) {
+                    ok = mbar_wait(smem_u32(mbars + 2 + pb), (ph_mma >> pb) & 1u, kVWaitLimit);
+                    ph_mma ^= 1u << pb;
+                    mma_pend &= ~(1u << pb);
+                    fence_after();
+                    if (ok) {
+#pragma unroll
+                        for (int q16 = 0; q16 < 2 * NB / 16; ++q16) {
+                            float v16[16];
+                            ld16(tl + TV_D + (uint32_t)pb * (2 * NB) + 16 * q16, v16);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) d[16 * q16 + e] = v16[e];
+                        }
+                    }
+                }
+                if (!ok) timed_out = true;
+                const float* ap = reinterpret_cast<const float*>(sm + Lay::AP) + pb * KC * KC;
+                const uint8_t* vb = sm + Lay::VB + (uint32_t)pb * Lay::VB_BYTES;
+                float u[KC];
+#pragma unroll
+                for (int t = 0; t < KC; ++t) {
+                    u[t] = 0.f;
+                    if (t >= K) continue;
+                    const size_t th = ((size_t)r * K + t) * H + h;
+                    float o = 0.f;
+                    if (t < pql && ok) {
+                        float acc = d[t] + d[NB + t];
+#pragma unroll
+                        for (int s0 = 0; s0 < t; ++s0) acc = fmaf(ap[t * KC + s0], u[s0], acc);
+                        u[t] = sbeta[pb * KC + t] * (act_at<kBf16In>(vb, t * 128 + c) - acc);
+                        o = d[KC + t] + d[NB + KC + t];
+#pragma unroll
+                        for (int s0 = 0; s0 <= t; ++s0) o = fmaf(ap[s0 * KC + t], u[s0], o);
+                    }
+                    store1<kBf16Out>(a.out, th * kD + c, o);
+                    a.rec_u[(rec0 + t) * kD + c] = u[t];
+                }
+                fence_before();
+                bar_named(2, 128);  // every row of the unit two back has read its v
+            }
+            if (it + 1 < nu) prefetch_v(it + 1);  // into the v buffer of the unit two back
+        } else if (have) {
+            // ---- warps 4-15: this unit's checkpoint rows into TMEM, once the MMAs of the unit
+            //      two back (same operand buffers) have completed
+            if (it >= 2 && meta[it - 2].y > 0) {
+                const int pb = (it - 2) % 3;
+                if (!mbar_wait(smem_u32(mbars + 2 + pb), (ph_mma >> pb) & 1u, kVWaitLimit)) timed_out = true;
+                ph_mma ^= 1u << pb;
+                fence_after();
+            }
+            if (ql > 0) {
+                if (warp < 12) {
+                    convert(buf, warp < 8 ? 1 : 2);
+                } else {
+                    convert(buf, 0);
+                    convert(buf, 3);
+                }
+                wait_st();
+            }
+            if (warp < 12) {
+                // channel i: the gates as running products of alpha; warps 4-7 write the gated
+                // keys / queries (B tile), warps 8-11 the K x K pair factors
+                const int i = tid & 127;
+                const uint8_t* kqg = sm + kqg_at(it);
+                float kt[KC], qt[KC], at[KC];
+#pragma unroll
+                for (int t = 0; t < KC; ++t) {
+                    kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
+                    qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
+                    at[t] = 1.f;
+                    if (t < ql) {
+                        // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
+                        const float gx = act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i);
+                        at[t] = (a.flags & KDA_GATE_LOG) ? __expf(gx) : __fdividef(1.f, 1.f + __expf(gx));
+                    }
+                }
+                if (warp < 8) {
+                    uint16_t* bt = reinterpret_cast<uint16_t*>(sm + Lay::BT + (uint32_t)buf * Lay::BT_BYTES);
+                    auto put = [&](int n, float val) {
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(val - __bfloat162float(hi));
+                        bt[(chunk_k(n, i & ~7, 2 * NB) + (i & 7) * 2) >> 1] = __bfloat16_as_ushort(hi);
+                        bt[(chunk_k(NB + n, i & ~7, 2 * NB) + (i & 7) * 2) >> 1] = __bfloat16_as_ushort(lo);
+                    };
+                    float cum = 1.f;  // e^{G_t}
+#pragma unroll
+                    for (int t = 0; t < KC; ++t) {
+                        cum *= at[t];
+                        put(t, kt[t] * cum);
+                        put(KC + t, qt[t] * cum);
+                    }
+#pragma unroll
+                    for (int n = 2 * KC; n < NB; ++n) put(n, 0.f);
+                } else {
+                    const int wg = warp - 8;
+                    float(*red)[KC][KC] = reinterpret_cast<float(*)[KC][KC]>(sm + Lay::RED);
+                    // pair sums over channels, e^{G_t - G_s} as running products of alpha:
+                    // value [a][b] = P_ab (a <= b) or A_ab (a > b), summed over the warp's 32 channels
+                    if constexpr (KC <= 8) {
+                        constexpr int NV = KC * KC < 32 ? 32 : KC * KC;
+                        float vals[NV];
+#pragma unroll
+                        for (int e = 0; e < NV; ++e) vals[e] = 0.f;
+#pragma unroll
+                        for (int s0 = 0; s0 < KC; ++s0) {
+                            float dec = 1.f;
+#pragma unroll
+                            for (int t = s0; t < KC; ++t) {
+                                if (t > s0) dec *= at[t];
+                                const bool live = t < ql;
+                                vals[s0 * KC + t] = live ? qt[t] * kt[s0] * dec : 0.f;
+                                if (t > s0) vals[t * KC + s0] = live ? kt[t] * kt[s0] * dec : 0.f;
+                            }
+                        }
+                        // butterfly reduce-scatter: lane l ends with the totals of entries l*M .. l*M+M-1
+                        int nn = NV;
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1) {
+                            const bool upper = (lane & off) != 0;
+                            const int half = nn / 2;
+#pragma unroll
+                            for (int e = 0; e < NV / 2; ++e) {
+                                if (e < half) {
+                                    const float send = upper ? vals[e] : vals[e + half];
+                                    const float keep = upper ? vals[e + half] : vals[e];
+                                    vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                }
+                            }
+                            nn = half;
+                        }
+                        constexpr int M = NV / 32;
+#pragma unroll
+                        for (int e = 0; e < M; ++e) {
+                            const int idx = lane * M + e;
+                            if (idx < KC * KC) red[wg][idx / KC][idx % KC] = vals[e];
+                        }
+                    } else {
+#pragma unroll
+                        for (int s0 = 0; s0 < KC; ++s0) {
+                            float dec = 1.f;
+#pragma unroll
+                            for (int t = s0; t < KC; ++t) {
+                                if (t > s0) dec *= at[t];
+                                const bool live = t < ql;
+                                const float pp = warp_sum(live ? qt[t] * kt[s0] * dec : 0.f);
+                                if (lane == 0) red[wg][s0][t] = pp;
+                                if (t > s0) {
+                                    const float pa = warp_sum(live ? kt[t] * kt[s0] * dec : 0.f);
+                                    if (lane == 0) red[wg][t][s0] = pa;
+                                }
+                            }
+                        }
+                    }
+                    bar_named(1, 128);  // warps 8-11
+                    float* ap = reinterpret_cast<float*>(sm + Lay::AP) + (it % 3) * KC * KC;
+                    for (int e = i; e < KC * KC; e += 128) {
+                        const int x0 = e / KC, x1 = e - x0 * KC;
+                        ap[e] = (red[0][x0][x1] + red[1][x0][x1]) + (red[2][x0][x1] + red[3][x0][x1]);
+                    }
+                }
+            } else {
+                // warps 12-15: activated beta, and the key and raw gate records exactly as given
+                // (zeros past the accepted length)
+                int r, h;
+                unit_rh(it, r, h);
+                if (tid - 384 < KC) {
+                    const int t = tid - 384;
+                    float bv = 0.f;
+                    if (t < ql) {
+                        const uint32_t w = reinterpret_cast<const uint32_t*>(sm + Lay::BRAW)[(it % NKQG) * KC + t];
+                        const size_t e = ((size_t)r * K + t) * H + h;
+                        bv = beta_act(kBf16In ? __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16))
+                                              : __uint_as_float(w),
+                                      a.flags);
+                    }
+                    sbeta[(it % 3) * KC + t] = bv;
+                }
+                const size_t rec0 = ((size_t)r * H + h) * K;
+                for (int e = tid - 384; e < 2 * K * CPR; e += 128) {
+                    const int t = e / (2 * CPR), rem = e - t * 2 * CPR, half = rem / CPR, ch = rem - half * CPR;
+                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                    if (t < ql)
+                        val = *reinterpret_cast<const uint4*>(
+                            sm + kqg_at(it) + (uint32_t)(((half ? 2 * KC : 0) + t) * 128 * ES + ch * 16));
+                    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.rec_kg) +
+                                              ((rec0 + t) * 2 * 128 + half * 128) * ES + ch * 16) = val;
+                }
+            }
+        }
+        fence_async_smem();
+        fence_before();
+        __syncthreads();
+        fence_after();
+        // ---- the checkpoint two units ahead (into the ring buffer read above) and the k, q, g
+        //      rows NKQG units ahead
+        if (have) {
+            if (it + 2 < nu && meta[it + 2].y > 0) {
+                if (tid == 0) {
+                    fence_async_smem();
+                    request_ckpt(it + 2);
+                }
+                raw_pend |= 1u << buf;
+            }
+            if (it + NKQG < nu) prefetch_kqg(it + NKQG);
+        }
+        cp_async_commit();
+    }
+    cp_async_wait_all();
+    timed_out = __syncthreads_or(timed_out);
+    if (timed_out) {
+        if (tid == 0) report(a.dev_status, KDA_DEV_TIMEOUT);
+        // bounded drain of what is still in flight before shared memory and TMEM are released
+        for (int b = 0; b < 2; ++b)
+            if (raw_pend & (1u << b)) mbar_wait(smem_u32(mbars + b), (ph_raw >> b) & 1u, kVWaitLimit);
+        if (warp < 4)
+            for (int b = 0; b < 3; ++b)
+                if (mma_pend & (1u << b)) mbar_wait(smem_u32(mbars + 2 + b), (ph_mma >> b) & 1u, kVWaitLimit);
+    }
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 32);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int KC>
-constexpr size_t verify_smem() {
-    constexpr int NB = 2 * KC < 16 ? 16 : 2 * KC;
-    return 1024 + 65536 + 2 * NB * 256 + 5 * KC * KC * 4 + KC * 4 + 32;
+// The tensor map's encoder from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
 }
 
 template <int KC, bool I, bool O>
-void launch_kc(const void* q, const void* k, const void* v, const void* b, const void* g, int32_t R,
-               int32_t K, const int32_t* ql, int32_t H, float scale, uint32_t flags,
-               const float* pool, int64_t P, const int32_t* ckpt, float* ru, void* rkg, void* out,
-               int32_t* st, cudaStream_t s) {
-    constexpr size_t smem = verify_smem<KC>();
-    cudaFuncSetAttribute(verify_kernel<KC, I, O>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    verify_kernel<KC, I, O><<<(unsigned)(R * H), kVThreads, smem, s>>>(
-        q, k, v, b, g, K, ql, H, scale, flags, pool, P, ckpt, ru, rkg, out, st);
+kda_status launch_kc(const CUtensorMap& map, const VerifyArgs& a, cudaStream_t s) {
+    constexpr size_t smem = VLayout<KC, I ? 2 : 4>::SMEM;
+    static_assert(smem <= 232448, "verify shared memory plan exceeds the per-CTA limit");
+    const int nsm = sm_count();
+    if (nsm <= 0) return KDA_ERR_CUDA;
+    int grid = a.n_units < nsm ? a.n_units : nsm;
+    const int need = (a.n_units + kMaxUnitsPerCta - 1) / kMaxUnitsPerCta;
+    if (grid < need) grid = need;
+    cudaFuncSetAttribute(verify_kernel<KC, I, O>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    verify_kernel<KC, I, O><<<(unsigned)grid, kVThreads, smem, s>>>(map, a);
+    return launch_status();
 }
 
 template <bool I, bool O>
-void launch(const void* q, const void* k, const void* v, const void* b, const void* g, int32_t R,
-            int32_t K, const int32_t* ql, int32_t H, float scale, uint32_t flags,
-            const float* pool, int64_t P, const int32_t* ckpt, float* ru, void* rkg, void* out,
-            int32_t* st, cudaStream_t s) {
-    if (K <= 2) launch_kc<2, I, O>(q, k, v, b, g, R, K, ql, H, scale, flags, pool, P, ckpt, ru, rkg, out, st, s);
-    else if (K <= 4) launch_kc<4, I, O>(q, k, v, b, g, R, K, ql, H, scale, flags, pool, P, ckpt, ru, rkg, out, st, s);
-    else if (K <= 8) launch_kc<8, I, O>(q, k, v, b, g, R, K, ql, H, scale, flags, pool, P, ckpt, ru, rkg, out, st, s);
-    else launch_kc<16, I, O>(q, k, v, b, g, R, K, ql, H, scale, flags, pool, P, ckpt, ru, rkg, out, st, s);
+kda_status launch(const CUtensorMap& map, const VerifyArgs& a, cudaStream_t s) {
+    if (a.K <= 2) return launch_kc<2, I, O>(map, a, s);
+    if (a.K <= 4) return launch_kc<4, I, O>(map, a, s);
+    if (a.K <= 8) return launch_kc<8, I, O>(map, a, s);
+    return launch_kc<16, I, O>(map, a, s);
 }
 
 }  // namespace
@@ -334,13 +604,28 @@ extern "C" kda_status kda_spec_verify(const void* q, const void* k, const void* 
     KDA_REQUIRE(K <= kMaxVerifyK, KDA_ERR_UNSUPPORTED);
     if (R == 0 || K == 0) return KDA_OK;
     KDA_REQUIRE((int64_t)R * H < (1ll << 31), KDA_ERR_UNSUPPORTED);
+    // the pool is read as a 2-D tensor of P*H*128 rows of 128 fp32 (a TMA row coordinate each)
+    KDA_REQUIRE(P * H * 128 < (1ll << 31), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, rec_kg, out};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return KDA_ERR_CUDA;
+    CUtensorMap map;
+    const cuuint64_t rows = P > 0 ? (cuuint64_t)P * H * 128 : 128;
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {128 * sizeof(float)};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(state_pool), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KDA_ERR_CUDA;
+    const VerifyArgs a{q, k, v, beta_raw, gate_raw, K, q_len, H, scale, flags, P, ckpt_slot,
+                       rec_u, rec_kg, out, dev_status, R * H};
     cudaStream_t s = as_stream(stream);
     const bool ib = in_dtype == KDA_BF16, ob = out_dtype == KDA_BF16;
-    if (ib && ob) launch<true, true>(q, k, v, beta_raw, gate_raw, R, K, q_len, H, scale, flags, state_pool, P, ckpt_slot, rec_u, rec_kg, out, dev_status, s);
-    else if (ib) launch<true, false>(q, k, v, beta_raw, gate_raw, R, K, q_len, H, scale, flags, state_pool, P, ckpt_slot, rec_u, rec_kg, out, dev_status, s);
-    else if (ob) launch<false, true>(q, k, v, beta_raw, gate_raw, R, K, q_len, H, scale, flags, state_pool, P, ckpt_slot, rec_u, rec_kg, out, dev_status, s);
-    else launch<false, false>(q, k, v, beta_raw, gate_raw, R, K, q_len, H, scale, flags, state_pool, P, ckpt_slot, rec_u, rec_kg, out, dev_status, s);
-    return launch_status();
+    if (ib && ob) return launch<true, true>(map, a, s);
+    if (ib) return launch<true, false>(map, a, s);
+    if (ob) return launch<false, true>(map, a, s);
+    return launch<false, false>(map, a, s);
 }
