@@ -11,13 +11,17 @@
 // so every state element is one fused sum of a+1 terms.
 //
 // Four CTAs per (request, head), each owning 32 rows of S^T, so that more
-// independent load chains are resident per SM.  Threads first walk the records
-// backwards per key channel to form F_t = exp(c_t) k_t and the total decay
-// exp(c_0) in shared memory, then each warp streams 8 rows of S^T: 16 KiB per
-// CTA read from the checkpoint and written to the destination slot (in place
-// allowed: each element is read and written by the same thread).
+// independent load chains are resident per SM.  Every load of a CTA is issued
+// up front: its 32 checkpoint rows into registers, and the a key / raw-gate
+// records (one contiguous block) and its rows of u_t into shared memory by
+// cp.async.  Threads then walk the records backwards per key channel to form
+// F_t = exp(c_t) k_t and the total decay exp(c_0) as running products of
+// alpha = exp(g) = 1 / (1 + e^x), and each warp streams 8 rows of S^T: 16 KiB
+// per CTA read from the checkpoint and written to the destination slot (in
+// place allowed: each element is read and written by the same thread).
 #include "kda_common.cuh"
 #include "kda_host.h"
+#include "umma.cuh"
 
 namespace kda {
 namespace {
@@ -35,11 +39,12 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     const int32_t* __restrict__ q_len, int32_t K, int32_t H, uint32_t flags,
     const float* __restrict__ rec_u, const void* __restrict__ rec_kg, int32_t* __restrict__ plan_out,
     int32_t* __restrict__ dev_status) {
-    using A = Act<kBf16Rec>;
-    extern __shared__ float sm[];
-    float* F = sm;                  // [a][128]
-    float* U = sm + K * kD;         // [a][128]
-    float* D = sm + 2 * K * kD;     // [128]
+    constexpr int ES = kBf16Rec ? 2 : 4;  // record element size
+    extern __shared__ __align__(16) float sm[];
+    float* F = sm;                                          // [K][128]
+    float* U = sm + K * kD;                                 // [K][32] this CTA's rows of u_t
+    float* D = U + K * 4 * kRowsPerWarp;                    // [128]
+    uint8_t* KG = reinterpret_cast<uint8_t*>(D + kD);       // [K][256] raw records (k, gate)
     const int unit = blockIdx.x / kCtasPerUnit;  // (request, head); the rest picks the row block
     const int part = blockIdx.x - unit * kCtasPerUnit;
     const int r = unit / H, h = unit - r * H;
@@ -71,28 +76,42 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
         }
         return;
     }
-    // issue the checkpoint loads early; they do not depend on the factors
+    // every load up front: checkpoint rows into registers, records into shared memory
+    const size_t rec0 = ((size_t)r * H + h) * K;
+    {
+        const uint32_t kg_s = umma::smem_u32(KG), u_s = umma::smem_u32(U);
+        const uint8_t* kg_g = static_cast<const uint8_t*>(rec_kg) + rec0 * 2 * kD * ES;
+        for (int e = threadIdx.x; e < a * 2 * kD * ES / 16; e += kCommitThreads)
+            umma::cp_async16(kg_s + 16 * e, kg_g + 16 * e, 16);
+        // u_t rows part*32 .. part*32+31: 8 chunks of 16 B per step
+        for (int e = threadIdx.x; e < a * 8; e += kCommitThreads) {
+            const int t = e >> 3, ch = e & 7;
+            umma::cp_async16(u_s + (uint32_t)(t * 128 + ch * 16),
+                             rec_u + (rec0 + t) * kD + part * (4 * kRowsPerWarp) + ch * 4, 16);
+        }
+        umma::cp_async_commit();
+    }
     float4 s[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
         s[i] = __ldcs(reinterpret_cast<const float4*>(S0 + (size_t)(row0 + i) * kD) + lane);
-    const size_t rec0 = ((size_t)r * H + h) * K;
+    umma::cp_async_wait_all();
+    __syncthreads();
     {
+        // F_t = k_t exp(c_t), c_t = sum over s in (t, a) of g_s: a running product of alpha from
+        // t = a - 1 down; D = exp(c_0 + g_0) = the product over every recorded step
         const int c = threadIdx.x;
-        float suffix = 0.f;  // c_t, accumulated from t = a down to 1
+        float prod = 1.f;
         for (int t = a - 1; t >= 0; --t) {
-            const float kv = A::load1(rec_kg, (rec0 + t) * 2 * kD + c);
-            const float gv = A::load1(rec_kg, (rec0 + t) * 2 * kD + kD + c);
-            F[t * kD + c] = expf(suffix) * kv;
-            suffix += gate_log(gv, flags);
+            const float kv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + c] << 16)
+                                      : reinterpret_cast<const float*>(KG)[t * 2 * kD + c];
+            const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
+                                      : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
+            F[t * kD + c] = prod * kv;
+            // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
+            prod *= (flags & KDA_GATE_LOG) ? __expf(gv) : __fdividef(1.f, 1.f + __expf(gv));
         }
-        D[c] = expf(suffix);
-    }
-    // this CTA's 64 rows of u_t for every recorded step
-    for (int i = threadIdx.x; i < a * 4 * kRowsPerWarp; i += blockDim.x) {
-        const int t = i / (4 * kRowsPerWarp);
-        const int cc = part * (4 * kRowsPerWarp) + (i - t * 4 * kRowsPerWarp);
-        U[t * kD + cc] = rec_u[(rec0 + t) * kD + cc];
+        D[c] = prod;
     }
     __syncthreads();
     const float4 dec = *reinterpret_cast<const float4*>(&D[4 * lane]);
@@ -103,7 +122,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
         float urow[kRowsPerWarp];
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp / 4; ++j) {
-            const float4 x = *reinterpret_cast<const float4*>(&U[t * kD + row0 + 4 * j]);
+            const float4 x =
+                *reinterpret_cast<const float4*>(&U[t * (4 * kRowsPerWarp) + warp * kRowsPerWarp + 4 * j]);
             urow[4 * j] = x.x;
             urow[4 * j + 1] = x.y;
             urow[4 * j + 2] = x.z;
@@ -137,7 +157,12 @@ extern "C" kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_
     const void* ptrs[] = {state_pool, ckpt_slot, num_accepted, rec_u, rec_kg};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
     cudaStream_t s = as_stream(stream);
-    const size_t smem = (size_t)(2 * K + 1) * kD * sizeof(float);
+    const size_t es = rec_dtype == KDA_BF16 ? 2 : 4;
+    const size_t smem = (size_t)(K * kD + K * 4 * kRowsPerWarp + kD) * sizeof(float) + (size_t)K * 2 * kD * es;
+    if (smem > 48 * 1024) {
+        cudaFuncSetAttribute(commit_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(commit_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    }
     if (rec_dtype == KDA_BF16)
         commit_kernel<true><<<(unsigned)(kCtasPerUnit * R * H), kCommitThreads, smem, s>>>(
             state_pool, P, ckpt_slot, dst_slot, num_accepted, q_len, K, H, flags, rec_u, rec_kg,

@@ -269,19 +269,29 @@ __global__ void __launch_bounds__(kVThreads, 1)
         const int buf = it & 1;
         const int ql = have ? meta[it].y : 0;
         // ---- this unit's token rows (all but the most recent cp.async group when the k, q, g
-        //      rows run two units ahead) and its checkpoint
+        //      rows run two units ahead), its checkpoint, and the MMAs of the unit two back (their
+        //      accumulator is solved and their operand buffers are rewritten below).  Thread 0
+        //      polls the barriers; the CTA barrier releases everyone else.
         if (have) {
             if constexpr (NKQG == 2)
                 cp_async_wait_1();
             else
                 cp_async_wait_all();
             if (raw_pend & (1u << buf)) {
-                if (!mbar_wait(smem_u32(mbars + buf), (ph_raw >> buf) & 1u, kVWaitLimit)) timed_out = true;
+                if (tid == 0 && !mbar_wait(smem_u32(mbars + buf), (ph_raw >> buf) & 1u, kVWaitLimit))
+                    timed_out = true;
                 ph_raw ^= 1u << buf;
                 raw_pend &= ~(1u << buf);
             }
         } else {
             cp_async_wait_all();
+        }
+        if (it >= 2 && (mma_pend & (1u << ((it - 2) % 3)))) {
+            const int pb = (it - 2) % 3;
+            if (tid == 0 && !mbar_wait(smem_u32(mbars + 2 + pb), (ph_mma >> pb) & 1u, kVWaitLimit))
+                timed_out = true;
+            ph_mma ^= 1u << pb;
+            mma_pend &= ~(1u << pb);
         }
         fence_before();
         if (__syncthreads_or(timed_out)) {
@@ -315,23 +325,16 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 const size_t rec0 = ((size_t)r * H + h) * K;
                 const int c = tid;
                 float d[2 * NB];
-                bool ok = true;
-                if (mma_pend & (1u << pb)) {
-                    ok = mbar_wait(smem_u32(mbars + 2 + pb), (ph_mma >> pb) & 1u, kVWaitLimit);
-                    ph_mma ^= 1u << pb;
-                    mma_pend &= ~(1u << pb);
-                    fence_after();
-                    if (ok) {
+                if (pql > 0) {
 #pragma unroll
-                        for (int q16 = 0; q16 < 2 * NB / 16; ++q16) {
-                            float v16[16];
-                            ld16(tl + TV_D + (uint32_t)pb * (2 * NB) + 16 * q16, v16);
+                    for (int q16 = 0; q16 < 2 * NB / 16; ++q16) {
+                        float v16[16];
+                        ld16(tl + TV_D + (uint32_t)pb * (2 * NB) + 16 * q16, v16);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) d[16 * q16 + e] = v16[e];
-                        }
+                        for (int e = 0; e < 16; ++e) d[16 * q16 + e] = v16[e];
                     }
                 }
-                if (!ok) timed_out = true;
+                const bool ok = true;
                 const float* ap = reinterpret_cast<const float*>(sm + Lay::AP) + pb * KC * KC;
                 const uint8_t* vb = sm + Lay::VB + (uint32_t)pb * Lay::VB_BYTES;
                 float u[KC];
@@ -358,14 +361,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
             }
             if (it + 1 < nu) prefetch_v(it + 1);  // into the v buffer of the unit two back
         } else if (have) {
-            // ---- warps 4-15: this unit's checkpoint rows into TMEM, once the MMAs of the unit
-            //      two back (same operand buffers) have completed
-            if (it >= 2 && meta[it - 2].y > 0) {
-                const int pb = (it - 2) % 3;
-                if (!mbar_wait(smem_u32(mbars + 2 + pb), (ph_mma >> pb) & 1u, kVWaitLimit)) timed_out = true;
-                ph_mma ^= 1u << pb;
-                fence_after();
-            }
+            // ---- warps 4-15: this unit's checkpoint rows into TMEM (the MMAs of the unit two
+            //      back, which read the same operand buffers, completed before the barrier above)
             if (ql > 0) {
                 if (warp < 12) {
                     convert(buf, warp < 8 ? 1 : 2);
@@ -528,11 +525,12 @@ __global__ void __launch_bounds__(kVThreads, 1)
     if (timed_out) {
         if (tid == 0) report(a.dev_status, KDA_DEV_TIMEOUT);
         // bounded drain of what is still in flight before shared memory and TMEM are released
-        for (int b = 0; b < 2; ++b)
-            if (raw_pend & (1u << b)) mbar_wait(smem_u32(mbars + b), (ph_raw >> b) & 1u, kVWaitLimit);
-        if (warp < 4)
+        if (tid == 0) {
+            for (int b = 0; b < 2; ++b)
+                if (raw_pend & (1u << b)) mbar_wait(smem_u32(mbars + b), (ph_raw >> b) & 1u, kVWaitLimit);
             for (int b = 0; b < 3; ++b)
                 if (mma_pend & (1u << b)) mbar_wait(smem_u32(mbars + 2 + b), (ph_mma >> b) & 1u, kVWaitLimit);
+        }
     }
     fence_before();
     __syncthreads();
