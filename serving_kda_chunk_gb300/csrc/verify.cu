@@ -44,6 +44,7 @@ using namespace umma;
 constexpr int kVThreads = 512;          // 16 warps: four per TMEM lane quarter
 constexpr int kMaxVerifyK = 16;
 constexpr int kMaxUnitsPerCta = 512;    // per-CTA unit table in shared memory
+constexpr int kIssuer = 0;              // thread 0 issues the MMAs (then joins the rows' solve)
 constexpr uint32_t kVWaitLimit = 1u << 22;  // polls; a checkpoint or an MMA batch lands in microseconds
 
 struct VerifyArgs {
@@ -75,8 +76,11 @@ struct VLayout {
     static constexpr uint32_t BT_BYTES = 2 * NB * 256;
     static constexpr uint32_t KQG_BYTES = 3 * KC * 128 * ES;  // k, q, g rows [3][KC][128]
     // two k, q, g buffers (rows requested two units ahead) where they fit, else one
+    // mid-reference decay tables for the K x K factors ([3][KC][TLD] fp32; K <= 8 only)
+    static constexpr int TLD = 132;
+    static constexpr uint32_t TAB_BYTES = KC <= 8 ? 3 * KC * TLD * 4 : 0;
     static constexpr int NKQG = 131072 + 2 * BT_BYTES + 2 * KQG_BYTES + 3 * KC * 128 * ES + 28 * KC * KC +
-                                            20 * KC + kMaxUnitsPerCta * 8 + 64 + 1024 <= 232448 ? 2 : 1;
+                                            20 * KC + TAB_BYTES + kMaxUnitsPerCta * 8 + 64 + 1024 <= 232448 ? 2 : 1;
     static constexpr uint32_t KQG = BT + 2 * BT_BYTES;
     static constexpr uint32_t VB = KQG + NKQG * KQG_BYTES;  // 3 x v rows [KC][128]
     static constexpr uint32_t VB_BYTES = KC * 128 * ES;
@@ -84,7 +88,8 @@ struct VLayout {
     static constexpr uint32_t RED = AP + 3 * KC * KC * 4;   // [4 warps][KC][KC]
     static constexpr uint32_t BETA = RED + 4 * KC * KC * 4; // 3 x [KC] activated beta
     static constexpr uint32_t BRAW = BETA + 3 * KC * 4;     // NKQG x [KC] 4-byte words holding raw beta
-    static constexpr uint32_t META = BRAW + 2 * KC * 4;     // [kMaxUnitsPerCta] (slot, q_len)
+    static constexpr uint32_t TAB = BRAW + 2 * KC * 4;      // pair-factor tables
+    static constexpr uint32_t META = TAB + TAB_BYTES;        // [kMaxUnitsPerCta] (slot, q_len)
     static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8;  // raw full [2], mma done [3]
     static constexpr uint32_t END = MBAR + 5 * 8 + 24;
     static constexpr size_t SMEM = END + 1024;  // + alignment slack
@@ -112,6 +117,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+
+// Named barrier that also returns whether any participating thread passed pred = true.
+__device__ __forceinline__ bool bar_named_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+constexpr float kVFactorMax = 1.8446744e19f;  // 2^64: largest decay factor the pair tables carry
 
 template <bool kBf16>
 __device__ __forceinline__ float act_at(const uint8_t* p, int idx) {
@@ -301,21 +319,21 @@ __global__ void __launch_bounds__(kVThreads, 1)
         fence_after();
         if (it >= 1 && it <= nu && meta[it - 1].y > 0) mma_pend |= 1u << ((it - 1) % 3);
 
+        // ---- MMAs of the previous unit: D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
+        if (tid == kIssuer && it >= 1 && it <= nu && meta[it - 1].y > 0) {
+            const int u = it - 1, ub = u & 1;
+            const uint32_t id2 = idesc_bf16(128, 2 * NB, false, false, false);
+            const uint32_t id1 = idesc_bf16(128, NB, false, false, false);
+            const uint32_t d = tmem + TV_D + (uint32_t)(u % 3) * (2 * NB);
+            const uint32_t sa = tmem + TV_SA + (uint32_t)ub * 128u;
+            const uint32_t b4 = sb4 + (Lay::BT + (uint32_t)ub * Lay::BT_BYTES) / 16;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) mma_ta(d, sa + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) mma_ta(d, sa + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
+            commit(smem_u32(mbars + 2 + u % 3));
+        }
         if (warp < 4) {
-            // ---- MMAs of the previous unit: D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
-            if (tid == 0 && it >= 1 && it <= nu && meta[it - 1].y > 0) {
-                const int u = it - 1, ub = u & 1;
-                const uint32_t id2 = idesc_bf16(128, 2 * NB, false, false, false);
-                const uint32_t id1 = idesc_bf16(128, NB, false, false, false);
-                const uint32_t d = tmem + TV_D + (uint32_t)(u % 3) * (2 * NB);
-                const uint32_t sa = tmem + TV_SA + (uint32_t)ub * 128u;
-                const uint32_t b4 = sb4 + (Lay::BT + (uint32_t)ub * Lay::BT_BYTES) / 16;
-#pragma unroll
-                for (int s = 0; s < 8; ++s) mma_ta(d, sa + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) mma_ta(d, sa + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
-                commit(smem_u32(mbars + 2 + u % 3));
-            }
             // ---- rows of the unit two back: triangular solve, outputs, u records
             if (it >= 2) {
                 const int pj = it - 2, pb = pj % 3;
@@ -377,16 +395,22 @@ __global__ void __launch_bounds__(kVThreads, 1)
                 // keys / queries (B tile), warps 8-11 the K x K pair factors
                 const int i = tid & 127;
                 const uint8_t* kqg = sm + kqg_at(it);
-                float kt[KC], qt[KC], at[KC];
+                float kt[KC], qt[KC], at[KC], iv[KC];  // key, scaled query, alpha, 1 / alpha
 #pragma unroll
                 for (int t = 0; t < KC; ++t) {
                     kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
                     qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
-                    at[t] = 1.f;
+                    at[t] = iv[t] = 1.f;
                     if (t < ql) {
                         // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
                         const float gx = act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i);
-                        at[t] = (a.flags & KDA_GATE_LOG) ? __expf(gx) : __fdividef(1.f, 1.f + __expf(gx));
+                        if (a.flags & KDA_GATE_LOG) {
+                            at[t] = __expf(gx);
+                            iv[t] = __expf(-gx);
+                        } else {
+                            iv[t] = 1.f + __expf(gx);
+                            at[t] = __fdividef(1.f, iv[t]);
+                        }
                     }
                 }
                 if (warp < 8) {
@@ -408,69 +432,129 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     for (int n = 2 * KC; n < NB; ++n) put(n, 0.f);
                 } else {
                     const int wg = warp - 8;
-                    float(*red)[KC][KC] = reinterpret_cast<float(*)[KC][KC]>(sm + Lay::RED);
-                    // pair sums over channels, e^{G_t - G_s} as running products of alpha:
-                    // value [a][b] = P_ab (a <= b) or A_ab (a > b), summed over the warp's 32 channels
+                    float* ap = reinterpret_cast<float*>(sm + Lay::AP) + (it % 3) * KC * KC;
+                    bool fallback = true;
                     if constexpr (KC <= 8) {
-                        constexpr int NV = KC * KC < 32 ? 32 : KC * KC;
-                        float vals[NV];
+                        // Tables with the reference at position m = KC/2 (factors span at most KC/2
+                        // steps): L_k[t] = k_t e^{G_t - G_m}, L_q[t] = q_t e^{G_t - G_m},
+                        // R[s] = k_s e^{G_m - G_s}; then A_ts = L_k[t] . R[s], P_ts = L_q[t] . R[s].
+                        constexpr int MID = KC / 2, TLD = Lay::TLD;
+                        float* lk = reinterpret_cast<float*>(sm + Lay::TAB);
+                        float* lq = lk + KC * TLD;
+                        float* rk = lq + KC * TLD;
+                        lk[MID * TLD + i] = kt[MID];
+                        lq[MID * TLD + i] = qt[MID];
+                        rk[MID * TLD + i] = kt[MID];
+                        float e = 1.f, rf = 1.f;
 #pragma unroll
-                        for (int e = 0; e < NV; ++e) vals[e] = 0.f;
-#pragma unroll
-                        for (int s0 = 0; s0 < KC; ++s0) {
-                            float dec = 1.f;
-#pragma unroll
-                            for (int t = s0; t < KC; ++t) {
-                                if (t > s0) dec *= at[t];
-                                const bool live = t < ql;
-                                vals[s0 * KC + t] = live ? qt[t] * kt[s0] * dec : 0.f;
-                                if (t > s0) vals[t * KC + s0] = live ? kt[t] * kt[s0] * dec : 0.f;
-                            }
+                        for (int t = MID + 1; t < KC; ++t) {
+                            e *= at[t];
+                            rf *= iv[t];
+                            lk[t * TLD + i] = kt[t] * e;
+                            lq[t * TLD + i] = qt[t] * e;
+                            rk[t * TLD + i] = kt[t] * rf;
                         }
-                        // butterfly reduce-scatter: lane l ends with the totals of entries l*M .. l*M+M-1
-                        int nn = NV;
+                        float big = rf;
+                        e = rf = 1.f;
 #pragma unroll
-                        for (int off = 16; off >= 1; off >>= 1) {
-                            const bool upper = (lane & off) != 0;
-                            const int half = nn / 2;
+                        for (int t = MID - 1; t >= 0; --t) {
+                            e *= iv[t + 1];
+                            rf *= at[t + 1];
+                            lk[t * TLD + i] = kt[t] * e;
+                            lq[t * TLD + i] = qt[t] * e;
+                            rk[t * TLD + i] = kt[t] * rf;
+                        }
+                        big = fmaxf(big, e);
+                        fallback = bar_named_or(1, 128, !(big <= kVFactorMax));
+                        if (!fallback) {
+                            // entry [x0][x1]: P (query x1, key x0) if x0 <= x1, else A (x0, x1); two
+                            // threads per entry, 64 channels each
+                            constexpr int NIT = KC * KC * 2;
+                            constexpr unsigned MASK = NIT >= 32 ? 0xffffffffu : (1u << NIT) - 1u;
+                            for (int e2 = i; e2 < NIT; e2 += 128) {
+                                const int entry = e2 >> 1, half = e2 & 1;
+                                const int x0 = entry / KC, x1 = entry - x0 * KC;
+                                const float* lrow = (x0 <= x1 ? lq + x1 * TLD : lk + x0 * TLD) + 64 * half;
+                                const float* rrow = rk + (x0 <= x1 ? x0 : x1) * TLD + 64 * half;
+                                float acc = 0.f;
 #pragma unroll
-                            for (int e = 0; e < NV / 2; ++e) {
-                                if (e < half) {
-                                    const float send = upper ? vals[e] : vals[e + half];
-                                    const float keep = upper ? vals[e + half] : vals[e];
-                                    vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                for (int j = 0; j < 16; ++j) {
+                                    const float4 l4 = *reinterpret_cast<const float4*>(lrow + 4 * j);
+                                    const float4 r4 = *reinterpret_cast<const float4*>(rrow + 4 * j);
+                                    acc = fmaf(l4.x, r4.x, acc);
+                                    acc = fmaf(l4.y, r4.y, acc);
+                                    acc = fmaf(l4.z, r4.z, acc);
+                                    acc = fmaf(l4.w, r4.w, acc);
                                 }
-                            }
-                            nn = half;
-                        }
-                        constexpr int M = NV / 32;
-#pragma unroll
-                        for (int e = 0; e < M; ++e) {
-                            const int idx = lane * M + e;
-                            if (idx < KC * KC) red[wg][idx / KC][idx % KC] = vals[e];
-                        }
-                    } else {
-#pragma unroll
-                        for (int s0 = 0; s0 < KC; ++s0) {
-                            float dec = 1.f;
-#pragma unroll
-                            for (int t = s0; t < KC; ++t) {
-                                if (t > s0) dec *= at[t];
-                                const bool live = t < ql;
-                                const float pp = warp_sum(live ? qt[t] * kt[s0] * dec : 0.f);
-                                if (lane == 0) red[wg][s0][t] = pp;
-                                if (t > s0) {
-                                    const float pa = warp_sum(live ? kt[t] * kt[s0] * dec : 0.f);
-                                    if (lane == 0) red[wg][t][s0] = pa;
-                                }
+                                acc += __shfl_xor_sync(MASK, acc, 1);
+                                if (half == 0) ap[entry] = acc;
                             }
                         }
                     }
-                    bar_named(1, 128);  // warps 8-11
-                    float* ap = reinterpret_cast<float*>(sm + Lay::AP) + (it % 3) * KC * KC;
-                    for (int e = i; e < KC * KC; e += 128) {
-                        const int x0 = e / KC, x1 = e - x0 * KC;
-                        ap[e] = (red[0][x0][x1] + red[1][x0][x1]) + (red[2][x0][x1] + red[3][x0][x1]);
+                    if (fallback) {
+                        float(*red)[KC][KC] = reinterpret_cast<float(*)[KC][KC]>(sm + Lay::RED);
+                        // pair sums over channels, e^{G_t - G_s} as running products of alpha:
+                        // value [a][b] = P_ab (a <= b) or A_ab (a > b), summed over the warp's 32 channels
+                        if constexpr (KC <= 8) {
+                            constexpr int NV = KC * KC < 32 ? 32 : KC * KC;
+                            float vals[NV];
+#pragma unroll
+                            for (int e = 0; e < NV; ++e) vals[e] = 0.f;
+#pragma unroll
+                            for (int s0 = 0; s0 < KC; ++s0) {
+                                float dec = 1.f;
+#pragma unroll
+                                for (int t = s0; t < KC; ++t) {
+                                    if (t > s0) dec *= at[t];
+                                    const bool live = t < ql;
+                                    vals[s0 * KC + t] = live ? qt[t] * kt[s0] * dec : 0.f;
+                                    if (t > s0) vals[t * KC + s0] = live ? kt[t] * kt[s0] * dec : 0.f;
+                                }
+                            }
+                            // butterfly reduce-scatter: lane l ends with the totals of entries l*M .. l*M+M-1
+                            int nn = NV;
+#pragma unroll
+                            for (int off = 16; off >= 1; off >>= 1) {
+                                const bool upper = (lane & off) != 0;
+                                const int half = nn / 2;
+#pragma unroll
+                                for (int e = 0; e < NV / 2; ++e) {
+                                    if (e < half) {
+                                        const float send = upper ? vals[e] : vals[e + half];
+                                        const float keep = upper ? vals[e + half] : vals[e];
+                                        vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                    }
+                                }
+                                nn = half;
+                            }
+                            constexpr int M = NV / 32;
+#pragma unroll
+                            for (int e = 0; e < M; ++e) {
+                                const int idx = lane * M + e;
+                                if (idx < KC * KC) red[wg][idx / KC][idx % KC] = vals[e];
+                            }
+                        } else {
+#pragma unroll
+                            for (int s0 = 0; s0 < KC; ++s0) {
+                                float dec = 1.f;
+#pragma unroll
+                                for (int t = s0; t < KC; ++t) {
+                                    if (t > s0) dec *= at[t];
+                                    const bool live = t < ql;
+                                    const float pp = warp_sum(live ? qt[t] * kt[s0] * dec : 0.f);
+                                    if (lane == 0) red[wg][s0][t] = pp;
+                                    if (t > s0) {
+                                        const float pa = warp_sum(live ? kt[t] * kt[s0] * dec : 0.f);
+                                        if (lane == 0) red[wg][t][s0] = pa;
+                                    }
+                                }
+                            }
+                        }
+                        bar_named(1, 128);  // warps 8-11
+                        for (int e = i; e < KC * KC; e += 128) {
+                            const int x0 = e / KC, x1 = e - x0 * KC;
+                            ap[e] = (red[0][x0][x1] + red[1][x0][x1]) + (red[2][x0][x1] + red[3][x0][x1]);
+                        }
                     }
                 }
             } else {
