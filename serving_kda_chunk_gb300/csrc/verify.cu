@@ -67,7 +67,10 @@ struct VerifyArgs {
     int32_t n_units;
 };
 
+constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
+
 // Shared-memory plan for a compile-time bound KC on K and the activation element size ES.
+// Every region starts on a 16-byte boundary (cp.async and vector accesses).
 template <int KC, int ES>
 struct VLayout {
     static constexpr int NB = 2 * KC < 16 ? 16 : 2 * KC;  // MMA N of one hi or lo half
@@ -75,24 +78,36 @@ struct VLayout {
     static constexpr uint32_t BT = 131072;                  // 2 x [B_hi; B_lo] tiles, K-major
     static constexpr uint32_t BT_BYTES = 2 * NB * 256;
     static constexpr uint32_t KQG_BYTES = 3 * KC * 128 * ES;  // k, q, g rows [3][KC][128]
-    // two k, q, g buffers (rows requested two units ahead) where they fit, else one
+    static constexpr uint32_t VB_BYTES = KC * 128 * ES;       // v rows [KC][128]
     // mid-reference decay tables for the K x K factors ([3][KC][TLD] fp32; K <= 8 only)
     static constexpr int TLD = 132;
     static constexpr uint32_t TAB_BYTES = KC <= 8 ? 3 * KC * TLD * 4 : 0;
-    static constexpr int NKQG = 131072 + 2 * BT_BYTES + 2 * KQG_BYTES + 3 * KC * 128 * ES + 28 * KC * KC +
-                                            20 * KC + TAB_BYTES + kMaxUnitsPerCta * 8 + 64 + 1024 <= 232448 ? 2 : 1;
+    // everything after the k, q, g buffers, for a given number of them
+    static constexpr uint32_t tail_from(uint32_t vb) {
+        return align16(align16(align16(align16(align16(align16(vb + 3 * VB_BYTES) + 3 * KC * KC * 4) +
+                                                   4 * KC * KC * 4) +
+                                           3 * KC * 4) +
+                                   2 * KC * 4) +
+                       TAB_BYTES) +
+               kMaxUnitsPerCta * 8 + 5 * 8 + 24;
+    }
+    // two k, q, g buffers (rows requested two units ahead) where they fit, else one
+    static constexpr int NKQG = tail_from(BT + 2 * BT_BYTES + 2 * KQG_BYTES) + 1024 <= 232448 ? 2 : 1;
     static constexpr uint32_t KQG = BT + 2 * BT_BYTES;
-    static constexpr uint32_t VB = KQG + NKQG * KQG_BYTES;  // 3 x v rows [KC][128]
-    static constexpr uint32_t VB_BYTES = KC * 128 * ES;
-    static constexpr uint32_t AP = VB + 3 * VB_BYTES;       // 3 x [KC][KC] fp32
-    static constexpr uint32_t RED = AP + 3 * KC * KC * 4;   // [4 warps][KC][KC]
-    static constexpr uint32_t BETA = RED + 4 * KC * KC * 4; // 3 x [KC] activated beta
-    static constexpr uint32_t BRAW = BETA + 3 * KC * 4;     // NKQG x [KC] 4-byte words holding raw beta
-    static constexpr uint32_t TAB = BRAW + 2 * KC * 4;      // pair-factor tables
-    static constexpr uint32_t META = TAB + TAB_BYTES;        // [kMaxUnitsPerCta] (slot, q_len)
-    static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8;  // raw full [2], mma done [3]
+    static constexpr uint32_t VB = align16(KQG + NKQG * KQG_BYTES);  // 3 x v rows
+    static constexpr uint32_t AP = align16(VB + 3 * VB_BYTES);       // 3 x [KC][KC] fp32
+    static constexpr uint32_t RED = align16(AP + 3 * KC * KC * 4);   // [4 warps][KC][KC]
+    static constexpr uint32_t BETA = align16(RED + 4 * KC * KC * 4); // 3 x [KC] activated beta
+    static constexpr uint32_t BRAW = align16(BETA + 3 * KC * 4);     // NKQG x [KC] raw beta words
+    static constexpr uint32_t TAB = align16(BRAW + 2 * KC * 4);      // pair-factor tables
+    static constexpr uint32_t META = align16(TAB + TAB_BYTES);       // [kMaxUnitsPerCta] (slot, q_len)
+    static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8;     // raw full [2], mma done [3]
     static constexpr uint32_t END = MBAR + 5 * 8 + 24;
     static constexpr size_t SMEM = END + 1024;  // + alignment slack
+    static_assert(BT % 1024 == 0 && BT_BYTES % 1024 == 0, "swizzled tiles on 1 KiB boundaries");
+    static_assert(KQG % 16 == 0 && VB % 16 == 0 && TAB % 16 == 0 && META % 8 == 0 && MBAR % 8 == 0,
+                  "region alignment");
+    static_assert(SMEM <= 232448, "verify shared memory plan exceeds the per-CTA limit");
 };
 
 // TMEM columns: checkpoint operands [S hi (64) | S lo (64)] x 2, then three accumulators

@@ -247,6 +247,28 @@ def test_verify_then_commit_small(kda, dtype):
     assert np.array_equal(pool.cpu().numpy()[dst[1]], s["pool"][s["ckpt"][1]])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("K", [2, 8, 16])
+def test_verify_strong_decay_and_k_bounds(kda, K, dtype):
+    # request 1 decays by ~e^-25 per step: its mid-reference factors leave the range the
+    # verify pair tables carry (> 2^64 over K/2 steps for K >= 4), so that unit takes the
+    # reduce-scatter path; the others take the table path in the same launch
+    R, H = 4, 2
+    s = W.spec_case(34 + K, R, K, H, P=6, dtype=dtype)
+    gate = s["gate"].copy()
+    strong = np.full(gate[K:2 * K].shape, 25.0, np.float32)
+    gate[K:2 * K] = W.f32_to_bf16_bits(strong) if dtype == "bf16" else strong
+    s["gate"] = gate
+    pool, rec_u, rec_kg, out, st = run_verify(kda, s)
+    assert st == 0
+    o_ref, ru_ref, rkg_ref, _ = oracle.verify(wid(s, "q"), wid(s, "k"), wid(s, "v"),
+                                              wid(s, "beta"), wid(s, "gate"), s["pool"],
+                                              s["ckpt"], K, q_len=s["q_len"])
+    assert rel_l2(to_np(out), o_ref) < tol_out(dtype)
+    assert rel_l2(rec_u.cpu().numpy(), ru_ref) < TOL_STATE
+    assert np.array_equal(to_np(rec_kg), rkg_ref)
+
+
 def test_commit_rejects_bad_accept(kda):
     s = W.spec_case(31, 3, 3, 1, P=4)
     pool, rec_u, rec_kg, _, _ = run_verify(kda, s)
