@@ -13,22 +13,22 @@
 //   o_t = (q_t e^{G_t}) . S_0 + sum_{s<=t} P_ts u_s,                P_ts = sum_i q_ti k_si e^{G_ti - G_si}
 // which is exactly K sequential steps of the recurrence.
 //
-// The work is a stream of 64 KiB checkpoints, one per (request, head) unit, so
-// the kernel is persistent: one CTA per SM walks its units as a pipeline.
-//   - The checkpoint of unit j + 2 is requested by TMA (a two-dimensional
-//     tensor map over the pool, 128-byte swizzle, four [128 rows x 32 fp32]
-//     boxes) into a two-deep ring while unit j is worked on; the token rows
-//     arrive by cp.async one unit ahead.
-//   - Each thread converts 32 columns of one checkpoint row into bf16 hi + lo
-//     and stores them into TMEM, where they are the A operand (lane = value
-//     channel) of D = S_0^T [K_G; Q_G]^T (M = 128, N = 2K padded to 16,
-//     K = 128).  The hi / lo splits of the gated keys and queries lie side by
-//     side along N, so D takes 16 MMAs: S_hi [B_hi; B_lo]^T and S_lo B_hi^T.
-//   - The rows solve their triangular systems two units behind: while unit j
-//     is converted and its gated keys, queries and K x K factors are built
-//     (warps 4-15), warps 0-3 issue the MMAs of unit j - 1 and solve unit
-//     j - 2 from its 2K TMEM results.
-// TMEM holds two checkpoint operands and three accumulators.
+// The work is a stream of 64 KiB checkpoints, one per (request, head) unit.
+// Two persistent CTAs per SM (256 threads, ~100 KiB of shared memory and 256
+// TMEM columns each) walk their units one after another; while one waits for
+// its MMAs or its next checkpoint the other computes.  Per unit:
+//   - the checkpoint arrives by TMA (a two-dimensional tensor map over the
+//     pool, 128-byte swizzle, four [128 rows x 32 fp32] boxes), requested as
+//     soon as the previous unit's rows were converted; the token rows and raw
+//     beta words arrive by cp.async one unit ahead;
+//   - each thread converts 64 columns of one checkpoint row into bf16 hi + lo
+//     in TMEM, the A operand (lane = value channel) of D = S_0^T [K_G; Q_G]^T
+//     (M = 128, N = 2K padded to 16, K = 128): 16 MMAs, the hi / lo halves of
+//     the gated keys and queries side by side along N;
+//   - warps 0-3 write the gated keys / queries, warps 4-7 the K x K factors
+//     (from mid-reference decay tables, one dot product per entry);
+//   - after the MMAs, each of the 128 rows reads its 2K results from TMEM and
+//     solves its K-step triangular system in registers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,10 +41,9 @@ namespace {
 
 using namespace umma;
 
-constexpr int kVThreads = 512;          // 16 warps: four per TMEM lane quarter
+constexpr int kVThreads = 256;          // 8 warps: two per TMEM lane quarter
 constexpr int kMaxVerifyK = 16;
 constexpr int kMaxUnitsPerCta = 512;    // per-CTA unit table in shared memory
-constexpr int kIssuer = 0;              // thread 0 issues the MMAs (then joins the rows' solve)
 constexpr uint32_t kVWaitLimit = 1u << 22;  // polls; a checkpoint or an MMA batch lands in microseconds
 
 struct VerifyArgs {
@@ -74,45 +73,31 @@ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
 template <int KC, int ES>
 struct VLayout {
     static constexpr int NB = 2 * KC < 16 ? 16 : 2 * KC;  // MMA N of one hi or lo half
-    static constexpr uint32_t RAW = 0;                      // 2 x 64 KiB checkpoint ring
-    static constexpr uint32_t BT = 131072;                  // 2 x [B_hi; B_lo] tiles, K-major
+    static constexpr int TLD = 132;                        // pair-table row stride (floats)
+    static constexpr uint32_t RAW = 0;                     // 64 KiB checkpoint (TMA, swizzled)
+    static constexpr uint32_t BT = 65536;                  // [B_hi; B_lo] tile, K-major
     static constexpr uint32_t BT_BYTES = 2 * NB * 256;
-    static constexpr uint32_t KQG_BYTES = 3 * KC * 128 * ES;  // k, q, g rows [3][KC][128]
-    static constexpr uint32_t VB_BYTES = KC * 128 * ES;       // v rows [KC][128]
-    // mid-reference decay tables for the K x K factors ([3][KC][TLD] fp32; K <= 8 only)
-    static constexpr int TLD = 132;
+    static constexpr uint32_t KQG = BT + BT_BYTES;         // k, q, g rows [3][KC][128]
+    static constexpr uint32_t KQG_BYTES = 3 * KC * 128 * ES;
+    static constexpr uint32_t VB = align16(KQG + KQG_BYTES);  // 2 x v rows [KC][128]
+    static constexpr uint32_t VB_BYTES = KC * 128 * ES;
+    static constexpr uint32_t AP = align16(VB + 2 * VB_BYTES);   // [KC][KC] fp32
+    static constexpr uint32_t RED = align16(AP + KC * KC * 4);   // [4 warps][KC][KC]
+    static constexpr uint32_t BETA = align16(RED + 4 * KC * KC * 4);  // [KC] activated beta
+    static constexpr uint32_t BRAW = align16(BETA + KC * 4);     // [KC] 4-byte words holding raw beta
+    static constexpr uint32_t TAB = align16(BRAW + KC * 4);      // [3][KC][TLD] fp32 (K <= 8)
     static constexpr uint32_t TAB_BYTES = KC <= 8 ? 3 * KC * TLD * 4 : 0;
-    // everything after the k, q, g buffers, for a given number of them
-    static constexpr uint32_t tail_from(uint32_t vb) {
-        return align16(align16(align16(align16(align16(align16(vb + 3 * VB_BYTES) + 3 * KC * KC * 4) +
-                                                   4 * KC * KC * 4) +
-                                           3 * KC * 4) +
-                                   2 * KC * 4) +
-                       TAB_BYTES) +
-               kMaxUnitsPerCta * 8 + 5 * 8 + 24;
-    }
-    // two k, q, g buffers (rows requested two units ahead) where they fit, else one
-    static constexpr int NKQG = tail_from(BT + 2 * BT_BYTES + 2 * KQG_BYTES) + 1024 <= 232448 ? 2 : 1;
-    static constexpr uint32_t KQG = BT + 2 * BT_BYTES;
-    static constexpr uint32_t VB = align16(KQG + NKQG * KQG_BYTES);  // 3 x v rows
-    static constexpr uint32_t AP = align16(VB + 3 * VB_BYTES);       // 3 x [KC][KC] fp32
-    static constexpr uint32_t RED = align16(AP + 3 * KC * KC * 4);   // [4 warps][KC][KC]
-    static constexpr uint32_t BETA = align16(RED + 4 * KC * KC * 4); // 3 x [KC] activated beta
-    static constexpr uint32_t BRAW = align16(BETA + 3 * KC * 4);     // NKQG x [KC] raw beta words
-    static constexpr uint32_t TAB = align16(BRAW + 2 * KC * 4);      // pair-factor tables
-    static constexpr uint32_t META = align16(TAB + TAB_BYTES);       // [kMaxUnitsPerCta] (slot, q_len)
-    static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8;     // raw full [2], mma done [3]
-    static constexpr uint32_t END = MBAR + 5 * 8 + 24;
+    static constexpr uint32_t META = align16(TAB + TAB_BYTES);   // [kMaxUnitsPerCta] (slot, q_len)
+    static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8; // checkpoint, MMA
+    static constexpr uint32_t END = MBAR + 2 * 8 + 16;
     static constexpr size_t SMEM = END + 1024;  // + alignment slack
     static_assert(BT % 1024 == 0 && BT_BYTES % 1024 == 0, "swizzled tiles on 1 KiB boundaries");
-    static_assert(KQG % 16 == 0 && VB % 16 == 0 && TAB % 16 == 0 && META % 8 == 0 && MBAR % 8 == 0,
-                  "region alignment");
+    static_assert(KQG % 16 == 0 && VB % 16 == 0 && TAB % 16 == 0 && META % 8 == 0, "region alignment");
     static_assert(SMEM <= 232448, "verify shared memory plan exceeds the per-CTA limit");
 };
 
-// TMEM columns: checkpoint operands [S hi (64) | S lo (64)] x 2, then three accumulators
-// [D_hi | D_lo] of 2 NB columns each.
-constexpr uint32_t TV_SA = 0, TV_D = 256;
+// TMEM columns: checkpoint operand [S hi (64) | S lo (64)], then the accumulator [D_hi | D_lo]
+constexpr uint32_t TV_SA = 0, TV_D = 128, TV_COLS = 256;
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
@@ -155,14 +140,13 @@ __device__ __forceinline__ float act_at(const uint8_t* p, int idx) {
 }
 
 template <int KC, bool kBf16In, bool kBf16Out>
-__global__ void __launch_bounds__(kVThreads, 1)
+__global__ void __launch_bounds__(kVThreads, 2)
     verify_kernel(const __grid_constant__ CUtensorMap tmap, const VerifyArgs a) {
     constexpr int ES = kBf16In ? 2 : 4;
     using Lay = VLayout<KC, ES>;
     constexpr int NB = Lay::NB;
     constexpr int CPR = 128 * ES / 16;  // 16-byte chunks per token row
-    constexpr int NKQG = Lay::NKQG;     // k, q, g rows are requested NKQG units ahead
-    static_assert(TV_D + 3 * 2 * NB <= 512, "TMEM plan");
+    static_assert(TV_D + 2 * NB <= TV_COLS, "TMEM plan");
 
     extern __shared__ uint8_t vraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vraw) + 1023) &
@@ -170,13 +154,15 @@ __global__ void __launch_bounds__(kVThreads, 1)
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     int2* meta = reinterpret_cast<int2*>(sm + Lay::META);
-    uint64_t* mbars = reinterpret_cast<uint64_t*>(sm + Lay::MBAR);  // raw full [2], mma done [3]
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbars + 5);
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sm + Lay::MBAR);  // checkpoint, MMA
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbars + 2);
     float* sbeta = reinterpret_cast<float*>(sm + Lay::BETA);
+    float* ap = reinterpret_cast<float*>(sm + Lay::AP);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, colhalf = warp >> 2;
     const int row = quarter * 32 + lane;
+    const int i = tid & 127;  // channel passes: key channel
     const int H = a.H, K = a.K;
     const int G = gridDim.x;
     const int nu = (a.n_units - (int)blockIdx.x + G - 1) / G;  // units of this CTA
@@ -196,9 +182,10 @@ __global__ void __launch_bounds__(kVThreads, 1)
         if (!(slot_ok && len_ok)) ql = 0;
         meta[idx] = make_int2(slot, ql);
     }
-    if (warp == 0) tmem_alloc(smem_u32(s_tmem), 512);
+    if (warp == 0) tmem_alloc(smem_u32(s_tmem), TV_COLS);
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(smem_u32(mbars + b), 1);
+        mbar_init(smem_u32(mbars), 1);
+        mbar_init(smem_u32(mbars + 1), 1);
     }
     fence_before();
     __syncthreads();
@@ -211,54 +198,43 @@ __global__ void __launch_bounds__(kVThreads, 1)
         r = unit / H;
         h = unit - r * H;
     };
-    // checkpoint of unit idx -> ring buffer idx & 1 (one thread; the unit must have q_len > 0)
+    // checkpoint of unit idx (q_len > 0) -> RAW, completing on the checkpoint barrier (one thread)
     auto request_ckpt = [&](int idx) {
         int r, h;
         unit_rh(idx, r, h);
-        const uint32_t mb = smem_u32(mbars + (idx & 1));
-        const uint32_t dst = sb + Lay::RAW + (uint32_t)(idx & 1) * 65536u;
+        const uint32_t mb = smem_u32(mbars);
         const int y = (meta[idx].x * H + h) * 128;
         mbar_expect_tx(mb, 65536u);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) tma_load_2d(dst + p * 16384, &tmap, 32 * p, y, mb);
+        for (int p = 0; p < 4; ++p) tma_load_2d(sb + Lay::RAW + p * 16384, &tmap, 32 * p, y, mb);
     };
-    // k, q, g rows and the raw beta words of unit idx -> KQG / BRAW [idx % NKQG] (all threads);
-    // v rows -> VB[idx % 3] (warps 0-3); rows past the accepted length are zero-filled
-    auto kqg_at = [&](int idx) { return Lay::KQG + (uint32_t)(idx % NKQG) * Lay::KQG_BYTES; };
-    auto prefetch_kqg = [&](int idx) {
+    // token rows of unit idx: k, q, g -> KQG, v -> VB[idx & 1], raw beta words -> BRAW;
+    // rows past the accepted length are zero-filled
+    auto prefetch_tokens = [&](int idx) {
         const int ql = meta[idx].y;
         int r, h;
         unit_rh(idx, r, h);
-        for (int e2 = tid; e2 < 3 * KC * CPR; e2 += kVThreads) {
+        for (int e2 = tid; e2 < 4 * KC * CPR; e2 += kVThreads) {
             const int x = e2 / (KC * CPR), rem = e2 - x * KC * CPR, t = rem / CPR, ch = rem - t * CPR;
-            const void* src = x == 0 ? a.k : x == 1 ? a.q : a.gate_raw;
+            const void* src = x == 0 ? a.k : x == 1 ? a.q : x == 2 ? a.gate_raw : a.v;
             const bool ok = t < ql;
             const size_t e = ok ? (((size_t)r * K + t) * H + h) * 128 : 0;
-            cp_async16(sb + kqg_at(idx) + (uint32_t)((x * KC + t) * 128 * ES + ch * 16),
-                       static_cast<const uint8_t*>(src) + e * ES + (ok ? ch * 16 : 0), ok ? 16u : 0u);
+            const uint32_t dst = x < 3 ? Lay::KQG + (uint32_t)((x * KC + t) * 128 * ES + ch * 16)
+                                       : Lay::VB + (uint32_t)(idx & 1) * Lay::VB_BYTES +
+                                             (uint32_t)(t * 128 * ES + ch * 16);
+            cp_async16(sb + dst, static_cast<const uint8_t*>(src) + e * ES + (ok ? ch * 16 : 0),
+                       ok ? 16u : 0u);
         }
         if (tid < KC) {  // the aligned 4-byte word holding beta of position tid
             const bool ok = tid < ql;
             const size_t e = ok ? ((size_t)r * K + tid) * H + h : 0;
-            cp_async4(sb + Lay::BRAW + (uint32_t)((idx % NKQG) * KC + tid) * 4,
+            cp_async4(sb + Lay::BRAW + (uint32_t)tid * 4,
                       static_cast<const uint8_t*>(a.beta_raw) + ((e * ES) & ~(size_t)3), ok ? 4u : 0u);
         }
     };
-    auto prefetch_v = [&](int idx) {
-        const int ql = meta[idx].y;
-        int r, h;
-        unit_rh(idx, r, h);
-        for (int e2 = tid; e2 < KC * CPR; e2 += 128) {
-            const int t = e2 / CPR, ch = e2 - t * CPR;
-            const bool ok = t < ql;
-            const size_t e = ok ? (((size_t)r * K + t) * H + h) * 128 : 0;
-            cp_async16(sb + Lay::VB + (uint32_t)(idx % 3) * Lay::VB_BYTES + (uint32_t)(t * 128 * ES + ch * 16),
-                       static_cast<const uint8_t*>(a.v) + e * ES + (ok ? ch * 16 : 0), ok ? 16u : 0u);
-        }
-    };
-    // checkpoint rows of ring buffer b, column quarter cq_ -> TMEM operand buffer b (hi | lo)
-    auto convert = [&](int b, int cq_) {
-        const uint8_t* raw = sm + Lay::RAW + (uint32_t)b * 65536u + (uint32_t)cq_ * 16384u;
+    // checkpoint rows, column quarter cq_ (32 columns of row `row`) -> TMEM operand (hi | lo)
+    auto convert = [&](int cq_) {
+        const uint8_t* raw = sm + Lay::RAW + (uint32_t)cq_ * 16384u;
         float x[32];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -273,58 +249,35 @@ __global__ void __launch_bounds__(kVThreads, 1)
             uint32_t sh[8], sl[8];
 #pragma unroll
             for (int q2 = 0; q2 < 8; ++q2) split2(x[16 * hh + 2 * q2], x[16 * hh + 2 * q2 + 1], sh[q2], sl[q2]);
-            const uint32_t col = TV_SA + (uint32_t)b * 128u + (uint32_t)cq_ * 16u + 8u * hh;
+            const uint32_t col = TV_SA + (uint32_t)cq_ * 16u + 8u * hh;
             st8u(tl + col, sh);
             st8u(tl + col + 64, sl);
         }
     };
 
-    // ---- prologue
-    uint32_t raw_pend = 0, mma_pend = 0;  // issued and not yet waited (raw: per ring buffer; mma: per unit % 3)
-    if (meta[0].y > 0) {
-        if (tid == 0) request_ckpt(0);
-        raw_pend |= 1u;
+    // ---- prologue: the first unit's checkpoint and token rows
+    uint32_t ph_raw = 0, ph_mma = 0;
+    bool raw_pend = false, mma_pend = false;
+    if (nu > 0) {
+        if (meta[0].y > 0) {
+            if (tid == 0) request_ckpt(0);
+            raw_pend = true;
+        }
+        prefetch_tokens(0);
+        cp_async_commit();
     }
-    if (nu > 1 && meta[1].y > 0) {
-        if (tid == 0) request_ckpt(1);
-        raw_pend |= 2u;
-    }
-    prefetch_kqg(0);
-    if (warp < 4) prefetch_v(0);
-    cp_async_commit();
-    if (NKQG == 2 && nu > 1) prefetch_kqg(1);
-    cp_async_commit();
-    uint32_t ph_raw = 0, ph_mma = 0;  // phase bits per barrier
     bool timed_out = false;
 
-    for (int it = 0; it < nu + 2; ++it) {
-        const bool have = it < nu;
-        const int buf = it & 1;
-        const int ql = have ? meta[it].y : 0;
-        // ---- this unit's token rows (all but the most recent cp.async group when the k, q, g
-        //      rows run two units ahead), its checkpoint, and the MMAs of the unit two back (their
-        //      accumulator is solved and their operand buffers are rewritten below).  Thread 0
-        //      polls the barriers; the CTA barrier releases everyone else.
-        if (have) {
-            if constexpr (NKQG == 2)
-                cp_async_wait_1();
-            else
-                cp_async_wait_all();
-            if (raw_pend & (1u << buf)) {
-                if (tid == 0 && !mbar_wait(smem_u32(mbars + buf), (ph_raw >> buf) & 1u, kVWaitLimit))
-                    timed_out = true;
-                ph_raw ^= 1u << buf;
-                raw_pend &= ~(1u << buf);
-            }
-        } else {
-            cp_async_wait_all();
-        }
-        if (it >= 2 && (mma_pend & (1u << ((it - 2) % 3)))) {
-            const int pb = (it - 2) % 3;
-            if (tid == 0 && !mbar_wait(smem_u32(mbars + 2 + pb), (ph_mma >> pb) & 1u, kVWaitLimit))
-                timed_out = true;
-            ph_mma ^= 1u << pb;
-            mma_pend &= ~(1u << pb);
+    for (int it = 0; it < nu; ++it) {
+        const int ql = meta[it].y;
+        int r, h;
+        unit_rh(it, r, h);
+        // ---- this unit's checkpoint (thread 0 polls) and token rows
+        cp_async_wait_all();
+        if (raw_pend) {
+            if (tid == 0 && !mbar_wait(smem_u32(mbars), ph_raw, kVWaitLimit)) timed_out = true;
+            ph_raw ^= 1u;
+            raw_pend = false;
         }
         fence_before();
         if (__syncthreads_or(timed_out)) {
@@ -332,272 +285,197 @@ __global__ void __launch_bounds__(kVThreads, 1)
             break;
         }
         fence_after();
-        if (it >= 1 && it <= nu && meta[it - 1].y > 0) mma_pend |= 1u << ((it - 1) % 3);
-
-        // ---- MMAs of the previous unit: D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
-        if (tid == kIssuer && it >= 1 && it <= nu && meta[it - 1].y > 0) {
-            const int u = it - 1, ub = u & 1;
-            const uint32_t id2 = idesc_bf16(128, 2 * NB, false, false, false);
-            const uint32_t id1 = idesc_bf16(128, NB, false, false, false);
-            const uint32_t d = tmem + TV_D + (uint32_t)(u % 3) * (2 * NB);
-            const uint32_t sa = tmem + TV_SA + (uint32_t)ub * 128u;
-            const uint32_t b4 = sb4 + (Lay::BT + (uint32_t)ub * Lay::BT_BYTES) / 16;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) mma_ta(d, sa + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) mma_ta(d, sa + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
-            commit(smem_u32(mbars + 2 + u % 3));
+        if (tid < KC) {
+            float bv = 0.f;
+            if (tid < ql) {
+                const uint32_t w = reinterpret_cast<const uint32_t*>(sm + Lay::BRAW)[tid];
+                const size_t e = ((size_t)r * K + tid) * H + h;
+                bv = beta_act(kBf16In ? __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16))
+                                      : __uint_as_float(w),
+                              a.flags);
+            }
+            sbeta[tid] = bv;
         }
-        if (warp < 4) {
-            // ---- rows of the unit two back: triangular solve, outputs, u records
-            if (it >= 2) {
-                const int pj = it - 2, pb = pj % 3;
-                const int pql = meta[pj].y;
-                int r, h;
-                unit_rh(pj, r, h);
-                const size_t rec0 = ((size_t)r * H + h) * K;
-                const int c = tid;
-                float d[2 * NB];
-                if (pql > 0) {
+        // ---- checkpoint rows -> TMEM operand (all warps, 64 columns each)
+        if (ql > 0) {
+            convert(2 * colhalf);
+            convert(2 * colhalf + 1);
+            wait_st();
+        }
+        // ---- channel i: gates; warps 0-3 the gated keys / queries and the key / raw gate
+        //      records, warps 4-7 the K x K factors
+        {
+            const uint8_t* kqg = sm + Lay::KQG;
+            float kt[KC], qt[KC], at[KC], iv[KC];  // key, scaled query, alpha, 1 / alpha
 #pragma unroll
-                    for (int q16 = 0; q16 < 2 * NB / 16; ++q16) {
-                        float v16[16];
-                        ld16(tl + TV_D + (uint32_t)pb * (2 * NB) + 16 * q16, v16);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) d[16 * q16 + e] = v16[e];
+            for (int t = 0; t < KC; ++t) {
+                kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
+                qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
+                at[t] = iv[t] = 1.f;
+                if (t < ql) {
+                    // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
+                    const float gx = act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i);
+                    if (a.flags & KDA_GATE_LOG) {
+                        at[t] = __expf(gx);
+                        iv[t] = __expf(-gx);
+                    } else {
+                        iv[t] = 1.f + __expf(gx);
+                        at[t] = __fdividef(1.f, iv[t]);
                     }
                 }
-                const bool ok = true;
-                const float* ap = reinterpret_cast<const float*>(sm + Lay::AP) + pb * KC * KC;
-                const uint8_t* vb = sm + Lay::VB + (uint32_t)pb * Lay::VB_BYTES;
-                float u[KC];
+            }
+            if (warp < 4) {
+                uint16_t* bt = reinterpret_cast<uint16_t*>(sm + Lay::BT);
+                auto put = [&](int n, float val) {
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(val - __bfloat162float(hi));
+                    bt[(chunk_k(n, i & ~7, 2 * NB) + (i & 7) * 2) >> 1] = __bfloat16_as_ushort(hi);
+                    bt[(chunk_k(NB + n, i & ~7, 2 * NB) + (i & 7) * 2) >> 1] = __bfloat16_as_ushort(lo);
+                };
+                float cum = 1.f;  // e^{G_t}
 #pragma unroll
                 for (int t = 0; t < KC; ++t) {
-                    u[t] = 0.f;
-                    if (t >= K) continue;
-                    const size_t th = ((size_t)r * K + t) * H + h;
-                    float o = 0.f;
-                    if (t < pql && ok) {
-                        float acc = d[t] + d[NB + t];
-#pragma unroll
-                        for (int s0 = 0; s0 < t; ++s0) acc = fmaf(ap[t * KC + s0], u[s0], acc);
-                        u[t] = sbeta[pb * KC + t] * (act_at<kBf16In>(vb, t * 128 + c) - acc);
-                        o = d[KC + t] + d[NB + KC + t];
-#pragma unroll
-                        for (int s0 = 0; s0 <= t; ++s0) o = fmaf(ap[s0 * KC + t], u[s0], o);
-                    }
-                    store1<kBf16Out>(a.out, th * kD + c, o);
-                    a.rec_u[(rec0 + t) * kD + c] = u[t];
+                    cum *= at[t];
+                    put(t, kt[t] * cum);
+                    put(KC + t, qt[t] * cum);
                 }
-                fence_before();
-                bar_named(2, 128);  // every row of the unit two back has read its v
-            }
-            if (it + 1 < nu) prefetch_v(it + 1);  // into the v buffer of the unit two back
-        } else if (have) {
-            // ---- warps 4-15: this unit's checkpoint rows into TMEM (the MMAs of the unit two
-            //      back, which read the same operand buffers, completed before the barrier above)
-            if (ql > 0) {
-                if (warp < 12) {
-                    convert(buf, warp < 8 ? 1 : 2);
-                } else {
-                    convert(buf, 0);
-                    convert(buf, 3);
-                }
-                wait_st();
-            }
-            if (warp < 12) {
-                // channel i: the gates as running products of alpha; warps 4-7 write the gated
-                // keys / queries (B tile), warps 8-11 the K x K pair factors
-                const int i = tid & 127;
-                const uint8_t* kqg = sm + kqg_at(it);
-                float kt[KC], qt[KC], at[KC], iv[KC];  // key, scaled query, alpha, 1 / alpha
 #pragma unroll
-                for (int t = 0; t < KC; ++t) {
-                    kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
-                    qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
-                    at[t] = iv[t] = 1.f;
-                    if (t < ql) {
-                        // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
-                        const float gx = act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i);
-                        if (a.flags & KDA_GATE_LOG) {
-                            at[t] = __expf(gx);
-                            iv[t] = __expf(-gx);
-                        } else {
-                            iv[t] = 1.f + __expf(gx);
-                            at[t] = __fdividef(1.f, iv[t]);
-                        }
-                    }
-                }
-                if (warp < 8) {
-                    uint16_t* bt = reinterpret_cast<uint16_t*>(sm + Lay::BT + (uint32_t)buf * Lay::BT_BYTES);
-                    auto put = [&](int n, float val) {
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(val);
-                        const __nv_bfloat16 lo = __float2bfloat16_rn(val - __bfloat162float(hi));
-                        bt[(chunk_k(n, i & ~7, 2 * NB) + (i & 7) * 2) >> 1] = __bfloat16_as_ushort(hi);
-                        bt[(chunk_k(NB + n, i & ~7, 2 * NB) + (i & 7) * 2) >> 1] = __bfloat16_as_ushort(lo);
-                    };
-                    float cum = 1.f;  // e^{G_t}
-#pragma unroll
-                    for (int t = 0; t < KC; ++t) {
-                        cum *= at[t];
-                        put(t, kt[t] * cum);
-                        put(KC + t, qt[t] * cum);
-                    }
-#pragma unroll
-                    for (int n = 2 * KC; n < NB; ++n) put(n, 0.f);
-                } else {
-                    const int wg = warp - 8;
-                    float* ap = reinterpret_cast<float*>(sm + Lay::AP) + (it % 3) * KC * KC;
-                    bool fallback = true;
-                    if constexpr (KC <= 8) {
-                        // Tables with the reference at position m = KC/2 (factors span at most KC/2
-                        // steps): L_k[t] = k_t e^{G_t - G_m}, L_q[t] = q_t e^{G_t - G_m},
-                        // R[s] = k_s e^{G_m - G_s}; then A_ts = L_k[t] . R[s], P_ts = L_q[t] . R[s].
-                        constexpr int MID = KC / 2, TLD = Lay::TLD;
-                        float* lk = reinterpret_cast<float*>(sm + Lay::TAB);
-                        float* lq = lk + KC * TLD;
-                        float* rk = lq + KC * TLD;
-                        lk[MID * TLD + i] = kt[MID];
-                        lq[MID * TLD + i] = qt[MID];
-                        rk[MID * TLD + i] = kt[MID];
-                        float e = 1.f, rf = 1.f;
-#pragma unroll
-                        for (int t = MID + 1; t < KC; ++t) {
-                            e *= at[t];
-                            rf *= iv[t];
-                            lk[t * TLD + i] = kt[t] * e;
-                            lq[t * TLD + i] = qt[t] * e;
-                            rk[t * TLD + i] = kt[t] * rf;
-                        }
-                        float big = rf;
-                        e = rf = 1.f;
-#pragma unroll
-                        for (int t = MID - 1; t >= 0; --t) {
-                            e *= iv[t + 1];
-                            rf *= at[t + 1];
-                            lk[t * TLD + i] = kt[t] * e;
-                            lq[t * TLD + i] = qt[t] * e;
-                            rk[t * TLD + i] = kt[t] * rf;
-                        }
-                        big = fmaxf(big, e);
-                        fallback = bar_named_or(1, 128, !(big <= kVFactorMax));
-                        if (!fallback) {
-                            // entry [x0][x1]: P (query x1, key x0) if x0 <= x1, else A (x0, x1); two
-                            // threads per entry, 64 channels each
-                            constexpr int NIT = KC * KC * 2;
-                            constexpr unsigned MASK = NIT >= 32 ? 0xffffffffu : (1u << NIT) - 1u;
-                            for (int e2 = i; e2 < NIT; e2 += 128) {
-                                const int entry = e2 >> 1, half = e2 & 1;
-                                const int x0 = entry / KC, x1 = entry - x0 * KC;
-                                const float* lrow = (x0 <= x1 ? lq + x1 * TLD : lk + x0 * TLD) + 64 * half;
-                                const float* rrow = rk + (x0 <= x1 ? x0 : x1) * TLD + 64 * half;
-                                float acc = 0.f;
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) {
-                                    const float4 l4 = *reinterpret_cast<const float4*>(lrow + 4 * j);
-                                    const float4 r4 = *reinterpret_cast<const float4*>(rrow + 4 * j);
-                                    acc = fmaf(l4.x, r4.x, acc);
-                                    acc = fmaf(l4.y, r4.y, acc);
-                                    acc = fmaf(l4.z, r4.z, acc);
-                                    acc = fmaf(l4.w, r4.w, acc);
-                                }
-                                acc += __shfl_xor_sync(MASK, acc, 1);
-                                if (half == 0) ap[entry] = acc;
-                            }
-                        }
-                    }
-                    if (fallback) {
-                        float(*red)[KC][KC] = reinterpret_cast<float(*)[KC][KC]>(sm + Lay::RED);
-                        // pair sums over channels, e^{G_t - G_s} as running products of alpha:
-                        // value [a][b] = P_ab (a <= b) or A_ab (a > b), summed over the warp's 32 channels
-                        if constexpr (KC <= 8) {
-                            constexpr int NV = KC * KC < 32 ? 32 : KC * KC;
-                            float vals[NV];
-#pragma unroll
-                            for (int e = 0; e < NV; ++e) vals[e] = 0.f;
-#pragma unroll
-                            for (int s0 = 0; s0 < KC; ++s0) {
-                                float dec = 1.f;
-#pragma unroll
-                                for (int t = s0; t < KC; ++t) {
-                                    if (t > s0) dec *= at[t];
-                                    const bool live = t < ql;
-                                    vals[s0 * KC + t] = live ? qt[t] * kt[s0] * dec : 0.f;
-                                    if (t > s0) vals[t * KC + s0] = live ? kt[t] * kt[s0] * dec : 0.f;
-                                }
-                            }
-                            // butterfly reduce-scatter: lane l ends with the totals of entries l*M .. l*M+M-1
-                            int nn = NV;
-#pragma unroll
-                            for (int off = 16; off >= 1; off >>= 1) {
-                                const bool upper = (lane & off) != 0;
-                                const int half = nn / 2;
-#pragma unroll
-                                for (int e = 0; e < NV / 2; ++e) {
-                                    if (e < half) {
-                                        const float send = upper ? vals[e] : vals[e + half];
-                                        const float keep = upper ? vals[e + half] : vals[e];
-                                        vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                                    }
-                                }
-                                nn = half;
-                            }
-                            constexpr int M = NV / 32;
-#pragma unroll
-                            for (int e = 0; e < M; ++e) {
-                                const int idx = lane * M + e;
-                                if (idx < KC * KC) red[wg][idx / KC][idx % KC] = vals[e];
-                            }
-                        } else {
-#pragma unroll
-                            for (int s0 = 0; s0 < KC; ++s0) {
-                                float dec = 1.f;
-#pragma unroll
-                                for (int t = s0; t < KC; ++t) {
-                                    if (t > s0) dec *= at[t];
-                                    const bool live = t < ql;
-                                    const float pp = warp_sum(live ? qt[t] * kt[s0] * dec : 0.f);
-                                    if (lane == 0) red[wg][s0][t] = pp;
-                                    if (t > s0) {
-                                        const float pa = warp_sum(live ? kt[t] * kt[s0] * dec : 0.f);
-                                        if (lane == 0) red[wg][t][s0] = pa;
-                                    }
-                                }
-                            }
-                        }
-                        bar_named(1, 128);  // warps 8-11
-                        for (int e = i; e < KC * KC; e += 128) {
-                            const int x0 = e / KC, x1 = e - x0 * KC;
-                            ap[e] = (red[0][x0][x1] + red[1][x0][x1]) + (red[2][x0][x1] + red[3][x0][x1]);
-                        }
-                    }
-                }
-            } else {
-                // warps 12-15: activated beta, and the key and raw gate records exactly as given
-                // (zeros past the accepted length)
-                int r, h;
-                unit_rh(it, r, h);
-                if (tid - 384 < KC) {
-                    const int t = tid - 384;
-                    float bv = 0.f;
-                    if (t < ql) {
-                        const uint32_t w = reinterpret_cast<const uint32_t*>(sm + Lay::BRAW)[(it % NKQG) * KC + t];
-                        const size_t e = ((size_t)r * K + t) * H + h;
-                        bv = beta_act(kBf16In ? __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16))
-                                              : __uint_as_float(w),
-                                      a.flags);
-                    }
-                    sbeta[(it % 3) * KC + t] = bv;
-                }
+                for (int n = 2 * KC; n < NB; ++n) put(n, 0.f);
+                // records: key and raw gate exactly as given, zeros past the accepted length
                 const size_t rec0 = ((size_t)r * H + h) * K;
-                for (int e = tid - 384; e < 2 * K * CPR; e += 128) {
+                for (int e = tid; e < 2 * K * CPR; e += 128) {
                     const int t = e / (2 * CPR), rem = e - t * 2 * CPR, half = rem / CPR, ch = rem - half * CPR;
                     uint4 val = make_uint4(0u, 0u, 0u, 0u);
                     if (t < ql)
                         val = *reinterpret_cast<const uint4*>(
-                            sm + kqg_at(it) + (uint32_t)(((half ? 2 * KC : 0) + t) * 128 * ES + ch * 16));
+                            sm + Lay::KQG + (uint32_t)(((half ? 2 * KC : 0) + t) * 128 * ES + ch * 16));
                     *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.rec_kg) +
                                               ((rec0 + t) * 2 * 128 + half * 128) * ES + ch * 16) = val;
+                }
+            } else {
+                const int wg = warp - 4;
+                bool fallback = true;
+                if constexpr (KC <= 8) {
+                    // Tables with the reference at position m = KC/2 (factors span at most KC/2
+                    // steps): L_k[t] = k_t e^{G_t - G_m}, L_q[t] = q_t e^{G_t - G_m},
+                    // R[s] = k_s e^{G_m - G_s}; then A_ts = L_k[t] . R[s], P_ts = L_q[t] . R[s].
+                    constexpr int MID = KC / 2, TLD = Lay::TLD;
+                    float* lk = reinterpret_cast<float*>(sm + Lay::TAB);
+                    float* lq = lk + KC * TLD;
+                    float* rk = lq + KC * TLD;
+                    lk[MID * TLD + i] = kt[MID];
+                    lq[MID * TLD + i] = qt[MID];
+                    rk[MID * TLD + i] = kt[MID];
+                    float e = 1.f, rf = 1.f;
+#pragma unroll
+                    for (int t = MID + 1; t < KC; ++t) {
+                        e *= at[t];
+                        rf *= iv[t];
+                        lk[t * TLD + i] = kt[t] * e;
+                        lq[t * TLD + i] = qt[t] * e;
+                        rk[t * TLD + i] = kt[t] * rf;
+                    }
+                    float big = rf;
+                    e = rf = 1.f;
+#pragma unroll
+                    for (int t = MID - 1; t >= 0; --t) {
+                        e *= iv[t + 1];
+                        rf *= at[t + 1];
+                        lk[t * TLD + i] = kt[t] * e;
+                        lq[t * TLD + i] = qt[t] * e;
+                        rk[t * TLD + i] = kt[t] * rf;
+                    }
+                    big = fmaxf(big, e);
+                    fallback = bar_named_or(1, 128, !(big <= kVFactorMax));
+                    if (!fallback) {
+                        // entry [x0][x1]: P (query x1, key x0) if x0 <= x1, else A (x0, x1); two
+                        // threads per entry, 64 channels each
+                        constexpr int NIT = KC * KC * 2;
+                        constexpr unsigned MASK = NIT >= 32 ? 0xffffffffu : (1u << NIT) - 1u;
+                        for (int e2 = i; e2 < NIT; e2 += 128) {
+                            const int entry = e2 >> 1, half = e2 & 1;
+                            const int x0 = entry / KC, x1 = entry - x0 * KC;
+                            const float* lrow = (x0 <= x1 ? lq + x1 * TLD : lk + x0 * TLD) + 64 * half;
+                            const float* rrow = rk + (x0 <= x1 ? x0 : x1) * TLD + 64 * half;
+                            float acc = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float4 l4 = *reinterpret_cast<const float4*>(lrow + 4 * j);
+                                const float4 r4 = *reinterpret_cast<const float4*>(rrow + 4 * j);
+                                acc = fmaf(l4.x, r4.x, acc);
+                                acc = fmaf(l4.y, r4.y, acc);
+                                acc = fmaf(l4.z, r4.z, acc);
+                                acc = fmaf(l4.w, r4.w, acc);
+                            }
+                            acc += __shfl_xor_sync(MASK, acc, 1);
+                            if (half == 0) ap[entry] = acc;
+                        }
+                    }
+                }
+                if (fallback) {
+                    // pair sums over channels, e^{G_t - G_s} as running products of alpha:
+                    // value [x0][x1] = P (x0 <= x1) or A (x0 > x1), summed over the warp's channels
+                    float(*red)[KC][KC] = reinterpret_cast<float(*)[KC][KC]>(sm + Lay::RED);
+                    if constexpr (KC <= 8) {
+                        constexpr int NV = KC * KC < 32 ? 32 : KC * KC;
+                        float vals[NV];
+#pragma unroll
+                        for (int e = 0; e < NV; ++e) vals[e] = 0.f;
+#pragma unroll
+                        for (int s0 = 0; s0 < KC; ++s0) {
+                            float dec = 1.f;
+#pragma unroll
+                            for (int t = s0; t < KC; ++t) {
+                                if (t > s0) dec *= at[t];
+                                const bool live = t < ql;
+                                vals[s0 * KC + t] = live ? qt[t] * kt[s0] * dec : 0.f;
+                                if (t > s0) vals[t * KC + s0] = live ? kt[t] * kt[s0] * dec : 0.f;
+                            }
+                        }
+                        // butterfly reduce-scatter: lane l ends with the totals of entries l*M .. l*M+M-1
+                        int nn = NV;
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1) {
+                            const bool upper = (lane & off) != 0;
+                            const int half = nn / 2;
+#pragma unroll
+                            for (int e = 0; e < NV / 2; ++e) {
+                                if (e < half) {
+                                    const float send = upper ? vals[e] : vals[e + half];
+                                    const float keep = upper ? vals[e + half] : vals[e];
+                                    vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                }
+                            }
+                            nn = half;
+                        }
+                        constexpr int M = NV / 32;
+#pragma unroll
+                        for (int e = 0; e < M; ++e) {
+                            const int idx = lane * M + e;
+                            if (idx < KC * KC) red[wg][idx / KC][idx % KC] = vals[e];
+                        }
+                    } else {
+#pragma unroll
+                        for (int s0 = 0; s0 < KC; ++s0) {
+                            float dec = 1.f;
+#pragma unroll
+                            for (int t = s0; t < KC; ++t) {
+                                if (t > s0) dec *= at[t];
+                                const bool live = t < ql;
+                                const float pp = warp_sum(live ? qt[t] * kt[s0] * dec : 0.f);
+                                if (lane == 0) red[wg][s0][t] = pp;
+                                if (t > s0) {
+                                    const float pa = warp_sum(live ? kt[t] * kt[s0] * dec : 0.f);
+                                    if (lane == 0) red[wg][t][s0] = pa;
+                                }
+                            }
+                        }
+                    }
+                    bar_named(1, 128);  // warps 4-7
+                    for (int e = i; e < KC * KC; e += 128) {
+                        const int x0 = e / KC, x1 = e - x0 * KC;
+                        ap[e] = (red[0][x0][x1] + red[1][x0][x1]) + (red[2][x0][x1] + red[3][x0][x1]);
+                    }
                 }
             }
         }
@@ -605,36 +483,94 @@ __global__ void __launch_bounds__(kVThreads, 1)
         fence_before();
         __syncthreads();
         fence_after();
-        // ---- the checkpoint two units ahead (into the ring buffer read above) and the k, q, g
-        //      rows NKQG units ahead
-        if (have) {
-            if (it + 2 < nu && meta[it + 2].y > 0) {
-                if (tid == 0) {
-                    fence_async_smem();
-                    request_ckpt(it + 2);
-                }
-                raw_pend |= 1u << buf;
+        // ---- the next unit's checkpoint (RAW has been converted) and token rows, then this
+        //      unit's MMAs: D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
+        if (it + 1 < nu) {
+            if (meta[it + 1].y > 0) {
+                if (tid == 0) request_ckpt(it + 1);
+                raw_pend = true;
             }
-            if (it + NKQG < nu) prefetch_kqg(it + NKQG);
         }
+        if (ql > 0) {
+            if (tid == 0) {
+                const uint32_t id2 = idesc_bf16(128, 2 * NB, false, false, false);
+                const uint32_t id1 = idesc_bf16(128, NB, false, false, false);
+                const uint32_t b4 = sb4 + Lay::BT / 16;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_ta(tmem + TV_D, tmem + TV_SA + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_ta(tmem + TV_D, tmem + TV_SA + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
+                commit(smem_u32(mbars + 1));
+            }
+            mma_pend = true;
+        }
+        // v rows of this unit stay in VB[it & 1] for the solve; the next unit's go to the other
+        if (it + 1 < nu) prefetch_tokens(it + 1);
         cp_async_commit();
+        if (mma_pend) {
+            if (tid == 0 && !mbar_wait(smem_u32(mbars + 1), ph_mma, kVWaitLimit)) timed_out = true;
+            ph_mma ^= 1u;
+            mma_pend = false;
+        }
+        fence_before();
+        if (__syncthreads_or(timed_out)) {
+            timed_out = true;
+            break;
+        }
+        fence_after();
+        // ---- rows (warps 0-3): triangular solve, outputs, u records
+        if (warp < 4) {
+            const size_t rec0 = ((size_t)r * H + h) * K;
+            const int c = tid;
+            float d[2 * NB];
+            if (ql > 0) {
+#pragma unroll
+                for (int q16 = 0; q16 < 2 * NB / 16; ++q16) {
+                    float v16[16];
+                    ld16(tl + TV_D + 16 * q16, v16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) d[16 * q16 + e] = v16[e];
+                }
+            }
+            const uint8_t* vb = sm + Lay::VB + (uint32_t)(it & 1) * Lay::VB_BYTES;
+            float u[KC];
+#pragma unroll
+            for (int t = 0; t < KC; ++t) {
+                u[t] = 0.f;
+                if (t >= K) continue;
+                const size_t th = ((size_t)r * K + t) * H + h;
+                float o = 0.f;
+                if (t < ql) {
+                    float acc = d[t] + d[NB + t];
+#pragma unroll
+                    for (int s0 = 0; s0 < t; ++s0) acc = fmaf(ap[t * KC + s0], u[s0], acc);
+                    u[t] = sbeta[t] * (act_at<kBf16In>(vb, t * 128 + c) - acc);
+                    o = d[KC + t] + d[NB + KC + t];
+#pragma unroll
+                    for (int s0 = 0; s0 <= t; ++s0) o = fmaf(ap[s0 * KC + t], u[s0], o);
+                }
+                store1<kBf16Out>(a.out, th * kD + c, o);
+                a.rec_u[(rec0 + t) * kD + c] = u[t];
+            }
+            fence_before();
+        }
     }
     cp_async_wait_all();
     timed_out = __syncthreads_or(timed_out);
     if (timed_out) {
-        if (tid == 0) report(a.dev_status, KDA_DEV_TIMEOUT);
-        // bounded drain of what is still in flight before shared memory and TMEM are released
         if (tid == 0) {
-            for (int b = 0; b < 2; ++b)
-                if (raw_pend & (1u << b)) mbar_wait(smem_u32(mbars + b), (ph_raw >> b) & 1u, kVWaitLimit);
-            for (int b = 0; b < 3; ++b)
-                if (mma_pend & (1u << b)) mbar_wait(smem_u32(mbars + 2 + b), (ph_mma >> b) & 1u, kVWaitLimit);
+            report(a.dev_status, KDA_DEV_TIMEOUT);
+            // bounded drain of what is still in flight before shared memory and TMEM are released
+            if (raw_pend) mbar_wait(smem_u32(mbars), ph_raw, kVWaitLimit);
+            if (mma_pend) mbar_wait(smem_u32(mbars + 1), ph_mma, kVWaitLimit);
         }
     }
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, TV_COLS);
 }
 
 // The tensor map's encoder from the driver, looked up once.
@@ -663,13 +599,19 @@ int sm_count() {
 template <int KC, bool I, bool O>
 kda_status launch_kc(const CUtensorMap& map, const VerifyArgs& a, cudaStream_t s) {
     constexpr size_t smem = VLayout<KC, I ? 2 : 4>::SMEM;
-    static_assert(smem <= 232448, "verify shared memory plan exceeds the per-CTA limit");
     const int nsm = sm_count();
     if (nsm <= 0) return KDA_ERR_CUDA;
-    int grid = a.n_units < nsm ? a.n_units : nsm;
+    cudaFuncSetAttribute(verify_kernel<KC, I, O>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // all of the unified L1 / shared storage as shared memory, so two CTAs fit on an SM
+    cudaFuncSetAttribute(verify_kernel<KC, I, O>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    // two CTAs per SM when two shared-memory plans (plus the 1 KiB each CTA reserves) fit in an
+    // SM's 228 KiB; registers allow two by the launch bounds, TMEM by 2 x 256 columns
+    const int per_sm = 2 * (smem + 1024) <= 233472 ? 2 : 1;
+    int grid = nsm * per_sm;
+    if (grid > a.n_units) grid = a.n_units;
     const int need = (a.n_units + kMaxUnitsPerCta - 1) / kMaxUnitsPerCta;
     if (grid < need) grid = need;
-    cudaFuncSetAttribute(verify_kernel<KC, I, O>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     verify_kernel<KC, I, O><<<(unsigned)grid, kVThreads, smem, s>>>(map, a);
     return launch_status();
 }
