@@ -252,7 +252,7 @@ class Step:
 
     # name -> (callable, kernel launches)
     def calls(self):
-        return [("prefill", self.prefill, 1), ("decode", self.decode, 1),
+        return [("prefill", self.prefill, 2), ("decode", self.decode, 1),
                 ("verify", self.verify, 1), ("commit", self.commit, 1),
                 ("slot_copy", self.slot_copy, 2)]
 
