@@ -298,23 +298,59 @@ def run_device(step, steps, warmup, rank, world):
 
 
 def run_e2e(step, steps, warmup):
-    """Prefill through the public call with host buffers: pinned H2D of the inputs,
-    the call, D2H of the output, all inside the timed region."""
+    """Prefill through the public call with host buffers, streamed per sequence: the pinned
+    H2D copies of a sequence's inputs (one stream, longest sequence first), its
+    kda_chunk_prefill call (one stream per sequence, so sequences overlap on the GPU) and the
+    D2H copy of its output rows (one stream) overlap with the other sequences' copies and
+    compute; everything is inside the timed region.  Every sequence is independent, so the
+    outputs, final states and snapshots are those of the one-call prefill."""
     import torch
 
-    stream = torch.cuda.current_stream()
+    c1 = step.c1
+    cu = c1["cu_seqlens"]
+    N = int(c1["N"])
+    order = sorted(range(N), key=lambda n: -(int(cu[n + 1]) - int(cu[n])))
     dev_in = step.pre
-    h2d = sum(t.numel() * t.element_size() for t in step.pre_host.values())
-    h2d += step.c1["cu_seqlens"].nbytes
+    host_in = step.pre_host
+    cu_host = [torch.tensor([0, int(cu[n + 1]) - int(cu[n])], dtype=torch.int32).pin_memory()
+               for n in range(N)]
+    cu_dev = [torch.empty(2, dtype=torch.int32, device=step.dev) for _ in range(N)]
+    # per-sequence slot / snapshot index arrays (own 16-byte-aligned allocations), resident like
+    # the pool, as in the one-call prefill
+    slot_n = [step.slots1[n:n + 1].clone() for n in range(N)]
+    track_n = [step.track1[n:n + 1].clone() for n in range(N)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + 8 * N
     d2h = step.out1.numel() * step.out1.element_size()
-    cu_host = torch.from_numpy(step.c1["cu_seqlens"]).pin_memory()
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    s_cmp = [torch.cuda.Stream() for _ in range(N)]
+    main = torch.cuda.current_stream()
 
     def once():
-        for n, t in step.pre_host.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        step.cu.copy_(cu_host, non_blocking=True)
-        step.prefill(dev_in)
-        step.out1_host.copy_(step.out1, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(main)
+        s_h2d.wait_event(start)
+        for n in order:
+            a, b = int(cu[n]), int(cu[n + 1])
+            with torch.cuda.stream(s_h2d):
+                for name, t in host_in.items():
+                    dev_in[name][a:b].copy_(t[a:b], non_blocking=True)
+                cu_dev[n].copy_(cu_host[n], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_h2d)
+            s_cmp[n].wait_event(ready)
+            with torch.cuda.stream(s_cmp[n]):
+                step.kda.kda_chunk_prefill(
+                    dev_in["q"][a:b], dev_in["k"][a:b], dev_in["v"][a:b], dev_in["beta"][a:b],
+                    dev_in["gate"][a:b], cu_dev[n], step.out1[a:b], state_pool=step.pool1,
+                    init_slot=slot_n[n], final_slot=slot_n[n],
+                    track_chunk_idx=track_n[n], track_state=step.snap1[n:n + 1],
+                    dev_status=step.status, stream=s_cmp[n])
+                done = torch.cuda.Event()
+                done.record(s_cmp[n])
+            s_d2h.wait_event(done)
+            with torch.cuda.stream(s_d2h):
+                step.out1_host[a:b].copy_(step.out1[a:b], non_blocking=True)
+        main.wait_stream(s_d2h)
 
     for _ in range(warmup):
         step.flush.zero_()
@@ -325,9 +361,9 @@ def run_e2e(step, steps, warmup):
         step.flush.zero_()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        a.record(main)
         once()
-        b.record(stream)
+        b.record(main)
         b.synchronize()
         ts.append(a.elapsed_time(b) * 1e-3)
     return statistics.mean(ts), h2d, d2h
