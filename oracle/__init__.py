@@ -17,6 +17,8 @@ Contents
     (RecoverSSM page, implementation breakdown step 4: rebuild the state in
     one shot in reverse order, not by re-running the recursion).
   * ``slot_copy`` and ``commit_plan`` -- memcpy and integer semantics.
+  * ``accept`` -- the accepted length of each speculative request from its
+    draft and sampled token ids (integer semantics).
 
 All arrays are float64 numpy arrays (bf16 inputs widened exactly by the
 caller).  Layouts follow the library: activations [tokens, heads, channels],
@@ -331,3 +333,41 @@ def commit_plan(ckpt, num_accepted, P, K, dst=None, q_len=None):
         ok = 0 <= src < P and 0 <= d < P and 0 <= ql <= K and 0 <= a <= ql
         plan[r] = (a if ok else -1, src, d)
     return plan
+
+
+def accept(tokens, sampled, K, q_len=None):
+    """Runtime accepted length per request (RecoverSSM page, implementation
+    breakdown step 4: the commit plan derives the accepted lengths on the GPU,
+    and num_accepted_tokens is written straight back to device buffers).
+
+    tokens[r, 0] is the request's last committed token and tokens[r, 1:q_len]
+    its drafts; sampled[r, i] is the target model's token for the position
+    after i.  Drafts are kept from the front while draft i+1 equals sampled
+    token i; the first mismatch ends the run.  The accepted length a counts the
+    positions whose update the state keeps: the committed token plus every
+    kept draft, so 1 <= a <= q_len.  The next input token is sampled[r, a-1].
+    q_len = 0 (a padding row) gives a = 0 and next = -1; q_len outside [0, K]
+    gives a = -1, next = -1 and the BAD_ACCEPT status bit.
+
+    Returns (a [R] int32, next [R] int32, status)."""
+    tokens = np.asarray(tokens, np.int64)
+    sampled = np.asarray(sampled, np.int64)
+    R = tokens.shape[0]
+    a_out = np.zeros(R, np.int32)
+    nxt = np.zeros(R, np.int32)
+    status = 0
+    for r in range(R):
+        ql = int(q_len[r]) if q_len is not None else K
+        if ql < 0 or ql > K:
+            a_out[r], nxt[r] = -1, -1
+            status |= BAD_ACCEPT
+            continue
+        if ql == 0:
+            a_out[r], nxt[r] = 0, -1
+            continue
+        kept = 0
+        while kept < ql - 1 and tokens[r, kept + 1] == sampled[r, kept]:
+            kept += 1
+        a_out[r] = kept + 1
+        nxt[r] = sampled[r, kept]
+    return a_out, nxt, status

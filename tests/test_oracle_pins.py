@@ -315,6 +315,61 @@ def test_commit_plan_and_invalid_requests():
     np.testing.assert_array_equal(newp[[2, 3, 4]], pool[[2, 3, 4]])  # skipped
 
 
+def _accept_bruteforce(tok, smp, ql):
+    """Largest j in [1, ql] whose first j-1 drafts equal the first j-1 sampled
+    tokens, found by trying every j (a maximum over prefixes, not a scan)."""
+    return max(j for j in range(1, ql + 1) if np.array_equal(tok[1:j], smp[:j - 1]))
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_accept_exhaustive_on_a_binary_alphabet(K):
+    """Every (drafts, sampled, q_len) over ids {0, 1}: the accepted length is the
+    longest agreeing prefix, and the tokens the step emits (kept drafts, then
+    the next token) are exactly the target's first a sampled tokens."""
+    import itertools
+    rows = [np.array(c, np.int32) for c in itertools.product([0, 1], repeat=K)]
+    for tok in rows:
+        for smp in rows:
+            for ql in range(0, K + 1):
+                a, nxt, st = oracle.accept(tok[None], smp[None], K, q_len=[ql])
+                assert st == 0
+                if ql == 0:
+                    assert (a[0], nxt[0]) == (0, -1)
+                    continue
+                assert a[0] == _accept_bruteforce(tok, smp, ql)
+                emitted = list(tok[1:a[0]]) + [nxt[0]]
+                assert emitted == list(smp[:a[0]])
+                assert a[0] == ql or tok[a[0]] != smp[a[0] - 1]
+
+
+def test_accept_special_cases_and_bad_lengths():
+    K = 5
+    tok = np.array([[7, 1, 2, 3, 4]] * 6, np.int32)
+    smp = np.array([[1, 2, 3, 4, 9],    # every draft agrees: a = q_len, bonus token next
+                    [5, 2, 3, 4, 9],    # the first draft disagrees: a = 1
+                    [1, 2, 8, 4, 9],    # agreement stops at the third draft
+                    [1, 2, 3, 4, 9],    # draftless request (q_len 1)
+                    [1, 2, 3, 4, 9],    # padding row (q_len 0)
+                    [1, 2, 3, 4, 9]],   # q_len past K
+                   np.int32)
+    ql = [5, 5, 5, 1, 0, 6]
+    a, nxt, st = oracle.accept(tok, smp, K, q_len=ql)
+    assert a.tolist() == [5, 1, 3, 1, 0, -1]
+    assert nxt.tolist() == [9, 5, 8, 1, -1, -1]
+    assert st == oracle.BAD_ACCEPT
+    _, _, st = oracle.accept(tok[:1], smp[:1], K, q_len=[-1])
+    assert st == oracle.BAD_ACCEPT
+    # q_len omitted means K; ids at or past q_len never matter
+    a2, _, _ = oracle.accept(tok[:1], smp[:1], K)
+    assert a2[0] == 5
+    junk = smp.copy()
+    junk[2, 3:] = [11, 12]
+    tok2 = tok.copy()
+    tok2[2, 4] = 13
+    a3, n3, _ = oracle.accept(tok2[2:3], junk[2:3], K, q_len=[3])
+    assert (a3[0], n3[0]) == (3, 8)
+
+
 def test_decode_skips_negative_slots():
     rng = np.random.default_rng(25)
     q, k, v, beta, gate = _rand_inputs(rng, 2, 1, 4, 4)

@@ -143,6 +143,22 @@ def spec_case(seed, R, K, H, *, P=None, dk=128, dv=128, dtype="bf16", q_len=None
                 q_len=ql, num_accepted=acc)
 
 
+def accept_case(seed, R, K, *, q_len=None, p_match=0.7, vocab=1 << 17):
+    """Draft and sampled token ids for R speculative requests of up to K
+    positions.  tokens[r, 0] is the last committed id, tokens[r, 1:] the drafts;
+    sampled[r, i] repeats draft i+1 with probability p_match and is a fresh
+    uniform id otherwise, so runs of agreement have a geometric length.
+    Entries at or past q_len are junk ids that the acceptance must ignore."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ql = np.full(R, K, np.int32) if q_len is None else np.asarray(q_len, np.int32)
+    tokens = rng.integers(0, vocab, size=(R, K), dtype=np.int64).astype(np.int32)
+    fresh = rng.integers(0, vocab, size=(R, K), dtype=np.int64).astype(np.int32)
+    keep = rng.random((R, K)) < p_match
+    sampled = fresh.copy()
+    sampled[:, :K - 1] = np.where(keep[:, :K - 1], tokens[:, 1:], fresh[:, :K - 1])
+    return dict(tokens=tokens, sampled=sampled, q_len=ql, R=R, K=K)
+
+
 def slot_copy_case(seed, P, n_src, fan_out, n_clear):
     """Disjoint parents, children and clears drawn from a P-slot pool."""
     rng = np.random.Generator(np.random.PCG64(seed))
