@@ -6,7 +6,10 @@ One step = one pass of every entry point over one batch of synthetic input:
                            d=128, chunk 64, bf16 in/out, fp32 state pool (64 slots,
                            in-place init/final) and one fp32 snapshot per sequence.
   * kda_recurrent_decode : 256 requests x 1 token, H=32, 1024-slot fp32 pool.
-  * kda_spec_verify + kda_spec_commit : 64 requests, K=7, H=32, in-place commit.
+  * kda_spec_verify + kda_spec_accept_commit : 64 requests, K=7, H=32; each
+                           draft agrees with the sampled token with probability
+                           0.7; the commit launch derives the accepted lengths
+                           from the token ids and rebuilds the states in place.
   * kda_slot_copy        : 256 parents x 8 children + 512 clears, 4096-slot pool
                            of 1 MiB fp32 states (H=16).
 `value` is the prefill throughput in tokens/s (device time of the prefill call,
@@ -81,8 +84,11 @@ def verify_work(R, K, H):
     return R * H * (STATE_BYTES + K * (4 * D * 2 + 2 + D * 2 + D * 4 + 2 * D * 2))
 
 
-def commit_work(acc, H):
-    return sum(H * (2 * STATE_BYTES + a * (D * 4 + 2 * D * 2)) for a in acc if a > 0)
+def commit_work(acc, H, K):
+    """Checkpoint read + state write and the a kept records per (request, head),
+    plus the token ids read and the lengths / next tokens written once each."""
+    ids = len(acc) * (2 * K * 4 + 2 * 4)
+    return ids + sum(H * (2 * STATE_BYTES + a * (D * 4 + 2 * D * 2)) for a in acc if a > 0)
 
 
 # --------------------------------------------------------------------------
@@ -204,7 +210,10 @@ class Step:
         self.spec = {n: to_dev(c3[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
         self.pool3 = torch.from_numpy(c3["pool"]).to(dev)
         self.ckpt3 = i32(c3["ckpt"], dev)
-        self.acc3 = i32(c3["num_accepted"], dev)
+        a3 = W.accept_case(3, 64, 7, p_match=0.7)
+        self.tok3, self.smp3 = i32(a3["tokens"], dev), i32(a3["sampled"], dev)
+        self.acc3 = torch.empty(64, dtype=torch.int32, device=dev)
+        self.next3 = torch.empty(64, dtype=torch.int32, device=dev)
         self.rec_u = torch.empty(64, 32, 7, D, device=dev)
         self.rec_kg = torch.empty(64, 32, 7, 2 * D, dtype=torch.bfloat16, device=dev)
         self.out3 = torch.empty(64 * 7, 32, D, dtype=torch.bfloat16, device=dev)
@@ -242,8 +251,10 @@ class Step:
                                  dev_status=self.status)
 
     def commit(self):
-        self.kda.kda_spec_commit(self.pool3, self.ckpt3, self.acc3, self.rec_u, self.rec_kg, K=7,
-                                 dev_status=self.status)
+        # accepted lengths from the token ids and the rebuild, one launch
+        self.kda.kda_spec_accept_commit(self.pool3, self.ckpt3, self.tok3, self.smp3, self.rec_u,
+                                        self.rec_kg, num_accepted=self.acc3,
+                                        next_token=self.next3, dev_status=self.status)
 
     def slot_copy(self):
         c = self.c4
@@ -459,7 +470,8 @@ def config_block():
     lengths = W.cfg1_lengths()
     return {"workload": (f"batched chunk prefill: 8 packed seqs, lengths {lengths} "
                          f"(sum {sum(lengths)}), H=32, d_k=d_v=128, chunk=64, bf16 in/out, "
-                         "fp32 state; step also runs decode 256xH32, spec verify+commit "
+                         "fp32 state; step also runs decode 256xH32, spec verify + fused "
+                         "accept/commit "
                          "64xK7xH32, slot copy 256x8 + 512 clears of 1 MiB states"),
             "global_batch": 8, "seq_len": max(lengths), "tokens": sum(lengths),
             "l2": "flushed (256 MiB write) before every timed call",
@@ -574,7 +586,7 @@ def main():
     t_hbm, t_tc = pb / (hbm * 1e9), pf / (tc * 1e12)
     dec_b = decode_work(256, 32)
     ver_b = verify_work(64, 7, 32)
-    com_b = commit_work(step.c3["num_accepted"].tolist(), 32)
+    com_b = commit_work(step.acc3.cpu().tolist(), 32, 7)
     cp_b = STATE_BYTES * 16 * (sum(step.n4))
     parts = {
         "prefill": {"us": mean["prefill"] * 1e6, "tokens_per_s": toks / mean["prefill"],
@@ -585,6 +597,7 @@ def main():
         "verify": {"us": mean["verify"] * 1e6, "bytes": ver_b,
                    "hbm_frac": ver_b / (hbm * 1e9) / mean["verify"]},
         "commit": {"us": mean["commit"] * 1e6, "bytes": com_b,
+                   "mean_accepted": float(step.acc3.float().mean().item()),
                    "hbm_frac": com_b / (hbm * 1e9) / mean["commit"]},
         "verify_commit_us_per_step": (mean["verify"] + mean["commit"]) * 1e6,
         "slot_copy": {"us": mean["slot_copy"] * 1e6, "bytes": cp_b,

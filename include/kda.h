@@ -166,6 +166,31 @@ kda_status kda_spec_verify(const void* q, const void* k, const void* v, const vo
                            kda_dtype out_dtype, int32_t* dev_status, void* stream);
 
 /*
+ * kda_spec_accept -- the accepted length of every speculative request, on the
+ * device (vLLM PR 51855 page, implementation breakdown item 4: the commit plan
+ * computes the runtime accepted lengths on the GPU, and num_accepted_tokens is
+ * written straight back to GPU buffers).  Its output feeds kda_spec_commit on
+ * the same stream with no host synchronisation.
+ *
+ *   tokens       : [R, K] int32, the verify step's input ids; tokens[r][0] is
+ *                  the last committed token, tokens[r][1..q_len_r-1] the drafts.
+ *   sampled      : [R, K] int32, the target's sampled ids; sampled[r][i] is the
+ *                  token for the position after i.
+ *   q_len        : [R] or NULL (= K).  Ids at or past q_len_r are never read.
+ *   num_accepted : [R] int32 out.  a_r = 1 + the number of leading drafts with
+ *                  tokens[r][i+1] == sampled[r][i]; 1 <= a_r <= q_len_r.
+ *                  q_len_r = 0 gives 0; q_len_r outside [0, K] gives -1 and
+ *                  KDA_DEV_BAD_ACCEPT (kda_spec_commit then skips the request).
+ *   next_token   : [R] int32 out or NULL: sampled[r][a_r - 1], the next input
+ *                  (the first rejected draft's replacement, or the bonus
+ *                  token when every draft is kept); -1 when a_r <= 0.
+ * 1 <= K <= 32 (else KDA_ERR_UNSUPPORTED).  Integer work: results are exact.
+ */
+kda_status kda_spec_accept(const int32_t* tokens, const int32_t* sampled, const int32_t* q_len,
+                           int32_t R, int32_t K, int32_t* num_accepted, int32_t* next_token,
+                           int32_t* dev_status, void* stream);
+
+/*
  * kda_spec_commit -- rebuild the state at the accepted length a_r in closed
  * form (vLLM PR 51855 page, implementation breakdown item 4: the commit plan
  * computes accepted lengths on the GPU, the commit kernel rebuilds the state
@@ -189,6 +214,29 @@ kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_t* ckpt_slo
                            int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
                            kda_dtype rec_dtype, int32_t* plan_out, int32_t* dev_status,
                            void* stream);
+
+/*
+ * kda_spec_accept_commit -- kda_spec_accept and kda_spec_commit in one launch:
+ * every commit block derives its request's accepted length from the token ids
+ * itself (same rule as kda_spec_accept), so the plan and the rebuild of the
+ * vLLM PR 51855 page (implementation breakdown item 4) cost one launch on the
+ * step's critical path.
+ *
+ *   tokens, sampled : [R, K] int32, as for kda_spec_accept (1 <= K <= 32).
+ *   num_accepted    : [R] int32 out or NULL: the accepted lengths (-1 for a
+ *                     q_len outside [0, K]).
+ *   next_token      : [R] int32 out or NULL, as for kda_spec_accept.
+ *   Every other argument is as for kda_spec_commit; the plan rows, the pool
+ *   and dev_status come out exactly as kda_spec_accept followed by
+ *   kda_spec_commit would leave them.
+ */
+kda_status kda_spec_accept_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+                                  const int32_t* dst_slot, const int32_t* tokens,
+                                  const int32_t* sampled, const int32_t* q_len, int32_t R,
+                                  int32_t K, int32_t H, int32_t dk, int32_t dv, uint32_t flags,
+                                  const float* rec_u, const void* rec_kg, kda_dtype rec_dtype,
+                                  int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,
+                                  int32_t* dev_status, void* stream);
 
 /*
  * kda_slot_copy -- one fused launch that clears, copies and fans out state

@@ -6,8 +6,8 @@ arithmetic runs in the library's CUDA kernels.  There is no CPU fallback: if
 libkda.so is missing the import of the library raises.
 
 Entry points (same names as the C ABI):
-  kda_chunk_prefill, kda_recurrent_decode, kda_spec_verify, kda_spec_commit,
-  kda_slot_copy, kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
+  kda_chunk_prefill, kda_recurrent_decode, kda_spec_verify, kda_spec_accept, kda_spec_commit,
+  kda_spec_accept_commit, kda_slot_copy, kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
 """
 from __future__ import annotations
 
@@ -18,8 +18,10 @@ import torch
 
 __all__ = [
     "KDA_BF16", "KDA_F32", "KDA_GATE_LOG", "KDA_BETA_ACT", "KdaError", "lib",
-    "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_commit",
-    "kda_slot_copy", "kda_chunk_prefill_workspace_size", "kda_slot_copy_workspace_size",
+    "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
+    "kda_spec_commit", "kda_spec_accept_commit", "kda_slot_copy",
+    "kda_chunk_prefill_workspace_size",
+    "kda_slot_copy_workspace_size",
     "kda_status_string", "kda_abi_version", "PoolDesc",
 ]
 
@@ -63,6 +65,9 @@ def lib():
                                       i32, f32, u32, vp, i64, vp, vp, vp, vp, ctypes.c_int, vp, vp]
         L.kda_spec_commit.argtypes = [vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, i32, u32, vp,
                                       vp, ctypes.c_int, vp, vp, vp]
+        L.kda_spec_accept.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp]
+        L.kda_spec_accept_commit.argtypes = [vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                             u32, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp]
         L.kda_slot_copy.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp, i32, i32,
                                     vp, sz, vp, vp]
         L.kda_slot_copy_noalloc.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp,
@@ -76,7 +81,8 @@ def lib():
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_abi_version.restype = i32
         for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify",
-                  "kda_spec_commit", "kda_slot_copy"):
+                  "kda_spec_accept", "kda_spec_commit", "kda_spec_accept_commit",
+                  "kda_slot_copy"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -180,6 +186,17 @@ def kda_spec_verify(q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, r
     _check(st, "kda_spec_verify")
 
 
+def kda_spec_accept(tokens, sampled, num_accepted, *, q_len=None, next_token=None,
+                    dev_status=None, stream=None):
+    """Accepted length per request from draft vs sampled ids (see include/kda.h).
+
+    tokens, sampled: int32 CUDA tensors [R, K]."""
+    R, K = tokens.shape
+    st = lib().kda_spec_accept(_p(tokens), _p(sampled), _p(q_len), R, K, _p(num_accepted),
+                               _p(next_token), _p(dev_status), _stream(stream))
+    _check(st, "kda_spec_accept")
+
+
 def kda_spec_commit(state_pool, ckpt_slot, num_accepted, rec_u, rec_kg, *, K, dst_slot=None,
                     q_len=None, flags=0, plan_out=None, dev_status=None, stream=None):
     """Closed-form rebuild at the accepted length (see include/kda.h)."""
@@ -190,6 +207,20 @@ def kda_spec_commit(state_pool, ckpt_slot, num_accepted, rec_u, rec_kg, *, K, ds
         dk, dv, int(flags), _p(rec_u), _p(rec_kg), _dt(rec_kg), _p(plan_out), _p(dev_status),
         _stream(stream))
     _check(st, "kda_spec_commit")
+
+
+def kda_spec_accept_commit(state_pool, ckpt_slot, tokens, sampled, rec_u, rec_kg, *,
+                           dst_slot=None, q_len=None, flags=0, num_accepted=None,
+                           next_token=None, plan_out=None, dev_status=None, stream=None):
+    """Accepted lengths from token ids and the closed-form rebuild, one launch
+    (see include/kda.h).  tokens, sampled: int32 CUDA tensors [R, K]."""
+    P, H, dv, dk = state_pool.shape
+    R, K = tokens.shape
+    st = lib().kda_spec_accept_commit(
+        _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(tokens), _p(sampled), _p(q_len), R,
+        K, H, dk, dv, int(flags), _p(rec_u), _p(rec_kg), _dt(rec_kg), _p(num_accepted),
+        _p(next_token), _p(plan_out), _p(dev_status), _stream(stream))
+    _check(st, "kda_spec_accept_commit")
 
 
 def kda_slot_copy(pools, clear_slots, src_slots, dst_offsets, dst_slots, workspace, *,

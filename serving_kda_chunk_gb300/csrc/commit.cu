@@ -32,10 +32,21 @@ constexpr int kCommitThreads = 128;  // 4 warps x 8 rows: a quarter of a state p
 constexpr int kRowsPerWarp = 8;
 constexpr int kCtasPerUnit = kD / (4 * kRowsPerWarp);
 
-template <bool kBf16Rec>
+// Accepted lengths: read from num_accepted, or (kTokens) found by every warp
+// of every CTA from the request's token ids, with the lengths and next tokens
+// written out once per request.
+struct AcceptArgs {
+    const int32_t* acc;      // [R] accepted lengths (plain commit)
+    const int32_t* tokens;   // [R, K] verify input ids (kTokens)
+    const int32_t* sampled;  // [R, K] sampled ids (kTokens)
+    int32_t* acc_out;        // [R] or null (kTokens)
+    int32_t* next_out;       // [R] or null (kTokens)
+};
+
+template <bool kBf16Rec, bool kTokens>
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     float* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
-    const int32_t* __restrict__ dst, const int32_t* __restrict__ acc,
+    const int32_t* __restrict__ dst, const AcceptArgs acc_args,
     const int32_t* __restrict__ q_len, int32_t K, int32_t H, uint32_t flags,
     const float* __restrict__ rec_u, const void* __restrict__ rec_kg, int32_t* __restrict__ plan_out,
     int32_t* __restrict__ dev_status) {
@@ -53,10 +64,19 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     const int src = ckpt[r];
     const int d = dst ? dst[r] : src;
     const int ql = q_len ? q_len[r] : K;
-    const int a = acc[r];
+    int a;
+    if constexpr (kTokens)
+        a = accepted_length(acc_args.tokens, acc_args.sampled, (size_t)r * K, ql, K, lane);
+    else
+        a = acc_args.acc[r];
     const bool slot_ok = src >= 0 && src < P && d >= 0 && d < P;
     const bool ok = slot_ok && ql >= 0 && ql <= K && a >= 0 && a <= ql;
     if (h == 0 && part == 0 && threadIdx.x == 0) {
+        if constexpr (kTokens) {
+            if (acc_args.acc_out) acc_args.acc_out[r] = a;
+            if (acc_args.next_out)
+                acc_args.next_out[r] = a > 0 ? acc_args.sampled[(size_t)r * K + a - 1] : -1;
+        }
         if (plan_out) {
             plan_out[3 * r + 0] = ok ? a : -1;
             plan_out[3 * r + 1] = src;
@@ -137,6 +157,47 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
         __stcs(reinterpret_cast<float4*>(SD + (size_t)(row0 + i) * kD) + lane, s[i]);
 }
 
+// Host checks and the launch shared by both commit entry points.
+kda_status launch_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+                         const int32_t* dst_slot, const AcceptArgs& acc, bool from_tokens,
+                         const int32_t* q_len, int32_t R, int32_t K, int32_t H, int32_t dk,
+                         int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
+                         kda_dtype rec_dtype, int32_t* plan_out, int32_t* dev_status,
+                         void* stream) {
+    KDA_REQUIRE(R >= 0 && K >= 0 && H > 0 && P >= 0, KDA_ERR_INVALID_ARG);
+    KDA_REQUIRE(dk == kD && dv == kD, KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE(dtype_ok(rec_dtype), KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE(K <= kMaxCommitK, KDA_ERR_UNSUPPORTED);
+    if (R == 0) return KDA_OK;
+    KDA_REQUIRE((int64_t)R * H < (1ll << 30), KDA_ERR_UNSUPPORTED);
+    const void* ptrs[] = {state_pool, ckpt_slot, rec_u, rec_kg};
+    for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
+    if (from_tokens) {
+        KDA_REQUIRE(K >= 1, KDA_ERR_INVALID_ARG);
+        const void* tok[] = {acc.tokens, acc.sampled};
+        for (const void* p : tok) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
+        const void* opt[] = {acc.acc_out, acc.next_out};
+        for (const void* p : opt) KDA_REQUIRE(p == nullptr || aligned16(p), KDA_ERR_INVALID_ARG);
+    } else {
+        KDA_REQUIRE(acc.acc != nullptr && aligned16(acc.acc), KDA_ERR_INVALID_ARG);
+    }
+    cudaStream_t s = as_stream(stream);
+    const size_t es = rec_dtype == KDA_BF16 ? 2 : 4;
+    const size_t smem = (size_t)(K * kD + K * 4 * kRowsPerWarp + kD) * sizeof(float) + (size_t)K * 2 * kD * es;
+    const unsigned grid = (unsigned)(kCtasPerUnit * R * H);
+    auto run = [&](auto kernel) {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kernel<<<grid, kCommitThreads, smem, s>>>(state_pool, P, ckpt_slot, dst_slot, acc, q_len, K,
+                                                  H, flags, rec_u, rec_kg, plan_out, dev_status);
+    };
+    if (rec_dtype == KDA_BF16)
+        from_tokens ? run(commit_kernel<true, true>) : run(commit_kernel<true, false>);
+    else
+        from_tokens ? run(commit_kernel<false, true>) : run(commit_kernel<false, false>);
+    return launch_status();
+}
+
 }  // namespace
 }  // namespace kda
 
@@ -148,28 +209,18 @@ extern "C" kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_
                                       int32_t dk, int32_t dv, uint32_t flags, const float* rec_u,
                                       const void* rec_kg, kda_dtype rec_dtype, int32_t* plan_out,
                                       int32_t* dev_status, void* stream) {
-    KDA_REQUIRE(R >= 0 && K >= 0 && H > 0 && P >= 0, KDA_ERR_INVALID_ARG);
-    KDA_REQUIRE(dk == kD && dv == kD, KDA_ERR_UNSUPPORTED);
-    KDA_REQUIRE(dtype_ok(rec_dtype), KDA_ERR_UNSUPPORTED);
-    KDA_REQUIRE(K <= kMaxCommitK, KDA_ERR_UNSUPPORTED);
-    if (R == 0) return KDA_OK;
-    KDA_REQUIRE((int64_t)R * H < (1ll << 30), KDA_ERR_UNSUPPORTED);
-    const void* ptrs[] = {state_pool, ckpt_slot, num_accepted, rec_u, rec_kg};
-    for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
-    cudaStream_t s = as_stream(stream);
-    const size_t es = rec_dtype == KDA_BF16 ? 2 : 4;
-    const size_t smem = (size_t)(K * kD + K * 4 * kRowsPerWarp + kD) * sizeof(float) + (size_t)K * 2 * kD * es;
-    if (smem > 48 * 1024) {
-        cudaFuncSetAttribute(commit_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(commit_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    }
-    if (rec_dtype == KDA_BF16)
-        commit_kernel<true><<<(unsigned)(kCtasPerUnit * R * H), kCommitThreads, smem, s>>>(
-            state_pool, P, ckpt_slot, dst_slot, num_accepted, q_len, K, H, flags, rec_u, rec_kg,
-            plan_out, dev_status);
-    else
-        commit_kernel<false><<<(unsigned)(kCtasPerUnit * R * H), kCommitThreads, smem, s>>>(
-            state_pool, P, ckpt_slot, dst_slot, num_accepted, q_len, K, H, flags, rec_u, rec_kg,
-            plan_out, dev_status);
-    return launch_status();
+    const AcceptArgs acc{num_accepted, nullptr, nullptr, nullptr, nullptr};
+    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, false, q_len, R, K, H, dk, dv,
+                         flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
+}
+
+extern "C" kda_status kda_spec_accept_commit(
+    float* state_pool, int64_t P, const int32_t* ckpt_slot, const int32_t* dst_slot,
+    const int32_t* tokens, const int32_t* sampled, const int32_t* q_len, int32_t R, int32_t K,
+    int32_t H, int32_t dk, int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
+    kda_dtype rec_dtype, int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,
+    int32_t* dev_status, void* stream) {
+    const AcceptArgs acc{nullptr, tokens, sampled, num_accepted, next_token};
+    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, true, q_len, R, K, H, dk, dv,
+                         flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
 }

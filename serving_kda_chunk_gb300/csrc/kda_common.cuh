@@ -108,6 +108,22 @@ __device__ __forceinline__ void report(int32_t* dev_status, int32_t bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Accepted length of one speculative request from the verify step's input ids
+// and the target's sampled ids (the request's rows start at `row`): 1 + the
+// number of leading drafts tokens[i+1] equal to sampled[i], so 1 <= a <= q_len;
+// 0 when q_len = 0 and -1 when q_len lies outside [0, K].  Warp-collective:
+// all 32 lanes call it for the same request; K <= 32, and no id at or past
+// q_len is read.
+__device__ __forceinline__ int accepted_length(const int32_t* __restrict__ tokens,
+                                               const int32_t* __restrict__ sampled, size_t row,
+                                               int ql, int K, int lane) {
+    if (ql < 0 || ql > K) return -1;
+    if (ql == 0) return 0;
+    // lane < ql - 1 implies lane + 1 < ql <= K; lane ql - 1 <= 31 always counts as a miss
+    const bool miss = lane >= ql - 1 || tokens[row + lane + 1] != sampled[row + lane];
+    return __ffs(__ballot_sync(0xffffffffu, miss));
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

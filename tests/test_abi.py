@@ -26,10 +26,10 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
 
 
-def test_header_declares_the_five_entry_points():
+def test_header_declares_the_entry_points():
     names = declared_functions()
-    for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_commit",
-              "kda_slot_copy"):
+    for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
+              "kda_spec_commit", "kda_slot_copy"):
         assert f in names
 
 
@@ -43,7 +43,7 @@ def test_status_strings_and_version(kda):
     assert kda.kda_status_string(0) == "KDA_OK"
     assert "INVALID_ARG" in kda.kda_status_string(1)
     assert "UNSUPPORTED" in kda.kda_status_string(2)
-    assert kda.kda_abi_version() >= 100
+    assert kda.kda_abi_version() >= 101
 
 
 def test_workspace_sizes(kda):
@@ -78,6 +78,19 @@ def test_host_checks_reject_bad_arguments(kda):
     st = L.kda_spec_commit(FAKE, 8, FAKE, None, FAKE, None, 4, 1000, 2, 128, 128, 0, FAKE, FAKE,
                            0, None, None, None)
     assert st == 2
+    # accept: K = 0, K above one warp, null or misaligned pointers
+    assert L.kda_spec_accept(FAKE, FAKE, None, 4, 0, FAKE, None, None, None) == 1
+    assert L.kda_spec_accept(FAKE, FAKE, None, 4, 33, FAKE, None, None, None) == 2
+    assert L.kda_spec_accept(FAKE, None, None, 4, 7, FAKE, None, None, None) == 1
+    assert L.kda_spec_accept(FAKE, FAKE, FAKE + 4, 4, 7, FAKE, None, None, None) == 1
+    assert L.kda_spec_accept(FAKE, FAKE, None, 4, 7, FAKE, FAKE + 8, None, None) == 1
+    assert L.kda_spec_accept(None, None, None, 0, 7, None, None, None, None) == 0
+    # fused accept + commit: missing sampled ids, K = 0, K above one warp
+    args = lambda tok, smp, K: (FAKE, 8, FAKE, None, tok, smp, None, 4, K, 2, 128, 128, 0,  # noqa: E731
+                                FAKE, FAKE, 0, None, None, None, None, None)
+    assert L.kda_spec_accept_commit(*args(FAKE, None, 7)) == 1
+    assert L.kda_spec_accept_commit(*args(FAKE, FAKE, 0)) == 1
+    assert L.kda_spec_accept_commit(*args(FAKE, FAKE, 33)) == 2
     # prefill: chunk other than 64
     st = L.kda_chunk_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 64, 2, 128, 128, 32, 1.0,
                              0, None, 0, None, None, None, 0, None, FAKE, 0, None, 0, None, None)

@@ -128,6 +128,41 @@ def test_cfg3_spec_verify_commit_full(kda):
     assert np.array_equal(pool.cpu().numpy()[zero], s["pool"][zero])
 
 
+def test_cfg3_accept_commit_chain_full(kda):
+    """The serving spec workload with accepted lengths computed on the device:
+    verify -> accept -> commit with no host round trip, and the fused
+    accept + commit launch that the benchmark times."""
+    s = W.cfg3()
+    c = W.accept_case(3, 64, 7, p_match=0.7)
+    pool = torch.from_numpy(s["pool"]).cuda()
+    pool_fused = pool.clone()
+    rec_u = torch.empty(64, 32, 7, 128, device="cuda")
+    rec_kg = torch.empty(64, 32, 7, 256, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(448, 32, 128, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(64, dtype=torch.int32, device="cuda")
+    acc_fused = torch.empty(64, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(64, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_spec_verify(*(dev_tensor(s[n], "bf16") for n in ("q", "k", "v", "beta", "gate")),
+                        pool, i32(s["ckpt"]), rec_u, rec_kg, out, K=7, dev_status=st)
+    kda.kda_spec_accept(i32(c["tokens"]), i32(c["sampled"]), acc, next_token=nxt, dev_status=st)
+    kda.kda_spec_commit(pool, i32(s["ckpt"]), acc, rec_u, rec_kg, K=7, dev_status=st)
+    # the fused launch the benchmark times leaves the same bits
+    kda.kda_spec_accept_commit(pool_fused, i32(s["ckpt"]), i32(c["tokens"]), i32(c["sampled"]),
+                               rec_u, rec_kg, num_accepted=acc_fused, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(pool_fused, pool) and torch.equal(acc_fused, acc)
+    a_ref, n_ref, _ = oracle.accept(c["tokens"], c["sampled"], 7)
+    assert np.array_equal(acc.cpu().numpy(), a_ref)
+    assert np.array_equal(nxt.cpu().numpy(), n_ref)
+    wid = lambda n: W.widen(s[n], "bf16")  # noqa: E731
+    _, ru_ref, rkg_ref, _ = oracle.verify(wid("q"), wid("k"), wid("v"), wid("beta"), wid("gate"),
+                                          s["pool"], s["ckpt"], 7)
+    p_ref, _, _ = oracle.commit(s["pool"], s["ckpt"], a_ref, ru_ref, rkg_ref, 7)
+    assert rel_l2(pool.cpu().numpy(), p_ref) < TOL_STATE
+
+
 def test_cfg4_long_prefill_sampled_heads(kda):
     c = W.cfg4_prefill()
     c["final_slot"] = np.array([0], np.int32)
