@@ -30,8 +30,9 @@
  *     beta is [rows, H].  `in_dtype` gives their element type (bf16 or fp32).
  *     Outputs are [rows, H, d_v] of `out_dtype`; bf16 outputs are rounded to
  *     nearest-even from the fp32 result.
- *   - States are fp32 and stored transposed: pool[slot][h][v][k] = S[k][v]
- *     (d_v rows of d_k contiguous floats, 64 KiB per head).
+ *   - States are stored transposed: pool[slot][h][v][k] = S[k][v] (d_v rows
+ *     of d_k contiguous elements): fp32 (64 KiB per head) unless flags hold
+ *     KDA_STATE_BF16 or KDA_STATE_F16 (32 KiB per head); see below.
  *   - d_k = d_v = 128 and chunk = 64 are the supported shapes; others return
  *     KDA_ERR_UNSUPPORTED.  Every device pointer must be 16-byte aligned.
  *   - Host-checkable errors (null pointer, bad size, misalignment) return a
@@ -41,6 +42,7 @@
  *     NULL) and the offending unit is skipped; kernels never trap.
  *   - flags: KDA_GATE_LOG = the gate input already holds g (log decay);
  *     KDA_BETA_ACT = the beta input already holds beta.  Default: both raw.
+ *     KDA_STATE_BF16 / KDA_STATE_F16 = the state type (default fp32).
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -67,6 +69,16 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  * of chunk by chunk on the tensor cores; used to measure the chunk-vs-recurrent
  * numerical gap ("state semantics" page, section 4 and its open item). */
 #define KDA_PREFILL_RECURRENT 4u
+/* Element type of every state the call reads or writes (pool slots, and the
+ * prefill's snapshots): fp32 by default, bf16 or fp16 with one of these bits
+ * (both set: KDA_ERR_UNSUPPORTED).  Computation stays fp32; loads widen
+ * exactly and each store rounds the fp32 result once, to nearest even, into
+ * the slot's type (SGLang PR 34820 page, key files: the fp32 snapshot is
+ * converted exactly once into the pool dtype, and an fp16 pool is never
+ * rounded through bf16 on the way).  A 16-bit state slot is 32 KiB per head;
+ * the pool layout is otherwise unchanged. */
+#define KDA_STATE_BF16 8u
+#define KDA_STATE_F16 16u
 
 /* bits OR-ed into *dev_status by the kernels */
 #define KDA_DEV_BAD_SLOT 1     /* slot index >= pool size (or required and < 0) */
@@ -88,7 +100,7 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *                    cu_seqlens[N] <= T_tot.  Sequence n is rows
  *                    [cu_seqlens[n], cu_seqlens[n+1]); chunks restart at each
  *                    sequence start and the last chunk may be partial.
- *   state_pool     : [P, H, d_v, d_k] fp32.  init_slot[n] >= 0 reads the
+ *   state_pool     : [P, H, d_v, d_k] states.  init_slot[n] >= 0 reads the
  *                    initial state from that slot (< 0: zero state);
  *                    final_slot[n] >= 0 receives the state after the whole
  *                    sequence (< 0: not written).  init and final may be the
@@ -98,9 +110,9 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *                    asks for the fp32 state after exactly j*chunk tokens of the
  *                    sequence (j = 0 is the initial state), j in
  *                    [0, n_chunks-1]; -1 = unused.
- *   track_state    : [N, M, H, d_v, d_k] fp32 snapshots (written only for
- *                    valid entries; the fp32 accumulator itself, never a
- *                    rounded copy).
+ *   track_state    : [N, M, H, d_v, d_k] snapshots in the state type (written
+ *                    only for valid entries; the fp32 accumulator itself, or
+ *                    with a 16-bit state type that accumulator rounded once).
  *   out            : [T_tot, H, d_v] out_dtype.
  *   workspace      : optional device scratch of ws_bytes >=
  *                    kda_chunk_prefill_workspace_size(...) bytes.  With it the
@@ -113,9 +125,9 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* beta_raw,
                              const void* gate_raw, kda_dtype in_dtype, const int32_t* cu_seqlens,
                              int32_t N, int32_t T_tot, int32_t H, int32_t dk, int32_t dv,
-                             int32_t chunk, float scale, uint32_t flags, float* state_pool,
+                             int32_t chunk, float scale, uint32_t flags, void* state_pool,
                              int64_t P, const int32_t* init_slot, const int32_t* final_slot,
-                             const int32_t* track_chunk_idx, int32_t M, float* track_state,
+                             const int32_t* track_chunk_idx, int32_t M, void* track_state,
                              void* out, kda_dtype out_dtype, void* workspace, size_t ws_bytes,
                              int32_t* dev_status, void* stream);
 
@@ -124,7 +136,7 @@ size_t kda_chunk_prefill_workspace_size(int32_t T_tot, int32_t N, int32_t H, int
 
 /*
  * kda_recurrent_decode -- one token per request, state updated in place in a
- * slot-indexed fp32 pool ("state semantics" page, section 4: decode applies
+ * slot-indexed state pool ("state semantics" page, section 4: decode applies
  * the gate activation inside the kernel).
  *
  *   q, k, gate_raw : [R, H, d_k];  v : [R, H, d_v];  beta_raw : [R, H]
@@ -137,7 +149,7 @@ size_t kda_chunk_prefill_workspace_size(int32_t T_tot, int32_t N, int32_t H, int
 kda_status kda_recurrent_decode(const void* q, const void* k, const void* v, const void* beta_raw,
                                 const void* gate_raw, kda_dtype in_dtype, int32_t R, int32_t H,
                                 int32_t dk, int32_t dv, float scale, uint32_t flags,
-                                float* state_pool, int64_t P, const int32_t* slot, void* out,
+                                void* state_pool, int64_t P, const int32_t* slot, void* out,
                                 kda_dtype out_dtype, int32_t* dev_status, void* stream);
 
 /*
@@ -161,7 +173,7 @@ kda_status kda_recurrent_decode(const void* q, const void* k, const void* v, con
 kda_status kda_spec_verify(const void* q, const void* k, const void* v, const void* beta_raw,
                            const void* gate_raw, kda_dtype in_dtype, int32_t R, int32_t K,
                            const int32_t* q_len, int32_t H, int32_t dk, int32_t dv, float scale,
-                           uint32_t flags, const float* state_pool, int64_t P,
+                           uint32_t flags, const void* state_pool, int64_t P,
                            const int32_t* ckpt_slot, float* rec_u, void* rec_kg, void* out,
                            kda_dtype out_dtype, int32_t* dev_status, void* stream);
 
@@ -208,7 +220,7 @@ kda_status kda_spec_accept(const int32_t* tokens, const int32_t* sampled, const 
  * a = 0 writes nothing when dst == src and copies S_0 otherwise.  Destinations
  * must be distinct and must not be another request's checkpoint.
  */
-kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                            const int32_t* dst_slot, const int32_t* num_accepted,
                            const int32_t* q_len, int32_t R, int32_t K, int32_t H, int32_t dk,
                            int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
@@ -230,7 +242,7 @@ kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_t* ckpt_slo
  *   and dev_status come out exactly as kda_spec_accept followed by
  *   kda_spec_commit would leave them.
  */
-kda_status kda_spec_accept_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+kda_status kda_spec_accept_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                                   const int32_t* dst_slot, const int32_t* tokens,
                                   const int32_t* sampled, const int32_t* q_len, int32_t R,
                                   int32_t K, int32_t H, int32_t dk, int32_t dv, uint32_t flags,

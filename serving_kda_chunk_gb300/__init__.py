@@ -17,7 +17,8 @@ from pathlib import Path
 import torch
 
 __all__ = [
-    "KDA_BF16", "KDA_F32", "KDA_GATE_LOG", "KDA_BETA_ACT", "KdaError", "lib",
+    "KDA_BF16", "KDA_F32", "KDA_GATE_LOG", "KDA_BETA_ACT", "KDA_STATE_BF16", "KDA_STATE_F16",
+    "KdaError", "lib",
     "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
     "kda_spec_commit", "kda_spec_accept_commit", "kda_slot_copy",
     "kda_chunk_prefill_workspace_size",
@@ -27,6 +28,7 @@ __all__ = [
 
 KDA_BF16, KDA_F32 = 0, 1
 KDA_GATE_LOG, KDA_BETA_ACT, KDA_PREFILL_RECURRENT = 1, 2, 4
+KDA_STATE_BF16, KDA_STATE_F16 = 8, 16
 KDA_DEV_BAD_SLOT, KDA_DEV_BAD_TRACK, KDA_DEV_BAD_ACCEPT = 1, 2, 4
 KDA_DEV_BAD_SEQLEN, KDA_DEV_OVERLAP, KDA_DEV_TIMEOUT = 8, 16, 32
 KDA_MAX_POOLS = 16
@@ -126,6 +128,22 @@ def _stream(stream):
     return int(stream)
 
 
+def _state_flag(*states) -> int:
+    """The state-type flag bit for the given state tensors (None entries are
+    ignored); every one of them must have the same dtype."""
+    dts = {t.dtype for t in states if t is not None}
+    if len(dts) > 1:
+        raise ValueError(f"state tensors of different dtypes: {dts}")
+    dt = dts.pop() if dts else torch.float32
+    if dt == torch.float32:
+        return 0
+    if dt == torch.bfloat16:
+        return KDA_STATE_BF16
+    if dt == torch.float16:
+        return KDA_STATE_F16
+    raise ValueError(f"unsupported state dtype {dt}")
+
+
 def _check(status: int, where: str):
     if status != 0:
         raise KdaError(status, where)
@@ -155,7 +173,8 @@ def kda_chunk_prefill(q, k, v, beta_raw, gate_raw, cu_seqlens, out, *, state_poo
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().kda_chunk_prefill(
         _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), _p(cu_seqlens), N, T_tot, H, dk,
-        dv, chunk, float(scale), int(flags), _p(state_pool), P, _p(init_slot), _p(final_slot),
+        dv, chunk, float(scale), int(flags) | _state_flag(state_pool, track_state),
+        _p(state_pool), P, _p(init_slot), _p(final_slot),
         _p(track_chunk_idx), M, _p(track_state), _p(out), _dt(out), _p(workspace), ws_bytes,
         _p(dev_status), _stream(stream))
     _check(st, "kda_chunk_prefill")
@@ -168,7 +187,8 @@ def kda_recurrent_decode(q, k, v, beta_raw, gate_raw, state_pool, slot, out, *, 
     dv = v.shape[2]
     st = lib().kda_recurrent_decode(
         _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), R, H, dk, dv, float(scale),
-        int(flags), _p(state_pool), int(state_pool.shape[0]), _p(slot), _p(out), _dt(out),
+        int(flags) | _state_flag(state_pool), _p(state_pool), int(state_pool.shape[0]),
+        _p(slot), _p(out), _dt(out),
         _p(dev_status), _stream(stream))
     _check(st, "kda_recurrent_decode")
 
@@ -181,7 +201,8 @@ def kda_spec_verify(q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, r
     R = RK // K
     st = lib().kda_spec_verify(
         _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), R, K, _p(q_len), H, dk, dv,
-        float(scale), int(flags), _p(state_pool), int(state_pool.shape[0]), _p(ckpt_slot),
+        float(scale), int(flags) | _state_flag(state_pool), _p(state_pool),
+        int(state_pool.shape[0]), _p(ckpt_slot),
         _p(rec_u), _p(rec_kg), _p(out), _dt(out), _p(dev_status), _stream(stream))
     _check(st, "kda_spec_verify")
 
@@ -204,8 +225,8 @@ def kda_spec_commit(state_pool, ckpt_slot, num_accepted, rec_u, rec_kg, *, K, ds
     R = ckpt_slot.shape[0]
     st = lib().kda_spec_commit(
         _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(num_accepted), _p(q_len), R, K, H,
-        dk, dv, int(flags), _p(rec_u), _p(rec_kg), _dt(rec_kg), _p(plan_out), _p(dev_status),
-        _stream(stream))
+        dk, dv, int(flags) | _state_flag(state_pool), _p(rec_u), _p(rec_kg), _dt(rec_kg),
+        _p(plan_out), _p(dev_status), _stream(stream))
     _check(st, "kda_spec_commit")
 
 
@@ -218,8 +239,8 @@ def kda_spec_accept_commit(state_pool, ckpt_slot, tokens, sampled, rec_u, rec_kg
     R, K = tokens.shape
     st = lib().kda_spec_accept_commit(
         _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(tokens), _p(sampled), _p(q_len), R,
-        K, H, dk, dv, int(flags), _p(rec_u), _p(rec_kg), _dt(rec_kg), _p(num_accepted),
-        _p(next_token), _p(plan_out), _p(dev_status), _stream(stream))
+        K, H, dk, dv, int(flags) | _state_flag(state_pool), _p(rec_u), _p(rec_kg), _dt(rec_kg),
+        _p(num_accepted), _p(next_token), _p(plan_out), _p(dev_status), _stream(stream))
     _check(st, "kda_spec_accept_commit")
 
 

@@ -17,8 +17,11 @@
 // cp.async.  Threads then walk the records backwards per key channel to form
 // F_t = exp(c_t) k_t and the total decay exp(c_0) as running products of
 // alpha = exp(g) = 1 / (1 + e^x), and each warp streams 8 rows of S^T: 16 KiB
-// per CTA read from the checkpoint and written to the destination slot (in
-// place allowed: each element is read and written by the same thread).
+// per CTA (8 KiB for 16-bit states) read from the checkpoint and written to
+// the destination slot (in place allowed: each element is read and written by
+// the same thread).
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "kda_host.h"
 #include "umma.cuh"
@@ -43,9 +46,9 @@ struct AcceptArgs {
     int32_t* next_out;       // [R] or null (kTokens)
 };
 
-template <bool kBf16Rec, bool kTokens>
+template <bool kBf16Rec, bool kTokens, int ST>
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
-    float* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
+    void* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
     const int32_t* __restrict__ dst, const AcceptArgs acc_args,
     const int32_t* __restrict__ q_len, int32_t K, int32_t H, uint32_t flags,
     const float* __restrict__ rec_u, const void* __restrict__ rec_kg, int32_t* __restrict__ plan_out,
@@ -85,14 +88,15 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
         if (!ok) report(dev_status, slot_ok ? KDA_DEV_BAD_ACCEPT : KDA_DEV_BAD_SLOT);
     }
     if (!ok) return;
-    const float* S0 = pool + ((size_t)src * H + h) * (kD * kD);
-    float* SD = pool + ((size_t)d * H + h) * (kD * kD);
+    using SIO = State<ST>;
+    const size_t S0 = state_elem(src, H, h), SD = state_elem(d, H, h);
     if (a == 0) {
         if (d == src) return;
 #pragma unroll 4
         for (int i = 0; i < kRowsPerWarp; ++i) {
-            const float4 x = __ldcs(reinterpret_cast<const float4*>(S0 + (size_t)(row0 + i) * kD) + lane);
-            __stcs(reinterpret_cast<float4*>(SD + (size_t)(row0 + i) * kD) + lane, x);
+            // a 16-bit value widens and rounds back to itself: the copy is exact
+            const float4 x = SIO::load4_cs(pool, S0 + (size_t)(row0 + i) * kD + 4 * lane);
+            SIO::store4_cs(pool, SD + (size_t)(row0 + i) * kD + 4 * lane, x);
         }
         return;
     }
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     float4 s[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
-        s[i] = __ldcs(reinterpret_cast<const float4*>(S0 + (size_t)(row0 + i) * kD) + lane);
+        s[i] = SIO::load4_cs(pool, S0 + (size_t)(row0 + i) * kD + 4 * lane);
     umma::cp_async_wait_all();
     __syncthreads();
     {
@@ -154,11 +158,11 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
-        __stcs(reinterpret_cast<float4*>(SD + (size_t)(row0 + i) * kD) + lane, s[i]);
+        SIO::store4_cs(pool, SD + (size_t)(row0 + i) * kD + 4 * lane, s[i]);
 }
 
 // Host checks and the launch shared by both commit entry points.
-kda_status launch_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                          const int32_t* dst_slot, const AcceptArgs& acc, bool from_tokens,
                          const int32_t* q_len, int32_t R, int32_t K, int32_t H, int32_t dk,
                          int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
@@ -168,6 +172,7 @@ kda_status launch_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
     KDA_REQUIRE(dk == kD && dv == kD, KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(dtype_ok(rec_dtype), KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(K <= kMaxCommitK, KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE(state_flags_ok(flags), KDA_ERR_UNSUPPORTED);
     if (R == 0) return KDA_OK;
     KDA_REQUIRE((int64_t)R * H < (1ll << 30), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {state_pool, ckpt_slot, rec_u, rec_kg};
@@ -191,10 +196,20 @@ kda_status launch_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
         kernel<<<grid, kCommitThreads, smem, s>>>(state_pool, P, ckpt_slot, dst_slot, acc, q_len, K,
                                                   H, flags, rec_u, rec_kg, plan_out, dev_status);
     };
+    auto by_state = [&](auto rec_bf16, auto tokens) {
+        constexpr bool B = decltype(rec_bf16)::value, T = decltype(tokens)::value;
+        switch (state_type(flags)) {
+            case kStateBF16: run(commit_kernel<B, T, kStateBF16>); break;
+            case kStateF16: run(commit_kernel<B, T, kStateF16>); break;
+            default: run(commit_kernel<B, T, kStateF32>);
+        }
+    };
+    using yes = std::true_type;
+    using no = std::false_type;
     if (rec_dtype == KDA_BF16)
-        from_tokens ? run(commit_kernel<true, true>) : run(commit_kernel<true, false>);
+        from_tokens ? by_state(yes{}, yes{}) : by_state(yes{}, no{});
     else
-        from_tokens ? run(commit_kernel<false, true>) : run(commit_kernel<false, false>);
+        from_tokens ? by_state(no{}, yes{}) : by_state(no{}, no{});
     return launch_status();
 }
 
@@ -203,7 +218,7 @@ kda_status launch_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
 
 using namespace kda;
 
-extern "C" kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_t* ckpt_slot,
+extern "C" kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                                       const int32_t* dst_slot, const int32_t* num_accepted,
                                       const int32_t* q_len, int32_t R, int32_t K, int32_t H,
                                       int32_t dk, int32_t dv, uint32_t flags, const float* rec_u,
@@ -215,7 +230,7 @@ extern "C" kda_status kda_spec_commit(float* state_pool, int64_t P, const int32_
 }
 
 extern "C" kda_status kda_spec_accept_commit(
-    float* state_pool, int64_t P, const int32_t* ckpt_slot, const int32_t* dst_slot,
+    void* state_pool, int64_t P, const int32_t* ckpt_slot, const int32_t* dst_slot,
     const int32_t* tokens, const int32_t* sampled, const int32_t* q_len, int32_t R, int32_t K,
     int32_t H, int32_t dk, int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
     kda_dtype rec_dtype, int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,

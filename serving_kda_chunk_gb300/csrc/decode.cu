@@ -1,5 +1,6 @@
 // decode.cu -- kda_recurrent_decode: one token per request, in place over a
-// slot-indexed fp32 state pool.
+// slot-indexed state pool (fp32, or bf16 / fp16 slots widened on load and
+// rounded once on store).
 //
 // "State semantics" page, section 4: decode applies the gate activation inside
 // the kernel and updates the per-head state in place.
@@ -9,7 +10,7 @@
 // A CTA's 16 KiB of state is loaded with 16-byte loads before any arithmetic,
 // the row dot products are warp reductions, and the updated rows are written
 // back in place; small CTAs keep many independent load chains resident.  The kernel is bound by HBM
-// traffic: 2 x 64 KiB of state per (request, head).
+// traffic: 2 x 64 KiB of fp32 state per (request, head), half that for 16-bit states.
 #include "kda_common.cuh"
 #include "kda_host.h"
 
@@ -20,13 +21,14 @@ constexpr int kDecThreads = 128;                   // 4 warps
 constexpr int kDecRows = 8;                        // state rows per warp
 constexpr int kDecCtas = kD / (4 * kDecRows);      // CTAs per (request, head)
 
-template <bool kBf16In, bool kBf16Out>
+template <bool kBf16In, bool kBf16Out, int ST>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(
     const void* __restrict__ q, const void* __restrict__ k, const void* __restrict__ v,
     const void* __restrict__ beta_raw, const void* __restrict__ gate_raw, int32_t H, float scale,
-    uint32_t flags, float* __restrict__ pool, int64_t P, const int32_t* __restrict__ slots,
+    uint32_t flags, void* __restrict__ pool, int64_t P, const int32_t* __restrict__ slots,
     void* __restrict__ out, int32_t* __restrict__ dev_status) {
     using A = Act<kBf16In>;
+    using SIO = State<ST>;
     const int unit = blockIdx.x / kDecCtas;
     const int part = blockIdx.x - unit * kDecCtas;
     const int r = unit / H, h = unit - r * H;
@@ -41,11 +43,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
                              make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
-    float* S = pool + ((size_t)slot * H + h) * (kD * kD);
+    const size_t S = state_elem(slot, H, h);
     float4 s[kDecRows];
 #pragma unroll
-    for (int i = 0; i < kDecRows; ++i)
-        s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(row0 + i) * kD) + lane);
+    for (int i = 0; i < kDecRows; ++i) s[i] = SIO::load4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane);
 
     StepIn in;
     const float4 g = A::load4(gate_raw, th * kD + 4 * lane);
@@ -65,17 +66,25 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
     float u_m = 0.f, o_m = 0.f;
     step_rows<kDecRows>(s, in, vrow, u_m, o_m, lane);
 #pragma unroll
-    for (int i = 0; i < kDecRows; ++i)
-        __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + i) * kD) + lane, s[i]);
+    for (int i = 0; i < kDecRows; ++i) SIO::store4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane, s[i]);
     if (lane < kDecRows) store1<kBf16Out>(out, th * kD + row0 + lane, o_m);
 }
 
 template <bool I, bool O>
 void launch(const void* q, const void* k, const void* v, const void* b, const void* g, int32_t R,
-            int32_t H, float scale, uint32_t flags, float* pool, int64_t P, const int32_t* slot,
+            int32_t H, float scale, uint32_t flags, void* pool, int64_t P, const int32_t* slot,
             void* out, int32_t* st, cudaStream_t s) {
-    decode_kernel<I, O><<<(unsigned)(kDecCtas * R * H), kDecThreads, 0, s>>>(
-        q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+    const unsigned grid = (unsigned)(kDecCtas * R * H);
+    switch (state_type(flags)) {
+        case kStateBF16:
+            decode_kernel<I, O, kStateBF16><<<grid, kDecThreads, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+            break;
+        case kStateF16:
+            decode_kernel<I, O, kStateF16><<<grid, kDecThreads, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+            break;
+        default:
+            decode_kernel<I, O, kStateF32><<<grid, kDecThreads, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+    }
 }
 
 }  // namespace
@@ -87,12 +96,13 @@ extern "C" kda_status kda_recurrent_decode(const void* q, const void* k, const v
                                            const void* beta_raw, const void* gate_raw,
                                            kda_dtype in_dtype, int32_t R, int32_t H, int32_t dk,
                                            int32_t dv, float scale, uint32_t flags,
-                                           float* state_pool, int64_t P, const int32_t* slot,
+                                           void* state_pool, int64_t P, const int32_t* slot,
                                            void* out, kda_dtype out_dtype, int32_t* dev_status,
                                            void* stream) {
     KDA_REQUIRE(R >= 0 && H > 0 && P >= 0, KDA_ERR_INVALID_ARG);
     KDA_REQUIRE(dk == kD && dv == kD, KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(dtype_ok(in_dtype) && dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE(state_flags_ok(flags), KDA_ERR_UNSUPPORTED);
     if (R == 0) return KDA_OK;
     KDA_REQUIRE((int64_t)R * H * kDecCtas < (1ll << 31), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {q, k, v, beta_raw, gate_raw, state_pool, slot, out};

@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -84,6 +85,111 @@ struct Act<false> {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ----------------------------------------------------------------------------
+// state element types (pool slots and snapshots): fp32 by default, bf16 or
+// fp16 under KDA_STATE_BF16 / KDA_STATE_F16.  Loads widen exactly; a store
+// rounds the fp32 value once, to nearest even, straight to the slot's type
+// (an fp16 slot never passes through bf16).
+
+enum StateType : int { kStateF32 = 0, kStateBF16 = 1, kStateF16 = 2 };
+
+__host__ __device__ constexpr int state_bytes(int st) { return st == kStateF32 ? 4 : 2; }
+
+__host__ __device__ inline int state_type(uint32_t flags) {
+    return (flags & KDA_STATE_BF16) ? kStateBF16 : (flags & KDA_STATE_F16) ? kStateF16 : kStateF32;
+}
+
+__host__ __device__ inline bool state_flags_ok(uint32_t flags) {
+    return !((flags & KDA_STATE_BF16) && (flags & KDA_STATE_F16));
+}
+
+template <int ST>
+struct State;
+
+template <>
+struct State<kStateF32> {
+    // four consecutive elements from element index i (i % 4 == 0); _cs = streaming
+    static __device__ __forceinline__ float4 load4(const void* p, size_t i) {
+        return *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+    }
+    static __device__ __forceinline__ float4 load4_cs(const void* p, size_t i) {
+        return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+    }
+    static __device__ __forceinline__ void store4(void* p, size_t i, float4 x) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p) + i) = x;
+    }
+    static __device__ __forceinline__ void store4_cs(void* p, size_t i, float4 x) {
+        __stcs(reinterpret_cast<float4*>(static_cast<float*>(p) + i), x);
+    }
+};
+
+template <>
+struct State<kStateBF16> {
+    static __device__ __forceinline__ float4 widen(uint2 w) {
+        return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    }
+    static __device__ __forceinline__ uint2 narrow(float4 x) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+        return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    }
+    static __device__ __forceinline__ float4 load4(const void* p, size_t i) {
+        return widen(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + i));
+    }
+    static __device__ __forceinline__ float4 load4_cs(const void* p, size_t i) {
+        return widen(__ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + i)));
+    }
+    static __device__ __forceinline__ void store4(void* p, size_t i, float4 x) {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p) + i) = narrow(x);
+    }
+    static __device__ __forceinline__ void store4_cs(void* p, size_t i, float4 x) {
+        __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(p) + i), narrow(x));
+    }
+};
+
+template <>
+struct State<kStateF16> {
+    static __device__ __forceinline__ float4 widen(uint2 w) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    static __device__ __forceinline__ uint2 narrow(float4 x) {
+        __half2 a = __floats2half2_rn(x.x, x.y), b = __floats2half2_rn(x.z, x.w);
+        return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    }
+    static __device__ __forceinline__ float4 load4(const void* p, size_t i) {
+        return widen(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + i));
+    }
+    static __device__ __forceinline__ float4 load4_cs(const void* p, size_t i) {
+        return widen(__ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + i)));
+    }
+    static __device__ __forceinline__ void store4(void* p, size_t i, float4 x) {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p) + i) = narrow(x);
+    }
+    static __device__ __forceinline__ void store4_cs(void* p, size_t i, float4 x) {
+        __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(p) + i), narrow(x));
+    }
+};
+
+// runtime-typed forms for the sites off the hot loops (initial / final states, snapshots)
+__device__ __forceinline__ float4 state_load4(const void* p, size_t i, int st) {
+    if (st == kStateBF16) return State<kStateBF16>::load4(p, i);
+    if (st == kStateF16) return State<kStateF16>::load4(p, i);
+    return State<kStateF32>::load4(p, i);
+}
+
+__device__ __forceinline__ void state_store4(void* p, size_t i, float4 x, int st) {
+    if (st == kStateBF16) State<kStateBF16>::store4(p, i, x);
+    else if (st == kStateF16) State<kStateF16>::store4(p, i, x);
+    else State<kStateF32>::store4(p, i, x);
+}
+
+// element offset of (slot, head) in a pool of 128 x 128 states, as a byte pointer
+__host__ __device__ inline size_t state_elem(int64_t slot, int H, int h) {
+    return ((size_t)slot * H + h) * (size_t)(kD * kD);
 }
 
 template <bool kBf16Out>

@@ -19,15 +19,16 @@ struct PrefillArgs {
     int32_t N, T_tot, H;
     float scale;
     uint32_t flags;
-    float* pool;
+    void* pool;  // states of type st (pool slots and snapshots alike)
     int64_t P;
     const int32_t* init_slot;
     const int32_t* final_slot;
     const int32_t* track;
     int32_t M;
-    float* track_state;
+    void* track_state;
     void* out;
     int32_t* dev_status;
+    int32_t st;  // StateType of pool and track_state
 };
 
 void launch_prefill_serial(const PrefillArgs& p, bool bf16_in, bool bf16_out, cudaStream_t s);

@@ -21,15 +21,16 @@ extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void
                                         kda_dtype in_dtype, const int32_t* cu_seqlens, int32_t N,
                                         int32_t T_tot, int32_t H, int32_t dk, int32_t dv,
                                         int32_t chunk, float scale, uint32_t flags,
-                                        float* state_pool, int64_t P, const int32_t* init_slot,
+                                        void* state_pool, int64_t P, const int32_t* init_slot,
                                         const int32_t* final_slot, const int32_t* track_chunk_idx,
-                                        int32_t M, float* track_state, void* out,
+                                        int32_t M, void* track_state, void* out,
                                         kda_dtype out_dtype, void* workspace, size_t ws_bytes,
                                         int32_t* dev_status, void* stream) {
     KDA_REQUIRE(N >= 0 && T_tot >= 0 && H > 0 && P >= 0 && M >= 0, KDA_ERR_INVALID_ARG);
     KDA_REQUIRE(dk == kD && dv == kD && chunk == kChunk, KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(dtype_ok(in_dtype) && dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(M <= kMaxTrack, KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE(state_flags_ok(flags), KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE((int64_t)N * H < (1ll << 31), KDA_ERR_UNSUPPORTED);
     if (N == 0) return KDA_OK;
     KDA_REQUIRE(cu_seqlens != nullptr && aligned16(cu_seqlens), KDA_ERR_INVALID_ARG);
@@ -45,7 +46,7 @@ extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void
     if (workspace) KDA_REQUIRE(aligned16(workspace), KDA_ERR_INVALID_ARG);
     PrefillArgs p{q,     k,         v,         beta_raw,   gate_raw,        cu_seqlens, N,
                   T_tot, H,         scale,     flags,      state_pool,      P,          init_slot,
-                  final_slot, track_chunk_idx, M, track_state, out, dev_status};
+                  final_slot, track_chunk_idx, M, track_state, out, dev_status, state_type(flags)};
     const bool bf16_in = in_dtype == KDA_BF16, bf16_out = out_dtype == KDA_BF16;
     if (!(flags & KDA_PREFILL_RECURRENT) && prefill_tc_supported(p, bf16_in))
         launch_prefill_tc(p, bf16_out, workspace, ws_bytes, as_stream(stream));

@@ -51,9 +51,9 @@ __global__ void __launch_bounds__(256) prefill_serial_kernel(PrefillArgs p) {
     }
     float4 s[16];
     if (init >= 0) {
-        const float* S = p.pool + ((size_t)init * p.H + h) * (kD * kD);
+        const size_t S = state_elem(init, p.H, h);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = reinterpret_cast<const float4*>(S + (size_t)(row0 + i) * kD)[lane];
+        for (int i = 0; i < 16; ++i) s[i] = state_load4(p.pool, S + (size_t)(row0 + i) * kD + 4 * lane, p.st);
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -71,10 +71,10 @@ __global__ void __launch_bounds__(256) prefill_serial_kernel(PrefillArgs p) {
                 const int j = local / kChunk;
                 for (int m = 0; m < p.M; ++m) {
                     if (trk[m] != j) continue;
-                    float* snap = p.track_state + (((size_t)n * p.M + m) * p.H + h) * (kD * kD);
+                    const size_t snap = state_elem((int64_t)n * p.M + m, p.H, h);
 #pragma unroll
                     for (int r = 0; r < 16; ++r)
-                        reinterpret_cast<float4*>(snap + (size_t)(row0 + r) * kD)[lane] = s[r];
+                        state_store4(p.track_state, snap + (size_t)(row0 + r) * kD + 4 * lane, s[r], p.st);
                 }
             }
             float u_m = 0.f, o_m = 0.f;
@@ -84,9 +84,9 @@ __global__ void __launch_bounds__(256) prefill_serial_kernel(PrefillArgs p) {
         }
     }
     if (fin >= 0) {
-        float* S = p.pool + ((size_t)fin * p.H + h) * (kD * kD);
+        const size_t S = state_elem(fin, p.H, h);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(S + (size_t)(row0 + i) * kD)[lane] = s[i];
+        for (int i = 0; i < 16; ++i) state_store4(p.pool, S + (size_t)(row0 + i) * kD + 4 * lane, s[i], p.st);
     }
 }
 

@@ -37,7 +37,8 @@
 //
 // The snapshot of chunk j (the state after j*64 tokens of the sequence, SGLang
 // PR 34820 page, the fp32 track-state snapshot) is written from the fp32 TMEM
-// accumulator when chunk j starts.
+// accumulator when chunk j starts; with a 16-bit state type it is that
+// accumulator rounded once, like the initial / final states of the pool.
 #include "kda_common.cuh"
 #include "kda_host.h"
 #include "prefill.h"
@@ -170,13 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 
     // ---- initial state into TMEM (row c = S^T row, this warp's 32 columns)
     {
-        const float* S0 = init >= 0 ? p.pool + ((size_t)init * H + h) * (kD * kD) : nullptr;
+        const size_t S0 = init >= 0 ? state_elem(init, H, h) + (size_t)row * kD : 0;
         const int col0 = cq * 32;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            float4 x = S0 ? reinterpret_cast<const float4*>(S0 + (size_t)row * kD + col0 + j)[0]
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 x = init >= 0 ? state_load4(p.pool, S0 + col0 + j, p.st)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             v[j] = x.x;
             v[j + 1] = x.y;
             v[j + 2] = x.z;
@@ -401,12 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 ld16(tl + TM_S + col0, v);
                 for (int m = 0; m < p.M; ++m) {
                     if (s_trk[m] != j) continue;
-                    float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
-                                  (size_t)row * kD + col0;
+                    const size_t snap = state_elem((int64_t)n * p.M + m, H, h) + (size_t)row * kD + col0;
 #pragma unroll
                     for (int q4 = 0; q4 < 16; q4 += 4)
-                        reinterpret_cast<float4*>(snap + q4)[0] =
-                            make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
+                        state_store4(p.track_state, snap + q4,
+                                     make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]), p.st);
                 }
                 uint32_t sh[8], sl[8];
 #pragma unroll
@@ -821,12 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 ld32(tl + TM_S + cq * 32, sv);
                 for (int m = 0; m < p.M; ++m) {
                     if (s_trk[m] != j) continue;
-                    float* snap = p.track_state + (((size_t)n * p.M + m) * H + h) * (kD * kD) +
-                                  (size_t)c * kD + cq * 32;
+                    const size_t snap = state_elem((int64_t)n * p.M + m, H, h) + (size_t)c * kD + cq * 32;
 #pragma unroll
                     for (int q4 = 0; q4 < 32; q4 += 4)
-                        reinterpret_cast<float4*>(snap + q4)[0] =
-                            make_float4(sv[q4], sv[q4 + 1], sv[q4 + 2], sv[q4 + 3]);
+                        state_store4(p.track_state, snap + q4,
+                                     make_float4(sv[q4], sv[q4 + 1], sv[q4 + 2], sv[q4 + 3]), p.st);
                 }
                 for (int t = 0; t < Lc; ++t) {
                     float d1 = 0.f;
@@ -881,14 +880,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
         mbar_wait(mbar, phase, kWaitLimit);
         if (pending_s) mbar_wait(mbar_s, phase_s, kWaitLimit);
     } else if (fin >= 0) {
-        float* SD = p.pool + ((size_t)fin * H + h) * (kD * kD);
+        const size_t SD = state_elem(fin, H, h) + (size_t)row * kD;
         const int col0 = cq * 32;
         float v[32];
         ld32(tl + TM_S + col0, v);
 #pragma unroll
         for (int q4 = 0; q4 < 32; q4 += 4)
-            reinterpret_cast<float4*>(SD + (size_t)row * kD + col0 + q4)[0] =
-                make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
+            state_store4(p.pool, SD + col0 + q4, make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]),
+                         p.st);
     }
     fence_before();
     __syncthreads();

@@ -18,7 +18,8 @@
 // TMEM columns each) walk their units one after another; while one waits for
 // its MMAs or its next checkpoint the other computes.  Per unit:
 //   - the checkpoint arrives by TMA (a two-dimensional tensor map over the
-//     pool, 128-byte swizzle, four [128 rows x 32 fp32] boxes), requested as
+//     pool, 128-byte swizzle, four [128 rows x 32 fp32] boxes, or two
+//     [128 x 64] boxes for 16-bit states, widened exactly), requested as
 //     soon as the previous unit's rows were converted; the token rows and raw
 //     beta words arrive by cp.async one unit ahead;
 //   - each thread converts 64 columns of one checkpoint row into bf16 hi + lo
@@ -64,6 +65,7 @@ struct VerifyArgs {
     void* out;
     int32_t* dev_status;
     int32_t n_units;
+    int32_t st;  // StateType of the pool
 };
 
 constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -204,9 +206,15 @@ __global__ void __launch_bounds__(kVThreads, 2)
         unit_rh(idx, r, h);
         const uint32_t mb = smem_u32(mbars);
         const int y = (meta[idx].x * H + h) * 128;
-        mbar_expect_tx(mb, 65536u);
+        if (a.st == kStateF32) {  // four [128 x 32] fp32 boxes
+            mbar_expect_tx(mb, 65536u);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) tma_load_2d(sb + Lay::RAW + p * 16384, &tmap, 32 * p, y, mb);
+            for (int p = 0; p < 4; ++p) tma_load_2d(sb + Lay::RAW + p * 16384, &tmap, 32 * p, y, mb);
+        } else {  // two [128 x 64] 16-bit boxes
+            mbar_expect_tx(mb, 32768u);
+#pragma unroll
+            for (int p = 0; p < 2; ++p) tma_load_2d(sb + Lay::RAW + p * 16384, &tmap, 64 * p, y, mb);
+        }
     };
     // token rows of unit idx: k, q, g -> KQG, v -> VB[idx & 1], raw beta words -> BRAW;
     // rows past the accepted length are zero-filled
@@ -234,15 +242,38 @@ __global__ void __launch_bounds__(kVThreads, 2)
     };
     // checkpoint rows, column quarter cq_ (32 columns of row `row`) -> TMEM operand (hi | lo)
     auto convert = [&](int cq_) {
-        const uint8_t* raw = sm + Lay::RAW + (uint32_t)cq_ * 16384u;
         float x[32];
+        if (a.st == kStateF32) {
+            // box cq_ holds columns 32 cq_ .. +31: eight 16-byte pieces per 128-byte row
+            const uint8_t* raw = sm + Lay::RAW + (uint32_t)cq_ * 16384u;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float4 f = *reinterpret_cast<const float4*>(raw + row * 128 + ((m ^ (row & 7)) << 4));
-            x[4 * m] = f.x;
-            x[4 * m + 1] = f.y;
-            x[4 * m + 2] = f.z;
-            x[4 * m + 3] = f.w;
+            for (int m = 0; m < 8; ++m) {
+                const float4 f = *reinterpret_cast<const float4*>(raw + row * 128 + ((m ^ (row & 7)) << 4));
+                x[4 * m] = f.x;
+                x[4 * m + 1] = f.y;
+                x[4 * m + 2] = f.z;
+                x[4 * m + 3] = f.w;
+            }
+        } else {
+            // box cq_ / 2 holds columns 64 (cq_ / 2) .. +63; this quarter is pieces 4 (cq_ & 1) .. +3
+            const uint8_t* raw = sm + Lay::RAW + (uint32_t)(cq_ >> 1) * 16384u;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int piece = 4 * (cq_ & 1) + m;
+                const uint4 w = *reinterpret_cast<const uint4*>(raw + row * 128 + ((piece ^ (row & 7)) << 4));
+                const float4 lo = a.st == kStateBF16 ? State<kStateBF16>::widen(make_uint2(w.x, w.y))
+                                                     : State<kStateF16>::widen(make_uint2(w.x, w.y));
+                const float4 hi = a.st == kStateBF16 ? State<kStateBF16>::widen(make_uint2(w.z, w.w))
+                                                     : State<kStateF16>::widen(make_uint2(w.z, w.w));
+                x[8 * m] = lo.x;
+                x[8 * m + 1] = lo.y;
+                x[8 * m + 2] = lo.z;
+                x[8 * m + 3] = lo.w;
+                x[8 * m + 4] = hi.x;
+                x[8 * m + 5] = hi.y;
+                x[8 * m + 6] = hi.z;
+                x[8 * m + 7] = hi.w;
+            }
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -633,7 +664,7 @@ extern "C" kda_status kda_spec_verify(const void* q, const void* k, const void* 
                                       const void* beta_raw, const void* gate_raw,
                                       kda_dtype in_dtype, int32_t R, int32_t K,
                                       const int32_t* q_len, int32_t H, int32_t dk, int32_t dv,
-                                      float scale, uint32_t flags, const float* state_pool,
+                                      float scale, uint32_t flags, const void* state_pool,
                                       int64_t P, const int32_t* ckpt_slot, float* rec_u,
                                       void* rec_kg, void* out, kda_dtype out_dtype,
                                       int32_t* dev_status, void* stream) {
@@ -641,26 +672,32 @@ extern "C" kda_status kda_spec_verify(const void* q, const void* k, const void* 
     KDA_REQUIRE(dk == kD && dv == kD, KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(dtype_ok(in_dtype) && dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(K <= kMaxVerifyK, KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE(state_flags_ok(flags), KDA_ERR_UNSUPPORTED);
     if (R == 0 || K == 0) return KDA_OK;
     KDA_REQUIRE((int64_t)R * H < (1ll << 31), KDA_ERR_UNSUPPORTED);
-    // the pool is read as a 2-D tensor of P*H*128 rows of 128 fp32 (a TMA row coordinate each)
+    // the pool is read as a 2-D tensor of P*H*128 rows of 128 states (a TMA row coordinate each)
     KDA_REQUIRE(P * H * 128 < (1ll << 31), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, rec_kg, out};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return KDA_ERR_CUDA;
     CUtensorMap map;
+    const int st = state_type(flags);
     const cuuint64_t rows = P > 0 ? (cuuint64_t)P * H * 128 : 128;
     const cuuint64_t dims[2] = {128, rows};
-    const cuuint64_t strides[1] = {128 * sizeof(float)};
-    const cuuint32_t box[2] = {32, 128};
+    // one 128-byte swizzle row per box row: 32 fp32 or 64 16-bit states
+    const cuuint64_t strides[1] = {128 * (cuuint64_t)state_bytes(st)};
+    const cuuint32_t box[2] = {st == kStateF32 ? 32u : 64u, 128};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(state_pool), dims, strides, box,
+    const CUtensorMapDataType et = st == kStateF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : st == kStateBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (enc(&map, et, 2, const_cast<void*>(state_pool), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return KDA_ERR_CUDA;
     const VerifyArgs a{q, k, v, beta_raw, gate_raw, K, q_len, H, scale, flags, P, ckpt_slot,
-                       rec_u, rec_kg, out, dev_status, R * H};
+                       rec_u, rec_kg, out, dev_status, R * H, st};
     cudaStream_t s = as_stream(stream);
     const bool ib = in_dtype == KDA_BF16, ob = out_dtype == KDA_BF16;
     if (ib && ob) return launch<true, true>(map, a, s);

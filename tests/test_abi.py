@@ -43,7 +43,7 @@ def test_status_strings_and_version(kda):
     assert kda.kda_status_string(0) == "KDA_OK"
     assert "INVALID_ARG" in kda.kda_status_string(1)
     assert "UNSUPPORTED" in kda.kda_status_string(2)
-    assert kda.kda_abi_version() >= 101
+    assert kda.kda_abi_version() >= 102
 
 
 def test_workspace_sizes(kda):
@@ -99,6 +99,11 @@ def test_host_checks_reject_bad_arguments(kda):
     st = L.kda_chunk_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 64, 2, 128, 128, 64, 1.0,
                              0, None, 0, None, None, FAKE, 1, None, FAKE, 0, None, 0, None, None)
     assert st == 1
+    # both 16-bit state types at once
+    both = kda.KDA_STATE_BF16 | kda.KDA_STATE_F16
+    st = L.kda_recurrent_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 2, 128, 128, 1.0, both, FAKE,
+                                8, FAKE, FAKE, 0, None, None)
+    assert st == 2
     # zero-sized work launches nothing and succeeds
     assert L.kda_recurrent_decode(None, None, None, None, None, 0, 0, 2, 128, 128, 1.0, 0, None,
                                   0, None, None, 0, None, None) == 0
