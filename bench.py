@@ -76,19 +76,19 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
 PREFILL_TRAFFIC_PER_TOKEN_HEAD = (277.5e6 + 59.2e6) / (8 * 2048 * 16)
 
 
-def decode_work(R, H):
-    return R * H * (2 * STATE_BYTES + 4 * D * 2 + 2 + D * 2)
+def decode_work(R, H, sb=STATE_BYTES):
+    return R * H * (2 * sb + 4 * D * 2 + 2 + D * 2)
 
 
-def verify_work(R, K, H):
-    return R * H * (STATE_BYTES + K * (4 * D * 2 + 2 + D * 2 + D * 4 + 2 * D * 2))
+def verify_work(R, K, H, sb=STATE_BYTES):
+    return R * H * (sb + K * (4 * D * 2 + 2 + D * 2 + D * 4 + 2 * D * 2))
 
 
-def commit_work(acc, H, K):
+def commit_work(acc, H, K, sb=STATE_BYTES):
     """Checkpoint read + state write and the a kept records per (request, head),
     plus the token ids read and the lengths / next tokens written once each."""
     ids = len(acc) * (2 * K * 4 + 2 * 4)
-    return ids + sum(H * (2 * STATE_BYTES + a * (D * 4 + 2 * D * 2)) for a in acc if a > 0)
+    return ids + sum(H * (2 * sb + a * (D * 4 + 2 * D * 2)) for a in acc if a > 0)
 
 
 # --------------------------------------------------------------------------
@@ -306,6 +306,53 @@ def run_device(step, steps, warmup, rank, world):
             times[name].append(a.elapsed_time(b) * 1e-3)
     launches = steps * sum(n for _, _, n in calls)
     return times, wall, clocks, launches
+
+
+def run_state_bf16(step, steps, warmup):
+    """decode, verify and the fused accept + commit on bf16 copies of their state pools
+    (KDA_STATE_BF16: 32 KiB per head), timed like the step's calls (L2 flushed before each
+    call, CUDA events on the launching stream).  Returns mean seconds per call."""
+    import torch
+
+    kda = step.kda
+    pool2, pool3 = step.pool2.to(torch.bfloat16), step.pool3.to(torch.bfloat16)
+    d, s = step.dec, step.spec
+
+    def decode():
+        kda.kda_recurrent_decode(d["q"], d["k"], d["v"], d["beta"], d["gate"], pool2, step.slot2,
+                                 step.out2, dev_status=step.status)
+
+    def verify():
+        kda.kda_spec_verify(s["q"], s["k"], s["v"], s["beta"], s["gate"], pool3, step.ckpt3,
+                            step.rec_u, step.rec_kg, step.out3, K=7, dev_status=step.status)
+
+    def commit():
+        kda.kda_spec_accept_commit(pool3, step.ckpt3, step.tok3, step.smp3, step.rec_u,
+                                   step.rec_kg, num_accepted=step.acc3, next_token=step.next3,
+                                   dev_status=step.status)
+
+    calls = [("decode", decode), ("verify", verify), ("commit", commit)]
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for _, fn in calls:
+            step.flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        for name, fn in calls:
+            step.flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((name, a, b))
+    torch.cuda.synchronize()
+    t = {name: [] for name, _ in calls}
+    for name, a, b in evs:
+        t[name].append(a.elapsed_time(b) * 1e-3)
+    return {k: statistics.mean(v) for k, v in t.items()}
 
 
 def run_e2e(step, steps, warmup):
@@ -573,6 +620,7 @@ def main():
     step = Step(dev)
     times, wall, clocks, launches = run_device(step, args.steps, args.warmup, rank, world)
     e2e_t, h2d, d2h = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
+    t16 = run_state_bf16(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
 
     hbm, tc, peak_kind = load_peaks()
     mean = {k: statistics.mean(v) for k, v in times.items()}
@@ -603,6 +651,14 @@ def main():
         "slot_copy": {"us": mean["slot_copy"] * 1e6, "bytes": cp_b,
                       "hbm_frac": cp_b / (hbm * 1e9) / mean["slot_copy"]},
     }
+    sb16 = STATE_BYTES // 2
+    w16 = {"decode": decode_work(256, 32, sb16), "verify": verify_work(64, 7, 32, sb16),
+           "commit": commit_work(step.acc3.cpu().tolist(), 32, 7, sb16)}
+    parts["state_bf16"] = {
+        name: {"us": t16[name] * 1e6, "bytes": w16[name],
+               "hbm_frac": w16[name] / (hbm * 1e9) / t16[name]} for name in w16}
+    parts["state_bf16"]["note"] = ("same calls on bf16 copies of the pools (KDA_STATE_BF16), "
+                                   "outside the timed step")
     step_s = sum(mean.values())
     status = int(step.status.item())
     if rank != 0:

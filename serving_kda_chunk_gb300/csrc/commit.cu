@@ -10,16 +10,15 @@
 //     c_t = sum_{t<s<=a} g_s  (c_0 = sum_{s<=a} g_s),
 // so every state element is one fused sum of a+1 terms.
 //
-// Four CTAs per (request, head), each owning 32 rows of S^T, so that more
-// independent load chains are resident per SM.  Every load of a CTA is issued
-// up front: its 32 checkpoint rows into registers, and the a key / raw-gate
-// records (one contiguous block) and its rows of u_t into shared memory by
-// cp.async.  Threads then walk the records backwards per key channel to form
-// F_t = exp(c_t) k_t and the total decay exp(c_0) as running products of
-// alpha = exp(g) = 1 / (1 + e^x), and each warp streams 8 rows of S^T: 16 KiB
-// per CTA (8 KiB for 16-bit states) read from the checkpoint and written to
-// the destination slot (in place allowed: each element is read and written by
-// the same thread).
+// Each CTA owns 16 KiB of one (request, head) state: 32 rows of S^T in fp32
+// (four CTAs per state) or 64 rows of 16-bit states (two).  Every load of a
+// CTA is issued up front with cp.async into shared memory, so the bytes in
+// flight cost no registers: its checkpoint rows, the a key / raw-gate records
+// (one contiguous block) and its rows of u_t.  Threads then walk the records
+// backwards per key channel to form F_t = exp(c_t) k_t and the total decay
+// exp(c_0) as running products of alpha = exp(g) = 1 / (1 + e^x), and each
+// warp updates its rows four at a time and streams them to the destination
+// slot (in place allowed: the checkpoint rows were staged before any store).
 #include <type_traits>
 
 #include "kda_common.cuh"
@@ -29,11 +28,16 @@
 namespace kda {
 namespace {
 
-constexpr int kMaxCommitK = 32;  // keeps the record staging under 48 KiB of shared memory
+constexpr int kMaxCommitK = 32;  // a request's records fit in shared memory beside the staged rows
 
-constexpr int kCommitThreads = 128;  // 4 warps x 8 rows: a quarter of a state per CTA
-constexpr int kRowsPerWarp = 8;
-constexpr int kCtasPerUnit = kD / (4 * kRowsPerWarp);
+constexpr int kCommitThreads = 128;  // 4 warps
+constexpr int kCommitStage = 16384;  // bytes of checkpoint rows per CTA, staged by cp.async
+// state rows per warp: 8 fp32 rows (a quarter of a state per CTA) or 16 rows of 16-bit
+// states (half a state per CTA)
+template <int ST>
+__host__ __device__ constexpr int commit_rows() { return kCommitStage / (4 * kD * state_bytes(ST)); }
+template <int ST>
+__host__ __device__ constexpr int commit_ctas() { return kD / (4 * commit_rows<ST>()); }
 
 // Accepted lengths: read from num_accepted, or (kTokens) found by every warp
 // of every CTA from the request's token ids, with the lengths and next tokens
@@ -54,16 +58,18 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     const float* __restrict__ rec_u, const void* __restrict__ rec_kg, int32_t* __restrict__ plan_out,
     int32_t* __restrict__ dev_status) {
     constexpr int ES = kBf16Rec ? 2 : 4;  // record element size
+    constexpr int RW = commit_rows<ST>(), CR = 4 * RW, CU = commit_ctas<ST>();  // rows / warp, CTA
     extern __shared__ __align__(16) float sm[];
-    float* F = sm;                                          // [K][128]
-    float* U = sm + K * kD;                                 // [K][32] this CTA's rows of u_t
-    float* D = U + K * 4 * kRowsPerWarp;                    // [128]
+    uint8_t* STG = reinterpret_cast<uint8_t*>(sm);          // [CR][128] checkpoint rows
+    float* F = sm + kCommitStage / 4;                       // [K][128]
+    float* U = F + K * kD;                                  // [K][CR] this CTA's rows of u_t
+    float* D = U + K * CR;                                  // [128]
     uint8_t* KG = reinterpret_cast<uint8_t*>(D + kD);       // [K][256] raw records (k, gate)
-    const int unit = blockIdx.x / kCtasPerUnit;  // (request, head); the rest picks the row block
-    const int part = blockIdx.x - unit * kCtasPerUnit;
+    const int unit = blockIdx.x / CU;  // (request, head); the rest picks the row block
+    const int part = blockIdx.x - unit * CU;
     const int r = unit / H, h = unit - r * H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = part * (4 * kRowsPerWarp) + warp * kRowsPerWarp;
+    const int row0 = part * CR + warp * RW;
     const int src = ckpt[r];
     const int d = dst ? dst[r] : src;
     const int ql = q_len ? q_len[r] : K;
@@ -93,32 +99,33 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     if (a == 0) {
         if (d == src) return;
 #pragma unroll 4
-        for (int i = 0; i < kRowsPerWarp; ++i) {
+        for (int i = 0; i < RW; ++i) {
             // a 16-bit value widens and rounds back to itself: the copy is exact
             const float4 x = SIO::load4_cs(pool, S0 + (size_t)(row0 + i) * kD + 4 * lane);
             SIO::store4_cs(pool, SD + (size_t)(row0 + i) * kD + 4 * lane, x);
         }
         return;
     }
-    // every load up front: checkpoint rows into registers, records into shared memory
+    // every load up front, into shared memory: checkpoint rows, key / raw-gate records, u rows
     const size_t rec0 = ((size_t)r * H + h) * K;
     {
-        const uint32_t kg_s = umma::smem_u32(KG), u_s = umma::smem_u32(U);
+        const uint32_t stg_s = umma::smem_u32(STG), kg_s = umma::smem_u32(KG), u_s = umma::smem_u32(U);
+        const uint8_t* s0_g = static_cast<const uint8_t*>(pool) + (S0 + (size_t)part * CR * kD) * state_bytes(ST);
+#pragma unroll
+        for (int e = threadIdx.x; e < kCommitStage / 16; e += kCommitThreads)
+            umma::cp_async16(stg_s + 16 * e, s0_g + 16 * e, 16);
         const uint8_t* kg_g = static_cast<const uint8_t*>(rec_kg) + rec0 * 2 * kD * ES;
         for (int e = threadIdx.x; e < a * 2 * kD * ES / 16; e += kCommitThreads)
             umma::cp_async16(kg_s + 16 * e, kg_g + 16 * e, 16);
-        // u_t rows part*32 .. part*32+31: 8 chunks of 16 B per step
-        for (int e = threadIdx.x; e < a * 8; e += kCommitThreads) {
-            const int t = e >> 3, ch = e & 7;
-            umma::cp_async16(u_s + (uint32_t)(t * 128 + ch * 16),
-                             rec_u + (rec0 + t) * kD + part * (4 * kRowsPerWarp) + ch * 4, 16);
+        // u_t rows part*CR .. part*CR+CR-1: CR/4 chunks of 16 B per step
+        constexpr int kChunks = CR / 4;
+        for (int e = threadIdx.x; e < a * kChunks; e += kCommitThreads) {
+            const int t = e / kChunks, ch = e - t * kChunks;
+            umma::cp_async16(u_s + (uint32_t)(t * CR * 4 + ch * 16),
+                             rec_u + (rec0 + t) * kD + part * CR + ch * 4, 16);
         }
         umma::cp_async_commit();
     }
-    float4 s[kRowsPerWarp];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i)
-        s[i] = SIO::load4_cs(pool, S0 + (size_t)(row0 + i) * kD + 4 * lane);
     umma::cp_async_wait_all();
     __syncthreads();
     {
@@ -139,26 +146,32 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     }
     __syncthreads();
     const float4 dec = *reinterpret_cast<const float4*>(&D[4 * lane]);
+    // this warp's rows in groups of 4 (row = index within the CTA's staged block)
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) s[i] = f4_mul(s[i], dec);
-    for (int t = 0; t < a; ++t) {
-        const float4 f = *reinterpret_cast<const float4*>(&F[t * kD + 4 * lane]);
-        float urow[kRowsPerWarp];
+    for (int g4 = 0; g4 < RW; g4 += 4) {
+        const int rb = warp * RW + g4;
+        float4 s[4];
 #pragma unroll
-        for (int j = 0; j < kRowsPerWarp / 4; ++j) {
-            const float4 x =
-                *reinterpret_cast<const float4*>(&U[t * (4 * kRowsPerWarp) + warp * kRowsPerWarp + 4 * j]);
-            urow[4 * j] = x.x;
-            urow[4 * j + 1] = x.y;
-            urow[4 * j + 2] = x.z;
-            urow[4 * j + 3] = x.w;
+        for (int i = 0; i < 4; ++i) {
+            float4 x;
+            if constexpr (ST == kStateF32)
+                x = *reinterpret_cast<const float4*>(STG + (rb + i) * 512 + lane * 16);
+            else
+                x = SIO::widen(*reinterpret_cast<const uint2*>(STG + (rb + i) * 256 + lane * 8));
+            s[i] = f4_mul(x, dec);
+        }
+        for (int t = 0; t < a; ++t) {
+            const float4 f = *reinterpret_cast<const float4*>(&F[t * kD + 4 * lane]);
+            const float4 u0 = *reinterpret_cast<const float4*>(&U[t * CR + rb]);
+            s[0] = f4_fma(u0.x, f, s[0]);
+            s[1] = f4_fma(u0.y, f, s[1]);
+            s[2] = f4_fma(u0.z, f, s[2]);
+            s[3] = f4_fma(u0.w, f, s[3]);
         }
 #pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) s[i] = f4_fma(urow[i], f, s[i]);
+        for (int i = 0; i < 4; ++i)
+            SIO::store4_cs(pool, SD + (size_t)(part * CR + rb + i) * kD + 4 * lane, s[i]);
     }
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i)
-        SIO::store4_cs(pool, SD + (size_t)(row0 + i) * kD + 4 * lane, s[i]);
 }
 
 // Host checks and the launch shared by both commit entry points.
@@ -188,8 +201,11 @@ kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
     }
     cudaStream_t s = as_stream(stream);
     const size_t es = rec_dtype == KDA_BF16 ? 2 : 4;
-    const size_t smem = (size_t)(K * kD + K * 4 * kRowsPerWarp + kD) * sizeof(float) + (size_t)K * 2 * kD * es;
-    const unsigned grid = (unsigned)(kCtasPerUnit * R * H);
+    const int st = state_type(flags);
+    const int rows = st == kStateF32 ? 4 * commit_rows<kStateF32>() : 4 * commit_rows<kStateBF16>();
+    const size_t smem = kCommitStage + (size_t)(K * kD + K * rows + kD) * sizeof(float) +
+                        (size_t)K * 2 * kD * es;
+    const unsigned grid = (unsigned)((kD / rows) * R * H);
     auto run = [&](auto kernel) {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -198,7 +214,7 @@ kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
     };
     auto by_state = [&](auto rec_bf16, auto tokens) {
         constexpr bool B = decltype(rec_bf16)::value, T = decltype(tokens)::value;
-        switch (state_type(flags)) {
+        switch (st) {
             case kStateBF16: run(commit_kernel<B, T, kStateBF16>); break;
             case kStateF16: run(commit_kernel<B, T, kStateF16>); break;
             default: run(commit_kernel<B, T, kStateF32>);

@@ -5,21 +5,39 @@
 // "State semantics" page, section 4: decode applies the gate activation inside
 // the kernel and updates the per-head state in place.
 //
-// Four CTAs per (request, head); their 4 warps each own 8 rows of S^T (a row =
-// one value channel, 128 contiguous key channels), a lane owns 4 key channels.
-// A CTA's 16 KiB of state is loaded with 16-byte loads before any arithmetic,
-// the row dot products are warp reductions, and the updated rows are written
-// back in place; small CTAs keep many independent load chains resident.  The kernel is bound by HBM
-// traffic: 2 x 64 KiB of fp32 state per (request, head), half that for 16-bit states.
+// A CTA of 4 warps owns 16 KiB of one (request, head) state: 32 rows of S^T in
+// fp32 or 64 rows of 16-bit states (a row = one value channel, 128 contiguous
+// key channels).  The whole block is requested at once with cp.async into
+// shared memory, so the bytes in flight cost no registers and many CTAs per SM
+// keep HBM busy; the token's activations load meanwhile.  Each warp then walks
+// its rows: a lane owns 4 key channels, the two row dot products are one
+// interleaved warp reduction, and the updated row goes straight back to the
+// slot with streaming stores.  Bound by HBM traffic: 2 x the state per
+// (request, head).
 #include "kda_common.cuh"
 #include "kda_host.h"
+#include "umma.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kDecThreads = 128;                   // 4 warps
-constexpr int kDecRows = 8;                        // state rows per warp
-constexpr int kDecCtas = kD / (4 * kDecRows);      // CTAs per (request, head)
+constexpr int kDecThreads = 128;       // 4 warps
+constexpr int kDecStage = 16384;       // bytes of state per CTA
+
+template <int ST>
+__host__ __device__ constexpr int dec_rows() { return kDecStage / (kD * state_bytes(ST)); }  // per CTA
+template <int ST>
+__host__ __device__ constexpr int dec_ctas() { return kD / dec_rows<ST>(); }  // per (request, head)
+
+template <int ST>
+__device__ __forceinline__ float4 smem_row4(const uint8_t* buf, int row, int lane) {
+    if constexpr (ST == kStateF32) {
+        return *reinterpret_cast<const float4*>(buf + row * 512 + lane * 16);
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(buf + row * 256 + lane * 8);
+        return State<ST>::widen(w);
+    }
+}
 
 template <bool kBf16In, bool kBf16Out, int ST>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(
@@ -29,25 +47,29 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
     void* __restrict__ out, int32_t* __restrict__ dev_status) {
     using A = Act<kBf16In>;
     using SIO = State<ST>;
-    const int unit = blockIdx.x / kDecCtas;
-    const int part = blockIdx.x - unit * kDecCtas;
+    constexpr int CR = dec_rows<ST>(), CU = dec_ctas<ST>(), RW = CR / 4;  // rows per CTA / warp
+    __shared__ __align__(16) uint8_t buf[kDecStage];
+    const int unit = blockIdx.x / CU;
+    const int part = blockIdx.x - unit * CU;
     const int r = unit / H, h = unit - r * H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = part * (4 * kDecRows) + warp * kDecRows;
     const size_t th = (size_t)r * H + h;
     const int slot = slots[r];
     if (slot < 0 || slot >= P) {
         if (slot >= P && threadIdx.x == 0 && part == 0) report(dev_status, KDA_DEV_BAD_SLOT);
-        if (threadIdx.x < 4 * kDecRows / 4)
-            store4<kBf16Out>(out, th * kD + part * 4 * kDecRows + 4 * threadIdx.x,
-                             make_float4(0.f, 0.f, 0.f, 0.f));
+        if (threadIdx.x < CR / 4)
+            store4<kBf16Out>(out, th * kD + part * CR + 4 * threadIdx.x, make_float4(0.f, 0.f, 0.f, 0.f));
         return;
     }
-    const size_t S = state_elem(slot, H, h);
-    float4 s[kDecRows];
+    const size_t S = state_elem(slot, H, h) + (size_t)part * CR * kD;  // this CTA's first row
+    {
+        const uint8_t* src = static_cast<const uint8_t*>(pool) + S * state_bytes(ST);
+        const uint32_t dst = umma::smem_u32(buf);
 #pragma unroll
-    for (int i = 0; i < kDecRows; ++i) s[i] = SIO::load4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane);
-
+        for (int e = threadIdx.x; e < kDecStage / 16; e += kDecThreads)
+            umma::cp_async16(dst + 16 * e, src + 16 * e, 16);
+        umma::cp_async_commit();
+    }
     StepIn in;
     const float4 g = A::load4(gate_raw, th * kD + 4 * lane);
     in.a = make_float4(expf(gate_log(g.x, flags)), expf(gate_log(g.y, flags)),
@@ -57,33 +79,40 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
     in.q = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);
     in.kq = warp_sum(f4_dot(in.k, in.q));
     in.beta = beta_act(A::load1(beta_raw, th), flags);
-    float vrow[kDecRows];
-    {
-        const float vm = lane < kDecRows ? A::load1(v, th * kD + row0 + lane) : 0.f;
-#pragma unroll
-        for (int i = 0; i < kDecRows; ++i) vrow[i] = __shfl_sync(0xffffffffu, vm, i);
+    const int row0 = warp * RW;  // within the CTA's rows
+    const float vm = lane < RW ? A::load1(v, th * kD + part * CR + row0 + lane) : 0.f;
+    umma::cp_async_wait_all();
+    __syncthreads();
+    float o_m = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < RW; ++i) {
+        const float4 x = f4_mul(smem_row4<ST>(buf, row0 + i, lane), in.a);
+        float d1 = f4_dot(x, in.k), d2 = f4_dot(x, in.q);
+        warp_sum2(d1, d2);
+        const float u = in.beta * (__shfl_sync(0xffffffffu, vm, i) - d1);
+        SIO::store4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane, f4_fma(u, in.k, x));
+        if (lane == i) o_m = fmaf(u, in.kq, d2);
     }
-    float u_m = 0.f, o_m = 0.f;
-    step_rows<kDecRows>(s, in, vrow, u_m, o_m, lane);
-#pragma unroll
-    for (int i = 0; i < kDecRows; ++i) SIO::store4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane, s[i]);
-    if (lane < kDecRows) store1<kBf16Out>(out, th * kD + row0 + lane, o_m);
+    if (lane < RW) store1<kBf16Out>(out, th * kD + part * CR + row0 + lane, o_m);
 }
 
 template <bool I, bool O>
 void launch(const void* q, const void* k, const void* v, const void* b, const void* g, int32_t R,
             int32_t H, float scale, uint32_t flags, void* pool, int64_t P, const int32_t* slot,
             void* out, int32_t* st, cudaStream_t s) {
-    const unsigned grid = (unsigned)(kDecCtas * R * H);
+    const unsigned units = (unsigned)(R * H);
     switch (state_type(flags)) {
         case kStateBF16:
-            decode_kernel<I, O, kStateBF16><<<grid, kDecThreads, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+            decode_kernel<I, O, kStateBF16><<<dec_ctas<kStateBF16>() * units, kDecThreads, 0, s>>>(
+                q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
             break;
         case kStateF16:
-            decode_kernel<I, O, kStateF16><<<grid, kDecThreads, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+            decode_kernel<I, O, kStateF16><<<dec_ctas<kStateF16>() * units, kDecThreads, 0, s>>>(
+                q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
             break;
         default:
-            decode_kernel<I, O, kStateF32><<<grid, kDecThreads, 0, s>>>(q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
+            decode_kernel<I, O, kStateF32><<<dec_ctas<kStateF32>() * units, kDecThreads, 0, s>>>(
+                q, k, v, b, g, H, scale, flags, pool, P, slot, out, st);
     }
 }
 
@@ -104,7 +133,7 @@ extern "C" kda_status kda_recurrent_decode(const void* q, const void* k, const v
     KDA_REQUIRE(dtype_ok(in_dtype) && dtype_ok(out_dtype), KDA_ERR_UNSUPPORTED);
     KDA_REQUIRE(state_flags_ok(flags), KDA_ERR_UNSUPPORTED);
     if (R == 0) return KDA_OK;
-    KDA_REQUIRE((int64_t)R * H * kDecCtas < (1ll << 31), KDA_ERR_UNSUPPORTED);
+    KDA_REQUIRE((int64_t)R * H * dec_ctas<kStateF32>() < (1ll << 31), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {q, k, v, beta_raw, gate_raw, state_pool, slot, out};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
     cudaStream_t s = as_stream(stream);

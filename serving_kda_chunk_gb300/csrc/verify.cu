@@ -530,9 +530,12 @@ __global__ void __launch_bounds__(kVThreads, 2)
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     mma_ta(tmem + TV_D, tmem + TV_SA + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
+                // a bf16 checkpoint splits exactly into hi with lo = 0: its lo products are zero
+                if (a.st != kStateBF16) {
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_ta(tmem + TV_D, tmem + TV_SA + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
+                    for (int s = 0; s < 8; ++s)
+                        mma_ta(tmem + TV_D, tmem + TV_SA + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
+                }
                 commit(smem_u32(mbars + 1));
             }
             mma_pend = true;
