@@ -176,56 +176,69 @@ def i32(a, dev):
 
 
 class Step:
-    """All five entry points on resident device buffers."""
+    """The entry points on resident device buffers.  `parts` selects which workloads are built
+    (all of them for the benchmark; one for a profiler capture).  compact_decode_pool keeps only
+    the 256 slots the decode batch touches (same work per call, 512 MiB instead of 2 GiB)."""
 
-    def __init__(self, dev):
+    PARTS = ("prefill", "decode", "spec", "copy")
+
+    def __init__(self, dev, parts=PARTS, compact_decode_pool=False):
         import torch
 
         import serving_kda_chunk_gb300 as kda
 
         self.kda = kda
         self.dev = dev
+        self.parts = tuple(parts)
         t0 = time.time()
-        c1 = _cfg1()
-        self.c1 = c1
-        self.pre = {n: to_dev(c1[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
-        self.pre_host = {n: torch.from_numpy(c1[n].view(np.int16)).view(torch.bfloat16).pin_memory()
-                         for n in ("q", "k", "v", "beta", "gate")}
-        self.cu = i32(c1["cu_seqlens"], dev)
-        self.pool1 = torch.from_numpy(c1["pool"]).to(dev)
-        self.slots1 = i32(c1["init_slot"], dev)
-        self.track1 = i32(c1["track"], dev)
-        self.snap1 = torch.empty(c1["N"], 1, 32, D, D, device=dev)
-        self.out1 = torch.empty(c1["T"], 32, D, dtype=torch.bfloat16, device=dev)
-        self.out1_host = torch.empty(c1["T"], 32, D, dtype=torch.bfloat16).pin_memory()
-        ws = kda.kda_chunk_prefill_workspace_size(c1["T"], c1["N"], 32)
-        self.ws1 = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-        c2 = W.cfg2()
-        self.dec = {n: to_dev(c2[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
-        self.pool2 = torch.from_numpy(c2["pool"]).to(dev)
-        self.slot2 = i32(c2["slot"], dev)
-        self.out2 = torch.empty(256, 32, D, dtype=torch.bfloat16, device=dev)
-        c3 = W.cfg3()
-        self.c3 = c3
-        self.spec = {n: to_dev(c3[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
-        self.pool3 = torch.from_numpy(c3["pool"]).to(dev)
-        self.ckpt3 = i32(c3["ckpt"], dev)
-        a3 = W.accept_case(3, 64, 7, p_match=0.7)
-        self.tok3, self.smp3 = i32(a3["tokens"], dev), i32(a3["sampled"], dev)
-        self.acc3 = torch.empty(64, dtype=torch.int32, device=dev)
-        self.next3 = torch.empty(64, dtype=torch.int32, device=dev)
-        self.rec_u = torch.empty(64, 32, 7, D, device=dev)
-        self.rec_kg = torch.empty(64, 32, 7, 2 * D, dtype=torch.bfloat16, device=dev)
-        self.out3 = torch.empty(64 * 7, 32, D, dtype=torch.bfloat16, device=dev)
-        c4 = W.cfg4_slot_copy()
-        g = torch.Generator(device=dev).manual_seed(4)
-        self.pool4 = torch.empty(4096, 16, D, D, device=dev)
-        for i in range(0, 4096, 512):
-            self.pool4[i:i + 512].normal_(0.0, 0.1, generator=g)
-        self.c4 = {n: i32(c4[n], dev) for n in ("clear", "src", "dst_offsets", "dst")}
-        self.n4 = (len(c4["src"]), len(c4["dst"]), len(c4["clear"]))
-        self.ws4 = torch.empty(kda.kda_slot_copy_workspace_size(4096), dtype=torch.uint8,
-                               device=dev)
+        if "prefill" in parts:
+            c1 = _cfg1()
+            self.c1 = c1
+            self.pre = {n: to_dev(c1[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+            self.pre_host = {n: torch.from_numpy(c1[n].view(np.int16)).view(torch.bfloat16)
+                             .pin_memory() for n in ("q", "k", "v", "beta", "gate")}
+            self.cu = i32(c1["cu_seqlens"], dev)
+            self.pool1 = torch.from_numpy(c1["pool"]).to(dev)
+            self.slots1 = i32(c1["init_slot"], dev)
+            self.track1 = i32(c1["track"], dev)
+            self.snap1 = torch.empty(c1["N"], 1, 32, D, D, device=dev)
+            self.out1 = torch.empty(c1["T"], 32, D, dtype=torch.bfloat16, device=dev)
+            self.out1_host = torch.empty(c1["T"], 32, D, dtype=torch.bfloat16).pin_memory()
+            ws = kda.kda_chunk_prefill_workspace_size(c1["T"], c1["N"], 32)
+            self.ws1 = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        if "decode" in parts:
+            c2 = W.cfg2()
+            self.dec = {n: to_dev(c2[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+            if compact_decode_pool:
+                self.pool2 = torch.from_numpy(c2["pool"][c2["slot"]]).to(dev)
+                self.slot2 = i32(np.arange(len(c2["slot"])), dev)
+            else:
+                self.pool2 = torch.from_numpy(c2["pool"]).to(dev)
+                self.slot2 = i32(c2["slot"], dev)
+            self.out2 = torch.empty(256, 32, D, dtype=torch.bfloat16, device=dev)
+        if "spec" in parts:
+            c3 = W.cfg3()
+            self.c3 = c3
+            self.spec = {n: to_dev(c3[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+            self.pool3 = torch.from_numpy(c3["pool"]).to(dev)
+            self.ckpt3 = i32(c3["ckpt"], dev)
+            a3 = W.accept_case(3, 64, 7, p_match=0.7)
+            self.tok3, self.smp3 = i32(a3["tokens"], dev), i32(a3["sampled"], dev)
+            self.acc3 = torch.empty(64, dtype=torch.int32, device=dev)
+            self.next3 = torch.empty(64, dtype=torch.int32, device=dev)
+            self.rec_u = torch.empty(64, 32, 7, D, device=dev)
+            self.rec_kg = torch.empty(64, 32, 7, 2 * D, dtype=torch.bfloat16, device=dev)
+            self.out3 = torch.empty(64 * 7, 32, D, dtype=torch.bfloat16, device=dev)
+        if "copy" in parts:
+            c4 = W.cfg4_slot_copy()
+            g = torch.Generator(device=dev).manual_seed(4)
+            self.pool4 = torch.empty(4096, 16, D, D, device=dev)
+            for i in range(0, 4096, 512):
+                self.pool4[i:i + 512].normal_(0.0, 0.1, generator=g)
+            self.c4 = {n: i32(c4[n], dev) for n in ("clear", "src", "dst_offsets", "dst")}
+            self.n4 = (len(c4["src"]), len(c4["dst"]), len(c4["clear"]))
+            self.ws4 = torch.empty(kda.kda_slot_copy_workspace_size(4096), dtype=torch.uint8,
+                                   device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         self.setup_s = time.time() - t0
@@ -261,11 +274,14 @@ class Step:
         self.kda.kda_slot_copy([self.pool4], c["clear"], c["src"], c["dst_offsets"], c["dst"],
                                self.ws4, dev_status=self.status)
 
-    # name -> (callable, kernel launches)
+    # name -> (callable, kernel launches), for the parts that were built
     def calls(self):
-        return [("prefill", self.prefill, 2), ("decode", self.decode, 1),
-                ("verify", self.verify, 1), ("commit", self.commit, 1),
-                ("slot_copy", self.slot_copy, 2)]
+        part = {"prefill": "prefill", "decode": "decode", "verify": "spec", "commit": "spec",
+                "slot_copy": "copy"}
+        every = [("prefill", self.prefill, 2), ("decode", self.decode, 1),
+                 ("verify", self.verify, 1), ("commit", self.commit, 1),
+                 ("slot_copy", self.slot_copy, 2)]
+        return [c for c in every if part[c[0]] in self.parts]
 
 
 def run_device(step, steps, warmup, rank, world):
@@ -424,7 +440,21 @@ def run_e2e(step, steps, warmup):
         b.record(main)
         b.synchronize()
         ts.append(a.elapsed_time(b) * 1e-3)
-    return statistics.mean(ts), h2d, d2h
+    # the host link's own rate on this machine, one direction at a time (256 MiB pinned copies)
+    link = {}
+    dev_buf, host_buf = step.out1.view(-1)[: 1 << 27], step.out1_host.view(-1)[: 1 << 27]
+    for name, dst, src in (("h2d_gbs", dev_buf, host_buf), ("d2h_gbs", host_buf, dev_buf)):
+        best = 0.0
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            dst.copy_(src, non_blocking=True)
+            b.record(main)
+            b.synchronize()
+            best = max(best, src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9)
+        link[name] = best
+    return statistics.mean(ts), h2d, d2h, link
 
 
 # --------------------------------------------------------------------------
@@ -576,8 +606,11 @@ def run_profile_case(name, reps):
                                   state_pool=pool, init_slot=sl, final_slot=sl,
                                   track_chunk_idx=tr, track_state=snap, workspace=ws)
     else:
-        step = Step(dev)
+        part = {"decode": "decode", "verify": "spec", "commit": "spec", "slot_copy": "copy"}[name]
+        step = Step(dev, parts=(part,), compact_decode_pool=True)
         fn = dict((n, f) for n, f, _ in step.calls())[name]
+        if name == "commit":
+            step.verify()  # records for the commit to read
     times = []
     for _ in range(reps):
         flush.zero_()
@@ -619,7 +652,7 @@ def main():
     dev = torch.device("cuda", local)
     step = Step(dev)
     times, wall, clocks, launches = run_device(step, args.steps, args.warmup, rank, world)
-    e2e_t, h2d, d2h = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
+    e2e_t, h2d, d2h, link = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t16 = run_state_bf16(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
 
     hbm, tc, peak_kind = load_peaks()
@@ -679,7 +712,9 @@ def main():
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "link_measured": link,
+                "link_bound_tokens_per_s": toks / (h2d / (link["h2d_gbs"] * 1e9)
+                                                   + d2h / (link["d2h_gbs"] * 1e9))},
         "gpu_launches": launches,
         "clocks": clocks,
         "parts": parts,
