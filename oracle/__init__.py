@@ -19,6 +19,8 @@ Contents
   * ``slot_copy`` and ``commit_plan`` -- memcpy and integer semantics.
   * ``accept`` -- the accepted length of each speculative request from its
     draft and sampled token ids (integer semantics).
+  * ``conv_compact`` -- the short-convolution window kept after acceptance
+    (copy semantics).
 
 All arrays are float64 numpy arrays (bf16 inputs widened exactly by the
 caller).  Layouts follow the library: activations [tokens, heads, channels],
@@ -371,3 +373,35 @@ def accept(tokens, sampled, K, q_len=None):
         a_out[r] = kept + 1
         nxt[r] = sampled[r, kept]
     return a_out, nxt, status
+
+
+def conv_compact(pools, slots, num_accepted, keep):
+    """Short-convolution history after a speculative step (RecoverSSM page,
+    implementation breakdown step 4: the commit compacts the conv history; the
+    "state semantics" page: the conv state is a sliding window moved by an
+    offset copy).
+
+    Each pool is [num_slots, rows, channels]: a slot's rows 0..keep-1 hold the
+    last `keep` inputs before the step, rows keep.. the step's inputs.  After
+    a accepted positions the window is the last `keep` inputs of the accepted
+    stream, i.e. rows a .. a+keep-1 move to rows 0 .. keep-1 (rows past keep
+    are left as they were).  slot < 0 skips the request; slot >= num_slots
+    sets BAD_SLOT; a < 0 or a + keep > rows sets BAD_ACCEPT; both skip.
+    Sources are read before any write (the ranges overlap when a < keep).
+    Returns (new pools, status)."""
+    outs = [np.array(pl, copy=True) for pl in pools]
+    status = 0
+    for i, pl in enumerate(pools):
+        n_slots, rows = pl.shape[0], pl.shape[1]
+        for r, sl in enumerate(slots):
+            sl, a = int(sl), int(num_accepted[r])
+            if sl < 0:
+                continue
+            if sl >= n_slots:
+                status |= BAD_SLOT
+                continue
+            if a < 0 or a + keep > rows:
+                status |= BAD_ACCEPT
+                continue
+            outs[i][sl, :keep] = pl[sl, a:a + keep]
+    return outs, status

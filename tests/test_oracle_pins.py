@@ -370,6 +370,49 @@ def test_accept_special_cases_and_bad_lengths():
     assert (a3[0], n3[0]) == (3, 8)
 
 
+@pytest.mark.parametrize("keep", [1, 3])
+def test_conv_window_is_the_tail_of_the_accepted_stream(keep):
+    """Run a sliding window of width `keep` over a token stream step by step:
+    each speculative step appends q_len inputs after the history, accepts a of
+    them, and the compacted window must be the last `keep` inputs of
+    everything accepted so far (a list tail, not an offset copy)."""
+    rng = np.random.default_rng(77)
+    K, C = 5, 3
+    stream = [rng.standard_normal(C) for _ in range(keep)]  # inputs before the first step
+    pool = np.zeros((2, keep + K, C))
+    pool[1, :keep] = np.stack(stream[-keep:])
+    for step in range(12):
+        q_len = int(rng.integers(1, K + 1))       # q_len = 1 is a draftless request
+        a = int(rng.integers(0, q_len + 1))
+        x = rng.standard_normal((q_len, C))
+        pool[1, keep:keep + q_len] = x
+        (pool,), st = oracle.conv_compact([pool], [1], [a], keep)
+        assert st == 0
+        stream += list(x[:a])
+        np.testing.assert_array_equal(pool[1, :keep], np.stack(stream[-keep:]))
+        assert (pool[0] == 0).all()
+
+
+def test_conv_compact_special_cases():
+    rng = np.random.default_rng(78)
+    pool = rng.standard_normal((4, 6, 2))
+    # a = 0 keeps the window; a = rows - keep moves the last rows to the front
+    (out,), st = oracle.conv_compact([pool], [0, 1, -1], [0, 3, 2], 3)
+    assert st == 0
+    np.testing.assert_array_equal(out[0], pool[0])
+    np.testing.assert_array_equal(out[1, :3], pool[1, 3:6])
+    np.testing.assert_array_equal(out[1, 3:], pool[1, 3:])
+    np.testing.assert_array_equal(out[2:], pool[2:])
+    # overlapping ranges read their sources first
+    (out,), _ = oracle.conv_compact([pool], [2], [1], 3)
+    np.testing.assert_array_equal(out[2, :3], pool[2, 1:4])
+    # bad slot and bad accepted length are flagged and skipped; several pools at once
+    (o1, o2), st = oracle.conv_compact([pool, pool[:, :, :1]], [4, 3], [1, 4], 3)
+    assert st == oracle.BAD_SLOT | oracle.BAD_ACCEPT
+    np.testing.assert_array_equal(o1, pool)
+    np.testing.assert_array_equal(o2, pool[:, :, :1])
+
+
 def test_decode_skips_negative_slots():
     rng = np.random.default_rng(25)
     q, k, v, beta, gate = _rand_inputs(rng, 2, 1, 4, 4)

@@ -159,6 +159,21 @@ def accept_case(seed, R, K, *, q_len=None, p_match=0.7, vocab=1 << 17):
     return dict(tokens=tokens, sampled=sampled, q_len=ql, R=R, K=K)
 
 
+def conv_case(seed, R, K, keep, channels, n_pools, P, *, dtype="bf16"):
+    """Short-convolution pools for R speculative requests: n_pools tensors of
+    [P, keep + K, channels] (the history rows, then room for K step inputs),
+    values ~ N(0, 1) stored as bf16 or fp32, distinct seeded slots, and
+    accepted lengths uniform in {0..K}."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    slots = rng.permutation(P)[:R].astype(np.int32)
+    acc = rng.integers(0, K + 1, size=R).astype(np.int32)
+    pools = []
+    for _ in range(n_pools):
+        x = rng.standard_normal((P, keep + K, channels)).astype(np.float32)
+        pools.append(f32_to_bf16_bits(x) if dtype == "bf16" else x)
+    return dict(slots=slots, num_accepted=acc, pools=pools, keep=keep, K=K, dtype=dtype)
+
+
 def slot_copy_case(seed, P, n_src, fan_out, n_clear):
     """Disjoint parents, children and clears drawn from a P-slot pool."""
     rng = np.random.Generator(np.random.PCG64(seed))
