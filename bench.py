@@ -9,7 +9,9 @@ One step = one pass of every entry point over one batch of synthetic input:
   * kda_spec_verify + kda_spec_accept_commit : 64 requests, K=7, H=32; each
                            draft agrees with the sampled token with probability
                            0.7; the commit launch derives the accepted lengths
-                           from the token ids and rebuilds the states in place.
+                           from the token ids, rebuilds the states in place and
+                           moves the q / k / v short-convolution windows of the
+                           same requests (4096 bf16 channels each, keep 3).
   * kda_slot_copy        : 256 parents x 8 children + 512 clears, 4096-slot pool
                            of 1 MiB fp32 states (H=16).
 `value` is the prefill throughput in tokens/s (device time of the prefill call,
@@ -229,6 +231,10 @@ class Step:
             self.rec_u = torch.empty(64, 32, 7, D, device=dev)
             self.rec_kg = torch.empty(64, 32, 7, 2 * D, dtype=torch.bfloat16, device=dev)
             self.out3 = torch.empty(64 * 7, 32, D, dtype=torch.bfloat16, device=dev)
+            # short-convolution windows of q, k and v: 4096 bf16 channels, width 4 (keep 3)
+            cc = W.conv_case(5, 64, 7, 3, 4096, 3, 64, dtype="bf16")
+            self.conv3 = [torch.from_numpy(x.view(np.int16)).to(dev) for x in cc["pools"]]
+            self.conv_slot3 = i32(cc["slots"], dev)
         if "copy" in parts:
             c4 = W.cfg4_slot_copy()
             g = torch.Generator(device=dev).manual_seed(4)
@@ -264,10 +270,17 @@ class Step:
                                  dev_status=self.status)
 
     def commit(self):
-        # accepted lengths from the token ids and the rebuild, one launch
+        # accepted lengths from the token ids, the recurrent-state rebuild and the q / k / v
+        # conv windows, one launch
         self.kda.kda_spec_accept_commit(self.pool3, self.ckpt3, self.tok3, self.smp3, self.rec_u,
                                         self.rec_kg, num_accepted=self.acc3,
-                                        next_token=self.next3, dev_status=self.status)
+                                        next_token=self.next3, convs=self.conv3,
+                                        conv_slot=self.conv_slot3, conv_keep=3,
+                                        dev_status=self.status)
+
+    def conv_compact(self):
+        self.kda.kda_conv_compact(self.conv3, self.conv_slot3, self.acc3, 3,
+                                  dev_status=self.status)
 
     def slot_copy(self):
         c = self.c4
@@ -277,11 +290,15 @@ class Step:
     # name -> (callable, kernel launches), for the parts that were built
     def calls(self):
         part = {"prefill": "prefill", "decode": "decode", "verify": "spec", "commit": "spec",
-                "slot_copy": "copy"}
+                "conv_compact": "spec", "slot_copy": "copy"}
         every = [("prefill", self.prefill, 2), ("decode", self.decode, 1),
                  ("verify", self.verify, 1), ("commit", self.commit, 1),
                  ("slot_copy", self.slot_copy, 2)]
         return [c for c in every if part[c[0]] in self.parts]
+
+    # entry points measured on their own, outside the step (profile cases)
+    def extra_calls(self):
+        return [("conv_compact", self.conv_compact, 1)] if "spec" in self.parts else []
 
 
 def run_device(step, steps, warmup, rank, world):
@@ -548,7 +565,7 @@ def config_block():
     return {"workload": (f"batched chunk prefill: 8 packed seqs, lengths {lengths} "
                          f"(sum {sum(lengths)}), H=32, d_k=d_v=128, chunk=64, bf16 in/out, "
                          "fp32 state; step also runs decode 256xH32, spec verify + fused "
-                         "accept/commit "
+                         "accept/commit + q/k/v conv-window compaction "
                          "64xK7xH32, slot copy 256x8 + 512 clears of 1 MiB states"),
             "global_batch": 8, "seq_len": max(lengths), "tokens": sum(lengths),
             "l2": "flushed (256 MiB write) before every timed call",
@@ -606,10 +623,11 @@ def run_profile_case(name, reps):
                                   state_pool=pool, init_slot=sl, final_slot=sl,
                                   track_chunk_idx=tr, track_state=snap, workspace=ws)
     else:
-        part = {"decode": "decode", "verify": "spec", "commit": "spec", "slot_copy": "copy"}[name]
+        part = {"decode": "decode", "verify": "spec", "commit": "spec", "conv_compact": "spec",
+                "slot_copy": "copy"}[name]
         step = Step(dev, parts=(part,), compact_decode_pool=True)
-        fn = dict((n, f) for n, f, _ in step.calls())[name]
-        if name == "commit":
+        fn = dict((n, f) for n, f, _ in step.calls() + step.extra_calls())[name]
+        if name in ("commit", "conv_compact"):
             step.verify()  # records for the commit to read
     times = []
     for _ in range(reps):
@@ -632,7 +650,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode", "verify", "commit", "slot_copy"],
+    ap.add_argument("--profile", choices=["prefill", "decode", "verify", "commit", "conv_compact",
+                                          "slot_copy"],
                     help="run one entry point a few times (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.profile:
@@ -667,7 +686,8 @@ def main():
     t_hbm, t_tc = pb / (hbm * 1e9), pf / (tc * 1e12)
     dec_b = decode_work(256, 32)
     ver_b = verify_work(64, 7, 32)
-    com_b = commit_work(step.acc3.cpu().tolist(), 32, 7)
+    conv_b = sum(3 * 2 * 3 * 4096 * 2 for a in step.acc3.cpu().tolist() if a > 0)
+    com_b = commit_work(step.acc3.cpu().tolist(), 32, 7) + conv_b
     cp_b = STATE_BYTES * 16 * (sum(step.n4))
     parts = {
         "prefill": {"us": mean["prefill"] * 1e6, "tokens_per_s": toks / mean["prefill"],
@@ -713,8 +733,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "link_measured": link,
-                "link_bound_tokens_per_s": toks / (h2d / (link["h2d_gbs"] * 1e9)
-                                                   + d2h / (link["d2h_gbs"] * 1e9))},
+                # the link is full duplex: the slower direction bounds the step
+                "link_bound_tokens_per_s": toks / max(h2d / (link["h2d_gbs"] * 1e9),
+                                                      d2h / (link["d2h_gbs"] * 1e9))},
         "gpu_launches": launches,
         "clocks": clocks,
         "parts": parts,

@@ -177,6 +177,17 @@ kda_status kda_spec_verify(const void* q, const void* k, const void* v, const vo
                            const int32_t* ckpt_slot, float* rec_u, void* rec_kg, void* out,
                            kda_dtype out_dtype, int32_t* dev_status, void* stream);
 
+/* One short-convolution state tensor (HOST descriptor): slot s starts at
+ * base + s*slot_stride_bytes and holds n_rows rows of row_bytes bytes (row j
+ * at + j*row_bytes; a row is one position, its channels contiguous). */
+typedef struct {
+    void* base;                /* device, 16-byte aligned                       */
+    int64_t slot_stride_bytes; /* multiple of 16, >= n_rows * row_bytes          */
+    int64_t row_bytes;         /* channels * element size, multiple of 16        */
+    int32_t n_rows;            /* keep history rows + room for the step's inputs */
+    int32_t num_slots;
+} kda_conv_desc;
+
 /*
  * kda_spec_accept -- the accepted length of every speculative request, on the
  * device (vLLM PR 51855 page, implementation breakdown item 4: the commit plan
@@ -238,9 +249,14 @@ kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot
  *   num_accepted    : [R] int32 out or NULL: the accepted lengths (-1 for a
  *                     q_len outside [0, K]).
  *   next_token      : [R] int32 out or NULL, as for kda_spec_accept.
+ *   convs, n_convs, conv_slot, conv_keep : optional (n_convs = 0: none) -- the
+ *                     short-convolution windows of the same requests, moved in
+ *                     the same launch exactly as kda_conv_compact(convs,
+ *                     n_convs, conv_slot, <the accepted lengths>, R, conv_keep)
+ *                     would; convs is a HOST array.
  *   Every other argument is as for kda_spec_commit; the plan rows, the pool
  *   and dev_status come out exactly as kda_spec_accept followed by
- *   kda_spec_commit would leave them.
+ *   kda_spec_commit (and kda_conv_compact) would leave them.
  */
 kda_status kda_spec_accept_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                                   const int32_t* dst_slot, const int32_t* tokens,
@@ -248,7 +264,30 @@ kda_status kda_spec_accept_commit(void* state_pool, int64_t P, const int32_t* ck
                                   int32_t K, int32_t H, int32_t dk, int32_t dv, uint32_t flags,
                                   const float* rec_u, const void* rec_kg, kda_dtype rec_dtype,
                                   int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,
+                                  const kda_conv_desc* convs, int32_t n_convs,
+                                  const int32_t* conv_slot, int32_t conv_keep,
                                   int32_t* dev_status, void* stream);
+
+/*
+ * kda_conv_compact -- the short-convolution window after a speculative step,
+ * on up to KDA_MAX_POOLS conv tensors in one launch (vLLM PR 51855 page,
+ * implementation breakdown item 4: the commit compacts the convolution
+ * history; the conv state is a sliding window moved by an offset copy).
+ *
+ *   convs        : HOST array of n_convs descriptors.
+ *   slot         : [R] int32 (device): the request's slot in every tensor;
+ *                  < 0 skips it, >= num_slots skips it with KDA_DEV_BAD_SLOT.
+ *   num_accepted : [R] int32 (device), e.g. from kda_spec_accept(_commit).
+ *   keep         : history rows (the conv width minus one), >= 1.
+ * Rows keep.. of a slot hold the step's inputs (position t at row keep+t).
+ * After a accepted positions, rows a .. a+keep-1 move to rows 0 .. keep-1
+ * (memmove semantics; rows past keep are left as they were); a = 0 changes
+ * nothing; a < 0 or a + keep > n_rows skips the request with
+ * KDA_DEV_BAD_ACCEPT.  Byte copy: any element type, results exact.
+ */
+kda_status kda_conv_compact(const kda_conv_desc* convs, int32_t n_convs, const int32_t* slot,
+                            const int32_t* num_accepted, int32_t R, int32_t keep,
+                            int32_t* dev_status, void* stream);
 
 /*
  * kda_slot_copy -- one fused launch that clears, copies and fans out state

@@ -7,7 +7,7 @@ libkda.so is missing the import of the library raises.
 
 Entry points (same names as the C ABI):
   kda_chunk_prefill, kda_recurrent_decode, kda_spec_verify, kda_spec_accept, kda_spec_commit,
-  kda_spec_accept_commit, kda_slot_copy, kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
+  kda_spec_accept_commit, kda_conv_compact, kda_slot_copy, kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
 """
 from __future__ import annotations
 
@@ -20,10 +20,10 @@ __all__ = [
     "KDA_BF16", "KDA_F32", "KDA_GATE_LOG", "KDA_BETA_ACT", "KDA_STATE_BF16", "KDA_STATE_F16",
     "KdaError", "lib",
     "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
-    "kda_spec_commit", "kda_spec_accept_commit", "kda_slot_copy",
+    "kda_spec_commit", "kda_spec_accept_commit", "kda_conv_compact", "kda_slot_copy",
     "kda_chunk_prefill_workspace_size",
     "kda_slot_copy_workspace_size",
-    "kda_status_string", "kda_abi_version", "PoolDesc",
+    "kda_status_string", "kda_abi_version", "PoolDesc", "ConvDesc",
 ]
 
 KDA_BF16, KDA_F32 = 0, 1
@@ -48,6 +48,12 @@ class PoolDesc(ctypes.Structure):
                 ("slot_bytes", ctypes.c_int64), ("num_slots", ctypes.c_int64)]
 
 
+class ConvDesc(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("slot_stride_bytes", ctypes.c_int64),
+                ("row_bytes", ctypes.c_int64), ("n_rows", ctypes.c_int32),
+                ("num_slots", ctypes.c_int32)]
+
+
 def lib():
     """The loaded C library with argument types set (raises if not built)."""
     global _lib
@@ -69,7 +75,9 @@ def lib():
                                       vp, ctypes.c_int, vp, vp, vp]
         L.kda_spec_accept.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp]
         L.kda_spec_accept_commit.argtypes = [vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
-                                             u32, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp]
+                                             u32, vp, vp, ctypes.c_int, vp, vp, vp,
+                                             ctypes.POINTER(ConvDesc), i32, vp, i32, vp, vp]
+        L.kda_conv_compact.argtypes = [ctypes.POINTER(ConvDesc), i32, vp, vp, i32, i32, vp, vp]
         L.kda_slot_copy.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp, i32, i32,
                                     vp, sz, vp, vp]
         L.kda_slot_copy_noalloc.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp,
@@ -84,7 +92,7 @@ def lib():
         L.kda_abi_version.restype = i32
         for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify",
                   "kda_spec_accept", "kda_spec_commit", "kda_spec_accept_commit",
-                  "kda_slot_copy"):
+                  "kda_conv_compact", "kda_slot_copy"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -109,6 +117,13 @@ def _p(t):
         return int(t)
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError("libkda takes contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _p_any(t):
+    """Device pointer of a CUDA tensor whose layout the caller describes itself."""
+    if not t.is_cuda:
+        raise ValueError("libkda takes CUDA tensors")
     return t.data_ptr()
 
 
@@ -230,18 +245,45 @@ def kda_spec_commit(state_pool, ckpt_slot, num_accepted, rec_u, rec_kg, *, K, ds
     _check(st, "kda_spec_commit")
 
 
+def _conv_descs(convs):
+    n = 0 if convs is None else len(convs)
+    descs = (ConvDesc * max(n, 1))()
+    for i, t in enumerate(convs or ()):
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError("conv tensors need contiguous rows")
+        descs[i] = ConvDesc(_p_any(t), t.stride(0) * t.element_size(),
+                            t.shape[2] * t.element_size(), t.shape[1], t.shape[0])
+    return descs, n
+
+
 def kda_spec_accept_commit(state_pool, ckpt_slot, tokens, sampled, rec_u, rec_kg, *,
                            dst_slot=None, q_len=None, flags=0, num_accepted=None,
-                           next_token=None, plan_out=None, dev_status=None, stream=None):
-    """Accepted lengths from token ids and the closed-form rebuild, one launch
-    (see include/kda.h).  tokens, sampled: int32 CUDA tensors [R, K]."""
+                           next_token=None, plan_out=None, convs=None, conv_slot=None,
+                           conv_keep=0, dev_status=None, stream=None):
+    """Accepted lengths from token ids, the closed-form rebuild and (optionally) the
+    short-convolution windows, one launch (see include/kda.h).  tokens, sampled: int32
+    CUDA tensors [R, K]; convs: list of CUDA tensors [num_slots, rows, channels]."""
     P, H, dv, dk = state_pool.shape
     R, K = tokens.shape
+    descs, n = _conv_descs(convs)
     st = lib().kda_spec_accept_commit(
         _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(tokens), _p(sampled), _p(q_len), R,
         K, H, dk, dv, int(flags) | _state_flag(state_pool), _p(rec_u), _p(rec_kg), _dt(rec_kg),
-        _p(num_accepted), _p(next_token), _p(plan_out), _p(dev_status), _stream(stream))
+        _p(num_accepted), _p(next_token), _p(plan_out), descs, n, _p(conv_slot),
+        int(conv_keep), _p(dev_status), _stream(stream))
     _check(st, "kda_spec_accept_commit")
+
+
+def kda_conv_compact(convs, slot, num_accepted, keep, *, dev_status=None, stream=None):
+    """Short-convolution window after acceptance on every conv tensor (see include/kda.h).
+
+    convs: list of CUDA tensors [num_slots, rows, channels] (slot = first dimension, a row
+    contiguous)."""
+    descs, n = _conv_descs(convs)
+    R = int(slot.numel())
+    st = lib().kda_conv_compact(descs, n, _p(slot), _p(num_accepted), R, int(keep),
+                                _p(dev_status), _stream(stream))
+    _check(st, "kda_conv_compact")
 
 
 def kda_slot_copy(pools, clear_slots, src_slots, dst_offsets, dst_slots, workspace, *,

@@ -50,10 +50,21 @@ struct AcceptArgs {
     int32_t* next_out;       // [R] or null (kTokens)
 };
 
+// Short-convolution windows moved in the same launch (kTokens only): n_ctas blocks at the
+// front of the grid, gy per (tensor, request), each a 128-chunk column range of the rows.
+struct ConvArgs {
+    ConvDescs convs;
+    int32_t n_convs;
+    const int32_t* slot;  // [R] conv slot of each request
+    int32_t keep;
+    int32_t gy;
+    int32_t n_ctas;       // 0: no conv work
+};
+
 template <bool kBf16Rec, bool kTokens, int ST>
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     void* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
-    const int32_t* __restrict__ dst, const AcceptArgs acc_args,
+    const int32_t* __restrict__ dst, const AcceptArgs acc_args, const ConvArgs conv,
     const int32_t* __restrict__ q_len, int32_t K, int32_t H, uint32_t flags,
     const float* __restrict__ rec_u, const void* __restrict__ rec_kg, int32_t* __restrict__ plan_out,
     int32_t* __restrict__ dev_status) {
@@ -65,10 +76,27 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
     float* U = F + K * kD;                                  // [K][CR] this CTA's rows of u_t
     float* D = U + K * CR;                                  // [128]
     uint8_t* KG = reinterpret_cast<uint8_t*>(D + kD);       // [K][256] raw records (k, gate)
-    const int unit = blockIdx.x / CU;  // (request, head); the rest picks the row block
-    const int part = blockIdx.x - unit * CU;
-    const int r = unit / H, h = unit - r * H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if constexpr (kTokens) {
+        if ((int)blockIdx.x < conv.n_ctas) {  // a conv block: its request's window only
+            const int pair = blockIdx.x / conv.gy, y = blockIdx.x - pair * conv.gy;
+            const int i = pair % conv.n_convs, rc = pair / conv.n_convs;
+            const kda_conv_desc c = conv.convs.d[i];
+            const int qlc = q_len ? q_len[rc] : K;
+            const int ac = accepted_length(acc_args.tokens, acc_args.sampled, (size_t)rc * K, qlc, K, lane);
+            const int sc = conv.slot[rc];
+            if (!conv_pair_ok(c, sc, ac, conv.keep, threadIdx.x == 0 && y == 0, dev_status)) return;
+            const int64_t chunk = (int64_t)y * kCommitThreads + threadIdx.x;
+            if (chunk < c.row_bytes / 16)
+                conv_move_rows(static_cast<uint8_t*>(c.base) + (int64_t)sc * c.slot_stride_bytes + chunk * 16,
+                               c.row_bytes, ac, conv.keep);
+            return;
+        }
+    }
+    const int bid = blockIdx.x - (kTokens ? conv.n_ctas : 0);
+    const int unit = bid / CU;  // (request, head); the rest picks the row block
+    const int part = bid - unit * CU;
+    const int r = unit / H, h = unit - r * H;
     const int row0 = part * CR + warp * RW;
     const int src = ckpt[r];
     const int d = dst ? dst[r] : src;
@@ -176,7 +204,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
 
 // Host checks and the launch shared by both commit entry points.
 kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
-                         const int32_t* dst_slot, const AcceptArgs& acc, bool from_tokens,
+                         const int32_t* dst_slot, const AcceptArgs& acc, const ConvArgs& conv,
+                         bool from_tokens,
                          const int32_t* q_len, int32_t R, int32_t K, int32_t H, int32_t dk,
                          int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
                          kda_dtype rec_dtype, int32_t* plan_out, int32_t* dev_status,
@@ -205,12 +234,13 @@ kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
     const int rows = st == kStateF32 ? 4 * commit_rows<kStateF32>() : 4 * commit_rows<kStateBF16>();
     const size_t smem = kCommitStage + (size_t)(K * kD + K * rows + kD) * sizeof(float) +
                         (size_t)K * 2 * kD * es;
-    const unsigned grid = (unsigned)((kD / rows) * R * H);
+    const unsigned grid = (unsigned)((kD / rows) * R * H + conv.n_ctas);
     auto run = [&](auto kernel) {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kernel<<<grid, kCommitThreads, smem, s>>>(state_pool, P, ckpt_slot, dst_slot, acc, q_len, K,
-                                                  H, flags, rec_u, rec_kg, plan_out, dev_status);
+        kernel<<<grid, kCommitThreads, smem, s>>>(state_pool, P, ckpt_slot, dst_slot, acc, conv,
+                                                  q_len, K, H, flags, rec_u, rec_kg, plan_out,
+                                                  dev_status);
     };
     auto by_state = [&](auto rec_bf16, auto tokens) {
         constexpr bool B = decltype(rec_bf16)::value, T = decltype(tokens)::value;
@@ -241,8 +271,9 @@ extern "C" kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t
                                       const void* rec_kg, kda_dtype rec_dtype, int32_t* plan_out,
                                       int32_t* dev_status, void* stream) {
     const AcceptArgs acc{num_accepted, nullptr, nullptr, nullptr, nullptr};
-    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, false, q_len, R, K, H, dk, dv,
-                         flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
+    const ConvArgs conv{};
+    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, conv, false, q_len, R, K, H, dk,
+                         dv, flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
 }
 
 extern "C" kda_status kda_spec_accept_commit(
@@ -250,8 +281,33 @@ extern "C" kda_status kda_spec_accept_commit(
     const int32_t* tokens, const int32_t* sampled, const int32_t* q_len, int32_t R, int32_t K,
     int32_t H, int32_t dk, int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
     kda_dtype rec_dtype, int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,
+    const kda_conv_desc* convs, int32_t n_convs, const int32_t* conv_slot, int32_t conv_keep,
     int32_t* dev_status, void* stream) {
     const AcceptArgs acc{nullptr, tokens, sampled, num_accepted, next_token};
-    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, true, q_len, R, K, H, dk, dv,
-                         flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
+    ConvArgs conv{};
+    KDA_REQUIRE(n_convs >= 0 && n_convs <= KDA_MAX_POOLS, KDA_ERR_INVALID_ARG);
+    if (n_convs > 0 && R > 0) {
+        KDA_REQUIRE(convs != nullptr && conv_keep >= 1, KDA_ERR_INVALID_ARG);
+        KDA_REQUIRE(conv_slot != nullptr && aligned16(conv_slot), KDA_ERR_INVALID_ARG);
+        int64_t max_chunks = 0;
+        for (int i = 0; i < n_convs; ++i) {
+            const kda_conv_desc& c = convs[i];
+            KDA_REQUIRE(c.base != nullptr && aligned16(c.base), KDA_ERR_INVALID_ARG);
+            KDA_REQUIRE(c.row_bytes > 0 && c.row_bytes % 16 == 0, KDA_ERR_INVALID_ARG);
+            KDA_REQUIRE(c.n_rows >= conv_keep && c.num_slots > 0, KDA_ERR_INVALID_ARG);
+            KDA_REQUIRE(c.slot_stride_bytes % 16 == 0 && c.slot_stride_bytes >= c.n_rows * c.row_bytes,
+                        KDA_ERR_INVALID_ARG);
+            conv.convs.d[i] = c;
+            if (c.row_bytes / 16 > max_chunks) max_chunks = c.row_bytes / 16;
+        }
+        const int64_t gy = (max_chunks + kCommitThreads - 1) / kCommitThreads;
+        KDA_REQUIRE((int64_t)R * n_convs * gy < (1ll << 30), KDA_ERR_UNSUPPORTED);
+        conv.n_convs = n_convs;
+        conv.slot = conv_slot;
+        conv.keep = conv_keep;
+        conv.gy = (int32_t)gy;
+        conv.n_ctas = (int32_t)(R * n_convs * gy);
+    }
+    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, conv, true, q_len, R, K, H, dk,
+                         dv, flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
 }

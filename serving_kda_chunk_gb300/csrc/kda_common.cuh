@@ -230,6 +230,43 @@ __device__ __forceinline__ int accepted_length(const int32_t* __restrict__ token
     return __ffs(__ballot_sync(0xffffffffu, miss));
 }
 
+// Short-convolution tensors of one call (descriptors by value in the kernel parameters).
+struct ConvDescs {
+    kda_conv_desc d[KDA_MAX_POOLS];
+};
+
+// One thread's 16-byte column of a conv slot: rows a .. a+keep-1 move to rows 0 .. keep-1
+// (a >= 1), in groups of up to 8 with every read of a group before its writes; later groups
+// read rows a+j.. >= j+1, above every row written so far, so overlapping ranges are safe.
+__device__ __forceinline__ void conv_move_rows(uint8_t* col, int64_t row_bytes, int a, int keep) {
+    for (int j = 0; j < keep; j += 8) {
+        const int n = keep - j < 8 ? keep - j : 8;
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < n) v[q] = __ldcs(reinterpret_cast<const uint4*>(col + (int64_t)(a + j + q) * row_bytes));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < n) __stcs(reinterpret_cast<uint4*>(col + (int64_t)(j + q) * row_bytes), v[q]);
+    }
+}
+
+// Checks of one (tensor, request) of a conv compaction; true when rows must move.  Reports
+// a bad slot / accepted length once per pair (lead thread).
+__device__ __forceinline__ bool conv_pair_ok(const kda_conv_desc& c, int s, int a, int keep,
+                                             bool lead, int32_t* dev_status) {
+    if (s < 0) return false;
+    if (s >= c.num_slots) {
+        if (lead) report(dev_status, KDA_DEV_BAD_SLOT);
+        return false;
+    }
+    if (a < 0 || a + keep > c.n_rows) {
+        if (lead) report(dev_status, KDA_DEV_BAD_ACCEPT);
+        return false;
+    }
+    return a > 0;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
-              "kda_spec_commit", "kda_slot_copy"):
+              "kda_spec_commit", "kda_spec_accept_commit", "kda_conv_compact", "kda_slot_copy"):
         assert f in names
 
 
@@ -43,7 +43,7 @@ def test_status_strings_and_version(kda):
     assert kda.kda_status_string(0) == "KDA_OK"
     assert "INVALID_ARG" in kda.kda_status_string(1)
     assert "UNSUPPORTED" in kda.kda_status_string(2)
-    assert kda.kda_abi_version() >= 102
+    assert kda.kda_abi_version() >= 103
 
 
 def test_workspace_sizes(kda):
@@ -87,10 +87,18 @@ def test_host_checks_reject_bad_arguments(kda):
     assert L.kda_spec_accept(None, None, None, 0, 7, None, None, None, None) == 0
     # fused accept + commit: missing sampled ids, K = 0, K above one warp
     args = lambda tok, smp, K: (FAKE, 8, FAKE, None, tok, smp, None, 4, K, 2, 128, 128, 0,  # noqa: E731
-                                FAKE, FAKE, 0, None, None, None, None, None)
+                                FAKE, FAKE, 0, None, None, None, None, 0, None, 0, None, None)
     assert L.kda_spec_accept_commit(*args(FAKE, None, 7)) == 1
     assert L.kda_spec_accept_commit(*args(FAKE, FAKE, 0)) == 1
     assert L.kda_spec_accept_commit(*args(FAKE, FAKE, 33)) == 2
+    # fused conv windows: more than KDA_MAX_POOLS tensors, or no conv slots
+    conv = (kda.ConvDesc * 1)()
+    conv[0] = kda.ConvDesc(FAKE, 10 * 8192, 8192, 10, 8)
+    a = list(args(FAKE, FAKE, 7))
+    a[19:23] = [conv, 17, FAKE, 3]
+    assert L.kda_spec_accept_commit(*a) == 1
+    a[19:23] = [conv, 1, None, 3]
+    assert L.kda_spec_accept_commit(*a) == 1
     # prefill: chunk other than 64
     st = L.kda_chunk_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 64, 2, 128, 128, 32, 1.0,
                              0, None, 0, None, None, None, 0, None, FAKE, 0, None, 0, None, None)
@@ -124,6 +132,27 @@ def test_slot_copy_host_checks(kda):
     descs[0] = kda.PoolDesc(FAKE, 64, 64, 1 << 20)
     assert L.kda_slot_copy(descs, 1, None, 0, None, FAKE, None, 0, 0, FAKE, 16, None,
                            None) == 1
+
+
+def test_conv_compact_host_checks(kda):
+    L = kda.lib()
+    descs = (kda.ConvDesc * 2)()
+    ok = kda.ConvDesc(FAKE, 10 * 8192, 8192, 10, 8)
+    descs[0] = ok
+    args = lambda n, keep: (descs, n, FAKE, FAKE, 4, keep, None, None)  # noqa: E731
+    assert L.kda_conv_compact(*args(0, 3)) == 1            # no tensors
+    assert L.kda_conv_compact(*args(17, 3)) == 1           # more than KDA_MAX_POOLS
+    assert L.kda_conv_compact(*args(1, 0)) == 1            # keep 0
+    assert L.kda_conv_compact(*args(1, 11)) == 1           # keep > rows
+    descs[0] = kda.ConvDesc(FAKE + 8, 10 * 8192, 8192, 10, 8)
+    assert L.kda_conv_compact(*args(1, 3)) == 1            # misaligned base
+    descs[0] = kda.ConvDesc(FAKE, 10 * 8200, 8200, 10, 8)
+    assert L.kda_conv_compact(*args(1, 3)) == 1            # row not a multiple of 16 bytes
+    descs[0] = kda.ConvDesc(FAKE, 9 * 8192, 8192, 10, 8)
+    assert L.kda_conv_compact(*args(1, 3)) == 1            # slots overlap
+    descs[0] = ok
+    assert L.kda_conv_compact(descs, 1, None, None, 0, 3, None, None) == 0  # nothing to do
+    assert L.kda_conv_compact(descs, 1, None, FAKE, 4, 3, None, None) == 1  # null slots
 
 
 def test_product_path_has_no_cpu_fallback():
