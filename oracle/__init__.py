@@ -21,6 +21,8 @@ Contents
     draft and sampled token ids (integer semantics).
   * ``conv_compact`` -- the short-convolution window kept after acceptance
     (copy semantics).
+  * ``align_plan`` -- the block boundary an accepted span crosses (integer
+    semantics); the state there is ``commit`` at that accepted length.
 
 All arrays are float64 numpy arrays (bf16 inputs widened exactly by the
 caller).  Layouts follow the library: activations [tokens, heads, channels],
@@ -405,3 +407,30 @@ def conv_compact(pools, slots, num_accepted, keep):
                 continue
             outs[i][sl, :keep] = pl[sl, a:a + keep]
     return outs, status
+
+
+def align_plan(seq_len0, num_accepted, block_size):
+    """Block boundary inside each request's accepted span (RecoverSSM page,
+    implementation breakdown step 4: in align mode the commit plan computes
+    the runtime accepted lengths and the align boundaries, and the running
+    block index is updated).
+
+    A request had seq_len0 tokens before the step and keeps a more; its
+    accepted span is positions seq_len0+1 .. seq_len0+a.  Block boundaries are
+    the multiples of block_size.  Returns (a_b, block_idx): a_b is the
+    accepted length that ends on the last boundary inside the span (the
+    state there is the commit at a_b), -1 when the span holds none; block_idx
+    is the number of whole blocks after the step, floor((seq_len0 + a) /
+    block_size).  A request with seq_len0 < 0 or a < 0 gets (-1, -1)."""
+    L0 = np.asarray(seq_len0, np.int64)
+    a = np.asarray(num_accepted, np.int64)
+    a_b = np.full(L0.shape, -1, np.int32)
+    idx = np.full(L0.shape, -1, np.int32)
+    for r in range(L0.shape[0]):
+        if L0[r] < 0 or a[r] < 0:
+            continue
+        hi = (L0[r] + a[r]) // block_size
+        idx[r] = hi
+        if hi > L0[r] // block_size:
+            a_b[r] = hi * block_size - L0[r]
+    return a_b, idx

@@ -413,6 +413,23 @@ def test_conv_compact_special_cases():
     np.testing.assert_array_equal(o2, pool[:, :, :1])
 
 
+def test_align_plan_matches_walking_the_span():
+    """Walk every position of the accepted span and note the multiples of the
+    block size: the last one fixes a_b; the count of multiples up to the end
+    is the block index."""
+    for B in (1, 2, 4, 7):
+        for L0 in range(0, 3 * B + 2):
+            for a in range(0, 9):
+                a_b, idx = oracle.align_plan([L0], [a], B)
+                hits = [p for p in range(L0 + 1, L0 + a + 1) if p % B == 0]
+                assert a_b[0] == (hits[-1] - L0 if hits else -1)
+                assert idx[0] == sum(1 for p in range(1, L0 + a + 1) if p % B == 0)
+                if a <= B:  # block_size >= accepted length: at most one boundary
+                    assert len(hits) <= 1
+    a_b, idx = oracle.align_plan([-1, 5], [3, -1], 4)
+    assert a_b.tolist() == [-1, -1] and idx.tolist() == [-1, -1]
+
+
 def test_decode_skips_negative_slots():
     rng = np.random.default_rng(25)
     q, k, v, beta, gate = _rand_inputs(rng, 2, 1, 4, 4)
