@@ -238,6 +238,36 @@ kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot
                            kda_dtype rec_dtype, int32_t* plan_out, int32_t* dev_status,
                            void* stream);
 
+/* Optional work of kda_spec_accept_commit, done in the same launch (HOST
+ * struct; NULL, or n_convs = 0 and seq_len0 = NULL, asks for none).
+ *   Short-convolution windows: convs (HOST array of n_convs descriptors),
+ *     conv_slot ([R] device), conv_keep -- moved exactly as kda_conv_compact
+ *     with the accepted lengths would.
+ *   Align mode (vLLM PR 51855 page, implementation breakdown item 4: the plan
+ *   computes the align boundaries and the running block index): seq_len0
+ *     ([R] device, tokens before the step) and block_size.  When the accepted
+ *     span seq_len0+1 .. seq_len0+a holds a multiple b of block_size, the
+ *     state after a_b = b - seq_len0 accepted positions (the state at the
+ *     boundary) is rebuilt from the same records into block_slot[r] (device
+ *     [R], < 0: not written; >= P: KDA_DEV_BAD_SLOT); block_idx_out[r]
+ *     (device [R] or NULL) receives floor((seq_len0 + a) / block_size), -1
+ *     for a skipped request.  block_size < K returns KDA_ERR_UNSUPPORTED:
+ *     with smaller blocks one step can cross two boundaries (the gap the
+ *     RecoverSSM page records for mamba_block_size < num_speculative_tokens
+ *     + 1).  Block slots must be distinct from every other slot of the call.
+ */
+typedef struct {
+    const kda_conv_desc* convs;
+    const int32_t* conv_slot;
+    const int32_t* seq_len0;
+    const int32_t* block_slot;
+    int32_t* block_idx_out;
+    int32_t n_convs;
+    int32_t conv_keep;
+    int32_t block_size;
+    int32_t reserved; /* 0 */
+} kda_commit_extras;
+
 /*
  * kda_spec_accept_commit -- kda_spec_accept and kda_spec_commit in one launch:
  * every commit block derives its request's accepted length from the token ids
@@ -249,11 +279,8 @@ kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot
  *   num_accepted    : [R] int32 out or NULL: the accepted lengths (-1 for a
  *                     q_len outside [0, K]).
  *   next_token      : [R] int32 out or NULL, as for kda_spec_accept.
- *   convs, n_convs, conv_slot, conv_keep : optional (n_convs = 0: none) -- the
- *                     short-convolution windows of the same requests, moved in
- *                     the same launch exactly as kda_conv_compact(convs,
- *                     n_convs, conv_slot, <the accepted lengths>, R, conv_keep)
- *                     would; convs is a HOST array.
+ *   extras          : HOST struct or NULL: optional work of the same launch
+ *                     (see kda_commit_extras).
  *   Every other argument is as for kda_spec_commit; the plan rows, the pool
  *   and dev_status come out exactly as kda_spec_accept followed by
  *   kda_spec_commit (and kda_conv_compact) would leave them.
@@ -264,9 +291,8 @@ kda_status kda_spec_accept_commit(void* state_pool, int64_t P, const int32_t* ck
                                   int32_t K, int32_t H, int32_t dk, int32_t dv, uint32_t flags,
                                   const float* rec_u, const void* rec_kg, kda_dtype rec_dtype,
                                   int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,
-                                  const kda_conv_desc* convs, int32_t n_convs,
-                                  const int32_t* conv_slot, int32_t conv_keep,
-                                  int32_t* dev_status, void* stream);
+                                  const kda_commit_extras* extras, int32_t* dev_status,
+                                  void* stream);
 
 /*
  * kda_conv_compact -- the short-convolution window after a speculative step,

@@ -23,7 +23,7 @@ __all__ = [
     "kda_spec_commit", "kda_spec_accept_commit", "kda_conv_compact", "kda_slot_copy",
     "kda_chunk_prefill_workspace_size",
     "kda_slot_copy_workspace_size",
-    "kda_status_string", "kda_abi_version", "PoolDesc", "ConvDesc",
+    "kda_status_string", "kda_abi_version", "PoolDesc", "ConvDesc", "CommitExtras",
 ]
 
 KDA_BF16, KDA_F32 = 0, 1
@@ -54,6 +54,14 @@ class ConvDesc(ctypes.Structure):
                 ("num_slots", ctypes.c_int32)]
 
 
+class CommitExtras(ctypes.Structure):
+    _fields_ = [("convs", ctypes.POINTER(ConvDesc)), ("conv_slot", ctypes.c_void_p),
+                ("seq_len0", ctypes.c_void_p), ("block_slot", ctypes.c_void_p),
+                ("block_idx_out", ctypes.c_void_p), ("n_convs", ctypes.c_int32),
+                ("conv_keep", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 def lib():
     """The loaded C library with argument types set (raises if not built)."""
     global _lib
@@ -76,7 +84,7 @@ def lib():
         L.kda_spec_accept.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp]
         L.kda_spec_accept_commit.argtypes = [vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                              u32, vp, vp, ctypes.c_int, vp, vp, vp,
-                                             ctypes.POINTER(ConvDesc), i32, vp, i32, vp, vp]
+                                             ctypes.POINTER(CommitExtras), vp, vp]
         L.kda_conv_compact.argtypes = [ctypes.POINTER(ConvDesc), i32, vp, vp, i32, i32, vp, vp]
         L.kda_slot_copy.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp, i32, i32,
                                     vp, sz, vp, vp]
@@ -259,18 +267,22 @@ def _conv_descs(convs):
 def kda_spec_accept_commit(state_pool, ckpt_slot, tokens, sampled, rec_u, rec_kg, *,
                            dst_slot=None, q_len=None, flags=0, num_accepted=None,
                            next_token=None, plan_out=None, convs=None, conv_slot=None,
-                           conv_keep=0, dev_status=None, stream=None):
-    """Accepted lengths from token ids, the closed-form rebuild and (optionally) the
-    short-convolution windows, one launch (see include/kda.h).  tokens, sampled: int32
-    CUDA tensors [R, K]; convs: list of CUDA tensors [num_slots, rows, channels]."""
+                           conv_keep=0, seq_len0=None, block_size=0, block_slot=None,
+                           block_idx_out=None, dev_status=None, stream=None):
+    """Accepted lengths from token ids, the closed-form rebuild and, optionally, the
+    short-convolution windows and the align-mode boundary states, one launch (see
+    include/kda.h).  tokens, sampled: int32 CUDA tensors [R, K]; convs: list of CUDA
+    tensors [num_slots, rows, channels]."""
     P, H, dv, dk = state_pool.shape
     R, K = tokens.shape
     descs, n = _conv_descs(convs)
+    extras = CommitExtras(descs, _p(conv_slot), _p(seq_len0), _p(block_slot),
+                          _p(block_idx_out), n, int(conv_keep), int(block_size), 0)
     st = lib().kda_spec_accept_commit(
         _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(tokens), _p(sampled), _p(q_len), R,
         K, H, dk, dv, int(flags) | _state_flag(state_pool), _p(rec_u), _p(rec_kg), _dt(rec_kg),
-        _p(num_accepted), _p(next_token), _p(plan_out), descs, n, _p(conv_slot),
-        int(conv_keep), _p(dev_status), _stream(stream))
+        _p(num_accepted), _p(next_token), _p(plan_out), ctypes.byref(extras), _p(dev_status),
+        _stream(stream))
     _check(st, "kda_spec_accept_commit")
 
 

@@ -61,10 +61,19 @@ struct ConvArgs {
     int32_t n_ctas;       // 0: no conv work
 };
 
+// Align mode (kTokens only): the state at the last block boundary inside each accepted span.
+struct AlignArgs {
+    const int32_t* seq_len0;   // [R] tokens before the step; null: no align work
+    const int32_t* block_slot; // [R] slot receiving the boundary state, or null
+    int32_t* block_idx_out;    // [R] floor((seq_len0 + a) / block_size), or null
+    int32_t block_size;
+};
+
 template <bool kBf16Rec, bool kTokens, int ST>
-__global__ void __launch_bounds__(kCommitThreads) commit_kernel(
+__global__ void __launch_bounds__(kCommitThreads, 8) commit_kernel(
     void* __restrict__ pool, int64_t P, const int32_t* __restrict__ ckpt,
     const int32_t* __restrict__ dst, const AcceptArgs acc_args, const ConvArgs conv,
+    const AlignArgs align,
     const int32_t* __restrict__ q_len, int32_t K, int32_t H, uint32_t flags,
     const float* __restrict__ rec_u, const void* __restrict__ rec_kg, int32_t* __restrict__ plan_out,
     int32_t* __restrict__ dev_status) {
@@ -108,6 +117,23 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
         a = acc_args.acc[r];
     const bool slot_ok = src >= 0 && src < P && d >= 0 && d < P;
     const bool ok = slot_ok && ql >= 0 && ql <= K && a >= 0 && a <= ql;
+    int a_b = -1, bslot = -1;  // align mode: accepted length ending on a block boundary, its slot
+    if constexpr (kTokens) {
+        if (align.seq_len0) {
+            const int L0 = align.seq_len0[r];
+            const bool valid = L0 >= 0 && a >= 0;
+            const int hi = valid ? (int)(((int64_t)L0 + a) / align.block_size) : -1;
+            if (valid && hi > L0 / align.block_size) {
+                a_b = (int)((int64_t)hi * align.block_size - L0);
+                bslot = align.block_slot ? align.block_slot[r] : -1;
+            }
+            if (h == 0 && part == 0 && threadIdx.x == 0) {
+                if (align.block_idx_out) align.block_idx_out[r] = hi;
+                if (ok && bslot >= P) report(dev_status, KDA_DEV_BAD_SLOT);
+            }
+            if (bslot >= P) bslot = -1;
+        }
+    }
     if (h == 0 && part == 0 && threadIdx.x == 0) {
         if constexpr (kTokens) {
             if (acc_args.acc_out) acc_args.acc_out[r] = a;
@@ -155,57 +181,65 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(
         umma::cp_async_commit();
     }
     umma::cp_async_wait_all();
-    __syncthreads();
-    {
-        // F_t = k_t exp(c_t), c_t = sum over s in (t, a) of g_s: a running product of alpha from
-        // t = a - 1 down; D = exp(c_0 + g_0) = the product over every recorded step
-        const int c = threadIdx.x;
-        float prod = 1.f;
-        for (int t = a - 1; t >= 0; --t) {
-            const float kv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + c] << 16)
-                                      : reinterpret_cast<const float*>(KG)[t * 2 * kD + c];
-            const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
-                                      : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
-            F[t * kD + c] = prod * kv;
-            // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
-            prod *= (flags & KDA_GATE_LOG) ? __expf(gv) : __fdividef(1.f, 1.f + __expf(gv));
+    // pass 0: the state after a steps -> the destination slot; pass 1 (align mode): the state
+    // after a_b steps -> the block slot.  The staged checkpoint rows are only read.
+    const int n_pass = bslot >= 0 ? 2 : 1;
+#pragma unroll 1
+    for (int pass = 0; pass < n_pass; ++pass) {
+        const int aa = pass ? a_b : a;
+        const size_t dst_elem = pass ? state_elem(bslot, H, h) : SD;
+        __syncthreads();  // staging landed / the previous pass finished with F and D
+        {
+            // F_t = k_t exp(c_t), c_t = sum over s in (t, aa) of g_s: a running product of alpha
+            // from t = aa - 1 down; D = exp(c_0 + g_0) = the product over the aa steps
+            const int c = threadIdx.x;
+            float prod = 1.f;
+            for (int t = aa - 1; t >= 0; --t) {
+                const float kv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + c] << 16)
+                                          : reinterpret_cast<const float*>(KG)[t * 2 * kD + c];
+                const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
+                                          : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
+                F[t * kD + c] = prod * kv;
+                // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
+                prod *= (flags & KDA_GATE_LOG) ? __expf(gv) : __fdividef(1.f, 1.f + __expf(gv));
+            }
+            D[c] = prod;
         }
-        D[c] = prod;
-    }
-    __syncthreads();
-    const float4 dec = *reinterpret_cast<const float4*>(&D[4 * lane]);
-    // this warp's rows in groups of 4 (row = index within the CTA's staged block)
+        __syncthreads();
+        const float4 dec = *reinterpret_cast<const float4*>(&D[4 * lane]);
+        // this warp's rows in groups of 4 (row = index within the CTA's staged block)
 #pragma unroll
-    for (int g4 = 0; g4 < RW; g4 += 4) {
-        const int rb = warp * RW + g4;
-        float4 s[4];
+        for (int g4 = 0; g4 < RW; g4 += 4) {
+            const int rb = warp * RW + g4;
+            float4 s[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float4 x;
-            if constexpr (ST == kStateF32)
-                x = *reinterpret_cast<const float4*>(STG + (rb + i) * 512 + lane * 16);
-            else
-                x = SIO::widen(*reinterpret_cast<const uint2*>(STG + (rb + i) * 256 + lane * 8));
-            s[i] = f4_mul(x, dec);
+            for (int i = 0; i < 4; ++i) {
+                float4 x;
+                if constexpr (ST == kStateF32)
+                    x = *reinterpret_cast<const float4*>(STG + (rb + i) * 512 + lane * 16);
+                else
+                    x = SIO::widen(*reinterpret_cast<const uint2*>(STG + (rb + i) * 256 + lane * 8));
+                s[i] = f4_mul(x, dec);
+            }
+            for (int t = 0; t < aa; ++t) {
+                const float4 f = *reinterpret_cast<const float4*>(&F[t * kD + 4 * lane]);
+                const float4 u0 = *reinterpret_cast<const float4*>(&U[t * CR + rb]);
+                s[0] = f4_fma(u0.x, f, s[0]);
+                s[1] = f4_fma(u0.y, f, s[1]);
+                s[2] = f4_fma(u0.z, f, s[2]);
+                s[3] = f4_fma(u0.w, f, s[3]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                SIO::store4_cs(pool, dst_elem + (size_t)(part * CR + rb + i) * kD + 4 * lane, s[i]);
         }
-        for (int t = 0; t < a; ++t) {
-            const float4 f = *reinterpret_cast<const float4*>(&F[t * kD + 4 * lane]);
-            const float4 u0 = *reinterpret_cast<const float4*>(&U[t * CR + rb]);
-            s[0] = f4_fma(u0.x, f, s[0]);
-            s[1] = f4_fma(u0.y, f, s[1]);
-            s[2] = f4_fma(u0.z, f, s[2]);
-            s[3] = f4_fma(u0.w, f, s[3]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            SIO::store4_cs(pool, SD + (size_t)(part * CR + rb + i) * kD + 4 * lane, s[i]);
     }
 }
 
 // Host checks and the launch shared by both commit entry points.
 kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                          const int32_t* dst_slot, const AcceptArgs& acc, const ConvArgs& conv,
-                         bool from_tokens,
+                         const AlignArgs& align, bool from_tokens,
                          const int32_t* q_len, int32_t R, int32_t K, int32_t H, int32_t dk,
                          int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
                          kda_dtype rec_dtype, int32_t* plan_out, int32_t* dev_status,
@@ -239,8 +273,8 @@ kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         kernel<<<grid, kCommitThreads, smem, s>>>(state_pool, P, ckpt_slot, dst_slot, acc, conv,
-                                                  q_len, K, H, flags, rec_u, rec_kg, plan_out,
-                                                  dev_status);
+                                                  align, q_len, K, H, flags, rec_u, rec_kg,
+                                                  plan_out, dev_status);
     };
     auto by_state = [&](auto rec_bf16, auto tokens) {
         constexpr bool B = decltype(rec_bf16)::value, T = decltype(tokens)::value;
@@ -272,8 +306,9 @@ extern "C" kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t
                                       int32_t* dev_status, void* stream) {
     const AcceptArgs acc{num_accepted, nullptr, nullptr, nullptr, nullptr};
     const ConvArgs conv{};
-    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, conv, false, q_len, R, K, H, dk,
-                         dv, flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
+    const AlignArgs align{};
+    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, conv, align, false, q_len, R, K,
+                         H, dk, dv, flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
 }
 
 extern "C" kda_status kda_spec_accept_commit(
@@ -281,33 +316,44 @@ extern "C" kda_status kda_spec_accept_commit(
     const int32_t* tokens, const int32_t* sampled, const int32_t* q_len, int32_t R, int32_t K,
     int32_t H, int32_t dk, int32_t dv, uint32_t flags, const float* rec_u, const void* rec_kg,
     kda_dtype rec_dtype, int32_t* num_accepted, int32_t* next_token, int32_t* plan_out,
-    const kda_conv_desc* convs, int32_t n_convs, const int32_t* conv_slot, int32_t conv_keep,
-    int32_t* dev_status, void* stream) {
+    const kda_commit_extras* extras, int32_t* dev_status, void* stream) {
     const AcceptArgs acc{nullptr, tokens, sampled, num_accepted, next_token};
     ConvArgs conv{};
-    KDA_REQUIRE(n_convs >= 0 && n_convs <= KDA_MAX_POOLS, KDA_ERR_INVALID_ARG);
-    if (n_convs > 0 && R > 0) {
-        KDA_REQUIRE(convs != nullptr && conv_keep >= 1, KDA_ERR_INVALID_ARG);
-        KDA_REQUIRE(conv_slot != nullptr && aligned16(conv_slot), KDA_ERR_INVALID_ARG);
+    AlignArgs align{};
+    const kda_commit_extras none{};
+    const kda_commit_extras& x = extras ? *extras : none;
+    KDA_REQUIRE(x.n_convs >= 0 && x.n_convs <= KDA_MAX_POOLS, KDA_ERR_INVALID_ARG);
+    if (x.n_convs > 0 && R > 0) {
+        KDA_REQUIRE(x.convs != nullptr && x.conv_keep >= 1, KDA_ERR_INVALID_ARG);
+        KDA_REQUIRE(x.conv_slot != nullptr && aligned16(x.conv_slot), KDA_ERR_INVALID_ARG);
         int64_t max_chunks = 0;
-        for (int i = 0; i < n_convs; ++i) {
-            const kda_conv_desc& c = convs[i];
+        for (int i = 0; i < x.n_convs; ++i) {
+            const kda_conv_desc& c = x.convs[i];
             KDA_REQUIRE(c.base != nullptr && aligned16(c.base), KDA_ERR_INVALID_ARG);
             KDA_REQUIRE(c.row_bytes > 0 && c.row_bytes % 16 == 0, KDA_ERR_INVALID_ARG);
-            KDA_REQUIRE(c.n_rows >= conv_keep && c.num_slots > 0, KDA_ERR_INVALID_ARG);
+            KDA_REQUIRE(c.n_rows >= x.conv_keep && c.num_slots > 0, KDA_ERR_INVALID_ARG);
             KDA_REQUIRE(c.slot_stride_bytes % 16 == 0 && c.slot_stride_bytes >= c.n_rows * c.row_bytes,
                         KDA_ERR_INVALID_ARG);
             conv.convs.d[i] = c;
             if (c.row_bytes / 16 > max_chunks) max_chunks = c.row_bytes / 16;
         }
         const int64_t gy = (max_chunks + kCommitThreads - 1) / kCommitThreads;
-        KDA_REQUIRE((int64_t)R * n_convs * gy < (1ll << 30), KDA_ERR_UNSUPPORTED);
-        conv.n_convs = n_convs;
-        conv.slot = conv_slot;
-        conv.keep = conv_keep;
+        KDA_REQUIRE((int64_t)R * x.n_convs * gy < (1ll << 30), KDA_ERR_UNSUPPORTED);
+        conv.n_convs = x.n_convs;
+        conv.slot = x.conv_slot;
+        conv.keep = x.conv_keep;
         conv.gy = (int32_t)gy;
-        conv.n_ctas = (int32_t)(R * n_convs * gy);
+        conv.n_ctas = (int32_t)(R * x.n_convs * gy);
     }
-    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, conv, true, q_len, R, K, H, dk,
-                         dv, flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
+    if (x.seq_len0 != nullptr) {
+        // a span of at most K accepted positions crosses at most one boundary only when
+        // block_size >= K; smaller blocks are the configuration the align path cannot serve
+        KDA_REQUIRE(x.block_size > 0, KDA_ERR_INVALID_ARG);
+        KDA_REQUIRE(x.block_size >= K, KDA_ERR_UNSUPPORTED);
+        const void* opt[] = {x.seq_len0, x.block_slot, x.block_idx_out};
+        for (const void* p : opt) KDA_REQUIRE(p == nullptr || aligned16(p), KDA_ERR_INVALID_ARG);
+        align = AlignArgs{x.seq_len0, x.block_slot, x.block_idx_out, x.block_size};
+    }
+    return launch_commit(state_pool, P, ckpt_slot, dst_slot, acc, conv, align, true, q_len, R, K,
+                         H, dk, dv, flags, rec_u, rec_kg, rec_dtype, plan_out, dev_status, stream);
 }

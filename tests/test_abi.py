@@ -43,7 +43,7 @@ def test_status_strings_and_version(kda):
     assert kda.kda_status_string(0) == "KDA_OK"
     assert "INVALID_ARG" in kda.kda_status_string(1)
     assert "UNSUPPORTED" in kda.kda_status_string(2)
-    assert kda.kda_abi_version() >= 103
+    assert kda.kda_abi_version() >= 104
 
 
 def test_workspace_sizes(kda):
@@ -87,7 +87,7 @@ def test_host_checks_reject_bad_arguments(kda):
     assert L.kda_spec_accept(None, None, None, 0, 7, None, None, None, None) == 0
     # fused accept + commit: missing sampled ids, K = 0, K above one warp
     args = lambda tok, smp, K: (FAKE, 8, FAKE, None, tok, smp, None, 4, K, 2, 128, 128, 0,  # noqa: E731
-                                FAKE, FAKE, 0, None, None, None, None, 0, None, 0, None, None)
+                                FAKE, FAKE, 0, None, None, None, None, None, None)
     assert L.kda_spec_accept_commit(*args(FAKE, None, 7)) == 1
     assert L.kda_spec_accept_commit(*args(FAKE, FAKE, 0)) == 1
     assert L.kda_spec_accept_commit(*args(FAKE, FAKE, 33)) == 2
@@ -95,9 +95,14 @@ def test_host_checks_reject_bad_arguments(kda):
     conv = (kda.ConvDesc * 1)()
     conv[0] = kda.ConvDesc(FAKE, 10 * 8192, 8192, 10, 8)
     a = list(args(FAKE, FAKE, 7))
-    a[19:23] = [conv, 17, FAKE, 3]
+    a[19] = ctypes.byref(kda.CommitExtras(conv, FAKE, None, None, None, 17, 3, 0, 0))
     assert L.kda_spec_accept_commit(*a) == 1
-    a[19:23] = [conv, 1, None, 3]
+    a[19] = ctypes.byref(kda.CommitExtras(conv, None, None, None, None, 1, 3, 0, 0))
+    assert L.kda_spec_accept_commit(*a) == 1
+    # align mode: block size below K cannot hold one step's span; zero block size
+    a[19] = ctypes.byref(kda.CommitExtras(conv, None, FAKE, FAKE, None, 0, 0, 6, 0))
+    assert L.kda_spec_accept_commit(*a) == 2
+    a[19] = ctypes.byref(kda.CommitExtras(conv, None, FAKE, FAKE, None, 0, 0, 0, 0))
     assert L.kda_spec_accept_commit(*a) == 1
     # prefill: chunk other than 64
     st = L.kda_chunk_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 64, 2, 128, 128, 32, 1.0,

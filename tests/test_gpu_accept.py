@@ -186,3 +186,58 @@ def test_fused_accept_commit_matches_two_launches(kda, dtype):
     assert np.array_equal(plan, plan_ref)
     assert st_ref == st[0]
     assert rel_l2(pool, p_ref) < TOL_STATE
+
+
+def test_align_mode_boundary_states(kda):
+    """Align mode: a request whose accepted span seq_len0+1 .. seq_len0+a holds
+    a multiple of the block size also gets the state at that boundary (the
+    commit at a_b = boundary - seq_len0) in its block slot; the block index
+    after the step comes out for every request."""
+    R, K, H, B = 16, 7, 2, 8
+    P = 3 * R
+    rng = np.random.default_rng(95)
+    s = W.spec_case(96, R, K, H, P=P)
+    c = W.accept_case(97, R, K, p_match=0.8)
+    seq0 = rng.integers(0, 40, size=R).astype(np.int32)
+    seq0[0], seq0[1] = 7, 1          # 7 + a crosses 8 for every a >= 1; 1 + a ends on 8 at a = 7
+    free = np.array(sorted(set(range(P)) - set(s["ckpt"].tolist())), np.int32)
+    block_slot = free[:R].copy()
+    block_slot[2] = -1               # boundary state not wanted
+    block_slot[3] = P + 5            # past the pool
+    a_ref, _, _ = oracle.accept(c["tokens"], c["sampled"], K)
+    a_b, idx = oracle.align_plan(seq0, a_ref, B)
+    assert (a_b > 0).sum() >= 4, "the seeded spans should cross several boundaries"
+    dt = "bf16"
+    pool = torch.from_numpy(s["pool"]).cuda()
+    rec_u = torch.empty(R, H, K, 128, device="cuda")
+    rec_kg = torch.empty(R, H, K, 256, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(R * K, H, 128, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(R, dtype=torch.int32, device="cuda")
+    bidx = torch.full((R,), -9, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_spec_verify(dev_tensor(s["q"], dt), dev_tensor(s["k"], dt), dev_tensor(s["v"], dt),
+                        dev_tensor(s["beta"], dt), dev_tensor(s["gate"], dt), pool,
+                        i32(s["ckpt"]), rec_u, rec_kg, out, K=K, dev_status=st)
+    kda.kda_spec_accept_commit(pool, i32(s["ckpt"]), i32(c["tokens"]), i32(c["sampled"]), rec_u,
+                               rec_kg, num_accepted=acc, seq_len0=i32(seq0), block_size=B,
+                               block_slot=i32(block_slot), block_idx_out=bidx, dev_status=st)
+    torch.cuda.synchronize()
+    crossing3 = a_b[3] > 0
+    assert int(st.item()) == (kda.KDA_DEV_BAD_SLOT if crossing3 else 0)
+    assert np.array_equal(acc.cpu().numpy(), a_ref)
+    assert np.array_equal(bidx.cpu().numpy(), idx)
+    got = pool.cpu().numpy()
+    _, ru_ref, rkg_ref, _ = oracle.verify(wid(s, "q"), wid(s, "k"), wid(s, "v"), wid(s, "beta"),
+                                          wid(s, "gate"), s["pool"], s["ckpt"], K)
+    run_ref, _, _ = oracle.commit(s["pool"], s["ckpt"], a_ref, ru_ref, rkg_ref, K)
+    assert rel_l2(got[s["ckpt"]], run_ref[s["ckpt"]]) < TOL_STATE
+    want_b = (a_b > 0) & (block_slot >= 0) & (block_slot < P)
+    bnd_ref, _, _ = oracle.commit(s["pool"], s["ckpt"], np.where(want_b, a_b, 0), ru_ref, rkg_ref,
+                                  K, dst=np.where(want_b, block_slot, s["ckpt"]))
+    for r in range(R):
+        if want_b[r]:
+            assert rel_l2(got[block_slot[r]], bnd_ref[block_slot[r]]) < TOL_STATE, r
+            if a_b[r] == a_ref[r]:  # the boundary is the end of the span: the same state
+                assert np.array_equal(got[block_slot[r]], got[s["ckpt"][r]])
+        elif 0 <= block_slot[r] < P:
+            assert np.array_equal(got[block_slot[r]], s["pool"][block_slot[r]]), r
