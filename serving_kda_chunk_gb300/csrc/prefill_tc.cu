@@ -876,8 +876,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     fence_after();
     if (timed_out) {
         if (tid == 0) report(p.dev_status, KDA_DEV_TIMEOUT);
-        // give in-flight MMAs a bounded chance to drain before TMEM is released
-        mbar_wait(mbar, phase, kWaitLimit);
+        // give in-flight MMAs a bounded chance to drain before TMEM is released: the last
+        // phase waited on of each barrier (it may be the one that timed out; a wait on a
+        // completed phase returns at once) and a state update issued but not yet waited on
+        mbar_wait(mbar, phase ^ 1u, kWaitLimit);
+        mbar_wait(mbar_s, phase_s ^ 1u, kWaitLimit);
         if (pending_s) mbar_wait(mbar_s, phase_s, kWaitLimit);
     } else if (fin >= 0) {
         const size_t SD = state_elem(fin, H, h) + (size_t)row * kD;

@@ -596,8 +596,13 @@ __global__ void __launch_bounds__(kVThreads, 2)
     if (timed_out) {
         if (tid == 0) {
             report(a.dev_status, KDA_DEV_TIMEOUT);
-            // bounded drain of what is still in flight before shared memory and TMEM are released
+            // bounded drain of what may still be in flight before shared memory and TMEM are
+            // released: the last checkpoint and MMA phases waited on (either may be the one that
+            // timed out; a wait on a completed phase returns at once) and whatever was issued but
+            // not yet waited on
+            mbar_wait(smem_u32(mbars), ph_raw ^ 1u, kVWaitLimit);
             if (raw_pend) mbar_wait(smem_u32(mbars), ph_raw, kVWaitLimit);
+            mbar_wait(smem_u32(mbars + 1), ph_mma ^ 1u, kVWaitLimit);
             if (mma_pend) mbar_wait(smem_u32(mbars + 1), ph_mma, kVWaitLimit);
         }
     }
