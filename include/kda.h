@@ -169,6 +169,7 @@ kda_status kda_recurrent_decode(const void* q, const void* k, const void* v, con
  *                    gate exactly as given.
  *   out            : [R*K, H, d_v] out_dtype.
  * Positions t >= q_len and skipped requests get zero outputs and records.
+ * K <= 16 (else KDA_ERR_UNSUPPORTED); K = 0 or R = 0 launches nothing.
  */
 kda_status kda_spec_verify(const void* q, const void* k, const void* v, const void* beta_raw,
                            const void* gate_raw, kda_dtype in_dtype, int32_t R, int32_t K,
@@ -229,7 +230,8 @@ kda_status kda_spec_accept(const int32_t* tokens, const int32_t* sampled, const 
  *                  that was skipped (bad slot or bad accepted length, with the
  *                  matching dev_status bit).
  * a = 0 writes nothing when dst == src and copies S_0 otherwise.  Destinations
- * must be distinct and must not be another request's checkpoint.
+ * must be distinct and must not be another request's checkpoint.  K <= 32
+ * (else KDA_ERR_UNSUPPORTED).
  */
 kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                            const int32_t* dst_slot, const int32_t* num_accepted,
