@@ -10,9 +10,12 @@
 // key channels).  The whole block is requested at once with cp.async into
 // shared memory, so the bytes in flight cost no registers and many CTAs per SM
 // keep HBM busy; the token's activations load meanwhile.  Each warp then walks
-// its rows: a lane owns 4 key channels, the two row dot products are one
-// interleaved warp reduction, and the updated row goes straight back to the
-// slot with streaming stores.  Bound by HBM traffic: 2 x the state per
+// its rows (a lane owns 4 key channels) and writes each updated row straight
+// back to the slot with streaming stores.  With fp32 rows the two row dot
+// products of a row are one interleaved warp reduction; 16-bit rows, half the
+// bytes for the same arithmetic, are issue-bound, so there the eight dot
+// products of four rows are reduce-scattered across the warp in 14 shuffles
+// instead of 40 (the same pairwise sums, so the same bits).  Bound by HBM traffic: 2 x the state per
 // (request, head).
 #include "kda_common.cuh"
 #include "kda_host.h"
@@ -80,20 +83,75 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
     in.kq = warp_sum(f4_dot(in.k, in.q));
     in.beta = beta_act(A::load1(beta_raw, th), flags);
     const int row0 = warp * RW;  // within the CTA's rows
-    const float vm = lane < RW ? A::load1(v, th * kD + part * CR + row0 + lane) : 0.f;
-    umma::cp_async_wait_all();
-    __syncthreads();
-    float o_m = 0.f;
+    if constexpr (ST == kStateF32) {
+        // one row at a time: the two row dot products are one interleaved warp reduction
+        const float vm = lane < RW ? A::load1(v, th * kD + part * CR + row0 + lane) : 0.f;
+        umma::cp_async_wait_all();
+        __syncthreads();
+        float o_m = 0.f;
 #pragma unroll 4
-    for (int i = 0; i < RW; ++i) {
-        const float4 x = f4_mul(smem_row4<ST>(buf, row0 + i, lane), in.a);
-        float d1 = f4_dot(x, in.k), d2 = f4_dot(x, in.q);
-        warp_sum2(d1, d2);
-        const float u = in.beta * (__shfl_sync(0xffffffffu, vm, i) - d1);
-        SIO::store4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane, f4_fma(u, in.k, x));
-        if (lane == i) o_m = fmaf(u, in.kq, d2);
+        for (int i = 0; i < RW; ++i) {
+            const float4 x = f4_mul(smem_row4<ST>(buf, row0 + i, lane), in.a);
+            float d1 = f4_dot(x, in.k), d2 = f4_dot(x, in.q);
+            warp_sum2(d1, d2);
+            const float u = in.beta * (__shfl_sync(0xffffffffu, vm, i) - d1);
+            SIO::store4_cs(pool, S + (size_t)(row0 + i) * kD + 4 * lane, f4_fma(u, in.k, x));
+            if (lane == i) o_m = fmaf(u, in.kq, d2);
+        }
+        if (lane < RW) store1<kBf16Out>(out, th * kD + part * CR + row0 + lane, o_m);
+    } else {
+        // 16-bit rows carry half the bytes for the same arithmetic, so the issue rate binds:
+        // rows in groups of four.  The eight partial row dot products of a group (d1 = x . k and
+        // d2 = x . q of each row) are reduce-scattered across the warp: after halving steps over
+        // lane bits 4, 3 and 2 and full sums over bits 1 and 0, lane l holds the total of value
+        // m = l >> 2, i.e. d1 of row m (m < 4) or d2 of row m - 4.  u is formed where its d1 is and
+        // broadcast for the row update; o is formed where its d2 is.
+        const int m = lane >> 2;
+        float vloc[RW / 4];  // v of row 4 g + m at the lanes that form u (m < 4)
+#pragma unroll
+        for (int g = 0; g < RW / 4; ++g)
+            vloc[g] = m < 4 ? A::load1(v, th * kD + part * CR + row0 + 4 * g + m) : 0.f;
+        umma::cp_async_wait_all();
+        __syncthreads();
+#pragma unroll
+        for (int g = 0; g < RW / 4; ++g) {
+            const int rg = row0 + 4 * g;
+            float4 x[4];
+            float vals[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[i] = f4_mul(smem_row4<ST>(buf, rg + i, lane), in.a);
+                vals[i] = f4_dot(x[i], in.k);
+                vals[4 + i] = f4_dot(x[i], in.q);
+            }
+#pragma unroll
+            for (int step = 0; step < 3; ++step) {  // offsets 16, 8, 4: 8 -> 4 -> 2 -> 1 values
+                const int off = 16 >> step, half = 4 >> step;
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (e < half) {
+                        const float send = upper ? vals[e] : vals[e + half];
+                        const float keep = upper ? vals[e + half] : vals[e];
+                        vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+            }
+            float tot = vals[0];
+            tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+            tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+            const float u_here = in.beta * (vloc[g] - tot);  // u of row m at lanes with m < 4
+            float uu[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) uu[i] = __shfl_sync(0xffffffffu, u_here, 4 * i);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                SIO::store4_cs(pool, S + (size_t)(rg + i) * kD + 4 * lane, f4_fma(uu[i], in.k, x[i]));
+            const float u_o = __shfl_sync(0xffffffffu, u_here, 4 * (m & 3));  // u of row m - 4
+            if (m >= 4 && (lane & 3) == 0)
+                store1<kBf16Out>(out, th * kD + part * CR + rg + (m - 4), fmaf(u_o, in.kq, tot));
+        }
     }
-    if (lane < RW) store1<kBf16Out>(out, th * kD + part * CR + row0 + lane, o_m);
 }
 
 template <bool I, bool O>
