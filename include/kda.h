@@ -382,6 +382,18 @@ kda_status kda_slot_copy_noalloc(const kda_pool_desc* pools, int32_t n_pools,
                                  const int32_t* dst_slots, int32_t n_src, int32_t n_dst,
                                  int32_t* dev_status, void* stream);
 
+/*
+ * kda_selftest_bounded_wait -- diagnostic: runs the kernels' bounded mbarrier
+ * wait on a barrier nothing arrives on, for `polls` polls, and ORs
+ * KDA_DEV_TIMEOUT into *dev_status when the wait gives up (it always does).
+ * *cycles (device, may be NULL) receives the SM cycles the wait took.  The
+ * kernels use 2^18 polls (a poll of a pending barrier suspends the thread for
+ * some microseconds, so about a second); a wait that gives up there reports
+ * the same bit and the call returns normally, with the context still usable.
+ */
+kda_status kda_selftest_bounded_wait(uint32_t polls, int32_t* dev_status,
+                                     unsigned long long* cycles, void* stream);
+
 const char* kda_status_string(kda_status s);
 
 /* Version of the library ABI (major * 100 + minor). */

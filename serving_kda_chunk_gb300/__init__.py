@@ -23,7 +23,8 @@ __all__ = [
     "kda_spec_commit", "kda_spec_accept_commit", "kda_conv_compact", "kda_slot_copy",
     "kda_chunk_prefill_workspace_size",
     "kda_slot_copy_workspace_size",
-    "kda_status_string", "kda_abi_version", "PoolDesc", "ConvDesc", "CommitExtras",
+    "kda_status_string", "kda_abi_version", "kda_selftest_bounded_wait", "PoolDesc",
+    "ConvDesc", "CommitExtras",
 ]
 
 KDA_BF16, KDA_F32 = 0, 1
@@ -86,6 +87,7 @@ def lib():
                                              u32, vp, vp, ctypes.c_int, vp, vp, vp,
                                              ctypes.POINTER(CommitExtras), vp, vp]
         L.kda_conv_compact.argtypes = [ctypes.POINTER(ConvDesc), i32, vp, vp, i32, i32, vp, vp]
+        L.kda_selftest_bounded_wait.argtypes = [u32, vp, vp, vp]
         L.kda_slot_copy.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp, i32, i32,
                                     vp, sz, vp, vp]
         L.kda_slot_copy_noalloc.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, i32, vp, vp, vp,
@@ -100,7 +102,7 @@ def lib():
         L.kda_abi_version.restype = i32
         for f in ("kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify",
                   "kda_spec_accept", "kda_spec_commit", "kda_spec_accept_commit",
-                  "kda_conv_compact", "kda_slot_copy"):
+                  "kda_conv_compact", "kda_slot_copy", "kda_selftest_bounded_wait"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -296,6 +298,13 @@ def kda_conv_compact(convs, slot, num_accepted, keep, *, dev_status=None, stream
     st = lib().kda_conv_compact(descs, n, _p(slot), _p(num_accepted), R, int(keep),
                                 _p(dev_status), _stream(stream))
     _check(st, "kda_conv_compact")
+
+
+def kda_selftest_bounded_wait(polls, dev_status, cycles=None, stream=None):
+    """Diagnostic: the kernels' bounded wait on a barrier nothing arrives on (see
+    include/kda.h).  dev_status: int32 CUDA tensor; cycles: int64 CUDA tensor or None."""
+    st = lib().kda_selftest_bounded_wait(int(polls), _p(dev_status), _p(cycles), _stream(stream))
+    _check(st, "kda_selftest_bounded_wait")
 
 
 def kda_slot_copy(pools, clear_slots, src_slots, dst_offsets, dst_slots, workspace, *,

@@ -94,7 +94,7 @@ constexpr uint32_t TM_KG_HI = 448, TM_KG_LO = 480;  // KG [i][s], K = 64 (until 
 constexpr uint32_t TM_U_HI = 448, TM_U_LO = 480;    // U^T [c][s], K = 64 (from MMA 3 on)
 constexpr uint32_t TM_COLS = 512;
 
-constexpr uint32_t kWaitLimit = 1u << 22;    // polls; a healthy MMA batch completes in microseconds
+constexpr uint32_t kWaitLimit = 1u << 18;    // polls of ~4 us (try_wait suspends): ~1 s; a healthy MMA batch takes microseconds
 constexpr float kFactorMax = 1.8446744e19f;  // 2^64
 
 __device__ __forceinline__ float bf16_at(const uint8_t* sm, uint32_t off) {

@@ -190,7 +190,7 @@ extern "C" const char* kda_status_string(kda_status st) {
     return "KDA_ERR_UNKNOWN";
 }
 
-extern "C" int32_t kda_abi_version(void) { return 104; }
+extern "C" int32_t kda_abi_version(void) { return 105; }
 
 // ----------------------------------------------------------------------------
 // Allocation-free variant.

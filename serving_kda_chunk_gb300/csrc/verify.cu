@@ -45,7 +45,7 @@ using namespace umma;
 constexpr int kVThreads = 256;          // 8 warps: two per TMEM lane quarter
 constexpr int kMaxVerifyK = 16;
 constexpr int kMaxUnitsPerCta = 512;    // per-CTA unit table in shared memory
-constexpr uint32_t kVWaitLimit = 1u << 22;  // polls; a checkpoint or an MMA batch lands in microseconds
+constexpr uint32_t kVWaitLimit = 1u << 18;  // polls of ~4 us (try_wait suspends): ~1 s; a checkpoint or an MMA batch lands in microseconds
 
 struct VerifyArgs {
     const void* q;
