@@ -420,6 +420,47 @@ def run_spec_graph(step, steps, warmup):
     return statistics.mean(ts)
 
 
+def run_prefill_long(step, reps):
+    """One long sequence (131 072 tokens, H = 16, snapshots every 64 chunks, final state to a
+    slot): the chunk recurrence leaves one (sequence, head) unit per head, so 16 SMs carry it.
+    Timed like the step's calls (L2 flushed, CUDA events), outside the timed step.  Returns
+    (mean seconds, tokens, algorithmic bytes)."""
+    import torch
+
+    c = W.cfg4_prefill()
+    dev = step.dev
+    t = {n: to_dev(c[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+    T, H = c["T"], c["H"]
+    pool = torch.zeros(1, H, D, D, device=dev)
+    cu = i32(c["cu_seqlens"], dev)
+    fin = i32([0], dev)
+    tr = i32(c["track"], dev)
+    snap = torch.empty(1, c["track"].shape[1], H, D, D, device=dev)
+    out = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(step.kda.kda_chunk_prefill_workspace_size(T, 1, H), 16),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        step.kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
+                                   state_pool=pool, final_slot=fin, track_chunk_idx=tr,
+                                   track_state=snap, workspace=ws, dev_status=step.status)
+
+    call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        step.flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    n_states = 1 + int((c["track"] >= 0).sum())  # final state + snapshots (no initial state)
+    return statistics.mean(ts), T, T * H * 1282 + n_states * H * STATE_BYTES
+
+
 def run_e2e(step, steps, warmup):
     """Prefill through the public call with host buffers, streamed per sequence: the pinned
     H2D copies of a sequence's inputs (one stream, longest sequence first), its
@@ -706,6 +747,7 @@ def main():
     e2e_t, h2d, d2h, link = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t16 = run_state_bf16(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t_graph = run_spec_graph(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
+    t_long, tok_long, b_long = run_prefill_long(step, 2)
 
     hbm, tc, peak_kind = load_peaks()
     mean = {k: statistics.mean(v) for k, v in times.items()}
@@ -735,6 +777,9 @@ def main():
                    "hbm_frac": com_b / (hbm * 1e9) / mean["commit"]},
         "verify_commit_us_per_step": (mean["verify"] + mean["commit"]) * 1e6,
         "verify_commit_graph_us": t_graph * 1e6,
+        "prefill_long": {"us": t_long * 1e6, "tokens_per_s": tok_long / t_long, "bytes": b_long,
+                         "hbm_frac": b_long / (hbm * 1e9) / t_long,
+                         "note": "1 x 131072 tokens, H=16: one unit per head, 16 SMs busy"},
         "slot_copy": {"us": mean["slot_copy"] * 1e6, "bytes": cp_b,
                       "hbm_frac": cp_b / (hbm * 1e9) / mean["slot_copy"]},
     }
