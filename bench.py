@@ -72,10 +72,11 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
 
 
 # DRAM traffic of the chunked prefill kernel measured with ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum = 277.5 MB + 59.2 MB) on the `--profile prefill` case
-# (8 x 2048 tokens, 16 heads); traffic grows with the token-heads processed, so a
-# launch is charged this much per token-head.  Re-measure when the kernel changes.
-PREFILL_TRAFFIC_PER_TOKEN_HEAD = (277.5e6 + 59.2e6) / (8 * 2048 * 16)
+# dram__bytes_write.sum = 277.63 MB + 58.95 MB) on the `--profile prefill` case
+# (8 x 2048 tokens, 16 heads) with the kernel as it stands; traffic grows with the
+# token-heads processed, so a launch is charged this much per token-head.  Re-measure
+# when the kernel changes.
+PREFILL_TRAFFIC_PER_TOKEN_HEAD = (277.63e6 + 58.95e6) / (8 * 2048 * 16)
 
 
 def decode_work(R, H, sb=STATE_BYTES):
