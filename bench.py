@@ -195,7 +195,7 @@ class Step:
         self.parts = tuple(parts)
         t0 = time.time()
         if "prefill" in parts:
-            c1 = _cfg1()
+            c1 = _batched_prefill()
             self.c1 = c1
             self.pre = {n: to_dev(c1[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
             self.pre_host = {n: torch.from_numpy(c1[n].view(np.int16)).view(torch.bfloat16)
@@ -210,7 +210,7 @@ class Step:
             ws = kda.kda_chunk_prefill_workspace_size(c1["T"], c1["N"], 32)
             self.ws1 = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         if "decode" in parts:
-            c2 = W.cfg2()
+            c2 = W.decode_256req_h32()
             self.dec = {n: to_dev(c2[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
             if compact_decode_pool:
                 self.pool2 = torch.from_numpy(c2["pool"][c2["slot"]]).to(dev)
@@ -220,7 +220,7 @@ class Step:
                 self.slot2 = i32(c2["slot"], dev)
             self.out2 = torch.empty(256, 32, D, dtype=torch.bfloat16, device=dev)
         if "spec" in parts:
-            c3 = W.cfg3()
+            c3 = W.spec_64req_k7_h32()
             self.c3 = c3
             self.spec = {n: to_dev(c3[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
             self.pool3 = torch.from_numpy(c3["pool"]).to(dev)
@@ -237,7 +237,7 @@ class Step:
             self.conv3 = [torch.from_numpy(x.view(np.int16)).to(dev) for x in cc["pools"]]
             self.conv_slot3 = i32(cc["slots"], dev)
         if "copy" in parts:
-            c4 = W.cfg4_slot_copy()
+            c4 = W.slot_fanout_256x8_pool4096()
             g = torch.Generator(device=dev).manual_seed(4)
             self.pool4 = torch.empty(4096, 16, D, D, device=dev)
             for i in range(0, 4096, 512):
@@ -428,7 +428,7 @@ def run_prefill_long(step, reps):
     (mean seconds, tokens, algorithmic bytes)."""
     import torch
 
-    c = W.cfg4_prefill()
+    c = W.long_prefill_131072_h16()
     dev = step.dev
     t = {n: to_dev(c[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
     T, H = c["T"], c["H"]
@@ -552,20 +552,20 @@ def run_e2e(step, steps, warmup):
 # CPU oracle on a bounded sample of the prefill workload
 
 
-_CFG1 = None
+_BATCHED_PREFILL = None
 
 
-def _cfg1():
-    global _CFG1
-    if _CFG1 is None:
-        _CFG1 = W.cfg1()
-    return _CFG1
+def _batched_prefill():
+    global _BATCHED_PREFILL
+    if _BATCHED_PREFILL is None:
+        _BATCHED_PREFILL = W.batched_prefill_8seq_h32()
+    return _BATCHED_PREFILL
 
 
 def cpu_oracle_sample(heads=(0, 1, 2, 3), threads=None):
     import oracle
 
-    c = _cfg1()
+    c = _batched_prefill()
     H = c["H"]
     hs = list(heads)
     wid = lambda n: W.widen(c[n], "bf16")[:, hs]  # noqa: E731
@@ -635,7 +635,7 @@ def sum_over_ranks(x, world):
 
 
 def config_block():
-    lengths = W.cfg1_lengths()
+    lengths = W.batched_prefill_lengths()
     return {"workload": (f"batched chunk prefill: 8 packed seqs, lengths {lengths} "
                          f"(sum {sum(lengths)}), H=32, d_k=d_v=128, chunk=64, bf16 in/out, "
                          "fp32 state; step also runs decode 256xH32, spec verify + fused "
@@ -659,7 +659,7 @@ def main_reference(args, rank, world):
         vals.append(cb["value"])
     value = statistics.mean(vals)
     cb["value"] = value
-    toks = sum(W.cfg1_lengths())
+    toks = sum(W.batched_prefill_lengths())
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": 1, "steps": steps, "warmup": min(args.warmup, 1),
             "ms_per_step": toks / value * 1e3, "higher_is_better": True, "scaling": "weak",

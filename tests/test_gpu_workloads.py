@@ -51,8 +51,8 @@ def _oracle_heads(c, heads, S0_all=None):
                           S0=S0, track=c["track"])
 
 
-def test_cfg0_tiny_prefill_fp32(kda):
-    c = W.cfg0()
+def test_tiny_prefill_fp32(kda):
+    c = W.tiny_prefill_512_h4()
     c["final_slot"] = np.array([0], np.int32)  # also read back the final state
     pool = np.zeros((1, 4, 128, 128), np.float32)
     out, pool_d, snap, st = _prefill_gpu(kda, c, pool)
@@ -63,8 +63,8 @@ def test_cfg0_tiny_prefill_fp32(kda):
     assert rel_l2(pool_d.cpu().numpy(), s_ref) < TOL_STATE
 
 
-def test_cfg1_batched_prefill_sampled_heads(kda):
-    c = W.cfg1()
+def test_batched_prefill_sampled_heads(kda):
+    c = W.batched_prefill_8seq_h32()
     S0_all = c["pool"][c["init_slot"]].astype(np.float64)
     out, pool, snap, st = _prefill_gpu(kda, c, c["pool"])
     assert st == 0
@@ -79,8 +79,8 @@ def test_cfg1_batched_prefill_sampled_heads(kda):
     assert not torch.isnan(snap).any()
 
 
-def test_cfg2_decode_full(kda):
-    d = W.cfg2()
+def test_decode_256req_full(kda):
+    d = W.decode_256req_h32()
     pool = torch.from_numpy(d["pool"]).cuda()
     out = torch.empty(256, 32, 128, dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -99,8 +99,8 @@ def test_cfg2_decode_full(kda):
                           d["pool"][untouched])
 
 
-def test_cfg3_spec_verify_commit_full(kda):
-    s = W.cfg3()
+def test_spec_64req_verify_commit_full(kda):
+    s = W.spec_64req_k7_h32()
     pool = torch.from_numpy(s["pool"]).cuda()
     rec_u = torch.empty(64, 32, 7, 128, device="cuda")
     rec_kg = torch.empty(64, 32, 7, 256, dtype=torch.bfloat16, device="cuda")
@@ -128,11 +128,11 @@ def test_cfg3_spec_verify_commit_full(kda):
     assert np.array_equal(pool.cpu().numpy()[zero], s["pool"][zero])
 
 
-def test_cfg3_accept_commit_chain_full(kda):
+def test_spec_64req_accept_commit_chain_full(kda):
     """The serving spec workload with accepted lengths computed on the device:
     verify -> accept -> commit with no host round trip, and the fused
     accept + commit launch that the benchmark times."""
-    s = W.cfg3()
+    s = W.spec_64req_k7_h32()
     c = W.accept_case(3, 64, 7, p_match=0.7)
     pool = torch.from_numpy(s["pool"]).cuda()
     pool_fused = pool.clone()
@@ -163,8 +163,8 @@ def test_cfg3_accept_commit_chain_full(kda):
     assert rel_l2(pool.cpu().numpy(), p_ref) < TOL_STATE
 
 
-def test_cfg4_long_prefill_sampled_heads(kda):
-    c = W.cfg4_prefill()
+def test_long_prefill_sampled_heads(kda):
+    c = W.long_prefill_131072_h16()
     c["final_slot"] = np.array([0], np.int32)
     c["init_slot"] = np.array([-1], np.int32)
     pool = np.zeros((1, 16, 128, 128), np.float32)
@@ -178,8 +178,8 @@ def test_cfg4_long_prefill_sampled_heads(kda):
     assert not torch.isnan(snap).any()
 
 
-def test_cfg4_slot_copy_sampled(kda):
-    sc = W.cfg4_slot_copy()
+def test_slot_fanout_sampled(kda):
+    sc = W.slot_fanout_256x8_pool4096()
     g = torch.Generator(device="cuda").manual_seed(4)
     pool = torch.empty(4096, 16, 128, 128, device="cuda")
     for i in range(0, 4096, 512):

@@ -188,23 +188,18 @@ def slot_copy_case(seed, P, n_src, fan_out, n_clear):
 # --------------------------------------------------------------------------
 # the five serving workloads (sizes of the published configurations)
 
-CFG0 = "tiny prefill: 1 seq T=512, H=4, fp32, S0=0, snapshot j=3"
-CFG1 = "batched prefill: 8 seqs L~U[1024,8192], H=32, bf16, 64-slot pool"
-CFG2 = "decode: 256 req, H=32, bf16, 1024-slot pool"
-CFG3 = "spec verify+commit: 64 req, K=7, H=32, bf16"
-CFG4 = "long prefill T=131072 H=16 + slot fan-out 256x8 + 512 clears, 4096-slot pool"
-
-
-def cfg0():
+def tiny_prefill_512_h4():
+    """1 sequence, T = 512, H = 4, fp32 throughout, S0 = 0, snapshot j = 3."""
     return prefill_case(0, [512], 4, dtype="f32", track=[[3]])
 
 
-def cfg1_lengths(seed=1):
+def batched_prefill_lengths(seed=1):
     rng = np.random.Generator(np.random.PCG64(seed))
     return [int(x) for x in rng.integers(1024, 8192 + 1, size=8)]
 
 
-def cfg1():
+def batched_prefill_8seq_h32():
+    """8 sequences, lengths ~ U[1024, 8192], H = 32, bf16, a 64-slot pool."""
     # lengths drawn first from the same stream, then slots, tracks, tokens, pool
     rng = np.random.Generator(np.random.PCG64(1))
     lengths = [int(x) for x in rng.integers(1024, 8192 + 1, size=8)]
@@ -224,19 +219,23 @@ def _prefill_from_rng(rng, lengths, H, dtype, pool_slots, dk=128, dv=128, chunk=
                 lengths=lengths)
 
 
-def cfg2():
+def decode_256req_h32():
+    """256 requests x 1 token, H = 32, bf16, a 1024-slot pool."""
     return decode_case(2, 256, 32, 1024)
 
 
-def cfg3():
+def spec_64req_k7_h32():
+    """Speculative verify + commit: 64 requests, K = 7, H = 32, bf16."""
     return spec_case(3, 64, 7, 32)
 
 
-def cfg4_prefill():
+def long_prefill_131072_h16():
+    """1 sequence, T = 131072, H = 16, snapshots every 64 chunks."""
     T = 131072
     track = [[64 * m for m in range(1, 32)]]
     return prefill_case(4, [T], 16, track=track, pool_slots=0)
 
 
-def cfg4_slot_copy():
+def slot_fanout_256x8_pool4096():
+    """256 parents fanned out to 8 children each, plus 512 clears, in a 4096-slot pool."""
     return slot_copy_case(4, 4096, 256, 8, 512)
