@@ -7,7 +7,8 @@ libkda.so is missing the import of the library raises.
 
 Entry points (same names as the C ABI):
   kda_chunk_prefill, kda_recurrent_decode, kda_spec_verify, kda_spec_accept, kda_spec_commit,
-  kda_spec_accept_commit, kda_conv_compact, kda_slot_copy, kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
+  kda_spec_accept_commit, kda_conv_compact, kda_slot_copy, kda_slot_copy_noalloc,
+  kda_chunk_prefill_workspace_size, kda_slot_copy_workspace_size.
 """
 from __future__ import annotations
 
@@ -21,7 +22,7 @@ __all__ = [
     "KdaError", "lib",
     "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
     "kda_spec_commit", "kda_spec_accept_commit", "kda_conv_compact", "kda_slot_copy",
-    "kda_chunk_prefill_workspace_size",
+    "kda_slot_copy_noalloc", "kda_chunk_prefill_workspace_size",
     "kda_slot_copy_workspace_size",
     "kda_status_string", "kda_abi_version", "kda_selftest_bounded_wait", "PoolDesc",
     "ConvDesc", "CommitExtras",
@@ -145,6 +146,28 @@ def _dt(t) -> int:
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
+def _acts(*ts) -> int:
+    """The one activation dtype of the given tensors (bf16 or fp32): the C ABI takes a
+    single in_dtype for q, k, v, beta and gate, so a mix is rejected here."""
+    dts = {t.dtype for t in ts if t is not None}
+    if len(dts) != 1:
+        raise ValueError(f"activations must share one dtype, got {sorted(map(str, dts))}")
+    return _dt(next(t for t in ts if t is not None))
+
+
+def _idx(t, name):
+    """Device pointer of an int32 index tensor (or None)."""
+    if t is not None and isinstance(t, torch.Tensor) and t.dtype != torch.int32:
+        raise ValueError(f"{name} must be an int32 tensor, got {t.dtype}")
+    return _p(t)
+
+
+def _f32(t, name):
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be an fp32 tensor, got {t.dtype}")
+    return _p(t)
+
+
 def _stream(stream):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -196,12 +219,14 @@ def kda_chunk_prefill(q, k, v, beta_raw, gate_raw, cu_seqlens, out, *, state_poo
     M = 0 if track_chunk_idx is None else int(track_chunk_idx.shape[-1])
     P = 0 if state_pool is None else int(state_pool.shape[0])
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    in_dt = _acts(q, k, v, beta_raw, gate_raw)
     st = lib().kda_chunk_prefill(
-        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), _p(cu_seqlens), N, T_tot, H, dk,
-        dv, chunk, float(scale), int(flags) | _state_flag(state_pool, track_state),
-        _p(state_pool), P, _p(init_slot), _p(final_slot),
-        _p(track_chunk_idx), M, _p(track_state), _p(out), _dt(out), _p(workspace), ws_bytes,
-        _p(dev_status), _stream(stream))
+        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), in_dt, _idx(cu_seqlens, "cu_seqlens"),
+        N, T_tot, H, dk, dv, chunk, float(scale),
+        int(flags) | _state_flag(state_pool, track_state), _p(state_pool), P,
+        _idx(init_slot, "init_slot"), _idx(final_slot, "final_slot"),
+        _idx(track_chunk_idx, "track_chunk_idx"), M, _p(track_state), _p(out), _dt(out),
+        _p(workspace), ws_bytes, _idx(dev_status, "dev_status"), _stream(stream))
     _check(st, "kda_chunk_prefill")
 
 
@@ -210,11 +235,11 @@ def kda_recurrent_decode(q, k, v, beta_raw, gate_raw, state_pool, slot, out, *, 
     """One token per request, in place on state_pool[slot] (see include/kda.h)."""
     R, H, dk = q.shape
     dv = v.shape[2]
+    in_dt = _acts(q, k, v, beta_raw, gate_raw)
     st = lib().kda_recurrent_decode(
-        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), R, H, dk, dv, float(scale),
+        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), in_dt, R, H, dk, dv, float(scale),
         int(flags) | _state_flag(state_pool), _p(state_pool), int(state_pool.shape[0]),
-        _p(slot), _p(out), _dt(out),
-        _p(dev_status), _stream(stream))
+        _idx(slot, "slot"), _p(out), _dt(out), _idx(dev_status, "dev_status"), _stream(stream))
     _check(st, "kda_recurrent_decode")
 
 
@@ -223,12 +248,18 @@ def kda_spec_verify(q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, r
     """K speculative positions per request from one checkpoint (see include/kda.h)."""
     RK, H, dk = q.shape
     dv = v.shape[2]
-    R = RK // K
+    K = int(K)
+    if K < 0 or (K > 0 and RK % K):
+        raise ValueError(f"q has {RK} rows, not a multiple of K = {K}")
+    R = RK // K if K > 0 else int(ckpt_slot.numel())  # K = 0 launches nothing
+    in_dt = _acts(q, k, v, beta_raw, gate_raw)
+    if rec_kg.dtype != q.dtype:
+        raise ValueError(f"rec_kg holds the activations' dtype {q.dtype}, got {rec_kg.dtype}")
     st = lib().kda_spec_verify(
-        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), _dt(q), R, K, _p(q_len), H, dk, dv,
-        float(scale), int(flags) | _state_flag(state_pool), _p(state_pool),
-        int(state_pool.shape[0]), _p(ckpt_slot),
-        _p(rec_u), _p(rec_kg), _p(out), _dt(out), _p(dev_status), _stream(stream))
+        _p(q), _p(k), _p(v), _p(beta_raw), _p(gate_raw), in_dt, R, K, _idx(q_len, "q_len"), H,
+        dk, dv, float(scale), int(flags) | _state_flag(state_pool), _p(state_pool),
+        int(state_pool.shape[0]), _idx(ckpt_slot, "ckpt_slot"), _f32(rec_u, "rec_u"),
+        _p(rec_kg), _p(out), _dt(out), _idx(dev_status, "dev_status"), _stream(stream))
     _check(st, "kda_spec_verify")
 
 
@@ -238,8 +269,10 @@ def kda_spec_accept(tokens, sampled, num_accepted, *, q_len=None, next_token=Non
 
     tokens, sampled: int32 CUDA tensors [R, K]."""
     R, K = tokens.shape
-    st = lib().kda_spec_accept(_p(tokens), _p(sampled), _p(q_len), R, K, _p(num_accepted),
-                               _p(next_token), _p(dev_status), _stream(stream))
+    st = lib().kda_spec_accept(_idx(tokens, "tokens"), _idx(sampled, "sampled"),
+                               _idx(q_len, "q_len"), R, K, _idx(num_accepted, "num_accepted"),
+                               _idx(next_token, "next_token"), _idx(dev_status, "dev_status"),
+                               _stream(stream))
     _check(st, "kda_spec_accept")
 
 
@@ -249,9 +282,10 @@ def kda_spec_commit(state_pool, ckpt_slot, num_accepted, rec_u, rec_kg, *, K, ds
     P, H, dv, dk = state_pool.shape
     R = ckpt_slot.shape[0]
     st = lib().kda_spec_commit(
-        _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(num_accepted), _p(q_len), R, K, H,
-        dk, dv, int(flags) | _state_flag(state_pool), _p(rec_u), _p(rec_kg), _dt(rec_kg),
-        _p(plan_out), _p(dev_status), _stream(stream))
+        _p(state_pool), P, _idx(ckpt_slot, "ckpt_slot"), _idx(dst_slot, "dst_slot"),
+        _idx(num_accepted, "num_accepted"), _idx(q_len, "q_len"), R, K, H, dk, dv,
+        int(flags) | _state_flag(state_pool), _f32(rec_u, "rec_u"), _p(rec_kg), _dt(rec_kg),
+        _idx(plan_out, "plan_out"), _idx(dev_status, "dev_status"), _stream(stream))
     _check(st, "kda_spec_commit")
 
 
@@ -278,12 +312,15 @@ def kda_spec_accept_commit(state_pool, ckpt_slot, tokens, sampled, rec_u, rec_kg
     P, H, dv, dk = state_pool.shape
     R, K = tokens.shape
     descs, n = _conv_descs(convs)
-    extras = CommitExtras(descs, _p(conv_slot), _p(seq_len0), _p(block_slot),
-                          _p(block_idx_out), n, int(conv_keep), int(block_size), 0)
+    extras = CommitExtras(descs, _idx(conv_slot, "conv_slot"), _idx(seq_len0, "seq_len0"),
+                          _idx(block_slot, "block_slot"), _idx(block_idx_out, "block_idx_out"),
+                          n, int(conv_keep), int(block_size), 0)
     st = lib().kda_spec_accept_commit(
-        _p(state_pool), P, _p(ckpt_slot), _p(dst_slot), _p(tokens), _p(sampled), _p(q_len), R,
-        K, H, dk, dv, int(flags) | _state_flag(state_pool), _p(rec_u), _p(rec_kg), _dt(rec_kg),
-        _p(num_accepted), _p(next_token), _p(plan_out), ctypes.byref(extras), _p(dev_status),
+        _p(state_pool), P, _idx(ckpt_slot, "ckpt_slot"), _idx(dst_slot, "dst_slot"),
+        _idx(tokens, "tokens"), _idx(sampled, "sampled"), _idx(q_len, "q_len"), R, K, H, dk, dv,
+        int(flags) | _state_flag(state_pool), _f32(rec_u, "rec_u"), _p(rec_kg), _dt(rec_kg),
+        _idx(num_accepted, "num_accepted"), _idx(next_token, "next_token"),
+        _idx(plan_out, "plan_out"), ctypes.byref(extras), _idx(dev_status, "dev_status"),
         _stream(stream))
     _check(st, "kda_spec_accept_commit")
 
@@ -295,15 +332,16 @@ def kda_conv_compact(convs, slot, num_accepted, keep, *, dev_status=None, stream
     contiguous)."""
     descs, n = _conv_descs(convs)
     R = int(slot.numel())
-    st = lib().kda_conv_compact(descs, n, _p(slot), _p(num_accepted), R, int(keep),
-                                _p(dev_status), _stream(stream))
+    st = lib().kda_conv_compact(descs, n, _idx(slot, "slot"), _idx(num_accepted, "num_accepted"),
+                                R, int(keep), _idx(dev_status, "dev_status"), _stream(stream))
     _check(st, "kda_conv_compact")
 
 
 def kda_selftest_bounded_wait(polls, dev_status, cycles=None, stream=None):
     """Diagnostic: the kernels' bounded wait on a barrier nothing arrives on (see
     include/kda.h).  dev_status: int32 CUDA tensor; cycles: int64 CUDA tensor or None."""
-    st = lib().kda_selftest_bounded_wait(int(polls), _p(dev_status), _p(cycles), _stream(stream))
+    st = lib().kda_selftest_bounded_wait(int(polls), _idx(dev_status, "dev_status"), _p(cycles),
+                                         _stream(stream))
     _check(st, "kda_selftest_bounded_wait")
 
 
@@ -312,6 +350,25 @@ def kda_slot_copy(pools, clear_slots, src_slots, dst_offsets, dst_slots, workspa
     """Clear / copy / fan out slots on every pool in one launch (see include/kda.h).
 
     pools: list of CUDA tensors [num_slots, ...] (slot = first dimension)."""
+    descs, n, sets = _slot_sets(pools, clear_slots, src_slots, dst_offsets, dst_slots)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().kda_slot_copy(descs, n, *sets, _p(workspace), ws_bytes,
+                             _idx(dev_status, "dev_status"), _stream(stream))
+    _check(st, "kda_slot_copy")
+
+
+def kda_slot_copy_noalloc(pools, clear_slots, src_slots, dst_offsets, dst_slots, *,
+                          dev_status=None, stream=None):
+    """The slot copy with the library's own fixed check scratch instead of a workspace
+    (pools of at most KDA_SLOT_COPY_NOALLOC_MAX_SLOTS slots; see include/kda.h)."""
+    descs, n, sets = _slot_sets(pools, clear_slots, src_slots, dst_offsets, dst_slots)
+    st = lib().kda_slot_copy_noalloc(descs, n, *sets, _idx(dev_status, "dev_status"),
+                                     _stream(stream))
+    _check(st, "kda_slot_copy_noalloc")
+
+
+def _slot_sets(pools, clear_slots, src_slots, dst_offsets, dst_slots):
+    """Pool descriptors and the (pointer, count) arguments of the slot sets."""
     n = len(pools)
     descs = (PoolDesc * max(n, 1))()
     for i, t in enumerate(pools):
@@ -320,8 +377,6 @@ def kda_slot_copy(pools, clear_slots, src_slots, dst_offsets, dst_slots, workspa
     n_clear = 0 if clear_slots is None else int(clear_slots.numel())
     n_src = 0 if src_slots is None else int(src_slots.numel())
     n_dst = 0 if dst_slots is None else int(dst_slots.numel())
-    ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().kda_slot_copy(descs, n, _p(clear_slots), n_clear, _p(src_slots), _p(dst_offsets),
-                             _p(dst_slots), n_src, n_dst, _p(workspace), ws_bytes,
-                             _p(dev_status), _stream(stream))
-    _check(st, "kda_slot_copy")
+    sets = (_idx(clear_slots, "clear_slots"), n_clear, _idx(src_slots, "src_slots"),
+            _idx(dst_offsets, "dst_offsets"), _idx(dst_slots, "dst_slots"), n_src, n_dst)
+    return descs, n, sets

@@ -166,3 +166,108 @@ def test_product_path_has_no_cpu_fallback():
     assert "oracle" not in src.replace("no oracle", "")
     for f in (ROOT / "serving_kda_chunk_gb300" / "csrc").glob("*"):
         assert "oracle" not in f.read_text().lower(), f
+
+
+def test_binding_rejects_mixed_activation_dtypes(kda):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(2, 1, 128, dtype=torch.bfloat16)
+    k = torch.zeros(2, 1, 128, dtype=torch.float32)  # one tensor of another dtype
+    beta = torch.zeros(2, 1, dtype=torch.bfloat16)
+    pool = torch.zeros(1, 1, 128, 128)
+    slot = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="one dtype"):
+        kda.kda_recurrent_decode(q, k, q, beta, q, pool, slot, q)
+
+
+def test_binding_rejects_index_tensors_that_are_not_int32(kda):
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="int32"):
+        kda._idx(torch.zeros(4, dtype=torch.int64), "slot")
+    with pytest.raises(ValueError, match="fp32"):
+        kda._f32(torch.zeros(4, dtype=torch.bfloat16), "rec_u")
+    assert kda._idx(None, "slot") is None
+
+
+def test_verify_binding_checks_rows_and_record_dtype(kda):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(10, 1, 128, dtype=torch.bfloat16)  # 10 rows: not R * K for K = 3
+    beta = torch.zeros(10, 1, dtype=torch.bfloat16)
+    pool = torch.zeros(1, 1, 128, 128)
+    ckpt = torch.zeros(3, dtype=torch.int32)
+    rec_u = torch.zeros(3, 1, 3, 128)
+    with pytest.raises(ValueError, match="multiple of K"):
+        kda.kda_spec_verify(x, x, x, beta, x, pool, ckpt, rec_u, x, x, K=3)
+    x9, beta9 = x[:9], beta[:9]
+    rec_kg = torch.zeros(3, 1, 3, 256)  # fp32 records for bf16 activations
+    with pytest.raises(ValueError, match="rec_kg"):
+        kda.kda_spec_verify(x9, x9, x9, beta9, x9, pool, ckpt, rec_u, rec_kg, x9, K=3)
+
+
+def test_marshalling_matches_the_declared_signatures(kda, monkeypatch):
+    """Every binding passes exactly the C signature's arguments, each convertible by its
+    declared ctypes type (checked against a recording stand-in for the library, on CPU
+    tensors, so no kernel runs)."""
+    torch = pytest.importorskip("torch")
+    real = kda.lib()
+    calls = {}
+
+    class Fake:
+        def __getattr__(self, name):
+            fn = getattr(real, name)
+
+            def call(*args):
+                assert len(args) == len(fn.argtypes), (name, len(args), len(fn.argtypes))
+                for a, t in zip(args, fn.argtypes):
+                    t.from_param(a)  # raises on a value the C type cannot take
+                calls[name] = args
+                return 0
+
+            return call
+
+    monkeypatch.setattr(kda, "_lib", Fake())
+    monkeypatch.setattr(kda, "_p", lambda t: None if t is None else (
+        t.data_ptr() if isinstance(t, torch.Tensor) else int(t)))
+    monkeypatch.setattr(kda, "_p_any", lambda t: t.data_ptr())
+    monkeypatch.setattr(kda, "_stream", lambda s: 0)
+    bf, i32 = torch.bfloat16, torch.int32
+    T, H, R, K = 128, 2, 3, 4
+    x = torch.zeros(T, H, 128, dtype=bf)
+    pool = torch.zeros(4, H, 128, 128)
+    st = torch.zeros(1, dtype=i32)
+    kda.kda_chunk_prefill(x, x, x, torch.zeros(T, H, dtype=bf), x,
+                          torch.tensor([0, 64, 128], dtype=i32), x, state_pool=pool,
+                          init_slot=torch.zeros(2, dtype=i32), final_slot=torch.ones(2, dtype=i32),
+                          track_chunk_idx=torch.zeros(2, 1, dtype=i32),
+                          track_state=torch.zeros(2, 1, H, 128, 128), dev_status=st)
+    xd = torch.zeros(R, H, 128, dtype=bf)
+    kda.kda_recurrent_decode(xd, xd, xd, torch.zeros(R, H, dtype=bf), xd, pool,
+                             torch.zeros(R, dtype=i32), xd, dev_status=st)
+    xs = torch.zeros(R * K, H, 128, dtype=bf)
+    rec_u = torch.zeros(R, H, K, 128)
+    rec_kg = torch.zeros(R, H, K, 256, dtype=bf)
+    idx = torch.zeros(R, dtype=i32)
+    kda.kda_spec_verify(xs, xs, xs, torch.zeros(R * K, H, dtype=bf), xs, pool, idx, rec_u, rec_kg,
+                        xs, K=K, q_len=idx, dev_status=st)
+    tok = torch.zeros(R, K, dtype=i32)
+    kda.kda_spec_accept(tok, tok, idx, q_len=idx, next_token=idx, dev_status=st)
+    kda.kda_spec_commit(pool, idx, idx, rec_u, rec_kg, K=K, dst_slot=idx, q_len=idx,
+                        plan_out=torch.zeros(R, 3, dtype=i32), dev_status=st)
+    conv = torch.zeros(4, 6, 64, dtype=bf)
+    kda.kda_spec_accept_commit(pool, idx, tok, tok, rec_u, rec_kg, dst_slot=idx, q_len=idx,
+                               num_accepted=idx, next_token=idx, convs=[conv, conv],
+                               conv_slot=idx, conv_keep=2, seq_len0=idx, block_size=16,
+                               block_slot=idx, block_idx_out=idx, dev_status=st)
+    kda.kda_conv_compact([conv], idx, idx, 2, dev_status=st)
+    sets = (torch.zeros(1, dtype=i32), torch.zeros(1, dtype=i32), torch.tensor([0, 1], dtype=i32),
+            torch.ones(1, dtype=i32))
+    kda.kda_slot_copy([pool], *sets, torch.zeros(64, dtype=torch.uint8), dev_status=st)
+    kda.kda_slot_copy_noalloc([pool], *sets, dev_status=st)
+    kda.kda_selftest_bounded_wait(8, st)
+    assert set(calls) == {"kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify",
+                          "kda_spec_accept", "kda_spec_commit", "kda_spec_accept_commit",
+                          "kda_conv_compact", "kda_slot_copy", "kda_slot_copy_noalloc",
+                          "kda_selftest_bounded_wait"}
+    # a few positions that matter: sizes and the state-type flag bits
+    assert calls["kda_spec_verify"][6:8] == (R, K)
+    assert calls["kda_spec_commit"][6:9] == (R, K, H)
+    assert calls["kda_slot_copy"][7:9] == (1, 1)
