@@ -283,6 +283,29 @@ def test_verify_then_commit_equals_repeated_decode():
                 np.testing.assert_allclose(cf, p[ckpt[r]], rtol=1e-12, atol=1e-13)
 
 
+def test_verify_stops_at_each_requests_length():
+    """Positions at or past q_len produce nothing (zero outputs and records); the
+    positions before it are the same decode steps as with no length given."""
+    rng = np.random.default_rng(25)
+    R, K, H, dk, dv = 4, 4, 2, 6, 5
+    q, k, v, beta, gate = _rand_inputs(rng, R * K, H, dk, dv)
+    pool = rng.standard_normal((4, H, dv, dk))
+    ckpt = np.array([1, 0, 3, 2], np.int32)
+    ql = np.array([4, 2, 0, 1], np.int32)
+    out, ru, rkg, st = oracle.verify(q, k, v, beta, gate, pool, ckpt, K, q_len=ql)
+    full, ru_full, rkg_full, _ = oracle.verify(q, k, v, beta, gate, pool, ckpt, K)
+    assert st == 0
+    for r in range(R):
+        for t in range(K):
+            row = r * K + t
+            if t < ql[r]:
+                np.testing.assert_array_equal(out[row], full[row])
+                np.testing.assert_array_equal(ru[r, :, t], ru_full[r, :, t])
+                np.testing.assert_array_equal(rkg[r, :, t], rkg_full[r, :, t])
+            else:
+                assert not out[row].any() and not ru[r, :, t].any() and not rkg[r, :, t].any()
+
+
 def test_commit_closed_form_matches_bruteforce_every_accept_length():
     rng = np.random.default_rng(23)
     K, dk, dv = 7, 5, 4
@@ -313,6 +336,15 @@ def test_commit_plan_and_invalid_requests():
     assert st & oracle.BAD_SLOT and st & oracle.BAD_ACCEPT
     np.testing.assert_array_equal(newp[5], pool[0])   # a = 0, dst != src: copy
     np.testing.assert_array_equal(newp[[2, 3, 4]], pool[[2, 3, 4]])  # skipped
+    # the bound is the request's own length, not K: a = 3 with q_len = 2 is skipped
+    ql = np.array([4, 2, 4, 4, 4], np.int32)
+    acc2 = np.array([1, 3, 2, 1, 1], np.int32)
+    ckpt2 = np.array([0, 1, 2, 3, 4], np.int32)
+    plan3 = oracle.commit_plan(ckpt2, acc2, P, K, q_len=ql)
+    assert plan3[:, 0].tolist() == [1, -1, 2, 1, 1]
+    newp3, plan4, st3 = oracle.commit(pool, ckpt2, acc2, ru, rkg, K, q_len=ql)
+    assert plan4.tolist() == plan3.tolist() and st3 == oracle.BAD_ACCEPT
+    np.testing.assert_array_equal(newp3[1], pool[1])
 
 
 def _accept_bruteforce(tok, smp, ql):
