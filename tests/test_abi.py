@@ -271,3 +271,57 @@ def test_marshalling_matches_the_declared_signatures(kda, monkeypatch):
     assert calls["kda_spec_verify"][6:8] == (R, K)
     assert calls["kda_spec_commit"][6:9] == (R, K, H)
     assert calls["kda_slot_copy"][7:9] == (1, 1)
+
+
+def _have(tool):
+    import shutil
+
+    return shutil.which(tool) is not None
+
+
+@pytest.mark.skipif(not (_have("gcc") and _have("g++")), reason="needs gcc and g++")
+def test_header_is_standalone_c_and_cxx(tmp_path):
+    import subprocess
+
+    src = tmp_path / "use.c"
+    src.write_text('#include "kda.h"\nint main(void) { return 0; }\n')
+    inc = f"-I{ROOT / 'include'}"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", inc,
+                    "-fsyntax-only", str(src)], check=True)
+    cxx = tmp_path / "use.cpp"
+    cxx.write_text(src.read_text())
+    subprocess.run(["g++", "-std=c++11", "-Wall", "-Wextra", "-pedantic", "-Werror", inc,
+                    "-fsyntax-only", str(cxx)], check=True)
+
+
+@pytest.mark.skipif(not _have("gcc"), reason="needs gcc")
+def test_plain_c_caller_links_and_gets_host_errors(kda, tmp_path):
+    """A C program built against the header and the shared library alone: it gets
+    the version and status strings, and host-checkable errors come back as status
+    codes before anything reaches a GPU."""
+    import subprocess
+
+    src = tmp_path / "caller.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "kda.h"
+int main(void) {
+    if (kda_abi_version() < 104) return 1;
+    if (strcmp(kda_status_string(KDA_OK), "KDA_OK") != 0) return 2;
+    /* d_k != 128 is unsupported: refused on the host, nothing launched */
+    kda_status s = kda_recurrent_decode(0, 0, 0, 0, 0, KDA_BF16, 1, 1, 64, 128, 1.0f, 0u,
+                                        0, 1, 0, 0, KDA_BF16, 0, 0);
+    if (s != KDA_ERR_UNSUPPORTED) return 3;
+    /* R = 0 launches nothing and succeeds */
+    if (kda_spec_accept(0, 0, 0, 0, 4, 0, 0, 0, 0) != KDA_OK) return 4;
+    puts("ok");
+    return 0;
+}
+''')
+    exe = tmp_path / "caller"
+    libdir = str(Path(kda.LIB_PATH).parent)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", f"-I{ROOT / 'include'}", str(src),
+                    f"-L{libdir}", "-lkda", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stderr)
