@@ -282,14 +282,21 @@ __device__ __forceinline__ void warp_sum2(float& a, float& b) {
     }
 }
 
+// Elementwise products and FMAs in packed fp32 pairs (each lane rounds as the scalar
+// operation does, so results are the scalar ones; half the instructions issue).
 __device__ __forceinline__ float4 f4_mul(float4 a, float4 b) {
-    return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+    const float2 lo = __fmul2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y));
+    const float2 hi = __fmul2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 __device__ __forceinline__ float f4_dot(float4 a, float4 b) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
 __device__ __forceinline__ float4 f4_fma(float s, float4 k, float4 x) {
-    return make_float4(fmaf(s, k.x, x.x), fmaf(s, k.y, x.y), fmaf(s, k.z, x.z), fmaf(s, k.w, x.w));
+    const float2 ss = make_float2(s, s);
+    const float2 lo = __ffma2_rn(ss, make_float2(k.x, k.y), make_float2(x.x, x.y));
+    const float2 hi = __ffma2_rn(ss, make_float2(k.z, k.w), make_float2(x.z, x.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // ----------------------------------------------------------------------------
