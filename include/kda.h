@@ -143,7 +143,9 @@ size_t kda_chunk_prefill_workspace_size(int32_t T_tot, int32_t N, int32_t H, int
  *   slot           : [R] int32.  slot < 0: padding request, skipped, its
  *                    output row is written as zeros.  slot >= P: skipped,
  *                    zero output, KDA_DEV_BAD_SLOT.  Slots of one call must be
- *                    distinct.
+ *                    distinct: this is not checked, and a slot listed twice
+ *                    leaves its state undefined (two blocks update it at once)
+ *                    with no dev_status bit set.
  *   out            : [R, H, d_v] out_dtype.
  */
 kda_status kda_recurrent_decode(const void* q, const void* k, const void* v, const void* beta_raw,
@@ -230,8 +232,9 @@ kda_status kda_spec_accept(const int32_t* tokens, const int32_t* sampled, const 
  *                  that was skipped (bad slot or bad accepted length, with the
  *                  matching dev_status bit).
  * a = 0 writes nothing when dst == src and copies S_0 otherwise.  Destinations
- * must be distinct and must not be another request's checkpoint.  K <= 32
- * (else KDA_ERR_UNSUPPORTED).
+ * must be distinct and must not be another request's checkpoint: this is not
+ * checked, and a violation leaves the states involved undefined with no
+ * dev_status bit set.  K <= 32 (else KDA_ERR_UNSUPPORTED).
  */
 kda_status kda_spec_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
                            const int32_t* dst_slot, const int32_t* num_accepted,
@@ -331,8 +334,9 @@ kda_status kda_conv_compact(const kda_conv_desc* convs, int32_t n_convs, const i
  *                 dst_offsets[n_src] = n_dst); dst_slots: [n_dst].  Source i
  *                 is copied byte for byte to dst_slots[dst_offsets[i] ..
  *                 dst_offsets[i+1]-1] in every pool.
- *   workspace   : >= kda_slot_copy_workspace_size(max slots over the pools)
- *                 bytes of device scratch (the disjointness check's bitmap).
+ *   workspace   : >= kda_slot_copy_workspace_size(smallest num_slots over the
+ *                 pools) bytes of device scratch (the disjointness check's
+ *                 bitmap over the slot ids, which are all below that size).
  * Precondition, checked on the GPU: destinations pairwise distinct and
  * disjoint from sources and clears; clears distinct and disjoint from sources;
  * every slot < num_slots of every pool.  On a violation nothing is copied and
@@ -351,7 +355,7 @@ kda_status kda_slot_copy(const kda_pool_desc* pools, int32_t n_pools, const int3
                          const int32_t* dst_slots, int32_t n_src, int32_t n_dst, void* workspace,
                          size_t ws_bytes, int32_t* dev_status, void* stream);
 
-size_t kda_slot_copy_workspace_size(int64_t max_slots);
+size_t kda_slot_copy_workspace_size(int64_t num_slots);
 
 /*
  * kda_slot_copy_noalloc -- kda_slot_copy without a caller-provided workspace.
@@ -367,9 +371,12 @@ size_t kda_slot_copy_workspace_size(int64_t max_slots);
  *   - Returns KDA_ERR_UNSUPPORTED when the smallest pool has more than
  *     KDA_SLOT_COPY_NOALLOC_MAX_SLOTS slots; nothing is launched then.
  *   - Allocates nothing: no cudaMalloc / cudaFree and no allocating library
- *     call.  The first call on each device looks the array's device address up
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     call.  The array's device address belongs to a CUDA context: the first
+ *     call in each context looks it up (cudaGetSymbolAddress, with that
+ *     context current) and caches it under the context's unique id, so a
+ *     context made later (after cudaDeviceReset, or another context the
+ *     caller makes current) gets its own lookup and never a stale address.
+ *     Make the first call in a context before any stream capture.
  *   - All calls share the one array; the kernel clears the part it uses on
  *     every call, but calls that may overlap on the GPU (different streams
  *     without ordering between them) race on it and must be serialised.

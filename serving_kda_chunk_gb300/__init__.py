@@ -205,8 +205,9 @@ def kda_chunk_prefill_workspace_size(T_tot, N, H, dk=128, dv=128, chunk=64) -> i
     return int(lib().kda_chunk_prefill_workspace_size(T_tot, N, H, dk, dv, chunk))
 
 
-def kda_slot_copy_workspace_size(max_slots) -> int:
-    return int(lib().kda_slot_copy_workspace_size(max_slots))
+def kda_slot_copy_workspace_size(num_slots) -> int:
+    """Workspace bytes of kda_slot_copy for pools whose smallest slot count is num_slots."""
+    return int(lib().kda_slot_copy_workspace_size(num_slots))
 
 
 def kda_chunk_prefill(q, k, v, beta_raw, gate_raw, cu_seqlens, out, *, state_pool=None,

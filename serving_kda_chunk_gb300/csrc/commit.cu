@@ -200,8 +200,7 @@ __global__ void __launch_bounds__(kCommitThreads, 8) commit_kernel(
                 const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
                                           : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
                 F[t * kD + c] = prod * kv;
-                // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
-                prod *= (flags & KDA_GATE_LOG) ? __expf(gv) : __fdividef(1.f, 1.f + __expf(gv));
+                prod *= alpha_of(gv, flags);
             }
             D[c] = prod;
         }

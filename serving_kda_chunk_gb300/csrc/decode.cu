@@ -75,8 +75,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
     }
     StepIn in;
     const float4 g = A::load4(gate_raw, th * kD + 4 * lane);
-    in.a = make_float4(expf(gate_log(g.x, flags)), expf(gate_log(g.y, flags)),
-                       expf(gate_log(g.z, flags)), expf(gate_log(g.w, flags)));
+    in.a = make_float4(alpha_of(g.x, flags), alpha_of(g.y, flags), alpha_of(g.z, flags),
+                       alpha_of(g.w, flags));
     in.k = A::load4(k, th * kD + 4 * lane);
     float4 qq = A::load4(q, th * kD + 4 * lane);
     in.q = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);

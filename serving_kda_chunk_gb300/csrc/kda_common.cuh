@@ -20,14 +20,37 @@ constexpr int kD = 128;  // d_k = d_v
 constexpr int kChunk = 64;
 
 // ----------------------------------------------------------------------------
-// activations (fp32; CUDA's expf / log1pf)
+// activations (fp32), one form for every kernel
+//
+// The decay of key channel i at one token is alpha = e^{g}, g = -softplus(x):
+// alpha = 1 / (1 + e^x), and 1 / alpha = 1 + e^x.  Every kernel (tensor-core and
+// token-serial prefill, decode, verify, commit) takes alpha and 1 / alpha from
+// decay_of(), so the same raw gate gives the same alpha bits everywhere: a state
+// rebuilt by the commit from a verify record decays exactly as decode decays it.
+// e^x is CUDA's __expf and the reciprocal __fdividef(1, .): raw -inf gives
+// alpha = 1 exactly; a raw gate above ~88 (e^x = inf) gives alpha = 0.  Under
+// KDA_GATE_LOG the input is g itself: alpha = e^g, 1 / alpha = e^{-g}.
 
-__device__ __forceinline__ float gate_log(float raw, uint32_t flags) {
-    if (flags & KDA_GATE_LOG) return raw;
-    // -softplus(x), split at 0 so exp never overflows
-    return raw > 0.f ? -(raw + log1pf(expf(-raw))) : -log1pf(expf(raw));
+struct Decay {
+    float a;    // alpha
+    float inv;  // 1 / alpha
+};
+
+__device__ __forceinline__ Decay decay_of(float raw, uint32_t flags) {
+    Decay d;
+    if (flags & KDA_GATE_LOG) {
+        d.a = __expf(raw);
+        d.inv = __expf(-raw);
+    } else {
+        d.inv = 1.f + __expf(raw);
+        d.a = __fdividef(1.f, d.inv);
+    }
+    return d;
 }
 
+__device__ __forceinline__ float alpha_of(float raw, uint32_t flags) { return decay_of(raw, flags).a; }
+
+// beta = sigmoid(raw beta) (raw -inf gives 0 exactly); KDA_BETA_ACT: beta given.
 __device__ __forceinline__ float beta_act(float raw, uint32_t flags) {
     if (flags & KDA_BETA_ACT) return raw;
     return 1.f / (1.f + expf(-raw));
@@ -363,8 +386,8 @@ __device__ __forceinline__ void stage_tokens(TokenTile<kTile>& tt, const void* q
         const float4 kk = A::load4(k, th * kD + 4 * lane);
         const float4 qq = A::load4(q, th * kD + 4 * lane);
         const float4 vv = A::load4(v, th * kD + 4 * lane);
-        const float4 a = make_float4(expf(gate_log(g.x, flags)), expf(gate_log(g.y, flags)),
-                                     expf(gate_log(g.z, flags)), expf(gate_log(g.w, flags)));
+        const float4 a = make_float4(alpha_of(g.x, flags), alpha_of(g.y, flags),
+                                     alpha_of(g.z, flags), alpha_of(g.w, flags));
         const float4 qs = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);
         *reinterpret_cast<float4*>(&tt.a[t][4 * lane]) = a;
         *reinterpret_cast<float4*>(&tt.k[t][4 * lane]) = kk;

@@ -265,13 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                 const int t = 16 * tq + u;
                 const float x = bf16_at(sm, RAW_G + t * 256 + ci * 2);
                 if (t < Lc) {
-                    if (p.flags & KDA_GATE_LOG) {
-                        al[u] = __expf(x);
-                        iv[u] = __expf(-x);
-                    } else {
-                        iv[u] = 1.f + __expf(x);  // 1/alpha = 1 + e^x
-                        al[u] = __fdividef(1.f, iv[u]);
-                    }
+                    const Decay dc = decay_of(x, p.flags);
+                    al[u] = dc.a;
+                    iv[u] = dc.inv;
                 } else {
                     al[u] = 1.f;
                     iv[u] = 1.f;

@@ -12,6 +12,9 @@
 // with 16-byte vector loads and stores.  A fan-out source piece is read once
 // into registers and written to each of its destinations.  The copy kernel
 // reads the verdict first and does nothing if the check failed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -123,10 +126,10 @@ __global__ void __launch_bounds__(kCopyThreads) slot_copy_kernel(
 
 using namespace kda;
 
-extern "C" size_t kda_slot_copy_workspace_size(int64_t max_slots) {
-    if (max_slots < 0) return 0;
+extern "C" size_t kda_slot_copy_workspace_size(int64_t num_slots) {
+    if (num_slots < 0) return 0;
     // verdict word (padded to 16 B) + one bit per slot, rounded to 16 B
-    return 16 + (size_t)((max_slots + 127) / 128) * 16;
+    return 16 + (size_t)((num_slots + 127) / 128) * 16;
 }
 
 extern "C" kda_status kda_slot_copy(const kda_pool_desc* pools, int32_t n_pools,
@@ -209,23 +212,71 @@ constexpr size_t kNoallocScratchBytes = 16 + ((size_t)KDA_SLOT_COPY_NOALLOC_MAX_
 
 static __device__ __align__(256) unsigned char g_slot_copy_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 128;
+// A symbol's device address belongs to a CUDA context, not to a device: a context made
+// after cudaDeviceReset, or a non-primary context the caller made current, has its own copy
+// of the array.  Addresses are therefore cached under the current context's unique id
+// (cuCtxGetId never reuses an id within a process, even when a context handle is reused).
+constexpr int kCacheSlots = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_cache_ctx[kCacheSlots] = {};  // 0 = empty (context ids start at 1)
+void* g_cache_ptr[kCacheSlots] = {};
+int g_cache_next = 0;
 
-// Device address of the scratch array on the current device (looked up once per
-// device; the name alone is only a host-side stand-in).
-kda_status scratch_address(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+struct CtxFns {
+    PFN_cuCtxGetCurrent_v4000 current = nullptr;
+    PFN_cuCtxGetId_v12000 id = nullptr;
+};
+
+CtxFns lookup_ctx_fns() {
+    CtxFns f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        f.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        f.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return f;
+}
+
+// Unique id of the context current on this thread (made current by the runtime if none is).
+kda_status current_context_id(unsigned long long* id) {
+    static const CtxFns fns = lookup_ctx_fns();
+    if (fns.current == nullptr || fns.id == nullptr) return KDA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (fns.current(&ctx) != CUDA_SUCCESS) return KDA_ERR_CUDA;
+    if (ctx == nullptr) {
+        // no context yet on this thread: a runtime call that needs one makes the device's
+        // primary context current (the lookup below is repeated under the lock anyway)
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_slot_copy_scratch) != cudaSuccess || p == nullptr)
-            return KDA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        if (cudaGetSymbolAddress(&p, g_slot_copy_scratch) != cudaSuccess) return KDA_ERR_CUDA;
+        if (fns.current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return KDA_ERR_CUDA;
     }
-    *out = g_scratch_ptr[dev];
+    if (fns.id(ctx, id) != CUDA_SUCCESS || *id == 0) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+// Device address of the scratch array in the current context (looked up once per context,
+// with that context current; the name alone is only a host-side stand-in).
+kda_status scratch_address(void** out) {
+    unsigned long long id = 0;
+    const kda_status st = current_context_id(&id);
+    if (st != KDA_OK) return st;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    for (int i = 0; i < kCacheSlots; ++i) {
+        if (g_cache_ctx[i] == id) {
+            *out = g_cache_ptr[i];
+            return KDA_OK;
+        }
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_slot_copy_scratch) != cudaSuccess || p == nullptr) return KDA_ERR_CUDA;
+    g_cache_ctx[g_cache_next] = id;
+    g_cache_ptr[g_cache_next] = p;
+    g_cache_next = (g_cache_next + 1) % kCacheSlots;
+    *out = p;
     return KDA_OK;
 }
 

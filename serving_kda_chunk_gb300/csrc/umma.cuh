@@ -231,6 +231,23 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
     return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
 }
 
+// The mbarrier's current phase completes once `bytes` more bytes have landed (and the one
+// arrival of this call): the form a bulk copy's completion counts against.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
+                 : "memory");
+}
+
+// Bulk (TMA, one-dimensional) copy of `bytes` contiguous bytes global -> this CTA's shared
+// memory, counted on mbar.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_smem),
+        "l"(src), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),

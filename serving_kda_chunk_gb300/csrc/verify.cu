@@ -101,11 +101,6 @@ struct VLayout {
 // TMEM columns: checkpoint operand [S hi (64) | S lo (64)], then the accumulator [D_hi | D_lo]
 constexpr uint32_t TV_SA = 0, TV_D = 128, TV_COLS = 256;
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
-                 : "memory");
-}
-
 // One box of the tensor map at (x = column, y = row) into shared memory, completing on mbar.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t mbar) {
@@ -344,15 +339,9 @@ __global__ void __launch_bounds__(kVThreads, 2)
                 qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
                 at[t] = iv[t] = 1.f;
                 if (t < ql) {
-                    // alpha = e^{-softplus(x)} = 1 / (1 + e^x); e^x for log-space gates
-                    const float gx = act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i);
-                    if (a.flags & KDA_GATE_LOG) {
-                        at[t] = __expf(gx);
-                        iv[t] = __expf(-gx);
-                    } else {
-                        iv[t] = 1.f + __expf(gx);
-                        at[t] = __fdividef(1.f, iv[t]);
-                    }
+                    const Decay dc = decay_of(act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i), a.flags);
+                    at[t] = dc.a;
+                    iv[t] = dc.inv;
                 }
             }
             if (warp < 4) {
@@ -612,19 +601,20 @@ __global__ void __launch_bounds__(kVThreads, 2)
     if (warp == 0) tmem_dealloc(tmem, TV_COLS);
 }
 
-// The tensor map's encoder from the driver, looked up once.
+// The tensor map's encoder from the driver, looked up once (a function-local static is
+// initialised exactly once even when several host threads make their first call together).
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encoder();
     return fn;
 }
 

@@ -39,3 +39,26 @@ def tol_out(dtype):
 
 
 TOL_STATE = 1e-4  # fp32 states and snapshots
+
+
+def worst_seq_head(x, y, cu_seqlens):
+    """Largest rel-L2 over the (sequence, head) blocks of [T, H, d] rows: a wrong
+    sequence or head cannot hide inside the whole-tensor figure."""
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    cu = np.asarray(cu_seqlens)
+    worst = 0.0
+    for n in range(len(cu) - 1):
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b > a:
+            for h in range(x.shape[1]):
+                worst = max(worst, rel_l2(x[a:b, h], y[a:b, h]))
+    return worst
+
+
+def worst_state(x, y):
+    """Largest rel-L2 over the 128 x 128 state blocks of two arrays shaped
+    [..., 128, 128] (one block per slot / snapshot and head)."""
+    x = np.asarray(x, np.float64).reshape(-1, 128 * 128)
+    y = np.asarray(y, np.float64).reshape(-1, 128 * 128)
+    return max((rel_l2(a, b) for a, b in zip(x, y)), default=0.0)

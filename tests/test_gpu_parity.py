@@ -7,7 +7,8 @@ import pytest
 
 import oracle
 import workloads as W
-from helpers import TOL_STATE, dev_tensor, i32, rel_l2, tol_out, to_np, wid
+from helpers import (TOL_STATE, dev_tensor, i32, rel_l2, tol_out, to_np, wid, worst_seq_head,
+                     worst_state)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,6 +77,10 @@ def test_prefill_ragged_small(kda, dtype):
     sn = snap.cpu().numpy()
     assert rel_l2(sn[valid], snap_ref[valid]) < TOL_STATE
     assert np.isnan(sn[~valid]).all()  # unused entries are never written
+    # per (sequence, head), every ragged length on its own
+    assert worst_seq_head(to_np(out), o_ref, c["cu_seqlens"]) < tol_out(dtype)
+    assert worst_state(pool.cpu().numpy()[c["final_slot"]], s_ref) < TOL_STATE
+    assert worst_state(sn[valid], snap_ref[valid]) < TOL_STATE
 
 
 def test_prefill_zero_initial_state_and_fp32_output(kda):

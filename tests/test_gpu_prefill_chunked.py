@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import workloads as W
-from helpers import TOL_STATE, dev_tensor, i32, rel_l2, to_np
+from helpers import TOL_STATE, dev_tensor, i32, rel_l2, to_np, worst_seq_head, worst_state
 
 pytestmark = pytest.mark.gpu
 
@@ -66,6 +66,13 @@ def check(c, got, flags=0, tol_o=5e-3):
     assert eo < tol_o, eo
     assert es < TOL_STATE, es
     assert en < TOL_STATE, en
+    # and per (sequence, head): outputs, final states and every valid snapshot
+    wo = worst_seq_head(to_np(out), o_ref, c["cu_seqlens"])
+    ws = worst_state(pool.cpu().numpy()[c["final_slot"]], s_ref)
+    wn = worst_state(snap.cpu().numpy()[valid], snap_ref[valid]) if valid.any() else 0.0
+    assert wo < tol_o, wo
+    assert ws < TOL_STATE, ws
+    assert wn < TOL_STATE, wn
     return eo, es, en
 
 

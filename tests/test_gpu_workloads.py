@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import workloads as W
-from helpers import TOL_STATE, dev_tensor, i32, rel_l2, to_np
+from helpers import TOL_STATE, dev_tensor, i32, rel_l2, to_np, worst_seq_head, worst_state
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +61,9 @@ def test_tiny_prefill_fp32(kda):
     assert rel_l2(to_np(out), o_ref) < 1e-4
     assert rel_l2(snap.cpu().numpy(), snap_ref) < TOL_STATE
     assert rel_l2(pool_d.cpu().numpy(), s_ref) < TOL_STATE
+    assert worst_seq_head(to_np(out), o_ref, c["cu_seqlens"]) < 1e-4
+    assert worst_state(snap.cpu().numpy(), snap_ref) < TOL_STATE
+    assert worst_state(pool_d.cpu().numpy(), s_ref) < TOL_STATE
 
 
 def test_batched_prefill_sampled_heads(kda):
@@ -68,12 +71,16 @@ def test_batched_prefill_sampled_heads(kda):
     S0_all = c["pool"][c["init_slot"]].astype(np.float64)
     out, pool, snap, st = _prefill_gpu(kda, c, c["pool"])
     assert st == 0
-    heads = [0, 17, 31]
+    heads = [0, 9, 18, 27, 31]  # a head from every quarter of the 32
     o_ref, s_ref, snap_ref, _ = _oracle_heads(c, heads, S0_all)
     assert rel_l2(to_np(out[:, heads]), o_ref) < 5e-3
     fin = pool.cpu().numpy()[c["final_slot"]][:, heads]
     assert rel_l2(fin, s_ref) < TOL_STATE
     assert rel_l2(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
+    # per (sequence, head): the short sequences cannot hide behind the long ones
+    assert worst_seq_head(to_np(out[:, heads]), o_ref, c["cu_seqlens"]) < 5e-3
+    assert worst_state(fin, s_ref) < TOL_STATE
+    assert worst_state(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
     # every head was written: final states differ from the initial ones
     assert not np.array_equal(pool.cpu().numpy()[c["final_slot"]], c["pool"][c["init_slot"]])
     assert not torch.isnan(snap).any()
@@ -176,6 +183,10 @@ def test_long_prefill_sampled_heads(kda):
     assert rel_l2(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
     assert rel_l2(pool_d.cpu().numpy()[:, heads], s_ref) < TOL_STATE
     assert not torch.isnan(snap).any()
+    # every snapshot of the sampled head on its own, and the output in 8 spans of 16384 tokens
+    assert worst_state(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
+    spans = np.arange(0, c["T"] + 1, 16384)
+    assert worst_seq_head(to_np(out[:, heads]), o_ref, spans) < 5e-3
 
 
 def test_slot_fanout_sampled(kda):
