@@ -71,12 +71,34 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
     return byts, flops
 
 
-# DRAM traffic of the chunked prefill kernel measured with ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum = 277.63 MB + 58.95 MB) on the `--profile prefill` case
-# (8 x 2048 tokens, 16 heads) with the kernel as it stands; traffic grows with the
-# token-heads processed, so a launch is charged this much per token-head.  Re-measure
-# when the kernel changes.
-PREFILL_TRAFFIC_PER_TOKEN_HEAD = (277.63e6 + 58.95e6) / (8 * 2048 * 16)
+# DRAM traffic of one two-phase prefill call, from ncu captures of its two kernels
+# (dram__bytes_read.sum + dram__bytes_write.sum of prep and sweep: 201.95 + 379.84 and
+# 551.47 + 65.06 MB) on the `--profile prefill` case (8 x 2048 tokens, 16 heads); traffic
+# grows with the token-heads processed, so a launch is charged this much per token-head.
+# The figure belongs to the kernel source it was captured on: the line reports null traffic
+# once that file's sha256 no longer starts with the recorded prefix.
+PREFILL_TRAFFIC = {
+    "source": "serving_kda_chunk_gb300/csrc/prefill_2p.cu",
+    "sha256_prefix": "233b0cead5c54b06",
+    "capture": "profiles/prefill_2p_prep_kernel_batched_8x2048_h16.md, "
+               "profiles/prefill_2p_sweep_kernel_batched_8x2048_h16.md",
+    "bytes_per_token_head": (201.948160e6 + 379.843328e6 + 551.474944e6 + 65.062656e6) / (8 * 2048 * 16),
+}
+
+
+def prefill_traffic(token_heads):
+    """Measured DRAM bytes of a prefill call over token_heads, or None if the kernel source has
+    changed since the capture."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, PREFILL_TRAFFIC["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if not digest.startswith(PREFILL_TRAFFIC["sha256_prefix"]):
+        return None
+    return PREFILL_TRAFFIC["bytes_per_token_head"] * token_heads
 
 
 def decode_work(R, H, sb=STATE_BYTES):
@@ -292,7 +314,7 @@ class Step:
     def calls(self):
         part = {"prefill": "prefill", "decode": "decode", "verify": "spec", "commit": "spec",
                 "conv_compact": "spec", "slot_copy": "copy"}
-        every = [("prefill", self.prefill, 2), ("decode", self.decode, 1),
+        every = [("prefill", self.prefill, 3), ("decode", self.decode, 1),
                  ("verify", self.verify, 1), ("commit", self.commit, 1),
                  ("slot_copy", self.slot_copy, 2)]
         return [c for c in every if part[c[0]] in self.parts]
@@ -675,22 +697,26 @@ def run_profile_case(name, reps):
     """One entry point on its workload, for an ncu capture (`--profile NAME`).
 
     prefill runs a reduced batch (8 sequences x 2048 tokens, H=16: 168 MB of
-    activations, above L2) so that a full-set capture ends quickly; the other
-    entry points run their serving workloads."""
+    activations, above L2) so that a full-set capture ends quickly, through the
+    two-phase kernels (prefill) or the single-pass kernel (prefill_single); the
+    other entry points run their serving workloads."""
     import torch
 
     import serving_kda_chunk_gb300 as kda
 
     dev = torch.device("cuda", 0)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    if name == "prefill":
+    if name in ("prefill", "prefill_single"):
+        # "prefill": the two-phase kernels (the workspace the benchmark passes); "prefill_single":
+        # the single-pass kernel (a workspace too small for the two-phase plan)
         c = W.prefill_case(11, [2048] * 8, 16, pool_slots=8)
         t = {n: to_dev(c[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
         pool = torch.from_numpy(c["pool"]).to(dev)
         sl, tr, cu = i32(c["init_slot"], dev), i32(c["track"], dev), i32(c["cu_seqlens"], dev)
         snap = torch.empty(8, 1, 16, D, D, device=dev)
         out = torch.empty(c["T"], 16, D, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(64, dtype=torch.uint8, device=dev)
+        need = kda.kda_chunk_prefill_workspace_size(c["T"], 8, 16)
+        ws = torch.empty(need if name == "prefill" else 64, dtype=torch.uint8, device=dev)
 
         def fn():
             kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
@@ -724,8 +750,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode", "verify", "commit", "conv_compact",
-                                          "slot_copy"],
+    ap.add_argument("--profile", choices=["prefill", "prefill_single", "decode", "verify", "commit",
+                                          "conv_compact", "slot_copy"],
                     help="run one entry point a few times (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.profile:
@@ -759,6 +785,7 @@ def main():
     e2e_val = sum_over_ranks(toks, world) / max_over_ranks(e2e_t, world)
     pb, pf = prefill_work(lengths, 32, 1)
     achieved = pb / mean["prefill"] / 1e9
+    traffic = prefill_traffic(toks * 32)
     t_hbm, t_tc = pb / (hbm * 1e9), pf / (tc * 1e12)
     dec_b = decode_work(256, 32)
     ver_b = verify_work(64, 7, 32)
@@ -806,9 +833,11 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; bf16 inputs, fp32 state)", "config": config_block(),
-        "roofline": {"bound": "hbm", "kernel": "kda_chunk_prefill", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": PREFILL_TRAFFIC_PER_TOKEN_HEAD * toks * 32,
+        "roofline": {"bound": "hbm", "kernel": "kda_chunk_prefill (plan + prep + sweep)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic,
+                     "traffic_over_algorithmic": (traffic / pb) if traffic else None,
+                     "traffic_source": PREFILL_TRAFFIC["capture"],
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -114,12 +114,20 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *                    only for valid entries; the fp32 accumulator itself, or
  *                    with a 16-bit state type that accumulator rounded once).
  *   out            : [T_tot, H, d_v] out_dtype.
- *   workspace      : optional device scratch of ws_bytes >=
- *                    kda_chunk_prefill_workspace_size(...) bytes.  With it the
- *                    kernel schedules the longest sequences first; with NULL
- *                    it runs them in input order (same results).
- * bf16 activations run on the tensor-core chunk kernel; fp32 activations and
- * KDA_PREFILL_RECURRENT run the token-serial kernel.
+ *   workspace      : optional device scratch of ws_bytes bytes.
+ *                    ws_bytes >= kda_chunk_prefill_workspace_size(...) (about
+ *                    2 KiB per token-head: every (chunk, head)'s prepared
+ *                    operands) runs the two-phase path: all chunks' state-
+ *                    independent work in parallel on every SM, then one
+ *                    sequential pass per (sequence, head).  A smaller
+ *                    workspace (>= 16 * ceil(N / 4) bytes) runs the single-pass
+ *                    kernel with the longest sequences first; NULL runs it in
+ *                    input order.  The paths agree within the stated
+ *                    tolerances; the single-pass results do not depend on the
+ *                    order (bit-identical).
+ * bf16 activations run on the tensor cores (two-phase with N <= 4096 and
+ * M <= 512, else single-pass); fp32 activations and KDA_PREFILL_RECURRENT run
+ * the token-serial kernel.
  * Units of work are (sequence, head); sequences must not share a final slot.
  */
 kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* beta_raw,

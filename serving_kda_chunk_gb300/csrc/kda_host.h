@@ -1,6 +1,8 @@
 // kda_host.h -- host-side argument checks shared by the libkda entry points.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,6 +15,22 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool dtype_ok(kda_dtype d) { return d == KDA_BF16 || d == KDA_F32; }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once per process: a
+// function-local static is initialised exactly once even when several host threads make their
+// first call together.  nullptr if the driver does not provide it.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return nullptr;
+    }();
+    return fn;
+}
 
 // Map the last launch error to a status (clears the sticky-free error state).
 inline kda_status launch_status() {

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/kda.h"
+
 namespace kda {
 
 constexpr int kMaxTrack = 1024;  // snapshot requests per sequence
@@ -32,6 +34,10 @@ struct PrefillArgs {
 };
 
 void launch_prefill_serial(const PrefillArgs& p, bool bf16_in, bool bf16_out, cudaStream_t s);
+
+bool prefill_2p_supported(const PrefillArgs& p, bool bf16_in);
+size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H);
+kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_out, void* workspace, cudaStream_t s);
 
 bool prefill_tc_supported(const PrefillArgs& p, bool bf16_in);
 size_t prefill_tc_workspace(int32_t N);

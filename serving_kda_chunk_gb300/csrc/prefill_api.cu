@@ -8,12 +8,12 @@ using namespace kda;
 
 extern "C" size_t kda_chunk_prefill_workspace_size(int32_t T_tot, int32_t N, int32_t H,
                                                    int32_t dk, int32_t dv, int32_t chunk) {
-    (void)T_tot;
-    (void)H;
     (void)dk;
     (void)dv;
     (void)chunk;
-    return prefill_tc_workspace(N);
+    const size_t two_phase = prefill_2p_workspace(T_tot, N, H);
+    const size_t single = prefill_tc_workspace(N);
+    return two_phase > single ? two_phase : single;
 }
 
 extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void* v,
@@ -48,7 +48,11 @@ extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void
                   T_tot, H,         scale,     flags,      state_pool,      P,          init_slot,
                   final_slot, track_chunk_idx, M, track_state, out, dev_status, state_type(flags)};
     const bool bf16_in = in_dtype == KDA_BF16, bf16_out = out_dtype == KDA_BF16;
-    if (!(flags & KDA_PREFILL_RECURRENT) && prefill_tc_supported(p, bf16_in))
+    const bool chunked = !(flags & KDA_PREFILL_RECURRENT);
+    const size_t ws_2p = prefill_2p_workspace(T_tot, N, H);
+    if (chunked && prefill_2p_supported(p, bf16_in) && workspace && ws_2p > 0 && ws_bytes >= ws_2p)
+        return launch_prefill_2p(p, bf16_out, workspace, as_stream(stream));
+    if (chunked && prefill_tc_supported(p, bf16_in))
         launch_prefill_tc(p, bf16_out, workspace, ws_bytes, as_stream(stream));
     else
         launch_prefill_serial(p, bf16_in, bf16_out, as_stream(stream));

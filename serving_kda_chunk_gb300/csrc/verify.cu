@@ -101,16 +101,6 @@ struct VLayout {
 // TMEM columns: checkpoint operand [S hi (64) | S lo (64)], then the accumulator [D_hi | D_lo]
 constexpr uint32_t TV_SA = 0, TV_D = 128, TV_COLS = 256;
 
-// One box of the tensor map at (x = column, y = row) into shared memory, completing on mbar.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t mbar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
-        : "memory");
-}
-
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -601,23 +591,6 @@ __global__ void __launch_bounds__(kVThreads, 2)
     if (warp == 0) tmem_dealloc(tmem, TV_COLS);
 }
 
-// The tensor map's encoder from the driver, looked up once (a function-local static is
-// initialised exactly once even when several host threads make their first call together).
-PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    return nullptr;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encoder();
-    return fn;
-}
-
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -677,7 +650,7 @@ extern "C" kda_status kda_spec_verify(const void* q, const void* k, const void* 
     KDA_REQUIRE(P * H * 128 < (1ll << 31), KDA_ERR_UNSUPPORTED);
     const void* ptrs[] = {q, k, v, beta_raw, gate_raw, state_pool, ckpt_slot, rec_u, rec_kg, out};
     for (const void* p : ptrs) KDA_REQUIRE(p != nullptr && aligned16(p), KDA_ERR_INVALID_ARG);
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return KDA_ERR_CUDA;
     CUtensorMap map;
     const int st = state_type(flags);

@@ -1,6 +1,7 @@
-"""The tensor-core chunked prefill: parity with the fp64 oracle across chunk
-boundaries, its large-decay fallback, the activation flags, the longest-first
-schedule, and the chunk-vs-recurrent numerical gap (reported, and bounded)."""
+"""The single-pass tensor-core chunked prefill (no workspace, or one too small
+for the two-phase plan): parity with the fp64 oracle across chunk boundaries,
+its large-decay fallback, the activation flags, the longest-first schedule, and
+the chunk-vs-recurrent numerical gap (reported, and bounded)."""
 import numpy as np
 import pytest
 
@@ -35,7 +36,9 @@ def run(kda, c, flags=0, workspace=False, out_dtype=torch.bfloat16):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = None
     if workspace:
-        ws = torch.empty(max(16, kda.kda_chunk_prefill_workspace_size(T, N, H)),
+        # one byte short of the two-phase plan: the single-pass kernel with its
+        # longest-first order (the two-phase path has its own tests)
+        ws = torch.empty(max(16, kda.kda_chunk_prefill_workspace_size(T, N, H) - 16),
                          dtype=torch.uint8, device="cuda")
     kda.kda_chunk_prefill(dev_tensor(c["q"], dt), dev_tensor(c["k"], dt), dev_tensor(c["v"], dt),
                           dev_tensor(c["beta"], dt), dev_tensor(c["gate"], dt),

@@ -1,0 +1,186 @@
+"""The two-phase chunked prefill (a parallel prep over every (chunk, head), then a
+sequential sweep per (sequence, head)), selected by a workspace of at least
+kda_chunk_prefill_workspace_size bytes: parity with the fp64 oracle over ragged
+lengths, the token path of chunks whose decay leaves the tensor-core range, fp32
+outputs, 16-bit state pools, the activation flags, snapshot placement, and
+agreement with the single-pass kernel."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import TOL_STATE, dev_tensor, i32, rel_l2, to_np, worst_seq_head, worst_state
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import serving_kda_chunk_gb300 as kda
+
+    return kda
+
+
+def run(kda, c, *, two_phase=True, flags=0, out_dtype=torch.bfloat16, ws_bytes=None):
+    dt = c["dtype"]
+    N, H, T = c["N"], c["H"], c["T"]
+    M = c["track"].shape[1]
+    pool = torch.from_numpy(c["pool"]).cuda()
+    out = torch.full((T, H, 128), float("nan"), dtype=out_dtype, device="cuda")
+    snap = torch.full((N, M, H, 128, 128), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = None
+    if two_phase:
+        n = ws_bytes if ws_bytes is not None else kda.kda_chunk_prefill_workspace_size(T, N, H)
+        ws = torch.empty(max(16, n), dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prefill(dev_tensor(c["q"], dt), dev_tensor(c["k"], dt), dev_tensor(c["v"], dt),
+                          dev_tensor(c["beta"], dt), dev_tensor(c["gate"], dt),
+                          i32(c["cu_seqlens"]), out, state_pool=pool,
+                          init_slot=i32(c["init_slot"]), final_slot=i32(c["final_slot"]),
+                          track_chunk_idx=i32(c["track"]), track_state=snap, dev_status=st,
+                          flags=flags, workspace=ws)
+    torch.cuda.synchronize()
+    return out, pool, snap, int(st.item())
+
+
+def check(c, got, flags=0, tol_o=5e-3):
+    out, pool, snap, st = got
+    S0 = c["pool"][c["init_slot"]].astype(np.float64)
+    dt = c["dtype"]
+    o_ref, s_ref, snap_ref, _ = oracle.prefill(
+        W.widen(c["q"], dt), W.widen(c["k"], dt), W.widen(c["v"], dt), W.widen(c["beta"], dt),
+        W.widen(c["gate"], dt), c["cu_seqlens"], S0=S0, track=c["track"], flags=flags & 3)
+    assert st == 0
+    valid = c["track"] >= 0
+    o = to_np(out)
+    fin = pool.cpu().numpy()[c["final_slot"]]
+    sn = snap.cpu().numpy()
+    assert rel_l2(o, o_ref) < tol_o
+    assert rel_l2(fin, s_ref) < TOL_STATE
+    assert worst_seq_head(o, o_ref, c["cu_seqlens"]) < tol_o
+    assert worst_state(fin, s_ref) < TOL_STATE
+    if valid.any():
+        assert rel_l2(sn[valid], snap_ref[valid]) < TOL_STATE
+        assert worst_state(sn[valid], snap_ref[valid]) < TOL_STATE
+    assert np.isnan(sn[~valid]).all()  # unused snapshot entries are never written
+    return o, fin, sn
+
+
+def test_ragged_lengths_and_snapshots(kda):
+    lengths = [0, 1, 63, 64, 65, 200, 130, 1000]
+    c = W.prefill_case(60, lengths, 3, pool_slots=16, track_per_seq=2)
+    check(c, run(kda, c))
+
+
+def test_one_long_sequence_few_heads(kda):
+    c = W.prefill_case(61, [4096 + 17], 2, pool_slots=2, track_per_seq=4)
+    check(c, run(kda, c))
+
+
+def test_fp32_output(kda):
+    c = W.prefill_case(62, [300, 77, 64], 2, pool_slots=6, track_per_seq=1)
+    check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3])
+def test_preactivated_flags(kda, flags):
+    c = W.prefill_case(63, [150, 64], 2, pool_slots=4)
+    if flags & 1:
+        g = -np.abs(W.bf16_bits_to_f32(c["gate"])) * 0.5
+        c["gate"] = W.f32_to_bf16_bits(g)
+    if flags & 2:
+        b = 1.0 / (1.0 + np.exp(-W.bf16_bits_to_f32(c["beta"])))
+        c["beta"] = W.f32_to_bf16_bits(b.astype(np.float32))
+    check(c, run(kda, c, flags=flags), flags=flags)
+
+
+def test_strong_decay_chunks_take_the_token_path(kda):
+    c = W.prefill_case(64, [256, 100], 2, pool_slots=4, track_per_seq=2)
+    g = W.bf16_bits_to_f32(c["gate"]).copy()
+    g[10:14] = 30.0        # chunk 0 of sequence 0, both heads
+    g[200:203, 1] = 45.0   # chunk 3 of sequence 0, head 1 only
+    g[300:302, 0] = 60.0   # the last (partial) chunk of sequence 1, head 0
+    c["gate"] = W.f32_to_bf16_bits(g)
+    check(c, run(kda, c))
+
+
+def test_agrees_with_the_single_pass_kernel(kda):
+    c = W.prefill_case(65, [700, 90, 1300], 4, pool_slots=6, track_per_seq=2)
+    a = check(c, run(kda, c, two_phase=True))
+    b = check(c, run(kda, c, two_phase=False))
+    # the same arithmetic in a different order: far inside the oracle tolerances
+    assert rel_l2(a[0], b[0]) < 5e-3 and rel_l2(a[1], b[1]) < 1e-5
+
+
+def test_snapshot_placement_is_bit_exact(kda):
+    # snapshot j of a full run == final state of a run over the first j*64 tokens
+    L, j = 300, 3
+    c = W.prefill_case(66, [L], 2, pool_slots=2, track=[[j, 0]])
+    _, _, snap, st = run(kda, c)
+    c2 = W.prefill_case(66, [L], 2, pool_slots=2, track=[[j, 0]])
+    T2 = j * 64
+    for key in ("q", "k", "v", "beta", "gate"):
+        c2[key] = c2[key][:T2]
+    c2["cu_seqlens"] = np.array([0, T2], np.int32)
+    c2["T"] = T2
+    c2["track"] = np.array([[0, -1]], np.int32)
+    _, pool2, _, st2 = run(kda, c2)
+    assert st == 0 and st2 == 0
+    fin = int(c["final_slot"][0])
+    assert torch.equal(snap[0, 0], pool2[fin])
+    init = torch.from_numpy(c["pool"][c["init_slot"][0]]).cuda()
+    assert torch.equal(snap[0, 1], init)
+
+
+def test_deterministic(kda):
+    c = W.prefill_case(67, [333, 64, 5], 2, pool_slots=6, track_per_seq=1)
+    a = run(kda, c)
+    b = run(kda, c)
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x.nan_to_num(), y.nan_to_num())
+
+
+def test_short_workspace_runs_the_single_pass_kernel(kda):
+    c = W.prefill_case(68, [200, 50], 2, pool_slots=4)
+    need = kda.kda_chunk_prefill_workspace_size(c["T"], c["N"], c["H"])
+    a = run(kda, c, ws_bytes=need - 16)  # one byte short of the two-phase plan
+    b = run(kda, c, two_phase=False)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("st_flag", ["bf16", "f16"])
+def test_16bit_state_pool(kda, st_flag):
+    c = W.prefill_case(69, [260, 64], 2, pool_slots=4, track_per_seq=1)
+    tdt = torch.bfloat16 if st_flag == "bf16" else torch.float16
+    N, H, T = c["N"], c["H"], c["T"]
+    pool = torch.from_numpy(c["pool"]).cuda().to(tdt)
+    snap = torch.zeros((N, 1, H, 128, 128), dtype=tdt, device="cuda")
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, N, H), dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prefill(*(dev_tensor(c[n], "bf16") for n in ("q", "k", "v", "beta", "gate")),
+                          i32(c["cu_seqlens"]), out, state_pool=pool, init_slot=i32(c["init_slot"]),
+                          final_slot=i32(c["final_slot"]), track_chunk_idx=i32(c["track"]),
+                          track_state=snap, dev_status=st, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    S0 = pool.float().cpu().numpy()  # the widened 16-bit initial states
+    wid = lambda n: W.widen(c[n], "bf16")  # noqa: E731
+    o_ref, s_ref, snap_ref, _ = oracle.prefill(wid("q"), wid("k"), wid("v"), wid("beta"),
+                                               wid("gate"), c["cu_seqlens"],
+                                               S0=torch.from_numpy(c["pool"]).to(tdt).float()
+                                               .numpy()[c["init_slot"]].astype(np.float64),
+                                               track=c["track"])
+    del S0
+    u = 2.0 ** -8 if st_flag == "bf16" else 2.0 ** -11
+    assert rel_l2(to_np(out), o_ref) < 5e-3
+    assert rel_l2(pool.float().cpu().numpy()[c["final_slot"]], s_ref) < u + TOL_STATE
+    valid = c["track"] >= 0
+    assert rel_l2(snap.float().cpu().numpy()[valid], snap_ref[valid]) < u + TOL_STATE

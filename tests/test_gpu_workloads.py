@@ -34,12 +34,17 @@ def _prefill_gpu(kda, c, pool_np):
     M = c["track"].shape[1]
     snap = torch.full((c["N"], M, c["H"], 128, 128), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # the workspace the benchmark passes (the two-phase plan for bf16 inputs)
+    ws = torch.empty(max(16, kda.kda_chunk_prefill_workspace_size(c["T"], c["N"], c["H"])),
+                     dtype=torch.uint8, device="cuda")
     kda.kda_chunk_prefill(dev_tensor(c["q"], dt), dev_tensor(c["k"], dt), dev_tensor(c["v"], dt),
                           dev_tensor(c["beta"], dt), dev_tensor(c["gate"], dt),
                           i32(c["cu_seqlens"]), out, state_pool=pool,
                           init_slot=i32(c["init_slot"]), final_slot=i32(c["final_slot"]),
-                          track_chunk_idx=i32(c["track"]), track_state=snap, dev_status=st)
+                          track_chunk_idx=i32(c["track"]), track_state=snap, dev_status=st,
+                          workspace=ws)
     torch.cuda.synchronize()
+    del ws
     return out, pool, snap, int(st.item())
 
 
