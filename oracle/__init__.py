@@ -40,6 +40,8 @@ import numpy as np
 
 GATE_LOG = 1  # gate input holds g itself
 BETA_ACT = 2  # beta input holds beta itself
+QK_L2NORM = 32  # q and k rows divided by sqrt(sum x^2 + L2NORM_EPS) before use
+L2NORM_EPS = 1e-6
 
 BAD_SLOT = 1
 BAD_TRACK = 2
@@ -229,6 +231,16 @@ def beta_act(raw, flags=0):
         return 1.0 / (1.0 + np.exp(-raw))
 
 
+def qk_rows(x, flags=0):
+    """q or k rows as the recurrence uses them: under QK_L2NORM each row (last axis) is
+    divided by sqrt(sum x^2 + L2NORM_EPS) (the per-head L2 normalisation of the serving
+    configurations, done inside the path); otherwise unchanged."""
+    x = np.asarray(x, np.float64)
+    if not flags & QK_L2NORM:
+        return x
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + L2NORM_EPS)
+
+
 # --------------------------------------------------------------------------
 # chunk (WY / UT-transform) form, fp64, for agreement checks only
 
@@ -247,6 +259,7 @@ def chunked_prefill(q, k, v, beta, gate, cu_seqlens, *, chunk, scale=1.0, flags=
     Returns (out [T,H,dv], S_final [N,H,dv,dk]) -- states in the transposed layout.
     """
     q, k, v, beta, gate = map(_f64, (q, k, v, beta, gate))
+    q, k = qk_rows(q, flags), qk_rows(k, flags)
     T, H, dk = q.shape
     dv = v.shape[2]
     cu = np.asarray(cu_seqlens, np.int64)
@@ -292,11 +305,11 @@ def commit_closed_form(S0, rec_k, rec_gate, rec_u, a, flags=0):
     S0 = _f64(S0)
     dv, dk = S0.shape
     g = gate_log(np.asarray(rec_gate, np.float64)[:a], flags)
+    kk = qk_rows(np.asarray(rec_k, np.float64), flags)  # records hold k as given
     acc = np.zeros((dk, dv))
     suffix = np.zeros(dk)  # sum_{t<s<=a} g_s
     for t in range(a - 1, -1, -1):
-        acc += (np.exp(suffix) * np.asarray(rec_k, np.float64)[t])[:, None] * \
-            np.asarray(rec_u, np.float64)[t][None, :]
+        acc += (np.exp(suffix) * kk[t])[:, None] * np.asarray(rec_u, np.float64)[t][None, :]
         suffix = suffix + g[t]
     return (np.exp(suffix)[:, None] * S0.T + acc).T
 

@@ -37,8 +37,10 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define ORC_GATE_LOG 1u /* gate input already holds g (log of the decay) */
-#define ORC_BETA_ACT 2u /* beta input already holds beta                 */
+#define ORC_GATE_LOG 1u    /* gate input already holds g (log of the decay)        */
+#define ORC_BETA_ACT 2u    /* beta input already holds beta                        */
+#define ORC_QK_L2NORM 32u  /* q and k of every row divided by sqrt(sum x^2 + eps)  */
+#define ORC_L2NORM_EPS 1e-6
 
 /* status bits returned by the oracle (host-side mirror of the semantics) */
 #define ORC_BAD_SLOT 1
@@ -60,6 +62,17 @@ static double orc_beta(double raw, unsigned flags)
     return 1.0 / (1.0 + exp(-raw));
 }
 
+/* The factor a row of q or k is multiplied by: 1 / sqrt(sum_i x_i^2 + eps) under
+ * ORC_QK_L2NORM (the per-head L2 normalisation of the serving configurations,
+ * "q, k ~ N(0,1) then L2-normalised per head", done inside the path), else 1. */
+static double orc_norm(const double *x, int n, unsigned flags)
+{
+    if (!(flags & ORC_QK_L2NORM)) return 1.0;
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+    return 1.0 / sqrt(ss + ORC_L2NORM_EPS);
+}
+
 /*
  * One recurrence step on the transposed state ST (dv rows of dk).
  * k, q, gate_raw: dk values; v: dv values.  Writes u (dv) and o (dv) if given.
@@ -70,6 +83,7 @@ static void orc_step(double *ST, int dk, int dv, const double *q, const double *
                      double *o_out)
 {
     double beta = orc_beta(beta_raw, flags);
+    const double nk = orc_norm(k, dk, flags), nq = orc_norm(q, dk, flags);
     for (int i = 0; i < dk; ++i) alpha_tmp[i] = exp(orc_gate(gate_raw[i], flags));
     for (int c = 0; c < dv; ++c) {
         double *row = ST + (size_t)c * dk;
@@ -77,14 +91,14 @@ static void orc_step(double *ST, int dk, int dv, const double *q, const double *
         double xk = 0.0;
         for (int i = 0; i < dk; ++i) {
             row[i] *= alpha_tmp[i];
-            xk += row[i] * k[i];
+            xk += row[i] * (k[i] * nk);
         }
         double u = beta * (v[c] - xk);
         /* S = X + k u^T ; o[c] = sum_i S[i][c] (scale q[i]) */
         double o = 0.0;
         for (int i = 0; i < dk; ++i) {
-            row[i] += k[i] * u;
-            o += row[i] * (scale * q[i]);
+            row[i] += (k[i] * nk) * u;
+            o += row[i] * (scale * (q[i] * nq));
         }
         if (u_out) u_out[c] = u;
         if (o_out) o_out[c] = o;
@@ -364,10 +378,11 @@ static void orc_commit_unit(void *vctx, long unit, double *scratch)
     for (int t = 0; t < a; ++t) {
         const double *u = c->rec_u + (((size_t)r * H + h) * K + t) * dv;
         const double *kg = c->rec_kg + (((size_t)r * H + h) * K + t) * 2 * dk;
+        const double nk = orc_norm(kg, dk, c->flags);  /* the record holds k as given */
         for (int i = 0; i < dk; ++i) alpha[i] = exp(orc_gate(kg[dk + i], c->flags));
         for (int cc = 0; cc < dv; ++cc)
             for (int i = 0; i < dk; ++i)
-                ST[(size_t)cc * dk + i] = alpha[i] * ST[(size_t)cc * dk + i] + kg[i] * u[cc];
+                ST[(size_t)cc * dk + i] = alpha[i] * ST[(size_t)cc * dk + i] + (kg[i] * nk) * u[cc];
     }
     if (a > 0 || dst != src)
         memcpy(c->pool + ((size_t)dst * H + h) * ssz, ST, ssz * sizeof(double));

@@ -20,10 +20,16 @@ C_MUTANTS = [
     ("correction sign flipped", "double u = beta * (v[c] - xk);", "double u = beta * (v[c] + xk);"),
     ("beta dropped", "double u = beta * (v[c] - xk);", "double u = (v[c] - xk);"),
     ("output read before the write",
-     "row[i] += k[i] * u;\n            o += row[i] * (scale * q[i]);",
-     "o += row[i] * (scale * q[i]);\n            row[i] += k[i] * u;"),
-    ("output uses the key", "o += row[i] * (scale * q[i]);", "o += row[i] * (scale * k[i]);"),
-    ("scale dropped", "o += row[i] * (scale * q[i]);", "o += row[i] * q[i];"),
+     "row[i] += (k[i] * nk) * u;\n            o += row[i] * (scale * (q[i] * nq));",
+     "o += row[i] * (scale * (q[i] * nq));\n            row[i] += (k[i] * nk) * u;"),
+    ("output uses the key", "o += row[i] * (scale * (q[i] * nq));", "o += row[i] * (scale * (k[i] * nk));"),
+    ("scale dropped", "o += row[i] * (scale * (q[i] * nq));", "o += row[i] * (q[i] * nq);"),
+    ("L2 norm: key not normalised in the write", "row[i] += (k[i] * nk) * u;", "row[i] += k[i] * u;"),
+    ("L2 norm: query not normalised", "o += row[i] * (scale * (q[i] * nq));",
+     "o += row[i] * (scale * q[i]);"),
+    ("L2 norm: commit uses the raw key record",
+     "+ (kg[i] * nk) * u[cc];", "+ kg[i] * u[cc];"),
+    ("L2 norm: eps dropped", "return 1.0 / sqrt(ss + ORC_L2NORM_EPS);", "return 1.0 / sqrt(ss);"),
     ("softplus term dropped for positive inputs",
      "if (raw > 0.0) return -(raw + log1p(exp(-raw)));",
      "if (raw > 0.0) return -(log1p(exp(-raw)));"),
@@ -56,8 +62,9 @@ PY_MUTANTS = [
     ("closed form: checkpoint not decayed", "commit_closed_form", "np.exp(suffix)[:, None] * S0.T",
      "S0.T"),
     ("closed form: suffix includes its own step", "commit_closed_form",
-     "acc += (np.exp(suffix) * np.asarray(rec_k, np.float64)[t])",
-     "acc += (np.exp(suffix + g[t]) * np.asarray(rec_k, np.float64)[t])"),
+     "acc += (np.exp(suffix) * kk[t])", "acc += (np.exp(suffix + g[t]) * kk[t])"),
+    ("closed form: raw key record under the L2 norm", "commit_closed_form",
+     "kk = qk_rows(np.asarray(rec_k, np.float64), flags)", "kk = np.asarray(rec_k, np.float64)"),
     ("chunk form: diagonal kept in A", "chunked_prefill", "np.tri(L, k=-1)", "np.tri(L, k=0)"),
     ("chunk form: correction sign flipped", "chunked_prefill", "U = Ut - W @ S", "U = Ut + W @ S"),
 ]

@@ -497,3 +497,85 @@ def test_bf16_storage_round_trip():
     # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: nearest-even keeps 1
     assert y[3] == 1.0 and y[4] == np.float32(1.0078125)
     assert y[0] == 0 and y[1] == 1 and y[2] == -2.5 and np.isinf(y[5]) and np.isinf(y[6])
+
+
+# --------------------------------------------------------------------------
+# in-path q / k L2 normalisation (QK_L2NORM)
+
+
+def test_l2norm_makes_the_delta_rule_read_back_for_any_key_length():
+    # The delta-rule write reads back exactly only with unit keys (S_t^T k_t = v_t needs
+    # |k_t| = 1).  With keys of arbitrary length, q = k and beta = 1, the flag must give
+    # o_t = v_t (up to the eps term, |k^|^2 = |k|^2 / (|k|^2 + eps)); without it, not.
+    rng = np.random.default_rng(31)
+    T, H, dk, dv = 40, 2, 12, 10
+    k = rng.standard_normal((T, H, dk))
+    k *= (rng.uniform(0.5, 5.0, (T, H, 1)) / np.linalg.norm(k, axis=-1, keepdims=True))
+    v = rng.standard_normal((T, H, dv))
+    gate = rng.standard_normal((T, H, dk))
+    beta = np.ones((T, H))
+    S0 = rng.standard_normal((1, H, dv, dk))
+    flags = oracle.BETA_ACT | oracle.QK_L2NORM
+    out, _, _, _ = oracle.prefill(k, k, v, beta, gate, [0, T], S0=S0, flags=flags)
+    np.testing.assert_allclose(out, v, rtol=0, atol=1e-4)
+    out0, _, _, _ = oracle.prefill(k, k, v, beta, gate, [0, T], S0=S0, flags=oracle.BETA_ACT)
+    assert np.max(np.abs(out0 - v)) > 1e-2
+
+
+def test_l2norm_is_invariant_to_the_scale_of_each_row():
+    rng = np.random.default_rng(32)
+    T, H, dk, dv = 70, 2, 16, 8
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, dk, dv, unit_k=False)
+    cu = [0, 30, T]
+    S0 = rng.standard_normal((2, H, dv, dk)) * 0.1
+    f = oracle.QK_L2NORM
+    # factors keep |x|^2 >= ~4, so the eps term moves a normalised row by < 1e-7 relative
+    cq = rng.uniform(0.5, 20.0, (T, H, 1))
+    ck = rng.uniform(0.5, 20.0, (T, H, 1))
+    o1, s1, _, _ = oracle.prefill(q, k, v, beta, gate, cu, S0=S0, flags=f)
+    o2, s2, _, _ = oracle.prefill(q * cq, k * ck, v, beta, gate, cu, S0=S0, flags=f)
+    np.testing.assert_allclose(o2, o1, rtol=1e-5, atol=1e-8)
+    np.testing.assert_allclose(s2, s1, rtol=1e-5, atol=1e-8)
+    # the chunk form applies the same normalisation
+    o_c, s_c = oracle.chunked_prefill(q * cq, k * ck, v, beta, gate, cu, chunk=8, S0=S0, flags=f)
+    assert np.max(np.abs(o_c - o2)) <= 1e-11 and np.max(np.abs(s_c - s2)) <= 1e-11
+
+
+def test_l2norm_verify_then_commit_equals_repeated_decode():
+    # the key record holds k as given; the commit must normalise it as the step did
+    rng = np.random.default_rng(33)
+    R, K, H, dk, dv = 2, 4, 2, 8, 6
+    q, k, v, beta, gate = _rand_inputs(rng, R * K, H, dk, dv, unit_k=False)
+    k *= 3.0
+    pool = rng.standard_normal((3, H, dv, dk))
+    ckpt = np.array([2, 0], np.int32)
+    f = oracle.QK_L2NORM
+    out, ru, rkg, _ = oracle.verify(q, k, v, beta, gate, pool, ckpt, K, flags=f)
+    np.testing.assert_array_equal(rkg[:, :, :, :dk], k.reshape(R, K, H, dk).transpose(0, 2, 1, 3))
+    for r in range(R):
+        p = pool.copy()
+        for t in range(K):
+            row = r * K + t
+            o1, p, _ = oracle.decode(q[row:row + 1], k[row:row + 1], v[row:row + 1],
+                                     beta[row:row + 1], gate[row:row + 1], p, [ckpt[r]], flags=f)
+            np.testing.assert_array_equal(out[row], o1[0])
+            pc, _, _ = oracle.commit(pool, ckpt[r:r + 1], [t + 1], ru[r:r + 1], rkg[r:r + 1], K,
+                                     flags=f)
+            np.testing.assert_allclose(pc[ckpt[r]], p[ckpt[r]], rtol=1e-12, atol=1e-13)
+            cf = np.stack([oracle.commit_closed_form(pool[ckpt[r], h], rkg[r, h, :, :dk],
+                                                     rkg[r, h, :, dk:], ru[r, h], t + 1, flags=f)
+                           for h in range(H)])
+            np.testing.assert_allclose(cf, p[ckpt[r]], rtol=1e-12, atol=1e-13)
+
+
+def test_l2norm_of_a_zero_row_is_zero():
+    # eps keeps a zero key finite: it writes nothing (u k^T = 0) and the state only decays
+    rng = np.random.default_rng(34)
+    T, H, dk, dv = 6, 1, 8, 4
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, dk, dv)
+    k[:] = 0.0
+    S0 = rng.standard_normal((1, H, dv, dk))
+    out, s, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0, flags=oracle.QK_L2NORM)
+    assert np.isfinite(out).all()
+    decay = np.exp(oracle.gate_log(gate).sum(0))  # [H, dk]
+    np.testing.assert_allclose(s[0], S0[0] * decay[:, None, :], rtol=1e-12, atol=1e-14)
