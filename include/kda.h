@@ -43,6 +43,7 @@
  *   - flags: KDA_GATE_LOG = the gate input already holds g (log decay);
  *     KDA_BETA_ACT = the beta input already holds beta.  Default: both raw.
  *     KDA_STATE_BF16 / KDA_STATE_F16 = the state type (default fp32).
+ *     KDA_QK_L2NORM = q and k normalised per (row, head) inside the kernels.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -79,6 +80,15 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  * the pool layout is otherwise unchanged. */
 #define KDA_STATE_BF16 8u
 #define KDA_STATE_F16 16u
+/* q and k are L2-normalised per (row, head) inside the kernels before any use,
+ * in fp32: x / sqrt(sum_i x_i^2 + 1e-6) (the serving configurations normalise
+ * q and k per head; this does it in the path instead of in a separate pass).
+ * kda_spec_verify's key record still holds k as given; kda_spec_commit and
+ * kda_spec_accept_commit with the same flag normalise the recorded key the
+ * same way.  kda_chunk_prefill honours it on the two-phase and token-serial
+ * paths (a call that would take the single-pass kernel takes the token-serial
+ * one instead). */
+#define KDA_QK_L2NORM 32u
 
 /* bits OR-ed into *dev_status by the kernels */
 #define KDA_DEV_BAD_SLOT 1     /* slot index >= pool size (or required and < 0) */

@@ -19,6 +19,7 @@ import torch
 
 __all__ = [
     "KDA_BF16", "KDA_F32", "KDA_GATE_LOG", "KDA_BETA_ACT", "KDA_STATE_BF16", "KDA_STATE_F16",
+    "KDA_QK_L2NORM",
     "KdaError", "lib",
     "kda_chunk_prefill", "kda_recurrent_decode", "kda_spec_verify", "kda_spec_accept",
     "kda_spec_commit", "kda_spec_accept_commit", "kda_conv_compact", "kda_slot_copy",
@@ -31,6 +32,7 @@ __all__ = [
 KDA_BF16, KDA_F32 = 0, 1
 KDA_GATE_LOG, KDA_BETA_ACT, KDA_PREFILL_RECURRENT = 1, 2, 4
 KDA_STATE_BF16, KDA_STATE_F16 = 8, 16
+KDA_QK_L2NORM = 32
 KDA_DEV_BAD_SLOT, KDA_DEV_BAD_TRACK, KDA_DEV_BAD_ACCEPT = 1, 2, 4
 KDA_DEV_BAD_SEQLEN, KDA_DEV_OVERLAP, KDA_DEV_TIMEOUT = 8, 16, 32
 KDA_MAX_POOLS = 16

@@ -181,6 +181,21 @@ __global__ void __launch_bounds__(kCommitThreads, 8) commit_kernel(
         umma::cp_async_commit();
     }
     umma::cp_async_wait_all();
+    // KDA_QK_L2NORM: the record holds k as given; its factor per step (a warp per record)
+    float* NRM = reinterpret_cast<float*>(KG + (size_t)K * 2 * kD * ES);  // [K]
+    const bool l2 = (flags & KDA_QK_L2NORM) != 0;
+    if (l2) {
+        __syncthreads();  // every thread's record copies have landed
+        for (int t = warp; t < a; t += kCommitThreads / 32) {
+            float4 x;
+            if constexpr (kBf16Rec)
+                x = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(KG + ((size_t)t * 2 * kD + 4 * lane) * 2));
+            else
+                x = *reinterpret_cast<const float4*>(KG + ((size_t)t * 2 * kD + 4 * lane) * 4);
+            const float ss = warp_sum(f4_dot(x, x));
+            if (lane == 0) NRM[t] = l2norm_factor(ss);
+        }
+    }
     // pass 0: the state after a steps -> the destination slot; pass 1 (align mode): the state
     // after a_b steps -> the block slot.  The staged checkpoint rows are only read.
     const int n_pass = bslot >= 0 ? 2 : 1;
@@ -199,7 +214,7 @@ __global__ void __launch_bounds__(kCommitThreads, 8) commit_kernel(
                                           : reinterpret_cast<const float*>(KG)[t * 2 * kD + c];
                 const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
                                           : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
-                F[t * kD + c] = prod * kv;
+                F[t * kD + c] = prod * (l2 ? kv * NRM[t] : kv);
                 prod *= alpha_of(gv, flags);
             }
             D[c] = prod;
@@ -266,7 +281,7 @@ kda_status launch_commit(void* state_pool, int64_t P, const int32_t* ckpt_slot,
     const int st = state_type(flags);
     const int rows = st == kStateF32 ? 4 * commit_rows<kStateF32>() : 4 * commit_rows<kStateBF16>();
     const size_t smem = kCommitStage + (size_t)(K * kD + K * rows + kD) * sizeof(float) +
-                        (size_t)K * 2 * kD * es;
+                        (size_t)K * 2 * kD * es + (size_t)((K + 3) / 4) * 16;  // + L2 factors
     const unsigned grid = (unsigned)((kD / rows) * R * H + conv.n_ctas);
     auto run = [&](auto kernel) {
         if (smem > 48 * 1024)

@@ -79,7 +79,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(
                        alpha_of(g.w, flags));
     in.k = A::load4(k, th * kD + 4 * lane);
     float4 qq = A::load4(q, th * kD + 4 * lane);
-    in.q = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);
+    float fq = scale;
+    if (flags & KDA_QK_L2NORM) {  // per (row, head), over the 128 channels the warp holds
+        float sk = f4_dot(in.k, in.k), sq = f4_dot(qq, qq);
+        warp_sum2(sk, sq);
+        const float fk = l2norm_factor(sk);
+        fq = scale * l2norm_factor(sq);
+        in.k = make_float4(in.k.x * fk, in.k.y * fk, in.k.z * fk, in.k.w * fk);
+    }
+    in.q = make_float4(qq.x * fq, qq.y * fq, qq.z * fq, qq.w * fq);
     in.kq = warp_sum(f4_dot(in.k, in.q));
     in.beta = beta_act(A::load1(beta_raw, th), flags);
     const int row0 = warp * RW;  // within the CTA's rows

@@ -50,6 +50,10 @@ __device__ __forceinline__ Decay decay_of(float raw, uint32_t flags) {
 
 __device__ __forceinline__ float alpha_of(float raw, uint32_t flags) { return decay_of(raw, flags).a; }
 
+// Under KDA_QK_L2NORM a row x of q or k is used as x * l2norm_factor(sum_i x_i^2).
+constexpr float kL2NormEps = 1e-6f;
+__device__ __forceinline__ float l2norm_factor(float sum_sq) { return rsqrtf(sum_sq + kL2NormEps); }
+
 // beta = sigmoid(raw beta) (raw -inf gives 0 exactly); KDA_BETA_ACT: beta given.
 __device__ __forceinline__ float beta_act(float raw, uint32_t flags) {
     if (flags & KDA_BETA_ACT) return raw;
@@ -383,12 +387,20 @@ __device__ __forceinline__ void stage_tokens(TokenTile<kTile>& tt, const void* q
     for (int t = warp; t < n_tok; t += (int)(blockDim.x >> 5)) {
         const size_t th = (row_base + t) * (size_t)H + h;
         const float4 g = A::load4(gate_raw, th * kD + 4 * lane);
-        const float4 kk = A::load4(k, th * kD + 4 * lane);
+        float4 kk = A::load4(k, th * kD + 4 * lane);
         const float4 qq = A::load4(q, th * kD + 4 * lane);
         const float4 vv = A::load4(v, th * kD + 4 * lane);
         const float4 a = make_float4(alpha_of(g.x, flags), alpha_of(g.y, flags),
                                      alpha_of(g.z, flags), alpha_of(g.w, flags));
-        const float4 qs = make_float4(qq.x * scale, qq.y * scale, qq.z * scale, qq.w * scale);
+        float fk = 1.f, fq = scale;
+        if (flags & KDA_QK_L2NORM) {
+            float sk = f4_dot(kk, kk), sq = f4_dot(qq, qq);
+            warp_sum2(sk, sq);
+            fk = l2norm_factor(sk);
+            fq = scale * l2norm_factor(sq);
+        }
+        kk = make_float4(kk.x * fk, kk.y * fk, kk.z * fk, kk.w * fk);
+        const float4 qs = make_float4(qq.x * fq, qq.y * fq, qq.z * fq, qq.w * fq);
         *reinterpret_cast<float4*>(&tt.a[t][4 * lane]) = a;
         *reinterpret_cast<float4*>(&tt.k[t][4 * lane]) = kk;
         *reinterpret_cast<float4*>(&tt.q[t][4 * lane]) = qs;

@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     float* s_beta = reinterpret_cast<float*>(sm + PR_MISC);  // 64
-    float* s_seg_a = s_beta + 64;                            // [4][128]: prod of alpha per token quarter
+    float* s_nk = s_beta + 64;                               // 64: L2 factors of the key rows
+    float* s_nq = s_nk + 64;                                 // 64: of the query rows (x scale)
+    float* s_seg_a = s_nq + 64;                              // [4][128]: prod of alpha per token quarter
     float* s_seg_i = s_seg_a + 512;                          // [4][128]: prod of 1/alpha per quarter
     uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_seg_i + 512);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 1);
@@ -225,6 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     const int64_t n_chunks_all = min((int64_t)plan[PL_META / 4], n_max);
     const int64_t items = n_chunks_all * H;
     if ((int64_t)blockIdx.x >= items) return;
+    const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
+    // raw key / query element (t, ci) as the recurrence uses it (q also times scale)
+    auto key_at = [&](int t) {
+        const float x = bf16_at(sm, PR_K + t * 256 + ci * 2);
+        return l2 ? x * s_nk[t] : x;
+    };
+    auto query_at = [&](int t) {
+        const float x = bf16_at(sm, PR_Q + t * 256 + ci * 2);
+        return l2 ? x * s_nq[t] : x * p.scale;
+    };
 
     if (warp == 0) tmem_alloc(smem_u32(s_tmem), PT_COLS);
     if (tid == 0) mbar_init(smem_u32(s_mbar), 1);
@@ -294,6 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
         cp_async_wait_all();
         if (tid < 64) s_beta[tid] = tid < Lc ? beta_act(__uint_as_float(beta_bits << 16), p.flags) : 0.f;
         __syncthreads();
+        if (l2) {
+            // KDA_QK_L2NORM: factors of the key and query rows, a warp per 4 rows
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                const int t = 4 * warp + tt;
+                const uint2 kw = *reinterpret_cast<const uint2*>(sm + PR_K + t * 256 + lane * 8);
+                const uint2 qw = *reinterpret_cast<const uint2*>(sm + PR_Q + t * 256 + lane * 8);
+                const float4 kx = State<kStateBF16>::widen(kw), qx = State<kStateBF16>::widen(qw);
+                float sk = f4_dot(kx, kx), sq = f4_dot(qx, qx);
+                warp_sum2(sk, sq);
+                if (lane == 0) {
+                    s_nk[t] = l2norm_factor(sk);
+                    s_nq[t] = l2norm_factor(sq) * p.scale;
+                }
+            }
+            __syncthreads();
+        }
 
         // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
         float al[16], iv[16];
@@ -347,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
 #pragma unroll
                 for (int w8 = 7; w8 >= 0; --w8) {
                     const int u = g8 * 8 + w8, t = 16 * tq + u;
-                    const float kk = bf16_at(sm, PR_K + t * 256 + ci * 2);
-                    const float qq = bf16_at(sm, PR_Q + t * 256 + ci * 2) * p.scale;
+                    const float kk = key_at(t);
+                    const float qq = query_at(t);
                     lk[w8] = kk * si;
                     lq[w8] = qq * si;
                     r[w8] = kk * sa;
@@ -379,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
 #pragma unroll
                 for (int w8 = 0; w8 < 8; ++w8) {
                     const int u = g8 * 8 + w8, t = 16 * tq + u;
-                    const float kk = bf16_at(sm, PR_K + t * 256 + ci * 2);
-                    const float qq = bf16_at(sm, PR_Q + t * 256 + ci * 2) * p.scale;
+                    const float kk = key_at(t);
+                    const float qq = query_at(t);
                     fa *= al[u];
                     fi *= iv[u];
                     lk[w8] = kk * fa;
@@ -436,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
                 for (int w8 = 0; w8 < 8; ++w8) {
                     const int u = 8 * c8 + w8, t = 16 * tq + u;
                     fw *= al[u];
-                    kg[w8] = bf16_at(sm, PR_K + t * 256 + ci * 2) * fw;
-                    qg[w8] = bf16_at(sm, PR_Q + t * 256 + ci * 2) * p.scale * fw;
+                    kg[w8] = key_at(t) * fw;
+                    qg[w8] = query_at(t) * fw;
                 }
                 const int s0 = 16 * tq + 8 * c8;
                 uint4 hi, lo;
@@ -458,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
 #pragma unroll
                 for (int w8 = 7; w8 >= 0; --w8) {
                     const int u = 8 * c8 + w8, t = 16 * tq + u;
-                    kt[w8] = bf16_at(sm, PR_K + t * 256 + ci * 2) * bw;
+                    kt[w8] = key_at(t) * bw;
                     bw *= al[u];
                 }
                 const int s0 = 16 * tq + 8 * c8;
@@ -750,7 +779,9 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     float* s_beta = reinterpret_cast<float*>(sm + SW_MISC);            // 64 (token path)
-    int* s_trk = reinterpret_cast<int*>(s_beta + 64);                  // kTrack2p
+    float* s_nk = s_beta + 64;                                         // 64: key-row L2 factors (token path)
+    float* s_nq = s_nk + 64;                                           // 64: query-row factors x scale
+    int* s_trk = reinterpret_cast<int*>(s_nq + 64);                    // kTrack2p
     // MMA, S update, part A + V, part B (one arrival each); S operand and U operand written
     // (one arrival per thread)
     uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_trk + kTrack2p);
@@ -1176,6 +1207,27 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                 cp_async_wait_all();
                 __syncthreads();
             }
+            if (!issuer) {
+                // the factors the key / query rows are used with (1 and scale without the flag)
+                const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt) {
+                    const int t = 4 * warp + tt;
+                    float fk = 1.f, fq = p.scale;
+                    if (l2) {
+                        const float4 kx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + SW_RAW_K + t * 256 + lane * 8));
+                        const float4 qx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + SW_RAW_Q + t * 256 + lane * 8));
+                        float sk = f4_dot(kx, kx), sq = f4_dot(qx, qx);
+                        warp_sum2(sk, sq);
+                        fk = l2norm_factor(sk);
+                        fq = l2norm_factor(sq) * p.scale;
+                    }
+                    if (lane == 0) {
+                        s_nk[t] = fk;
+                        s_nq[t] = fq;
+                    }
+                }
+            }
             float* alpha = reinterpret_cast<float*>(sm + SW_ALPHA);
             if (!issuer) {
 #pragma unroll
@@ -1208,10 +1260,11 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                     float d1 = 0.f;
                     if (!issuer) {
 #pragma unroll
+                        const float fk = s_nk[t];
                         for (int q = 0; q < 32; ++q) {
                             const int i = cq * 32 + q;
                             sv[q] *= alpha[t * kD + i];
-                            d1 = fmaf(sv[q], bf16_at(sm, SW_RAW_K + t * 256 + i * 2), d1);
+                            d1 = fmaf(sv[q], bf16_at(sm, SW_RAW_K + t * 256 + i * 2) * fk, d1);
                         }
                         red[cq * 128 + c] = d1;
                     }
@@ -1222,10 +1275,11 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                         const float uu = s_beta[t] * (vt - d1);
                         float o = 0.f;
 #pragma unroll
+                        const float fk = s_nk[t], fq = s_nq[t];
                         for (int q = 0; q < 32; ++q) {
                             const int i = cq * 32 + q;
-                            sv[q] = fmaf(uu, bf16_at(sm, SW_RAW_K + t * 256 + i * 2), sv[q]);
-                            o = fmaf(sv[q], bf16_at(sm, SW_RAW_Q + t * 256 + i * 2) * p.scale, o);
+                            sv[q] = fmaf(uu, bf16_at(sm, SW_RAW_K + t * 256 + i * 2) * fk, sv[q]);
+                            o = fmaf(sv[q], bf16_at(sm, SW_RAW_Q + t * 256 + i * 2) * fq, o);
                         }
                         red[512 + cq * 128 + c] = o;
                     }

@@ -910,7 +910,9 @@ __global__ void __launch_bounds__(1024) prefill_order_kernel(const int32_t* __re
 
 }  // namespace
 
-bool prefill_tc_supported(const PrefillArgs& p, bool bf16_in) { return bf16_in && p.M <= kTrackTc; }
+bool prefill_tc_supported(const PrefillArgs& p, bool bf16_in) {
+    return bf16_in && p.M <= kTrackTc && !(p.flags & KDA_QK_L2NORM);
+}
 
 size_t prefill_tc_workspace(int32_t N) {
     return N > 0 && N <= kMaxOrderN ? (size_t)((N + 3) / 4) * 16 : 0;

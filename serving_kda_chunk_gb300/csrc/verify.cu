@@ -87,7 +87,8 @@ struct VLayout {
     static constexpr uint32_t RED = align16(AP + KC * KC * 4);   // [4 warps][KC][KC]
     static constexpr uint32_t BETA = align16(RED + 4 * KC * KC * 4);  // [KC] activated beta
     static constexpr uint32_t BRAW = align16(BETA + KC * 4);     // [KC] 4-byte words holding raw beta
-    static constexpr uint32_t TAB = align16(BRAW + KC * 4);      // [3][KC][TLD] fp32 (K <= 8)
+    static constexpr uint32_t NRM = align16(BRAW + KC * 4);      // [2][KC] L2 factors of k, q
+    static constexpr uint32_t TAB = align16(NRM + 2 * KC * 4);   // [3][KC][TLD] fp32 (K <= 8)
     static constexpr uint32_t TAB_BYTES = KC <= 8 ? 3 * KC * TLD * 4 : 0;
     static constexpr uint32_t META = align16(TAB + TAB_BYTES);   // [kMaxUnitsPerCta] (slot, q_len)
     static constexpr uint32_t MBAR = META + kMaxUnitsPerCta * 8; // checkpoint, MMA
@@ -312,12 +313,34 @@ __global__ void __launch_bounds__(kVThreads, 2)
             }
             sbeta[tid] = bv;
         }
+        // ---- KDA_QK_L2NORM: the factors of the key and query rows (a warp per row)
+        float* nrm = reinterpret_cast<float*>(sm + Lay::NRM);
+        const bool l2 = (a.flags & KDA_QK_L2NORM) != 0;
+        if (l2) {
+            const uint8_t* kqg = sm + Lay::KQG;
+            for (int t = warp; t < KC; t += kVThreads / 32) {
+                float sk = 0.f, sq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float kx = act_at<kBf16In>(kqg, t * 128 + 4 * lane + e);
+                    const float qx = act_at<kBf16In>(kqg, (KC + t) * 128 + 4 * lane + e);
+                    sk = fmaf(kx, kx, sk);
+                    sq = fmaf(qx, qx, sq);
+                }
+                warp_sum2(sk, sq);
+                if (lane == 0) {
+                    nrm[t] = l2norm_factor(sk);
+                    nrm[KC + t] = l2norm_factor(sq);
+                }
+            }
+        }
         // ---- checkpoint rows -> TMEM operand (all warps, 64 columns each)
         if (ql > 0) {
             convert(2 * colhalf);
             convert(2 * colhalf + 1);
             wait_st();
         }
+        if (l2) __syncthreads();  // the factors above, for every channel thread below
         // ---- channel i: gates; warps 0-3 the gated keys / queries and the key / raw gate
         //      records, warps 4-7 the K x K factors
         {
@@ -327,6 +350,10 @@ __global__ void __launch_bounds__(kVThreads, 2)
             for (int t = 0; t < KC; ++t) {
                 kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
                 qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
+                if (l2) {
+                    kt[t] *= nrm[t];
+                    qt[t] *= nrm[KC + t];
+                }
                 at[t] = iv[t] = 1.f;
                 if (t < ql) {
                     const Decay dc = decay_of(act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i), a.flags);
