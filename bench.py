@@ -722,6 +722,18 @@ def run_profile_case(name, reps):
             kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
                                   state_pool=pool, init_slot=sl, final_slot=sl,
                                   track_chunk_idx=tr, track_state=snap, workspace=ws)
+    elif name == "slot_copy_small":
+        # the fused copy kernel on a reduced pool (512 slots of 1 MiB states, 32 parents x 8
+        # children + 64 clears: 352 MiB moved, above L2) so that a multi-pass capture holds
+        # well under a few GB
+        sc = W.slot_copy_case(12, 512, 32, 8, 64)
+        pool = torch.empty(512, 16, D, D, device=dev)
+        pool.normal_(0.0, 0.1, generator=torch.Generator(device=dev).manual_seed(12))
+        args = [i32(sc[n], dev) for n in ("clear", "src", "dst_offsets", "dst")]
+        ws = torch.empty(kda.kda_slot_copy_workspace_size(512), dtype=torch.uint8, device=dev)
+
+        def fn():
+            kda.kda_slot_copy([pool], *args, ws)
     else:
         part = {"decode": "decode", "verify": "spec", "commit": "spec", "conv_compact": "spec",
                 "slot_copy": "copy"}[name]
@@ -751,7 +763,7 @@ def main():
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["prefill", "prefill_single", "decode", "verify", "commit",
-                                          "conv_compact", "slot_copy"],
+                                          "conv_compact", "slot_copy", "slot_copy_small"],
                     help="run one entry point a few times (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.profile:
