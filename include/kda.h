@@ -135,9 +135,10 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *                    input order.  The paths agree within the stated
  *                    tolerances; the single-pass results do not depend on the
  *                    order (bit-identical).
- * bf16 activations run on the tensor cores (two-phase with N <= 4096 and
- * M <= 512, else single-pass); fp32 activations and KDA_PREFILL_RECURRENT run
- * the token-serial kernel.
+ * The chunk algorithm runs on the tensor cores: two-phase (bf16 or fp32
+ * activations, N <= 4096, M <= 512, a workspace of the size above), else
+ * single-pass (bf16 activations).  fp32 activations without that workspace,
+ * and any call with KDA_PREFILL_RECURRENT, run the token-serial kernel.
  * Units of work are (sequence, head); sequences must not share a final slot.
  */
 kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* beta_raw,

@@ -35,9 +35,10 @@ struct PrefillArgs {
 
 void launch_prefill_serial(const PrefillArgs& p, bool bf16_in, bool bf16_out, cudaStream_t s);
 
-bool prefill_2p_supported(const PrefillArgs& p, bool bf16_in);
+// the two-phase kernels take bf16 or fp32 activations and either output type
+bool prefill_2p_supported(const PrefillArgs& p);
 size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H);
-kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_out, void* workspace, cudaStream_t s);
+kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_in, bool bf16_out, void* workspace, cudaStream_t s);
 
 bool prefill_tc_supported(const PrefillArgs& p, bool bf16_in);
 size_t prefill_tc_workspace(int32_t N);

@@ -202,7 +202,7 @@ static_assert(PR_SMEM <= 232448, "prep shared memory plan exceeds the per-CTA li
 // TMEM (256 columns): [A;P] accumulator (hi-R | lo-R parts), W^T, KG hi/lo A operand
 constexpr uint32_t PT_AP = 0, PT_W = 128, PT_KG_HI = 192, PT_KG_LO = 224, PT_COLS = 256;
 
-template <bool kBf16Out>
+template <bool kBf16Out, bool kF32In>
 __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p, const int32_t* __restrict__ plan,
                                                                    int64_t n_max, uint8_t* __restrict__ ops) {
     extern __shared__ uint8_t smem_raw[];
@@ -228,15 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     const int64_t items = n_chunks_all * H;
     if ((int64_t)blockIdx.x >= items) return;
     const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
-    // raw key / query element (t, ci) as the recurrence uses it (q also times scale)
-    auto key_at = [&](int t) {
-        const float x = bf16_at(sm, PR_K + t * 256 + ci * 2);
-        return l2 ? x * s_nk[t] : x;
-    };
-    auto query_at = [&](int t) {
-        const float x = bf16_at(sm, PR_Q + t * 256 + ci * 2);
-        return l2 ? x * s_nq[t] : x * p.scale;
-    };
 
     if (warp == 0) tmem_alloc(smem_u32(s_tmem), PT_COLS);
     if (tid == 0) mbar_init(smem_u32(s_mbar), 1);
@@ -269,26 +260,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     // item w is (chunk w / H, head w % H); consecutive items of this CTA are gridDim.x apart
     const int64_t step_c = gridDim.x / H;
     const int step_h = (int)(gridDim.x - step_c * H);
-    // raw q, k, g tiles of an item (rows past the sequence zero-filled); its raw beta bits
+    // raw q, k, g tiles of an item (bf16: rows past the sequence zero-filled); its raw beta bits
     auto prefetch = [&](const Item& it, uint32_t& beta_bits) {
+        if constexpr (!kF32In) {
 #pragma unroll
-        for (int e = tid; e < 64 * 16; e += kThreads) {
-            const int t = e >> 4, ch = e & 15;
-            const bool ok = t < it.Lc;
-            const size_t off = ok ? ((size_t)(it.c0 + t) * H + it.h) * kD + ch * 8 : 0;
-            const uint32_t nb = ok ? 16u : 0u;
-            cp_async16(sb + PR_Q + t * 256 + ch * 16, gq + off, nb);
-            cp_async16(sb + PR_K + t * 256 + ch * 16, gk + off, nb);
-            cp_async16(sb + PR_G + t * 256 + ch * 16, gg + off, nb);
+            for (int e = tid; e < 64 * 16; e += kThreads) {
+                const int t = e >> 4, ch = e & 15;
+                const bool ok = t < it.Lc;
+                const size_t off = ok ? ((size_t)(it.c0 + t) * H + it.h) * kD + ch * 8 : 0;
+                const uint32_t nb = ok ? 16u : 0u;
+                cp_async16(sb + PR_Q + t * 256 + ch * 16, gq + off, nb);
+                cp_async16(sb + PR_K + t * 256 + ch * 16, gk + off, nb);
+                cp_async16(sb + PR_G + t * 256 + ch * 16, gg + off, nb);
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
-        if (tid < 64)
-            beta_bits = __ldg(static_cast<const unsigned short*>(p.beta_raw) +
-                              (size_t)(it.c0 + min(tid, it.Lc - 1)) * H + it.h);
+        if (tid < 64) {
+            const size_t bi = (size_t)(it.c0 + min(tid, it.Lc - 1)) * H + it.h;
+            if constexpr (kF32In)
+                beta_bits = __float_as_uint(__ldg(static_cast<const float*>(p.beta_raw) + bi));
+            else
+                beta_bits = __ldg(static_cast<const unsigned short*>(p.beta_raw) + bi);
+        }
     };
 
     uint32_t beta_bits = 0;
     Item cur = item_at(blockIdx.x / H, (int)(blockIdx.x % H));
+    // raw element (t, ci) of the current item: bf16 from its staged tile, fp32 activations
+    // straight from global memory (rows past the sequence read as 0 either way)
+    auto raw_at = [&](const void* g32, uint32_t tile, int t) -> float {
+        if constexpr (kF32In) {
+            return t < cur.Lc ? __ldg(static_cast<const float*>(g32) + ((size_t)(cur.c0 + t) * H + cur.h) * kD + ci)
+                              : 0.f;
+        } else {
+            return bf16_at(sm, tile + t * 256 + ci * 2);
+        }
+    };
+    // key / query element (t, ci) as the recurrence uses it (q also times scale)
+    auto key_at = [&](int t) {
+        const float x = raw_at(p.k, PR_K, t);
+        return l2 ? x * s_nk[t] : x;
+    };
+    auto query_at = [&](int t) {
+        const float x = raw_at(p.q, PR_Q, t);
+        return l2 ? x * s_nq[t] : x * p.scale;
+    };
     prefetch(cur, beta_bits);
     for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
         const int64_t w_next = w + gridDim.x;
@@ -304,16 +320,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
         uint8_t* blk = ops + ((size_t)cur.c * H + h) * OP_BYTES;
 
         cp_async_wait_all();
-        if (tid < 64) s_beta[tid] = tid < Lc ? beta_act(__uint_as_float(beta_bits << 16), p.flags) : 0.f;
+        if (tid < 64) {
+            const float braw = __uint_as_float(kF32In ? beta_bits : beta_bits << 16);
+            s_beta[tid] = tid < Lc ? beta_act(braw, p.flags) : 0.f;
+        }
         __syncthreads();
         if (l2) {
             // KDA_QK_L2NORM: factors of the key and query rows, a warp per 4 rows
 #pragma unroll
             for (int tt = 0; tt < 4; ++tt) {
                 const int t = 4 * warp + tt;
-                const uint2 kw = *reinterpret_cast<const uint2*>(sm + PR_K + t * 256 + lane * 8);
-                const uint2 qw = *reinterpret_cast<const uint2*>(sm + PR_Q + t * 256 + lane * 8);
-                const float4 kx = State<kStateBF16>::widen(kw), qx = State<kStateBF16>::widen(qw);
+                float4 kx, qx;
+                if constexpr (kF32In) {
+                    kx = qx = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (t < Lc) {
+                        const size_t e = ((size_t)(cur.c0 + t) * H + h) * kD + lane * 4;
+                        kx = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.k) + e));
+                        qx = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + e));
+                    }
+                } else {
+                    kx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + PR_K + t * 256 + lane * 8));
+                    qx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + PR_Q + t * 256 + lane * 8));
+                }
                 float sk = f4_dot(kx, kx), sq = f4_dot(qx, qx);
                 warp_sum2(sk, sq);
                 if (lane == 0) {
@@ -332,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int t = 16 * tq + u;
-                const float x = bf16_at(sm, PR_G + t * 256 + ci * 2);
+                const float x = raw_at(p.gate_raw, PR_G, t);
                 if (t < Lc) {
                     const Decay dc = decay_of(x, p.flags);
                     al[u] = dc.a;
@@ -744,15 +772,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
 // sweep: one (sequence, head) through its chunks, state in TMEM
 
 constexpr uint32_t SW_OPS = 0;                   // operand block image (parts A and B)
-constexpr uint32_t SW_V = SW_OPS + OP_BYTES;     // V, MN-major (two 64-channel TMA boxes), two buffers
+// V, MN-major (two 64-channel boxes, 128-byte swizzled), one buffer: the next chunk's copy is
+// issued only after MMA 3, which ends after this chunk's U~ (the one MMA reading V).  fp32
+// activations use the second 16 KiB for the lo half of V's bf16 split.
+constexpr uint32_t SW_V = SW_OPS + OP_BYTES;
 constexpr uint32_t SW_OST = SW_V + 32768;        // bf16 output rows [64][128], two buffers
 constexpr uint32_t SW_RED = SW_OST + 32768;      // token path: partial row sums [2][4][128] fp32
 constexpr uint32_t SW_MISC = SW_RED + 4096;
 constexpr uint32_t SW_SMEM = SW_MISC + 8192 + 1024;
-// token path (a flagged chunk): raw q, k, g over the part-A region, alpha over part B
+// token path (a flagged chunk): raw q, k (and g for bf16) over the part-A region, alpha over part B
 constexpr uint32_t SW_RAW_Q = SW_OPS, SW_RAW_K = SW_OPS + 16384, SW_RAW_G = SW_OPS + 32768;
+constexpr uint32_t SW_RAW_Q32 = SW_OPS, SW_RAW_K32 = SW_OPS + 32768;  // fp32 rows [t][128]
 constexpr uint32_t SW_ALPHA = SW_OPS + OP_KTP;
 static_assert(SW_RAW_G + 16384 <= SW_OPS + OP_GAM, "raw tiles overlap the flag word");
+static_assert(SW_RAW_K32 + 32768 <= SW_OPS + OP_GAM, "fp32 raw tiles overlap the flag word");
 static_assert(SW_ALPHA + 32768 <= SW_OPS + OP_BYTES, "alpha table overlaps the V buffers");
 static_assert(SW_SMEM <= 232448, "sweep shared memory plan exceeds the per-CTA limit");
 
@@ -767,7 +800,7 @@ constexpr uint32_t TM_COLS = 512;
 constexpr int kIssuerWarp = 16;                  // after the 16 compute warps
 constexpr int kSweepThreads = kThreads + 32;
 
-template <bool kBf16Out>
+template <bool kBf16Out, bool kF32In>
 __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const __grid_constant__ CUtensorMap vmap,
                                                                          const __grid_constant__ CUtensorMap omap,
                                                                          PrefillArgs p, const int32_t* __restrict__ plan,
@@ -850,14 +883,16 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     bool pend_a = false, pend_b = false;  // copies issued, not yet waited on
     const uint32_t na = opa_bytes(kBf16Out), nb = opb_bytes(kBf16Out);
     auto block_of = [&](int jj) { return ops + ((size_t)(cbase + jj) * H + h) * OP_BYTES; };
-    // part A of chunk jj and its V tile (two 64-channel boxes of the tensor map over v,
-    // 128-byte swizzled: the MN-major MMA operand), one barrier
+    // part A of chunk jj and, for bf16 activations, its V tile (two 64-channel boxes of the
+    // tensor map over v, 128-byte swizzled: the MN-major MMA operand), one barrier.  fp32 V is
+    // split into bf16 hi/lo tiles by the compute threads at the chunk's start instead.
     auto load_a = [&](int jj) {
-        mbar_expect_tx(mbar_a, na + 16384u);
+        mbar_expect_tx(mbar_a, na + (kF32In ? 0u : 16384u));
         bulk_load(sb + SW_OPS, block_of(jj), na, mbar_a);
-        const uint32_t vb = sb + SW_V + (uint32_t)(jj & 1) * 16384;
-        tma_load_2d(vb, &vmap, h * kD, t0 + jj * kChunk, mbar_a);
-        tma_load_2d(vb + 8192, &vmap, h * kD + 64, t0 + jj * kChunk, mbar_a);
+        if constexpr (!kF32In) {
+            tma_load_2d(sb + SW_V, &vmap, h * kD, t0 + jj * kChunk, mbar_a);
+            tma_load_2d(sb + SW_V + 8192, &vmap, h * kD + 64, t0 + jj * kChunk, mbar_a);
+        }
     };
     // part B of chunk jj: one bulk copy, or two around the unused P lo tile
     auto load_b = [&](int jj) {
@@ -875,16 +910,25 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         const uint8_t* b2 = block_of(jj);
         bulk_prefetch_l2(b2, opa_bytes(kBf16Out));
         bulk_prefetch_l2(b2 + OP_KTP, OP_BYTES - OP_KTP);
-        tma_prefetch_2d(&vmap, h * kD, t0 + jj * kChunk);
-        tma_prefetch_2d(&vmap, h * kD + 64, t0 + jj * kChunk);
+        if constexpr (!kF32In) {
+            tma_prefetch_2d(&vmap, h * kD, t0 + jj * kChunk);
+            tma_prefetch_2d(&vmap, h * kD + 64, t0 + jj * kChunk);
+        }
     };
-    // U~^T = V^T [T_b hi; T_b lo]^T into [U_a | U_b]
-    auto issue_u_tilde = [&](uint32_t vbuf) {
+    // U~^T = V^T [T_b hi; T_b lo]^T into [U_a | U_b]; fp32 V adds V_lo^T T_b hi^T into U_a
+    auto issue_u_tilde = [&]() {
         const uint32_t idv = idesc_bf16(128, 128, true, false, false);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-            mma(tmem + TM_UA, desc_mn4(sb4 + vbuf / 16, 8192, 1024, s),
+            mma(tmem + TM_UA, desc_mn4(sb4 + SW_V / 16, 8192, 1024, s),
                 desc_k4(sb4 + (SW_OPS + OP_TB) / 16, 128, s), idv, s != 0);
+        if constexpr (kF32In) {
+            const uint32_t idv1 = idesc_bf16(128, 64, true, false, false);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma(tmem + TM_UA, desc_mn4(sb4 + (SW_V + 16384) / 16, 8192, 1024, s),
+                    desc_k4(sb4 + (SW_OPS + OP_TB) / 16, 128, s), idv1, 1u);
+        }
     };
 
     // ---- initial state into TMEM; O columns cleared (MMA 3 accumulates into them)
@@ -960,21 +1004,46 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
             phase_a ^= 1;
             pend_a = false;
         }
-        const uint32_t v_cur = SW_V + (uint32_t)(j & 1) * 16384;
         const bool partial = Lc < kChunk;
+        // V written by the compute threads (fp32 split, or rows past a partial chunk cleared):
+        // U~ then waits for their arrivals on mbar_s1
+        const bool v_by_threads = kF32In || partial;
         // the token path's first barrier decides a timeout for every thread; the chunk path
         // decides at its barrier after MMA 3
         const bool flagged = !timed_out && *reinterpret_cast<const int32_t*>(sm + SW_OPS + OP_FLAG) != 0;
 
         if (!flagged) {
-            if (partial && !timed_out && !issuer) {
+            if constexpr (kF32In) {
+                if (!timed_out && !issuer) {
+                    // fp32 V -> bf16 hi/lo tiles in the TMA box layout (rows past the sequence 0)
+                    const float* gv = static_cast<const float*>(p.v);
+#pragma unroll
+                    for (int e = tid; e < 64 * 16; e += kThreads) {
+                        const int t = e >> 4, g8 = e & 15;
+                        float x[8];
+                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                        if (t < Lc) {
+                            const float4* src = reinterpret_cast<const float4*>(gv + ((size_t)(c0 + t) * H + h) * kD + 8 * g8);
+                            a = __ldg(src);
+                            b = __ldg(src + 1);
+                        }
+                        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+                        uint4 hi, lo;
+                        split8(x, hi, lo);
+                        const uint32_t off = chunk_mn(8 * g8, t, 8192, 1024);
+                        st16(sm, SW_V + off, hi);
+                        st16(sm, SW_V + 16384 + off, lo);
+                    }
+                    fence_async_smem();
+                }
+            } else if (partial && !timed_out && !issuer) {
                 // V rows past the sequence (the next sequence's, or zero-filled past T_tot) -> 0,
-                // so that no other row's values (possibly non-finite) enter this chunk; U~ then
-                // waits for every compute thread's arrival below
+                // so that no other row's values (possibly non-finite) enter this chunk
                 for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
                     const int a = e >> 9, t = (e >> 3) & 63, c16 = e & 7;
                     if (t >= Lc)
-                        st16(sm, v_cur + a * 8192 + (t >> 3) * 1024 + (t & 7) * 128 + c16 * 16,
+                        st16(sm, SW_V + a * 8192 + (t >> 3) * 1024 + (t & 7) * 128 + c16 * 16,
                              make_uint4(0, 0, 0, 0));
                 }
                 fence_async_smem();
@@ -1001,10 +1070,10 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
             //      also S_hi^T QG_lo^T.  U^T = U_a + U_b.  U~ runs first (it needs only this
             //      chunk's operands), then the L2 prefetch two chunks ahead.
             if (lead) {
-                if (!u_early && !partial) issue_u_tilde(v_cur);
+                if (!u_early && !v_by_threads) issue_u_tilde();
                 if (mbar_wait(mbar_s1, ph_s1, kWaitLimit)) {
                     fence_after();
-                    if (partial && !u_early) issue_u_tilde(v_cur);
+                    if (v_by_threads && !u_early) issue_u_tilde();
                     const uint32_t id3 = idesc_bf16(128, 192, false, true, false);
                     const uint32_t id2 = idesc_bf16(128, 128, false, true, false);
 #pragma unroll
@@ -1127,9 +1196,9 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                     commit(mbar_s);
                     // the next chunk's U~ queues behind MMA 4 if its part A and V have already
                     // landed (a full chunk, not flagged); otherwise it is issued at its start
-                    if (more && t1 - (c0 + kChunk) >= kChunk && mbar_test(mbar_a, phase_a) &&
+                    if (!kF32In && more && t1 - (c0 + kChunk) >= kChunk && mbar_test(mbar_a, phase_a) &&
                         *reinterpret_cast<const int32_t*>(sm + SW_OPS + OP_FLAG) == 0) {
-                        issue_u_tilde(SW_V + (uint32_t)((j + 1) & 1) * 16384);
+                        issue_u_tilde();
                         u_early = true;
                     }
                 } else {
@@ -1186,27 +1255,50 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
             }
             if (issuer) store_o_rows();  // the previous chunk's rows, if staged
             {
-                const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
-                const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-                const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.gate_raw);
-                for (int it = tid; it < 64 * 16; it += kSweepThreads) {
-                    const int t = it >> 4, ch = it & 15;
-                    const bool ok = t < Lc;
-                    const size_t e = ok ? ((size_t)(c0 + t) * H + h) * kD + ch * 8 : 0;
-                    const uint32_t nbt = ok ? 16u : 0u;
-                    cp_async16(sb + SW_RAW_Q + t * 256 + ch * 16, gq + e, nbt);
-                    cp_async16(sb + SW_RAW_K + t * 256 + ch * 16, gk + e, nbt);
-                    cp_async16(sb + SW_RAW_G + t * 256 + ch * 16, gg + e, nbt);
+                if constexpr (kF32In) {
+                    const float* gq = static_cast<const float*>(p.q);
+                    const float* gk = static_cast<const float*>(p.k);
+                    for (int it = tid; it < 64 * 32; it += kSweepThreads) {
+                        const int t = it >> 5, ch = it & 31;
+                        const bool ok = t < Lc;
+                        const size_t e = ok ? ((size_t)(c0 + t) * H + h) * kD + ch * 4 : 0;
+                        const uint32_t nbt = ok ? 16u : 0u;
+                        cp_async16(sb + SW_RAW_Q32 + t * 512 + ch * 16, gq + e, nbt);
+                        cp_async16(sb + SW_RAW_K32 + t * 512 + ch * 16, gk + e, nbt);
+                    }
+                } else {
+                    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
+                    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
+                    const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.gate_raw);
+                    for (int it = tid; it < 64 * 16; it += kSweepThreads) {
+                        const int t = it >> 4, ch = it & 15;
+                        const bool ok = t < Lc;
+                        const size_t e = ok ? ((size_t)(c0 + t) * H + h) * kD + ch * 8 : 0;
+                        const uint32_t nbt = ok ? 16u : 0u;
+                        cp_async16(sb + SW_RAW_Q + t * 256 + ch * 16, gq + e, nbt);
+                        cp_async16(sb + SW_RAW_K + t * 256 + ch * 16, gk + e, nbt);
+                        cp_async16(sb + SW_RAW_G + t * 256 + ch * 16, gg + e, nbt);
+                    }
                 }
                 cp_async_commit();
                 if (tid < 64) {
-                    const uint32_t bits = __ldg(static_cast<const unsigned short*>(p.beta_raw) +
-                                                (size_t)(c0 + min(tid, Lc - 1)) * H + h);
-                    s_beta[tid] = tid < Lc ? beta_act(__uint_as_float(bits << 16), p.flags) : 0.f;
+                    const size_t bi = (size_t)(c0 + min(tid, Lc - 1)) * H + h;
+                    const float braw = kF32In ? __ldg(static_cast<const float*>(p.beta_raw) + bi)
+                                              : __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short*>(p.beta_raw) + bi) << 16);
+                    s_beta[tid] = tid < Lc ? beta_act(braw, p.flags) : 0.f;
                 }
                 cp_async_wait_all();
                 __syncthreads();
             }
+            // raw key / query element (t, i) of this chunk, and the raw value (t, c)
+            auto raw_k = [&](int t, int i) {
+                if constexpr (kF32In) return *reinterpret_cast<const float*>(sm + SW_RAW_K32 + t * 512 + i * 4);
+                else return bf16_at(sm, SW_RAW_K + t * 256 + i * 2);
+            };
+            auto raw_q = [&](int t, int i) {
+                if constexpr (kF32In) return *reinterpret_cast<const float*>(sm + SW_RAW_Q32 + t * 512 + i * 4);
+                else return bf16_at(sm, SW_RAW_Q + t * 256 + i * 2);
+            };
             if (!issuer) {
                 // the factors the key / query rows are used with (1 and scale without the flag)
                 const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
@@ -1215,8 +1307,14 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                     const int t = 4 * warp + tt;
                     float fk = 1.f, fq = p.scale;
                     if (l2) {
-                        const float4 kx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + SW_RAW_K + t * 256 + lane * 8));
-                        const float4 qx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + SW_RAW_Q + t * 256 + lane * 8));
+                        float4 kx, qx;
+                        if constexpr (kF32In) {
+                            kx = *reinterpret_cast<const float4*>(sm + SW_RAW_K32 + t * 512 + lane * 16);
+                            qx = *reinterpret_cast<const float4*>(sm + SW_RAW_Q32 + t * 512 + lane * 16);
+                        } else {
+                            kx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + SW_RAW_K + t * 256 + lane * 8));
+                            qx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + SW_RAW_Q + t * 256 + lane * 8));
+                        }
                         float sk = f4_dot(kx, kx), sq = f4_dot(qx, qx);
                         warp_sum2(sk, sq);
                         fk = l2norm_factor(sk);
@@ -1233,7 +1331,13 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int t = 16 * tq + u;
-                    alpha[t * kD + ci] = t < Lc ? alpha_of(bf16_at(sm, SW_RAW_G + t * 256 + ci * 2), p.flags) : 1.f;
+                    float graw = 0.f;
+                    if constexpr (kF32In) {
+                        if (t < Lc) graw = __ldg(static_cast<const float*>(p.gate_raw) + ((size_t)(c0 + t) * H + h) * kD + ci);
+                    } else {
+                        graw = bf16_at(sm, SW_RAW_G + t * 256 + ci * 2);
+                    }
+                    alpha[t * kD + ci] = t < Lc ? alpha_of(graw, p.flags) : 1.f;
                 }
             }
             fence_before();
@@ -1259,27 +1363,31 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                 for (int t = 0; t < Lc; ++t) {
                     float d1 = 0.f;
                     if (!issuer) {
-#pragma unroll
                         const float fk = s_nk[t];
+#pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             const int i = cq * 32 + q;
                             sv[q] *= alpha[t * kD + i];
-                            d1 = fmaf(sv[q], bf16_at(sm, SW_RAW_K + t * 256 + i * 2) * fk, d1);
+                            d1 = fmaf(sv[q], raw_k(t, i) * fk, d1);
                         }
                         red[cq * 128 + c] = d1;
                     }
                     __syncthreads();
                     if (!issuer) {
                         d1 = (red[c] + red[128 + c]) + (red[256 + c] + red[384 + c]);
-                        const float vt = bf16_at(sm, v_cur + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
+                        float vt;
+                        if constexpr (kF32In)
+                            vt = __ldg(static_cast<const float*>(p.v) + ((size_t)(c0 + t) * H + h) * kD + c);
+                        else
+                            vt = bf16_at(sm, SW_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
                         const float uu = s_beta[t] * (vt - d1);
                         float o = 0.f;
-#pragma unroll
                         const float fk = s_nk[t], fq = s_nq[t];
+#pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             const int i = cq * 32 + q;
-                            sv[q] = fmaf(uu, bf16_at(sm, SW_RAW_K + t * 256 + i * 2) * fk, sv[q]);
-                            o = fmaf(sv[q], bf16_at(sm, SW_RAW_Q + t * 256 + i * 2) * fq, o);
+                            sv[q] = fmaf(uu, raw_k(t, i) * fk, sv[q]);
+                            o = fmaf(sv[q], raw_q(t, i) * fq, o);
                         }
                         red[512 + cq * 128 + c] = o;
                     }
@@ -1350,9 +1458,7 @@ int sm_count() {
 
 }  // namespace
 
-bool prefill_2p_supported(const PrefillArgs& p, bool bf16_in) {
-    return bf16_in && p.M <= kTrack2p && p.N <= kMaxOrderN;
-}
+bool prefill_2p_supported(const PrefillArgs& p) { return p.M <= kTrack2p && p.N <= kMaxOrderN; }
 
 size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
     if (N <= 0 || N > kMaxOrderN || T_tot < 0 || H <= 0) return 0;
@@ -1360,15 +1466,29 @@ size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
     return ops_offset(n_max) + (size_t)n_max * (size_t)H * OP_BYTES;
 }
 
-kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_out, void* workspace, cudaStream_t s) {
+namespace {
+
+template <bool kBf16Out, bool kF32In>
+void launch_2p(const CUtensorMap& vmap, const CUtensorMap& omap, const PrefillArgs& p, const int32_t* plan,
+               int64_t n_max, uint8_t* ops, unsigned prep_grid, unsigned units, cudaStream_t s) {
+    cudaFuncSetAttribute(prefill_prep_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
+    cudaFuncSetAttribute(prefill_sweep_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SW_SMEM);
+    if (prep_grid > 0) prefill_prep_kernel<kBf16Out, kF32In><<<prep_grid, kThreads, PR_SMEM, s>>>(p, plan, n_max, ops);
+    prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(vmap, omap, p, plan, n_max, ops);
+}
+
+}  // namespace
+
+kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_in, bool bf16_out, void* workspace, cudaStream_t s) {
     const int64_t n_max = max_chunks(p.T_tot, p.N);
     int32_t* plan = static_cast<int32_t*>(workspace);
     uint8_t* ops = static_cast<uint8_t*>(workspace) + ops_offset(n_max);
-    // v as a 2-D tensor [T_tot rows][H * 128 bf16]: the sweep loads each chunk's V as two
+    // bf16 v as a 2-D tensor [T_tot rows][H * 128]: the sweep loads each chunk's V as two
     // 64-channel x 64-token boxes, 128-byte swizzled (the MN-major MMA operand layout)
     CUtensorMap vmap;
     memset(&vmap, 0, sizeof(vmap));
-    if (p.T_tot > 0) {
+    if (p.T_tot > 0 && bf16_in) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
         if (enc == nullptr) return KDA_ERR_CUDA;
         const cuuint64_t dims[2] = {(cuuint64_t)p.H * kD, (cuuint64_t)p.T_tot};
@@ -1399,17 +1519,14 @@ kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_out, void* workspac
     const int sms = sm_count() > 0 ? sm_count() : 1;
     const unsigned prep_grid = (unsigned)(items < (int64_t)sms ? items : sms);
     const unsigned units = (unsigned)(p.N * p.H);
-    if (bf16_out) {
-        cudaFuncSetAttribute(prefill_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
-        cudaFuncSetAttribute(prefill_sweep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SW_SMEM);
-        if (prep_grid > 0) prefill_prep_kernel<true><<<prep_grid, kThreads, PR_SMEM, s>>>(p, plan, n_max, ops);
-        prefill_sweep_kernel<true><<<units, kSweepThreads, SW_SMEM, s>>>(vmap, omap, p, plan, n_max, ops);
-    } else {
-        cudaFuncSetAttribute(prefill_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
-        cudaFuncSetAttribute(prefill_sweep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SW_SMEM);
-        if (prep_grid > 0) prefill_prep_kernel<false><<<prep_grid, kThreads, PR_SMEM, s>>>(p, plan, n_max, ops);
-        prefill_sweep_kernel<false><<<units, kSweepThreads, SW_SMEM, s>>>(vmap, omap, p, plan, n_max, ops);
-    }
+    if (bf16_in && bf16_out)
+        launch_2p<true, false>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+    else if (bf16_in)
+        launch_2p<false, false>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+    else if (bf16_out)
+        launch_2p<true, true>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+    else
+        launch_2p<false, true>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
     return launch_status();
 }
 

@@ -50,8 +50,8 @@ extern "C" kda_status kda_chunk_prefill(const void* q, const void* k, const void
     const bool bf16_in = in_dtype == KDA_BF16, bf16_out = out_dtype == KDA_BF16;
     const bool chunked = !(flags & KDA_PREFILL_RECURRENT);
     const size_t ws_2p = prefill_2p_workspace(T_tot, N, H);
-    if (chunked && prefill_2p_supported(p, bf16_in) && workspace && ws_2p > 0 && ws_bytes >= ws_2p)
-        return launch_prefill_2p(p, bf16_out, workspace, as_stream(stream));
+    if (chunked && prefill_2p_supported(p) && workspace && ws_2p > 0 && ws_bytes >= ws_2p)
+        return launch_prefill_2p(p, bf16_in, bf16_out, workspace, as_stream(stream));
     if (chunked && prefill_tc_supported(p, bf16_in))
         launch_prefill_tc(p, bf16_out, workspace, ws_bytes, as_stream(stream));
     else

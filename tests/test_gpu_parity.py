@@ -35,7 +35,7 @@ def _status():
 # prefill
 
 
-def run_prefill(kda, c, out_dtype=None, init=True):
+def run_prefill(kda, c, out_dtype=None, init=True, workspace=False):
     dt = c["dtype"]
     odt = out_dtype or (torch.bfloat16 if dt == "bf16" else torch.float32)
     N, H, T = c["N"], c["H"], c["T"]
@@ -44,12 +44,16 @@ def run_prefill(kda, c, out_dtype=None, init=True):
     out = torch.full((max(T, 1), H, 128), float("nan"), dtype=odt, device="cuda")[:T]
     snap = torch.full((N, M, H, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
     st = _status()
+    ws = None
+    if workspace:  # the two-phase chunk path (bf16 or fp32 activations)
+        ws = torch.empty(max(16, kda.kda_chunk_prefill_workspace_size(T, N, H)), dtype=torch.uint8,
+                         device="cuda")
     kda.kda_chunk_prefill(dev_tensor(c["q"], dt), dev_tensor(c["k"], dt), dev_tensor(c["v"], dt),
                           dev_tensor(c["beta"], dt), dev_tensor(c["gate"], dt),
                           i32(c["cu_seqlens"]), out, state_pool=pool,
                           init_slot=i32(c["init_slot"]) if init else None,
                           final_slot=i32(c["final_slot"]), track_chunk_idx=i32(c["track"]),
-                          track_state=snap, dev_status=st)
+                          track_state=snap, dev_status=st, workspace=ws)
     torch.cuda.synchronize()
     return out, pool, snap, int(st.item())
 
@@ -63,12 +67,14 @@ def oracle_prefill(c, init=True):
                           c["cu_seqlens"], S0=S0, track=c["track"])
 
 
+@pytest.mark.parametrize("workspace", [False, True], ids=["no_workspace", "workspace"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_prefill_ragged_small(kda, dtype):
+def test_prefill_ragged_small(kda, dtype, workspace):
+    # without a workspace: single-pass (bf16) or token-serial (f32); with one: two-phase chunks
     lengths = [0, 1, 63, 64, 65, 200, 130]
     track = [[-1, -1], [0, -1], [0, -1], [0, -1], [1, 0], [3, 1], [2, -1]]
     c = W.prefill_case(7, lengths, 3, dtype=dtype, pool_slots=12, track=track)
-    out, pool, snap, st = run_prefill(kda, c)
+    out, pool, snap, st = run_prefill(kda, c, workspace=workspace)
     o_ref, s_ref, snap_ref, st_ref = oracle_prefill(c)
     assert st == 0 and st_ref == 0
     assert rel_l2(to_np(out), o_ref) < tol_out(dtype)

@@ -2,8 +2,9 @@
 sequential sweep per (sequence, head)), selected by a workspace of at least
 kda_chunk_prefill_workspace_size bytes: parity with the fp64 oracle over ragged
 lengths, the token path of chunks whose decay leaves the tensor-core range, fp32
-outputs, 16-bit state pools, the activation flags, snapshot placement, and
-agreement with the single-pass kernel."""
+outputs, fp32 activations (the chunk algorithm with fp32 inputs split into bf16
+hi/lo operands), 16-bit state pools, the activation flags, snapshot placement,
+and agreement with the single-pass and token-serial kernels."""
 import numpy as np
 import pytest
 
@@ -184,3 +185,76 @@ def test_16bit_state_pool(kda, st_flag):
     assert rel_l2(pool.float().cpu().numpy()[c["final_slot"]], s_ref) < u + TOL_STATE
     valid = c["track"] >= 0
     assert rel_l2(snap.float().cpu().numpy()[valid], snap_ref[valid]) < u + TOL_STATE
+
+
+# ---- fp32 activations: the same two kernels, the operands split from fp32 inputs
+
+
+def test_fp32_activations_ragged_and_snapshots(kda):
+    lengths = [0, 1, 63, 64, 65, 200, 130, 700]
+    c = W.prefill_case(70, lengths, 3, dtype="f32", pool_slots=16, track_per_seq=2)
+    check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
+
+
+def test_fp32_activations_bf16_output(kda):
+    c = W.prefill_case(71, [300, 77, 64], 2, dtype="f32", pool_slots=6, track_per_seq=1)
+    check(c, run(kda, c, out_dtype=torch.bfloat16))
+
+
+def test_fp32_activations_strong_decay_token_path(kda):
+    c = W.prefill_case(72, [256, 100], 2, dtype="f32", pool_slots=4, track_per_seq=2)
+    g = c["gate"].copy()
+    g[10:14] = 30.0        # chunk 0 of sequence 0, both heads
+    g[200:203, 1] = 45.0   # chunk 3 of sequence 0, head 1 only
+    g[300:302, 0] = 60.0   # the last (partial) chunk of sequence 1, head 0
+    c["gate"] = g
+    check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
+
+
+@pytest.mark.parametrize("flags", [1, 2])
+def test_fp32_activations_preactivated_flags(kda, flags):
+    c = W.prefill_case(73, [150, 64], 2, dtype="f32", pool_slots=4)
+    if flags & 1:
+        c["gate"] = (-np.abs(c["gate"]) * 0.5).astype(np.float32)
+    if flags & 2:
+        c["beta"] = (1.0 / (1.0 + np.exp(-c["beta"]))).astype(np.float32)
+    check(c, run(kda, c, flags=flags, out_dtype=torch.float32), flags=flags, tol_o=TOL_STATE)
+
+
+def test_fp32_activations_agree_with_token_serial(kda):
+    # no workspace: fp32 activations run the token-serial kernel, the recurrence itself
+    c = W.prefill_case(74, [500, 64, 3], 2, dtype="f32", pool_slots=6, track_per_seq=2)
+    a = check(c, run(kda, c, two_phase=True, out_dtype=torch.float32), tol_o=TOL_STATE)
+    b = check(c, run(kda, c, two_phase=False, out_dtype=torch.float32), tol_o=TOL_STATE)
+    assert rel_l2(a[0], b[0]) < TOL_STATE and rel_l2(a[1], b[1]) < TOL_STATE
+
+
+def test_fp32_activations_l2norm(kda):
+    c = W.prefill_case(75, [300, 1, 64, 190], 3, dtype="f32", pool_slots=8, track_per_seq=2)
+    rng = np.random.default_rng(75)
+    for name in ("q", "k"):
+        c[name] = (c[name] * rng.uniform(0.3, 4.0, c[name].shape[:-1] + (1,))).astype(np.float32)
+    c["gate"][40:43, 1] = 40.0  # a chunk of head 1 that runs token by token
+    flags = kda.KDA_QK_L2NORM
+    N, H, T = c["N"], c["H"], c["T"]
+    M = c["track"].shape[1]
+    pool = torch.from_numpy(c["pool"]).cuda()
+    out = torch.empty(T, H, 128, dtype=torch.float32, device="cuda")
+    snap = torch.full((N, M, H, 128, 128), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, N, H), dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prefill(*(dev_tensor(c[n], "f32") for n in ("q", "k", "v", "beta", "gate")),
+                          i32(c["cu_seqlens"]), out, state_pool=pool, init_slot=i32(c["init_slot"]),
+                          final_slot=i32(c["final_slot"]), track_chunk_idx=i32(c["track"]),
+                          track_state=snap, dev_status=st, workspace=ws, flags=flags, scale=0.7)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    S0 = c["pool"][c["init_slot"]].astype(np.float64)
+    wid = lambda n: c[n].astype(np.float64)  # noqa: E731
+    o_ref, s_ref, snap_ref, _ = oracle.prefill(wid("q"), wid("k"), wid("v"), wid("beta"), wid("gate"),
+                                               c["cu_seqlens"], S0=S0, track=c["track"],
+                                               flags=oracle.QK_L2NORM, scale=0.7)
+    valid = c["track"] >= 0
+    assert worst_seq_head(to_np(out), o_ref, c["cu_seqlens"]) < TOL_STATE
+    assert worst_state(pool.cpu().numpy()[c["final_slot"]], s_ref) < TOL_STATE
+    assert worst_state(snap.cpu().numpy()[valid], snap_ref[valid]) < TOL_STATE
