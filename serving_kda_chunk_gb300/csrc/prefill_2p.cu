@@ -203,7 +203,10 @@ static_assert(PR_SMEM <= 232448, "prep shared memory plan exceeds the per-CTA li
 constexpr uint32_t PT_AP = 0, PT_W = 128, PT_KG_HI = 192, PT_KG_LO = 224, PT_COLS = 256;
 
 template <bool kBf16Out, bool kF32In>
-__global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p, const int32_t* __restrict__ plan,
+__global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                                   const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap gmap,
+                                                                   PrefillArgs p, const int32_t* __restrict__ plan,
                                                                    int64_t n_max, uint8_t* __restrict__ ops) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     float* s_nq = s_nk + 64;                                 // 64: of the query rows (x scale)
     float* s_seg_a = s_nq + 64;                              // [4][128]: prod of alpha per token quarter
     float* s_seg_i = s_seg_a + 512;                          // [4][128]: prod of 1/alpha per quarter
-    uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_seg_i + 512);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 1);
+    uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_seg_i + 512);  // MMA, raw tiles
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -230,18 +233,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
 
     if (warp == 0) tmem_alloc(smem_u32(s_tmem), PT_COLS);
-    if (tid == 0) mbar_init(smem_u32(s_mbar), 1);
+    if (tid == 0) {
+        mbar_init(smem_u32(s_mbar), 1);
+        mbar_init(smem_u32(s_mbar + 1), 1);
+    }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t mbar = smem_u32(s_mbar);
-    uint32_t phase = 0;
+    const uint32_t mbar = smem_u32(s_mbar), mbar_raw = smem_u32(s_mbar + 1);
+    uint32_t phase = 0, phase_raw = 0;
+    bool raw_pending = false;  // a raw-tile copy issued and not yet waited on (every thread tracks it)
     bool timed_out = false;
-    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
-    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-    const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.gate_raw);
 
     struct Item {
         int64_t c;
@@ -260,20 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     // item w is (chunk w / H, head w % H); consecutive items of this CTA are gridDim.x apart
     const int64_t step_c = gridDim.x / H;
     const int step_h = (int)(gridDim.x - step_c * H);
-    // raw q, k, g tiles of an item (bf16: rows past the sequence zero-filled); its raw beta bits
+    // raw q, k, g tiles of an item (bf16: three 128-channel x 64-token tensor-map boxes, rows
+    // past the sequence cleared once they land); its raw beta bits.  Called by every thread
+    // once every thread is past its reads of the tiles.
     auto prefetch = [&](const Item& it, uint32_t& beta_bits) {
         if constexpr (!kF32In) {
-#pragma unroll
-            for (int e = tid; e < 64 * 16; e += kThreads) {
-                const int t = e >> 4, ch = e & 15;
-                const bool ok = t < it.Lc;
-                const size_t off = ok ? ((size_t)(it.c0 + t) * H + it.h) * kD + ch * 8 : 0;
-                const uint32_t nb = ok ? 16u : 0u;
-                cp_async16(sb + PR_Q + t * 256 + ch * 16, gq + off, nb);
-                cp_async16(sb + PR_K + t * 256 + ch * 16, gk + off, nb);
-                cp_async16(sb + PR_G + t * 256 + ch * 16, gg + off, nb);
+            if (tid == 0) {
+                fence_async_smem();
+                mbar_expect_tx(mbar_raw, 3u * 16384u);
+                tma_load_2d(sb + PR_Q, &qmap, it.h * kD, it.c0, mbar_raw);
+                tma_load_2d(sb + PR_K, &kmap, it.h * kD, it.c0, mbar_raw);
+                tma_load_2d(sb + PR_G, &gmap, it.h * kD, it.c0, mbar_raw);
             }
-            cp_async_commit();
+            raw_pending = true;
         }
         if (tid < 64) {
             const size_t bi = (size_t)(it.c0 + min(tid, it.Lc - 1)) * H + it.h;
@@ -286,6 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
 
     uint32_t beta_bits = 0;
     Item cur = item_at(blockIdx.x / H, (int)(blockIdx.x % H));
+    // the item gridDim.x after `it`
+    auto next_of = [&](const Item& it) {
+        int64_t c2 = it.c + step_c;
+        int h2 = it.h + step_h;
+        if (h2 >= H) {
+            h2 -= H;
+            ++c2;
+        }
+        return item_at(c2, h2);
+    };
     // raw element (t, ci) of the current item: bf16 from its staged tile, fp32 activations
     // straight from global memory (rows past the sequence read as 0 either way)
     auto raw_at = [&](const void* g32, uint32_t tile, int t) -> float {
@@ -309,17 +322,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
     for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
         const int64_t w_next = w + gridDim.x;
         const bool has_next = w_next < items;
-        int64_t nc = cur.c + step_c;
-        int nh = cur.h + step_h;
-        if (nh >= H) {
-            nh -= H;
-            ++nc;
-        }
-        const Item nxt = has_next ? item_at(nc, nh) : cur;
+        const bool has_next2 = w_next + gridDim.x < items;
+        const Item nxt = has_next ? next_of(cur) : cur;
+        // the item after it, for the L2 prefetch: its 8-byte load is issued here, used much later
+        const Item nxt2 = has_next2 ? next_of(nxt) : nxt;
         const int Lc = cur.Lc, h = cur.h;
         uint8_t* blk = ops + ((size_t)cur.c * H + h) * OP_BYTES;
 
-        cp_async_wait_all();
+        if constexpr (!kF32In) {
+            const bool okr = mbar_wait(mbar_raw, phase_raw, kWaitLimit);
+            phase_raw ^= 1;
+            raw_pending = false;
+            if (__syncthreads_or(!okr)) {
+                timed_out = true;
+                break;
+            }
+            if (Lc < kChunk) {
+                // rows past the sequence (the next one's, or zero-filled past T_tot) -> 0, so that
+                // no other row's values (possibly non-finite) enter this chunk
+                for (int e = tid; e < 2 * 64 * 16; e += kThreads) {
+                    const int t = (e >> 4) & 63, ch = e & 15;
+                    if (t >= Lc) st16(sm, (e >> 10 ? PR_K : PR_Q) + t * 256 + ch * 16, make_uint4(0, 0, 0, 0));
+                }
+            }
+        }
         if (tid < 64) {
             const float braw = __uint_as_float(kF32In ? beta_bits : beta_bits << 16);
             s_beta[tid] = tid < Lc ? beta_act(braw, p.flags) : 0.f;
@@ -537,8 +563,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
                 break;
             }
         }
-        // every raw read of this item is done: the next item's tiles may land
+        // every raw read of this item is done: the next item's tiles may land, and the one after
+        // it is pulled into L2
         if (has_next) prefetch(nxt, beta_bits);
+        if constexpr (!kF32In) {
+            if (tid == 0 && has_next2) {
+                tma_prefetch_2d(&qmap, nxt2.h * kD, nxt2.c0);
+                tma_prefetch_2d(&kmap, nxt2.h * kD, nxt2.c0);
+                tma_prefetch_2d(&gmap, nxt2.h * kD, nxt2.c0);
+            }
+        }
 
         // ---- A -> N = Diag(beta) A (strict lower, stored transposed: Nt[s][t] = N[t][s]),
         //      P -> bf16 operand (lower incl. diagonal)
@@ -755,12 +789,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(PrefillArgs p
         }
         cur = nxt;
     }
-    cp_async_wait_all();
     if (tid == 0) bulk_wait_all();  // the image stores have read shared memory and landed
     timed_out = __syncthreads_or(timed_out);
     if (timed_out) {
         if (tid == 0) report(p.dev_status, KDA_DEV_TIMEOUT);
         mbar_wait(mbar, phase ^ 1u, kWaitLimit);  // the phase that timed out, bounded
+        if (raw_pending) mbar_wait(mbar_raw, phase_raw, kWaitLimit);
+        mbar_wait(mbar_raw, phase_raw ^ 1u, kWaitLimit);
     }
     fence_before();
     __syncthreads();
@@ -1468,13 +1503,19 @@ size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
 
 namespace {
 
+struct RawMaps {
+    CUtensorMap q, k, g, v;
+};
+
 template <bool kBf16Out, bool kF32In>
-void launch_2p(const CUtensorMap& vmap, const CUtensorMap& omap, const PrefillArgs& p, const int32_t* plan,
-               int64_t n_max, uint8_t* ops, unsigned prep_grid, unsigned units, cudaStream_t s) {
+void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, const int32_t* plan, int64_t n_max,
+               uint8_t* ops, unsigned prep_grid, unsigned units, cudaStream_t s) {
     cudaFuncSetAttribute(prefill_prep_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
     cudaFuncSetAttribute(prefill_sweep_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          SW_SMEM);
-    if (prep_grid > 0) prefill_prep_kernel<kBf16Out, kF32In><<<prep_grid, kThreads, PR_SMEM, s>>>(p, plan, n_max, ops);
+    if (prep_grid > 0)
+        prefill_prep_kernel<kBf16Out, kF32In><<<prep_grid, kThreads, PR_SMEM, s>>>(m.q, m.k, m.g, p, plan, n_max, ops);
+    const CUtensorMap& vmap = m.v;
     prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(vmap, omap, p, plan, n_max, ops);
 }
 
@@ -1484,18 +1525,28 @@ kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_in, bool bf16_out, 
     const int64_t n_max = max_chunks(p.T_tot, p.N);
     int32_t* plan = static_cast<int32_t*>(workspace);
     uint8_t* ops = static_cast<uint8_t*>(workspace) + ops_offset(n_max);
-    // bf16 v as a 2-D tensor [T_tot rows][H * 128]: the sweep loads each chunk's V as two
-    // 64-channel x 64-token boxes, 128-byte swizzled (the MN-major MMA operand layout)
-    CUtensorMap vmap;
-    memset(&vmap, 0, sizeof(vmap));
+    // bf16 activations as 2-D tensors [T_tot rows][H * 128]: the prep loads a (chunk, head)'s
+    // raw q, k, g as one 128-channel x 64-token box each (row-major, unswizzled); the sweep loads
+    // its V as two 64-channel x 64-token boxes, 128-byte swizzled (the MN-major MMA operand
+    // layout).  Rows past T_tot read as zero.
+    RawMaps maps;
+    memset(&maps, 0, sizeof(maps));
     if (p.T_tot > 0 && bf16_in) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
         if (enc == nullptr) return KDA_ERR_CUDA;
         const cuuint64_t dims[2] = {(cuuint64_t)p.H * kD, (cuuint64_t)p.T_tot};
         const cuuint64_t strides[1] = {(cuuint64_t)p.H * kD * 2};
-        const cuuint32_t box[2] = {64, 64};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.v), dims, strides, box, estr,
+        const cuuint32_t box_raw[2] = {128, 64};
+        const void* raw[3] = {p.q, p.k, p.gate_raw};
+        CUtensorMap* dst[3] = {&maps.q, &maps.k, &maps.g};
+        for (int i = 0; i < 3; ++i)
+            if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(raw[i]), dims, strides, box_raw,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return KDA_ERR_CUDA;
+        const cuuint32_t box[2] = {64, 64};
+        if (enc(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.v), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return KDA_ERR_CUDA;
@@ -1520,13 +1571,13 @@ kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_in, bool bf16_out, 
     const unsigned prep_grid = (unsigned)(items < (int64_t)sms ? items : sms);
     const unsigned units = (unsigned)(p.N * p.H);
     if (bf16_in && bf16_out)
-        launch_2p<true, false>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<true, false>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
     else if (bf16_in)
-        launch_2p<false, false>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<false, false>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
     else if (bf16_out)
-        launch_2p<true, true>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<true, true>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
     else
-        launch_2p<false, true>(vmap, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<false, true>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
     return launch_status();
 }
 
