@@ -613,7 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         }
         __syncthreads();
         // ---- T = (I + N)^-1 (unit lower triangular): 16x16 diagonal blocks by forward
-        //      substitution, then the off-diagonal blocks by block substitution
+        //      substitution, then the off-diagonal blocks by block substitution, level by level
+        //      (16 -> 32 -> 64).  The level products split their sums over 2-4 threads (shuffle
+        //      reductions), and the last one writes T_b = T Diag(beta) as the bf16 hi/lo operand.
+        //      Only entries on or below the diagonal of T are read: the 16x16 blocks above the
+        //      diagonal are never written.
         {
             const float* Nt = reinterpret_cast<const float*>(sm + PR_N);
             float* Tm = reinterpret_cast<float*>(sm + PR_T);
@@ -641,11 +645,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Tm[(o + r) * NLD + o + jc] = x[r];
-            } else if (tid < 64 + 256) {
-                // the blocks above the diagonal pairs, (0,1) and (2,3), are zero
-                const int e = tid - 64, r = e >> 4, c = e & 15;
-                Tm[r * NLD + 16 + c] = 0.f;
-                Tm[(32 + r) * NLD + 48 + c] = 0.f;
             }
             __syncthreads();
             // level 1: T[a][a-1] = -T_aa N[a][a-1] T_{a-1,a-1}, a in {1, 3}; a thread owns
@@ -656,9 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
             if (tid < 128) {
                 float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float nv = Nt[(ob + s) * NLD + oa + r1];
-                    const float4 tv = *reinterpret_cast<const float4*>(&Tm[(ob + s) * NLD + ob + c1]);
+                for (int u = 0; u < 16; ++u) {
+                    const float nv = Nt[(ob + u) * NLD + oa + r1];
+                    const float4 tv = *reinterpret_cast<const float4*>(&Tm[(ob + u) * NLD + ob + c1]);
                     y.x = fmaf(nv, tv.x, y.x);
                     y.y = fmaf(nv, tv.y, y.y);
                     y.z = fmaf(nv, tv.z, y.z);
@@ -668,67 +667,91 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
             }
             __syncthreads();
             if (tid < 128) {
+                // T_aa is lower triangular: terms s > r1 are zero (and read as zero)
                 float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float tv = Tm[(oa + r1) * NLD + oa + s];
-                    const float4 yv = *reinterpret_cast<const float4*>(&Y1[(w1 * 16 + s) * 20 + c1]);
+                for (int s2 = 0; s2 < 16; ++s2) {
+                    const float tv = Tm[(oa + r1) * NLD + oa + s2];
+                    const float4 yv = *reinterpret_cast<const float4*>(&Y1[(w1 * 16 + s2) * 20 + c1]);
                     z.x = fmaf(tv, yv.x, z.x);
                     z.y = fmaf(tv, yv.y, z.y);
                     z.z = fmaf(tv, yv.z, z.z);
                     z.w = fmaf(tv, yv.w, z.w);
                 }
-                *reinterpret_cast<float4*>(&Tm[(oa + r1) * NLD + ob + c1]) =
-                    make_float4(-z.x, -z.y, -z.z, -z.w);
+                *reinterpret_cast<float4*>(&Tm[(oa + r1) * NLD + ob + c1]) = make_float4(-z.x, -z.y, -z.z, -z.w);
             }
             __syncthreads();
-            // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]).
-            // First product: warp = 4-column group c2, lane = row; T[0:32, 0:32] is lower
-            // triangular, so the sum starts at u = c2.
+            // level 2, first product: Y2 = N[32:64, 0:32] T[0:32, 0:32].  Warp = (4-column group
+            // c2, half of the rows); lane = (row, parity of the sum), the parities meet by shuffle.
+            // T[u][c] is zero for u < c, so the sum starts at c2.
             float* Y2 = reinterpret_cast<float*>(sm + PR_Y2);  // [32][36]
-            if (tid < 256) {
-                const int c2 = 4 * warp;
+            {
+                const int c2 = 4 * (warp & 7), r2 = 16 * (warp >> 3) + (lane & 15), par = lane >> 4;
                 float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-                for (int u = c2; u < 32; ++u) {
-                    const float nv = Nt[u * NLD + 32 + lane];
+                for (int u = c2 + par; u < 32; u += 2) {
+                    const float nv = Nt[u * NLD + 32 + r2];
                     const float4 tv = *reinterpret_cast<const float4*>(&Tm[u * NLD + c2]);
                     y.x = fmaf(nv, tv.x, y.x);
                     y.y = fmaf(nv, tv.y, y.y);
                     y.z = fmaf(nv, tv.z, y.z);
                     y.w = fmaf(nv, tv.w, y.w);
                 }
-                *reinterpret_cast<float4*>(&Y2[lane * 36 + c2]) = y;
+                y.x += __shfl_xor_sync(0xffffffffu, y.x, 16);
+                y.y += __shfl_xor_sync(0xffffffffu, y.y, 16);
+                y.z += __shfl_xor_sync(0xffffffffu, y.z, 16);
+                y.w += __shfl_xor_sync(0xffffffffu, y.w, 16);
+                if (par == 0) *reinterpret_cast<float4*>(&Y2[r2 * 36 + c2]) = y;
             }
             __syncthreads();
-            if (tid < 256) {
-                const int r = tid >> 3, c = (tid & 7) * 4;
+            // level 2, second product, and T_b = T Diag(beta) -> bf16 hi/lo operand [t][s].
+            // Thread = (row pair t_lo / 32 + t_lo, column quad c4 of 16).  Rows 0-31 and the
+            // quads right of column 32 are copies of T (zero above the diagonal); the quads
+            // of T[32:64, 0:32] = -T[32:64, 32:64] Y2 split their sum between lanes c4 and
+            // c4 + 8 (even / odd terms).
+            {
+                const int c4 = tid & 15, t_lo = tid >> 4;
+                auto emit = [&](int t, float4 x) {
+                    const int s0 = 4 * c4;
+                    x.x *= s_beta[s0];
+                    x.y *= s_beta[s0 + 1];
+                    x.z *= s_beta[s0 + 2];
+                    x.w *= s_beta[s0 + 3];
+                    uint2 hi, lo;
+                    split2(x.x, x.y, hi.x, lo.x);
+                    split2(x.z, x.w, hi.y, lo.y);
+                    const uint32_t off = PR_IMG + OP_TB + chunk_k(t, s0 & ~7, 64) + (s0 & 4) * 2;
+                    *reinterpret_cast<uint2*>(sm + off) = hi;
+                    *reinterpret_cast<uint2*>(sm + off + 8192) = lo;
+                };
+                auto copy_of = [&](int t) {  // T[t][4 c4 .. 4 c4 + 3], zero above the diagonal
+                    const int s0 = 4 * c4;
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (s0 <= t) {
+                        x = *reinterpret_cast<const float4*>(&Tm[t * NLD + s0]);
+                        if (s0 + 1 > t) x.y = 0.f;
+                        if (s0 + 2 > t) x.z = 0.f;
+                        if (s0 + 3 > t) x.w = 0.f;
+                    }
+                    return x;
+                };
+                emit(t_lo, (t_lo < 32 && c4 < 8) ? copy_of(t_lo) : make_float4(0.f, 0.f, 0.f, 0.f));
+                const int t = 32 + t_lo, cq2 = c4 & 7;
                 float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int s = 0; s < 32; ++s) {
-                    const float tv = Tm[(32 + r) * NLD + 32 + s];
-                    const float4 yv = *reinterpret_cast<const float4*>(&Y2[s * 36 + c]);
+#pragma unroll 4
+                for (int s2 = c4 >> 3; s2 <= t_lo; s2 += 2) {
+                    const float tv = Tm[t * NLD + 32 + s2];
+                    const float4 yv = *reinterpret_cast<const float4*>(&Y2[s2 * 36 + 4 * cq2]);
                     z.x = fmaf(tv, yv.x, z.x);
                     z.y = fmaf(tv, yv.y, z.y);
                     z.z = fmaf(tv, yv.z, z.z);
                     z.w = fmaf(tv, yv.w, z.w);
                 }
-                *reinterpret_cast<float4*>(&Tm[(32 + r) * NLD + c]) = make_float4(-z.x, -z.y, -z.z, -z.w);
-            }
-            __syncthreads();
-            // T_b = T Diag(beta) -> bf16 hi/lo operand [t][s] (lower triangle only)
-            {
-                const int t = tid >> 3, s0 = (tid & 7) * 8;
-                float x[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int s = s0 + q;
-                    x[q] = s <= t ? Tm[t * NLD + s] * s_beta[s] : 0.f;
-                }
-                uint4 hi, lo;
-                split8(x, hi, lo);
-                st16(sm, PR_IMG + OP_TB + chunk_k(t, s0, 64), hi);
-                st16(sm, PR_IMG + OP_TB + 8192 + chunk_k(t, s0, 64), lo);
+                z.x += __shfl_xor_sync(0xffffffffu, z.x, 8);
+                z.y += __shfl_xor_sync(0xffffffffu, z.y, 8);
+                z.z += __shfl_xor_sync(0xffffffffu, z.z, 8);
+                z.w += __shfl_xor_sync(0xffffffffu, z.w, 8);
+                emit(t, c4 < 8 ? make_float4(-z.x, -z.y, -z.z, -z.w) : copy_of(t));
             }
         }
         fence_async_smem();  // the image tiles are read by MMA 2 and the bulk store
