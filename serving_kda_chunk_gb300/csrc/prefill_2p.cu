@@ -344,13 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                     const int t = (e >> 4) & 63, ch = e & 15;
                     if (t >= Lc) st16(sm, (e >> 10 ? PR_K : PR_Q) + t * 256 + ch * 16, make_uint4(0, 0, 0, 0));
                 }
+                __syncthreads();
             }
         }
+        // beta is first read after the channel pass's barrier
         if (tid < 64) {
             const float braw = __uint_as_float(kF32In ? beta_bits : beta_bits << 16);
             s_beta[tid] = tid < Lc ? beta_act(braw, p.flags) : 0.f;
         }
-        __syncthreads();
         if (l2) {
             // KDA_QK_L2NORM: factors of the key and query rows, a warp per 4 rows
 #pragma unroll
