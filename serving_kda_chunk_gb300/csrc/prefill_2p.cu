@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
     const int cq = warp >> 2;      // column quarter this warp takes in TMEM passes
     const int row = quarter * 32 + lane;
     const int ci = tid & 127, tq = tid >> 7;  // channel passes: key channel, token quarter
+    const bool store_lane = lane == 0 && warp >= 7 && warp <= 9;  // issue the image's bulk stores
     const int H = p.H;
     const int64_t n_chunks_all = min((int64_t)plan[PL_META / 4], n_max);
     const int64_t items = n_chunks_all * H;
@@ -269,12 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
     // once every thread is past its reads of the tiles.
     auto prefetch = [&](const Item& it, uint32_t& beta_bits) {
         if constexpr (!kF32In) {
-            if (tid == 0) {
+            // one copy per issuing thread, in three warps (a copy that lands before the expected
+            // byte count is posted only takes the count below zero while the arrival is pending)
+            if (lane == 0 && warp >= 1 && warp <= 3) {
                 fence_async_smem();
-                mbar_expect_tx(mbar_raw, 3u * 16384u);
-                tma_load_2d(sb + PR_Q, &qmap, it.h * kD, it.c0, mbar_raw);
-                tma_load_2d(sb + PR_K, &kmap, it.h * kD, it.c0, mbar_raw);
-                tma_load_2d(sb + PR_G, &gmap, it.h * kD, it.c0, mbar_raw);
+                if (warp == 1) mbar_expect_tx(mbar_raw, 3u * 16384u);
+                tma_load_2d(sb + (warp == 1 ? PR_Q : warp == 2 ? PR_K : PR_G),
+                            warp == 1 ? &qmap : warp == 2 ? &kmap : &gmap, it.h * kD, it.c0, mbar_raw);
             }
             raw_pending = true;
         }
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
         if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
         if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
-        if (tid == 0) bulk_wait_read_all();  // the previous item's image has left shared memory
+        if (store_lane) bulk_wait_read_all();  // the previous item's image has left shared memory
         if (__syncthreads_or(bad)) {
             // the sweep evaluates this chunk token by token from the raw inputs
             if (tid == 0) *reinterpret_cast<int32_t*>(blk + OP_FLAG) = 1;
@@ -568,11 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         // it is pulled into L2
         if (has_next) prefetch(nxt, beta_bits);
         if constexpr (!kF32In) {
-            if (tid == 0 && has_next2) {
-                tma_prefetch_2d(&qmap, nxt2.h * kD, nxt2.c0);
-                tma_prefetch_2d(&kmap, nxt2.h * kD, nxt2.c0);
-                tma_prefetch_2d(&gmap, nxt2.h * kD, nxt2.c0);
-            }
+            if (lane == 0 && warp >= 4 && warp <= 6 && has_next2)
+                tma_prefetch_2d(warp == 4 ? &qmap : warp == 5 ? &kmap : &gmap, nxt2.h * kD, nxt2.c0);
         }
 
         // ---- A -> N = Diag(beta) A (strict lower, stored transposed: Nt[s][t] = N[t][s]),
@@ -800,20 +799,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         fence_before();
         __syncthreads();
         fence_after();
-        // ---- the block image -> the workspace, by bulk copies the next item does not wait for
-        if (tid == 0) {
-            bulk_store(blk, sb + PR_IMG, opa_bytes(kBf16Out));
-            if constexpr (kBf16Out) {
-                bulk_store(blk + OP_KTP, sb + PR_IMG + OP_KTP, OPB1_BYTES_BF16);
-                bulk_store(blk + OP_KTLO, sb + PR_IMG + OP_KTLO, OPB2_BYTES_BF16);
+        // ---- the block image -> the workspace, by bulk copies the next item does not wait for,
+        //      one per issuing thread (lane 0 of warps 7-9), each in its own bulk group
+        if (store_lane) {
+            if (warp == 7) {
+                bulk_store(blk, sb + PR_IMG, opa_bytes(kBf16Out));
+            } else if constexpr (kBf16Out) {
+                if (warp == 8) bulk_store(blk + OP_KTP, sb + PR_IMG + OP_KTP, OPB1_BYTES_BF16);
+                else bulk_store(blk + OP_KTLO, sb + PR_IMG + OP_KTLO, OPB2_BYTES_BF16);
             } else {
-                bulk_store(blk + OP_KTP, sb + PR_IMG + OP_KTP, OP_BYTES - OP_KTP);
+                if (warp == 8) bulk_store(blk + OP_KTP, sb + PR_IMG + OP_KTP, OP_BYTES - OP_KTP);
             }
             bulk_commit();
         }
         cur = nxt;
     }
-    if (tid == 0) bulk_wait_all();  // the image stores have read shared memory and landed
+    if (store_lane) bulk_wait_all();  // the image stores have read shared memory and landed
     timed_out = __syncthreads_or(timed_out);
     if (timed_out) {
         if (tid == 0) report(p.dev_status, KDA_DEV_TIMEOUT);
