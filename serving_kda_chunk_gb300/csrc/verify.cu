@@ -289,19 +289,10 @@ __global__ void __launch_bounds__(kVThreads, 2)
         const int ql = meta[it].y;
         int r, h;
         unit_rh(it, r, h);
-        // ---- this unit's checkpoint (thread 0 polls) and token rows
+        // ---- this unit's token rows (its checkpoint is waited for after the channel work below,
+        //      which does not read it)
         cp_async_wait_all();
-        if (raw_pend) {
-            if (tid == 0 && !mbar_wait(smem_u32(mbars), ph_raw, kVWaitLimit)) timed_out = true;
-            ph_raw ^= 1u;
-            raw_pend = false;
-        }
-        fence_before();
-        if (__syncthreads_or(timed_out)) {
-            timed_out = true;
-            break;
-        }
-        fence_after();
+        __syncthreads();
         if (tid < KC) {
             float bv = 0.f;
             if (tid < ql) {
@@ -333,12 +324,6 @@ __global__ void __launch_bounds__(kVThreads, 2)
                     nrm[KC + t] = l2norm_factor(sq);
                 }
             }
-        }
-        // ---- checkpoint rows -> TMEM operand (all warps, 64 columns each)
-        if (ql > 0) {
-            convert(2 * colhalf);
-            convert(2 * colhalf + 1);
-            wait_st();
         }
         if (l2) __syncthreads();  // the factors above, for every channel thread below
         // ---- channel i: gates; warps 0-3 the gated keys / queries and the key / raw gate
@@ -516,15 +501,31 @@ __global__ void __launch_bounds__(kVThreads, 2)
                 }
             }
         }
+        // ---- this unit's checkpoint (every thread waits on its barrier) -> TMEM operand (all
+        //      warps, 64 columns each)
+        if (raw_pend) {
+            if (!mbar_wait(smem_u32(mbars), ph_raw, kVWaitLimit)) timed_out = true;
+            ph_raw ^= 1u;
+            raw_pend = false;
+        }
+        if (ql > 0 && !timed_out) {
+            convert(2 * colhalf);
+            convert(2 * colhalf + 1);
+            wait_st();
+        }
         fence_async_smem();
         fence_before();
-        __syncthreads();
+        if (__syncthreads_or(timed_out)) {
+            timed_out = true;
+            break;
+        }
         fence_after();
-        // ---- the next unit's checkpoint (RAW has been converted) and token rows, then this
-        //      unit's MMAs: D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
+        // ---- the next unit's checkpoint (RAW has been converted; requested by warp 1, so that
+        //      thread 0 goes straight to the MMAs) and token rows, then this unit's MMAs:
+        //      D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
         if (it + 1 < nu) {
             if (meta[it + 1].y > 0) {
-                if (tid == 0) request_ckpt(it + 1);
+                if (tid == 32) request_ckpt(it + 1);
                 raw_pend = true;
             }
         }
