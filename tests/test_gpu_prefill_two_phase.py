@@ -258,3 +258,32 @@ def test_fp32_activations_l2norm(kda):
     assert worst_seq_head(to_np(out), o_ref, c["cu_seqlens"]) < TOL_STATE
     assert worst_state(pool.cpu().numpy()[c["final_slot"]], s_ref) < TOL_STATE
     assert worst_state(snap.cpu().numpy()[valid], snap_ref[valid]) < TOL_STATE
+
+
+# ---- edge cases of the plan: nothing to do, one head, the most snapshot requests
+
+
+def test_all_sequences_empty(kda):
+    # no tokens at all: the final states are the initial ones, bit for bit; nothing else written
+    c = W.prefill_case(76, [0, 0, 0], 2, pool_slots=4, track_per_seq=1)
+    assert c["T"] == 0 and (c["track"] == -1).all()
+    out, pool, snap, st = run(kda, c)
+    assert st == 0
+    init = torch.from_numpy(c["pool"][c["init_slot"]]).cuda()
+    assert torch.equal(pool[torch.from_numpy(c["final_slot"]).long().cuda()], init)
+    assert torch.isnan(snap).all()
+
+
+def test_single_head(kda):
+    c = W.prefill_case(77, [300, 65, 1], 1, pool_slots=4, track_per_seq=2)
+    check(c, run(kda, c))
+
+
+@pytest.mark.parametrize("M", [512, 513])
+def test_most_snapshot_requests(kda, M):
+    # M = 512 is the two-phase plan's limit (duplicates and unused entries mixed); M = 513
+    # takes the single-pass kernel with the same workspace
+    track = np.full((1, M), -1, np.int32)
+    track[0, [0, 100, 300, M - 1]] = [0, 2, 2, 4]
+    c = W.prefill_case(78, [300], 1, pool_slots=2, track=track)
+    check(c, run(kda, c))
