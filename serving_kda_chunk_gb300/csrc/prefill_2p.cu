@@ -443,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
                 uint4 hi, lo;
                 const int tt = 16 * tq + g8 * 8;
-                split8(lk, hi, lo);
+                split8p(lk, hi, lo);
                 st16(sm, PR_L_HI + chunk_mn(tt, ci, 1024, 2048), hi);
                 st16(sm, PR_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
-                split8(lq, hi, lo);
+                split8p(lq, hi, lo);
                 st16(sm, PR_L_HI + chunk_mn(64 + tt, ci, 1024, 2048), hi);
                 st16(sm, PR_L_LO + chunk_mn(64 + tt, ci, 1024, 2048), lo);
-                split8(r, hi, lo);
+                split8p(r, hi, lo);
                 st16(sm, PR_R_HI + chunk_mn(tt, ci, 1024, 1024), hi);
                 st16(sm, PR_R_LO + chunk_mn(tt, ci, 1024, 1024), lo);
             }
@@ -475,13 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
                 uint4 hi, lo;
                 const int tt = 16 * tq + g8 * 8;
-                split8(lk, hi, lo);
+                split8p(lk, hi, lo);
                 st16(sm, PR_L_HI + chunk_mn(tt, ci, 1024, 2048), hi);
                 st16(sm, PR_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
-                split8(lq, hi, lo);
+                split8p(lq, hi, lo);
                 st16(sm, PR_L_HI + chunk_mn(64 + tt, ci, 1024, 2048), hi);
                 st16(sm, PR_L_LO + chunk_mn(64 + tt, ci, 1024, 2048), lo);
-                split8(r, hi, lo);
+                split8p(r, hi, lo);
                 st16(sm, PR_R_HI + chunk_mn(tt, ci, 1024, 1024), hi);
                 st16(sm, PR_R_LO + chunk_mn(tt, ci, 1024, 1024), lo);
             }
@@ -527,13 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
                 const int s0 = 16 * tq + 8 * c8;
                 uint4 hi, lo;
-                split8(kg, hi, lo);
+                split8p(kg, hi, lo);
                 kgh[4 * c8] = hi.x; kgh[4 * c8 + 1] = hi.y; kgh[4 * c8 + 2] = hi.z; kgh[4 * c8 + 3] = hi.w;
                 kgl[4 * c8] = lo.x; kgl[4 * c8 + 1] = lo.y; kgl[4 * c8 + 2] = lo.z; kgl[4 * c8 + 3] = lo.w;
                 if constexpr (kBf16Out) {
                     st16(sm, PR_IMG + OP_QW + chunk_mn(s0, ci, 1024, 1024), pack8(qg));
                 } else {
-                    split8(qg, hi, lo);
+                    split8p(qg, hi, lo);
                     st16(sm, PR_IMG + OP_QW + chunk_mn(s0, ci, 1024, 1024), hi);
                     st16(sm, PR_IMG + OP_QGLO + chunk_mn(s0, ci, 1024, 1024), lo);
                 }
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
                 const int s0 = 16 * tq + 8 * c8;
                 uint4 hi, lo;
-                split8(kt, hi, lo);
+                split8p(kt, hi, lo);
                 st16(sm, PR_IMG + OP_KTP + chunk_k(ci, s0, 128), hi);
                 st16(sm, PR_IMG + OP_KTLO + chunk_k(ci, s0, 128), lo);
             }
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                         st16(sm, PR_IMG + OP_KTP + 16384 + chunk_k(t, cq * 16 + 8 * c8, 64), pack8(v + 8 * c8));
                     } else {
                         uint4 hi, lo;
-                        split8(v + 8 * c8, hi, lo);
+                        split8p(v + 8 * c8, hi, lo);
                         st16(sm, PR_IMG + OP_KTP + 16384 + chunk_k(t, cq * 16 + 8 * c8, 64), hi);
                         st16(sm, PR_IMG + OP_PLO + chunk_k(t, cq * 16 + 8 * c8, 64), lo);
                     }
@@ -718,8 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                     x.z *= s_beta[s0 + 2];
                     x.w *= s_beta[s0 + 3];
                     uint2 hi, lo;
-                    split2(x.x, x.y, hi.x, lo.x);
-                    split2(x.z, x.w, hi.y, lo.y);
+                    split2p(x.x, x.y, hi.x, lo.x);
+                    split2p(x.z, x.w, hi.y, lo.y);
                     const uint32_t off = PR_IMG + OP_TB + chunk_k(t, s0 & ~7, 64) + (s0 & 4) * 2;
                     *reinterpret_cast<uint2*>(sm + off) = hi;
                     *reinterpret_cast<uint2*>(sm + off + 8192) = lo;
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
 #pragma unroll
             for (int c8 = 0; c8 < 2; ++c8) {
                 uint4 hi, lo;
-                split8(v + 8 * c8, hi, lo);
+                split8p(v + 8 * c8, hi, lo);
                 const int t = cq * 16 + 8 * c8;
                 st16(sm, PR_IMG + OP_QW + 16384 + chunk_mn(t, row, 1024, 1024), hi);
                 st16(sm, PR_IMG + OP_QW + 32768 + chunk_mn(t, row, 1024, 1024), lo);
@@ -1069,7 +1069,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                 ld16(tl + TM_S + cq * 32 + 16 * hh, v);
                 uint32_t sh[8], sl[8];
 #pragma unroll
-                for (int q2 = 0; q2 < 8; ++q2) split2(v[2 * q2], v[2 * q2 + 1], sh[q2], sl[q2]);
+                for (int q2 = 0; q2 < 8; ++q2) split2p(v[2 * q2], v[2 * q2 + 1], sh[q2], sl[q2]);
                 st8u(tl + TM_SA_HI + cq * 16 + 8 * hh, sh);
                 st8u(tl + TM_SA_LO + cq * 16 + 8 * hh, sl);
             }
@@ -1106,7 +1106,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
                         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
                         uint4 hi, lo;
-                        split8(x, hi, lo);
+                        split8p(x, hi, lo);
                         const uint32_t off = chunk_mn(8 * g8, t, 8192, 1024);
                         st16(sm, SW_V + off, hi);
                         st16(sm, SW_V + 16384 + off, lo);
@@ -1219,7 +1219,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                 for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(ra[q]) + __uint_as_float(rb[q]);
                 uint32_t uh[8], ul[8];
 #pragma unroll
-                for (int q2 = 0; q2 < 8; ++q2) split2(v[2 * q2], v[2 * q2 + 1], uh[q2], ul[q2]);
+                for (int q2 = 0; q2 < 8; ++q2) split2p(v[2 * q2], v[2 * q2 + 1], uh[q2], ul[q2]);
                 st8u(tl + TM_U_HI + cq * 8, uh);
                 st8u(tl + TM_U_LO + cq * 8, ul);
                 wait_st();
