@@ -487,7 +487,8 @@ def run_prefill_long(step, reps):
 def run_e2e(step, steps, warmup):
     """Prefill through the public call with host buffers, streamed per sequence: the pinned
     H2D copies of a sequence's inputs (one stream, longest sequence first), its
-    kda_chunk_prefill call (one stream per sequence, so sequences overlap on the GPU) and the
+    kda_chunk_prefill call (one stream and one workspace per sequence, so sequences overlap on
+    the GPU and each takes the two-phase path) and the
     D2H copy of its output rows (one stream) overlap with the other sequences' copies and
     compute; everything is inside the timed region.  Every sequence is independent, so the
     outputs, final states and snapshots are those of the one-call prefill."""
@@ -506,6 +507,10 @@ def run_e2e(step, steps, warmup):
     # the pool, as in the one-call prefill
     slot_n = [step.slots1[n:n + 1].clone() for n in range(N)]
     track_n = [step.track1[n:n + 1].clone() for n in range(N)]
+    # one workspace per sequence (the calls run concurrently): the two-phase path
+    H = int(c1["H"])
+    ws_n = [torch.empty(max(16, step.kda.kda_chunk_prefill_workspace_size(int(cu[n + 1]) - int(cu[n]), 1, H)),
+                        dtype=torch.uint8, device=step.dev) for n in range(N)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + 8 * N
     d2h = step.out1.numel() * step.out1.element_size()
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
@@ -531,7 +536,7 @@ def run_e2e(step, steps, warmup):
                     dev_in["gate"][a:b], cu_dev[n], step.out1[a:b], state_pool=step.pool1,
                     init_slot=slot_n[n], final_slot=slot_n[n],
                     track_chunk_idx=track_n[n], track_state=step.snap1[n:n + 1],
-                    dev_status=step.status, stream=s_cmp[n])
+                    workspace=ws_n[n], dev_status=step.status, stream=s_cmp[n])
                 done = torch.cuda.Event()
                 done.record(s_cmp[n])
             s_d2h.wait_event(done)
@@ -567,7 +572,7 @@ def run_e2e(step, steps, warmup):
             b.synchronize()
             best = max(best, src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9)
         link[name] = best
-    return statistics.mean(ts), h2d, d2h, link
+    return ts, h2d, d2h, link
 
 
 # --------------------------------------------------------------------------
@@ -783,7 +788,8 @@ def main():
     dev = torch.device("cuda", local)
     step = Step(dev)
     times, wall, clocks, launches = run_device(step, args.steps, args.warmup, rank, world)
-    e2e_t, h2d, d2h, link = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
+    e2e_steps, h2d, d2h, link = run_e2e(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
+    e2e_t = statistics.mean(e2e_steps)
     t16 = run_state_bf16(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t_graph = run_spec_graph(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t_long, tok_long, b_long = run_prefill_long(step, 2)
@@ -856,7 +862,8 @@ def main():
                 "d2h_bytes_per_step": d2h, "link_measured": link,
                 # the link is full duplex: the slower direction bounds the step
                 "link_bound_tokens_per_s": toks / max(h2d / (link["h2d_gbs"] * 1e9),
-                                                      d2h / (link["d2h_gbs"] * 1e9))},
+                                                      d2h / (link["d2h_gbs"] * 1e9)),
+                "ms_per_step_each": [round(t * 1e3, 3) for t in e2e_steps]},
         "gpu_launches": launches,
         "clocks": clocks,
         "parts": parts,
