@@ -287,3 +287,28 @@ def test_most_snapshot_requests(kda, M):
     track[0, [0, 100, 300, M - 1]] = [0, 2, 2, 4]
     c = W.prefill_case(78, [300], 1, pool_slots=2, track=track)
     check(c, run(kda, c))
+
+
+def test_fp32_activations_bf16_state_pool(kda):
+    c = W.prefill_case(79, [260, 64, 3], 2, dtype="f32", pool_slots=4, track_per_seq=1)
+    N, H, T = c["N"], c["H"], c["T"]
+    pool = torch.from_numpy(c["pool"]).cuda().to(torch.bfloat16)
+    snap = torch.zeros((N, 1, H, 128, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(T, H, 128, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, N, H), dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prefill(*(dev_tensor(c[n], "f32") for n in ("q", "k", "v", "beta", "gate")),
+                          i32(c["cu_seqlens"]), out, state_pool=pool, init_slot=i32(c["init_slot"]),
+                          final_slot=i32(c["final_slot"]), track_chunk_idx=i32(c["track"]),
+                          track_state=snap, dev_status=st, workspace=ws, flags=kda.KDA_STATE_BF16)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    S0 = torch.from_numpy(c["pool"]).to(torch.bfloat16).float().numpy()[c["init_slot"]].astype(np.float64)
+    wid = lambda n: c[n].astype(np.float64)  # noqa: E731
+    o_ref, s_ref, snap_ref, _ = oracle.prefill(wid("q"), wid("k"), wid("v"), wid("beta"), wid("gate"),
+                                               c["cu_seqlens"], S0=S0, track=c["track"])
+    u = 2.0 ** -8
+    assert worst_seq_head(to_np(out), o_ref, c["cu_seqlens"]) < TOL_STATE
+    assert worst_state(pool.float().cpu().numpy()[c["final_slot"]], s_ref) < u + TOL_STATE
+    valid = c["track"] >= 0
+    assert rel_l2(snap.float().cpu().numpy()[valid], snap_ref[valid]) < u + TOL_STATE
