@@ -202,12 +202,17 @@ static_assert(PR_SMEM <= 232448, "prep shared memory plan exceeds the per-CTA li
 // TMEM (256 columns): [A;P] accumulator (hi-R | lo-R parts), W^T, KG hi/lo A operand
 constexpr uint32_t PT_AP = 0, PT_W = 128, PT_KG_HI = 192, PT_KG_LO = 224, PT_COLS = 256;
 
+// The prep's 512 threads synchronise on barrier 1 with an explicit count, so that a CTA of a
+// wider launch (the pipelined long-sequence path) can run it while its other warps exit.
+constexpr int kPrepBar = 1;
+
+// The items of chunks [c_begin, c_end) (global chunk index), walked by CTA `cta` of `ncta`.
 template <bool kBf16Out, bool kF32In>
-__global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_constant__ CUtensorMap qmap,
-                                                                   const __grid_constant__ CUtensorMap kmap,
-                                                                   const __grid_constant__ CUtensorMap gmap,
-                                                                   PrefillArgs p, const int32_t* __restrict__ plan,
-                                                                   int64_t n_max, uint8_t* __restrict__ ops) {
+__device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtensorMap* kmap,
+                                          const CUtensorMap* gmap, const PrefillArgs& p,
+                                          const int32_t* __restrict__ plan, int64_t n_max,
+                                          uint8_t* __restrict__ ops, int cta, int ncta, int64_t c_begin,
+                                          int64_t c_end) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -229,8 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
     const bool store_lane = lane == 0 && warp >= 7 && warp <= 9;  // issue the image's bulk stores
     const int H = p.H;
     const int64_t n_chunks_all = min((int64_t)plan[PL_META / 4], n_max);
-    const int64_t items = n_chunks_all * H;
-    if ((int64_t)blockIdx.x >= items) return;
+    const int64_t w_lo = c_begin * H;                          // this call's first item
+    const int64_t items = min(n_chunks_all, c_end) * H;        // one past its last
+    if (w_lo + cta >= items) return;
     const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
 
     if (warp == 0) tmem_alloc(smem_u32(s_tmem), PT_COLS);
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         mbar_init(smem_u32(s_mbar + 1), 1);
     }
     fence_before();
-    __syncthreads();
+    bar_named(kPrepBar, kThreads);
     fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -262,9 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         it.Lc = ci2.y;
         return it;
     };
-    // item w is (chunk w / H, head w % H); consecutive items of this CTA are gridDim.x apart
-    const int64_t step_c = gridDim.x / H;
-    const int step_h = (int)(gridDim.x - step_c * H);
+    // item w is (chunk w / H, head w % H); consecutive items of this CTA are ncta apart
+    const int64_t step_c = ncta / H;
+    const int step_h = (int)(ncta - step_c * H);
     // raw q, k, g tiles of an item (bf16: three 128-channel x 64-token tensor-map boxes, rows
     // past the sequence cleared once they land); its raw beta bits.  Called by every thread
     // once every thread is past its reads of the tiles.
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 fence_async_smem();
                 if (warp == 1) mbar_expect_tx(mbar_raw, 3u * 16384u);
                 tma_load_2d(sb + (warp == 1 ? PR_Q : warp == 2 ? PR_K : PR_G),
-                            warp == 1 ? &qmap : warp == 2 ? &kmap : &gmap, it.h * kD, it.c0, mbar_raw);
+                            warp == 1 ? qmap : warp == 2 ? kmap : gmap, it.h * kD, it.c0, mbar_raw);
             }
             raw_pending = true;
         }
@@ -290,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
     };
 
     uint32_t beta_bits = 0;
-    Item cur = item_at(blockIdx.x / H, (int)(blockIdx.x % H));
-    // the item gridDim.x after `it`
+    Item cur = item_at((w_lo + cta) / H, (int)((w_lo + cta) % H));
+    // the item ncta after `it`
     auto next_of = [&](const Item& it) {
         int64_t c2 = it.c + step_c;
         int h2 = it.h + step_h;
@@ -321,10 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         return l2 ? x * s_nq[t] : x * p.scale;
     };
     prefetch(cur, beta_bits);
-    for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
-        const int64_t w_next = w + gridDim.x;
+    for (int64_t w = w_lo + cta; w < items; w += ncta) {
+        const int64_t w_next = w + ncta;
         const bool has_next = w_next < items;
-        const bool has_next2 = w_next + gridDim.x < items;
+        const bool has_next2 = w_next + ncta < items;
         const Item nxt = has_next ? next_of(cur) : cur;
         // the item after it, for the L2 prefetch: its 8-byte load is issued here, used much later
         const Item nxt2 = has_next2 ? next_of(nxt) : nxt;
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
             const bool okr = mbar_wait(mbar_raw, phase_raw, kWaitLimit);
             phase_raw ^= 1;
             raw_pending = false;
-            if (__syncthreads_or(!okr)) {
+            if (bar_named_or(kPrepBar, kThreads, !okr)) {
                 timed_out = true;
                 break;
             }
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                     const int t = (e >> 4) & 63, ch = e & 15;
                     if (t >= Lc) st16(sm, (e >> 10 ? PR_K : PR_Q) + t * 256 + ch * 16, make_uint4(0, 0, 0, 0));
                 }
-                __syncthreads();
+                bar_named(kPrepBar, kThreads);
             }
         }
         // beta is first read after the channel pass's barrier
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                     s_nq[t] = l2norm_factor(sq) * p.scale;
                 }
             }
-            __syncthreads();
+            bar_named(kPrepBar, kThreads);
         }
 
         // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
@@ -405,13 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
             s_seg_a[tq * 128 + ci] = pa;
             s_seg_i[tq * 128 + ci] = pi;
         }
-        __syncthreads();
+        bar_named(kPrepBar, kThreads);
         bool bad = false;
         // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
         if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
         if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
         if (store_lane) bulk_wait_read_all();  // the previous item's image has left shared memory
-        if (__syncthreads_or(bad)) {
+        if (bar_named_or(kPrepBar, kThreads, bad)) {
             // the sweep evaluates this chunk token by token from the raw inputs
             if (tid == 0) *reinterpret_cast<int32_t*>(blk + OP_FLAG) = 1;
             if (has_next) prefetch(nxt, beta_bits);  // every thread is past its raw reads
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         }
         fence_async_smem();
         fence_before();
-        __syncthreads();
+        bar_named(kPrepBar, kThreads);
         fence_after();
         // ---- MMA 1: [A; P] = [L_k; L_q] R^T: L_hi [R_hi; R_lo]^T (N = 128) + L_lo R_hi^T
         if (tid == 0) {
@@ -561,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
             const bool ok1 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
-            if (__syncthreads_or(!ok1)) {
+            if (bar_named_or(kPrepBar, kThreads, !ok1)) {
                 timed_out = true;
                 break;
             }
@@ -571,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         if (has_next) prefetch(nxt, beta_bits);
         if constexpr (!kF32In) {
             if (lane == 0 && warp >= 4 && warp <= 6 && has_next2)
-                tma_prefetch_2d(warp == 4 ? &qmap : warp == 5 ? &kmap : &gmap, nxt2.h * kD, nxt2.c0);
+                tma_prefetch_2d(warp == 4 ? qmap : warp == 5 ? kmap : gmap, nxt2.h * kD, nxt2.c0);
         }
 
         // ---- A -> N = Diag(beta) A (strict lower, stored transposed: Nt[s][t] = N[t][s]),
@@ -611,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
             }
         }
-        __syncthreads();
+        bar_named(kPrepBar, kThreads);
         // ---- T = (I + N)^-1 (unit lower triangular): 16x16 diagonal blocks by forward
         //      substitution, then the off-diagonal blocks by block substitution, level by level
         //      (16 -> 32 -> 64).  The level products split their sums over 2-4 threads (shuffle
@@ -646,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Tm[(o + r) * NLD + o + jc] = x[r];
             }
-            __syncthreads();
+            bar_named(kPrepBar, kThreads);
             // level 1: T[a][a-1] = -T_aa N[a][a-1] T_{a-1,a-1}, a in {1, 3}; a thread owns
             // row r and 4 adjacent columns of one 16x16 block
             float* Y1 = reinterpret_cast<float*>(sm + PR_Y1);  // [2][16][20]
@@ -665,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
                 *reinterpret_cast<float4*>(&Y1[(w1 * 16 + r1) * 20 + c1]) = y;
             }
-            __syncthreads();
+            bar_named(kPrepBar, kThreads);
             if (tid < 128) {
                 // T_aa is lower triangular: terms s > r1 are zero (and read as zero)
                 float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -680,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 }
                 *reinterpret_cast<float4*>(&Tm[(oa + r1) * NLD + ob + c1]) = make_float4(-z.x, -z.y, -z.z, -z.w);
             }
-            __syncthreads();
+            bar_named(kPrepBar, kThreads);
             // level 2, first product: Y2 = N[32:64, 0:32] T[0:32, 0:32].  Warp = (4-column group
             // c2, half of the rows); lane = (row, parity of the sum), the parities meet by shuffle.
             // T[u][c] is zero for u < c, so the sum starts at c2.
@@ -703,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
                 y.w += __shfl_xor_sync(0xffffffffu, y.w, 16);
                 if (par == 0) *reinterpret_cast<float4*>(&Y2[r2 * 36 + c2]) = y;
             }
-            __syncthreads();
+            bar_named(kPrepBar, kThreads);
             // level 2, second product, and T_b = T Diag(beta) -> bf16 hi/lo operand [t][s].
             // Thread = (row pair t_lo / 32 + t_lo, column quad c4 of 16).  Rows 0-31 and the
             // quads right of column 32 are copies of T (zero above the diagonal); the quads
@@ -756,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         }
         fence_async_smem();  // the image tiles are read by MMA 2 and the bulk store
         fence_before();
-        __syncthreads();
+        bar_named(kPrepBar, kThreads);
         fence_after();
         // ---- MMA 2: W^T = KG T_b^T (hi*hi + hi*lo + lo*hi)
         if (tid == 0) {
@@ -775,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
             const bool ok2 = mbar_wait(mbar, phase, kWaitLimit);
             phase ^= 1;
             fence_after();
-            if (__syncthreads_or(!ok2)) {
+            if (bar_named_or(kPrepBar, kThreads, !ok2)) {
                 timed_out = true;
                 break;
             }
@@ -797,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         }
         fence_async_smem();
         fence_before();
-        __syncthreads();
+        bar_named(kPrepBar, kThreads);
         fence_after();
         // ---- the block image -> the workspace, by bulk copies the next item does not wait for,
         //      one per issuing thread (lane 0 of warps 7-9), each in its own bulk group
@@ -815,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         cur = nxt;
     }
     if (store_lane) bulk_wait_all();  // the image stores have read shared memory and landed
-    timed_out = __syncthreads_or(timed_out);
+    timed_out = bar_named_or(kPrepBar, kThreads, timed_out);
     if (timed_out) {
         if (tid == 0) report(p.dev_status, KDA_DEV_TIMEOUT);
         mbar_wait(mbar, phase ^ 1u, kWaitLimit);  // the phase that timed out, bounded
@@ -823,9 +829,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_
         mbar_wait(mbar_raw, phase_raw ^ 1u, kWaitLimit);
     }
     fence_before();
-    __syncthreads();
+    bar_named(kPrepBar, kThreads);
     fence_after();
     if (warp == 0) tmem_dealloc(tmem, PT_COLS);
+}
+
+template <bool kBf16Out, bool kF32In>
+__global__ void __launch_bounds__(kThreads, 1) prefill_prep_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                                   const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap gmap,
+                                                                   PrefillArgs p, const int32_t* __restrict__ plan,
+                                                                   int64_t n_max, uint8_t* __restrict__ ops,
+                                                                   int64_t c_begin, int64_t c_end) {
+    prep_body<kBf16Out, kF32In>(&qmap, &kmap, &gmap, p, plan, n_max, ops, blockIdx.x, gridDim.x, c_begin, c_end);
 }
 
 // ----------------------------------------------------------------------------
@@ -860,12 +876,15 @@ constexpr uint32_t TM_COLS = 512;
 constexpr int kIssuerWarp = 16;                  // after the 16 compute warps
 constexpr int kSweepThreads = kThreads + 32;
 
+// Unit `unit` over its chunks [j_begin, j_end) (chunk index within the sequence).  The state
+// enters from the initial slot when j_begin = 0, else from `scratch` (fp32 [unit][v][k], left by
+// the call that ran the chunks before); it leaves to the final slot when the range reaches the
+// sequence's end, else to `scratch` for the call that runs the chunks after.
 template <bool kBf16Out, bool kF32In>
-__global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const __grid_constant__ CUtensorMap vmap,
-                                                                         const __grid_constant__ CUtensorMap omap,
-                                                                         PrefillArgs p, const int32_t* __restrict__ plan,
-                                                                         int64_t n_max,
-                                                                         const uint8_t* __restrict__ ops) {
+__device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtensorMap* omap, const PrefillArgs& p,
+                                           const int32_t* __restrict__ plan, int64_t n_max,
+                                           const uint8_t* __restrict__ ops, int unit, int j_begin, int j_end,
+                                           float* __restrict__ scratch) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -892,7 +911,6 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     const int row = quarter * 32 + lane;
     const int ci = tid & 127, tq = tid >> 7;
     const int H = p.H;
-    const int unit = blockIdx.x;
     const int n = plan[PL_ORDER / 4 + unit / H];
     const int h = unit - (unit / H) * H;
 
@@ -914,6 +932,11 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         if (tid == 0 && h == 0) report(p.dev_status, KDA_DEV_BAD_SLOT);
         return;
     }
+    // this call's chunks; a range that starts past the sequence's end has nothing left to do
+    // (the call that reached the end wrote the final state)
+    const int jb = j_begin, je = min(n_chunks, j_end);
+    if (jb > 0 && jb >= n_chunks) return;
+    const bool state_in_scratch = jb > 0, state_to_scratch = j_end < n_chunks;
     for (int m = tid; m < p.M; m += kSweepThreads) {
         const int jj = p.track[(size_t)n * p.M + m];
         const bool ok = jj >= -1 && jj < n_chunks;
@@ -936,7 +959,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     const uint32_t mbar_a = smem_u32(s_mbar + 2), mbar_b = smem_u32(s_mbar + 3);
     const uint32_t mbar_s1 = smem_u32(s_mbar + 4), mbar_u = smem_u32(s_mbar + 5);
     uint32_t ph_s1 = 0, ph_u = 0;
-    int next_snap = next_tracked(s_trk, p.M, -1);  // the next chunk with a snapshot request
+    int next_snap = next_tracked(s_trk, p.M, jb - 1);  // the next chunk with a snapshot request
     // every thread tracks the phases in step; the waits are done by the threads that need them
     uint32_t phase = 0, phase_s = 0, phase_a = 0, phase_b = 0;
     bool pending_s = false;               // state update issued, not yet waited on
@@ -950,8 +973,8 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         mbar_expect_tx(mbar_a, na + (kF32In ? 0u : 16384u));
         bulk_load(sb + SW_OPS, block_of(jj), na, mbar_a);
         if constexpr (!kF32In) {
-            tma_load_2d(sb + SW_V, &vmap, h * kD, t0 + jj * kChunk, mbar_a);
-            tma_load_2d(sb + SW_V + 8192, &vmap, h * kD + 64, t0 + jj * kChunk, mbar_a);
+            tma_load_2d(sb + SW_V, vmap, h * kD, t0 + jj * kChunk, mbar_a);
+            tma_load_2d(sb + SW_V + 8192, vmap, h * kD + 64, t0 + jj * kChunk, mbar_a);
         }
     };
     // part B of chunk jj: one bulk copy, or two around the unused P lo tile
@@ -971,8 +994,8 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         bulk_prefetch_l2(b2, opa_bytes(kBf16Out));
         bulk_prefetch_l2(b2 + OP_KTP, OP_BYTES - OP_KTP);
         if constexpr (!kF32In) {
-            tma_prefetch_2d(&vmap, h * kD, t0 + jj * kChunk);
-            tma_prefetch_2d(&vmap, h * kD + 64, t0 + jj * kChunk);
+            tma_prefetch_2d(vmap, h * kD, t0 + jj * kChunk);
+            tma_prefetch_2d(vmap, h * kD + 64, t0 + jj * kChunk);
         }
     };
     // U~^T = V^T [T_b hi; T_b lo]^T into [U_a | U_b]; fp32 V adds V_lo^T T_b hi^T into U_a
@@ -995,10 +1018,15 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     if (!issuer) {
         const size_t S0 = init >= 0 ? state_elem(init, H, h) + (size_t)row * kD : 0;
         const int col0 = cq * 32;
+        const float* sc = scratch + ((size_t)unit * kD + row) * kD + col0;
         float v[32];
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 4) {
-            float4 x = init >= 0 ? state_load4(p.pool, S0 + col0 + jj, p.st) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (state_in_scratch)
+                x = *reinterpret_cast<const float4*>(sc + jj);
+            else if (init >= 0)
+                x = state_load4(p.pool, S0 + col0 + jj, p.st);
             v[jj] = x.x;
             v[jj + 1] = x.y;
             v[jj + 2] = x.z;
@@ -1011,11 +1039,11 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         st16f(tl + TM_O + cq * 16, z);
         wait_st();
     }
-    if (n_chunks > 0) {
+    if (je > jb) {
         if (lead) {
-            load_a(0);
-            load_b(0);
-            if (n_chunks > 1) prefetch_l2(1);
+            load_a(jb);
+            load_b(jb);
+            if (jb + 1 < je) prefetch_l2(jb + 1);
         }
         pend_a = pend_b = true;
     }
@@ -1032,7 +1060,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         if (!o_pending) return;
         bulk_wait_read_all();  // the stores of two chunks ago have read that staging buffer
         if (o_Lc == kChunk) {
-            if (lane == 0) tma_store_2d(&omap, h * kD, o_c0, sb + SW_OST + o_buf * 16384);
+            if (lane == 0) tma_store_2d(omap, h * kD, o_c0, sb + SW_OST + o_buf * 16384);
         } else {
             for (int t = lane; t < o_Lc; t += 32)
                 bulk_store(static_cast<__nv_bfloat16*>(p.out) + ((size_t)(o_c0 + t) * H + h) * kD,
@@ -1043,10 +1071,10 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     };
 
     // every exit from the loop is decided at a barrier (uniform across the CTA)
-    for (int j = 0; j < n_chunks; ++j) {
+    for (int j = jb; j < je; ++j) {
         const int c0 = t0 + j * kChunk;
         const int Lc = min(kChunk, t1 - c0);
-        const bool more = j + 1 < n_chunks;
+        const bool more = j + 1 < je;
         const bool snap_here = j == next_snap;
         // the previous chunk's state update: the compute warps read S next; its end frees part B
         if (pending_s) {
@@ -1054,7 +1082,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
             phase_s ^= 1;
             pending_s = false;
         }
-        if (!timed_out && j > 0) {
+        if (!timed_out && j > jb) {
             if (lead) load_b(j);
             pend_b = true;
         }
@@ -1159,7 +1187,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                 } else {
                     timed_out = true;  // the others' MMA 3 wait below then gives up as well
                 }
-                if (j + 2 < n_chunks) prefetch_l2(j + 2);  // under MMA 3, off the serial path
+                if (j + 2 < je) prefetch_l2(j + 2);  // under MMA 3, off the serial path
             }
             ph_s1 ^= 1;
             // ---- state pass, second half (under MMA 3, which does not touch the S columns):
@@ -1494,6 +1522,13 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
         if (pending_s) mbar_wait(mbar_s, phase_s, kWaitLimit);
         if (pend_a) mbar_wait(mbar_a, phase_a, kWaitLimit);
         if (pend_b) mbar_wait(mbar_b, phase_b, kWaitLimit);
+    } else if (state_to_scratch && !issuer) {
+        float* sc = scratch + ((size_t)unit * kD + row) * kD + cq * 32;
+        float v[32];
+        ld32(tl + TM_S + cq * 32, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 32; q4 += 4)
+            *reinterpret_cast<float4*>(sc + q4) = make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
     } else if (fin >= 0 && !issuer) {
         const size_t SD = state_elem(fin, H, h) + (size_t)row * kD;
         const int col0 = cq * 32;
@@ -1507,6 +1542,35 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
     __syncthreads();
     fence_after();
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+template <bool kBf16Out, bool kF32In>
+__global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const __grid_constant__ CUtensorMap vmap,
+                                                                         const __grid_constant__ CUtensorMap omap,
+                                                                         PrefillArgs p, const int32_t* __restrict__ plan,
+                                                                         int64_t n_max,
+                                                                         const uint8_t* __restrict__ ops, int j_begin,
+                                                                         int j_end, float* __restrict__ scratch) {
+    sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, blockIdx.x, j_begin, j_end, scratch);
+}
+
+// One long sequence: the sweep over chunks [sj_begin, sj_end) on CTAs 0 .. units-1 (one per
+// unit) and, on the other CTAs, the prep of the chunks after them, [pc_begin, pc_end).  The two
+// halves share no data and never wait on each other; the next launch sweeps what this one
+// prepared.
+template <bool kBf16Out, bool kF32In>
+__global__ void __launch_bounds__(kSweepThreads, 1) prefill_pipe_kernel(
+    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap gmap, PrefillArgs p, const int32_t* __restrict__ plan, int64_t n_max,
+    uint8_t* __restrict__ ops, float* __restrict__ scratch, int units, int sj_begin, int sj_end, int64_t pc_begin,
+    int64_t pc_end) {
+    if ((int)blockIdx.x < units) {
+        sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, blockIdx.x, sj_begin, sj_end, scratch);
+    } else if ((int)threadIdx.x < kThreads) {  // the prep's 512 threads; the 17th warp has no part
+        prep_body<kBf16Out, kF32In>(&qmap, &kmap, &gmap, p, plan, n_max, ops, (int)blockIdx.x - units,
+                                    (int)gridDim.x - units, pc_begin, pc_end);
+    }
 }
 
 int sm_count() {
@@ -1523,7 +1587,8 @@ bool prefill_2p_supported(const PrefillArgs& p) { return p.M <= kTrack2p && p.N 
 size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
     if (N <= 0 || N > kMaxOrderN || T_tot < 0 || H <= 0) return 0;
     const int64_t n_max = max_chunks(T_tot, N);
-    return ops_offset(n_max) + (size_t)n_max * (size_t)H * OP_BYTES;
+    // plan, operand blocks, then one fp32 state per (sequence, head) for the pipelined path
+    return ops_offset(n_max) + (size_t)n_max * (size_t)H * OP_BYTES + (size_t)N * H * kD * kD * 4;
 }
 
 namespace {
@@ -1532,16 +1597,49 @@ struct RawMaps {
     CUtensorMap q, k, g, v;
 };
 
+constexpr uint32_t PIPE_SMEM = PR_SMEM > SW_SMEM ? PR_SMEM : SW_SMEM;
+
 template <bool kBf16Out, bool kF32In>
 void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, const int32_t* plan, int64_t n_max,
-               uint8_t* ops, unsigned prep_grid, unsigned units, cudaStream_t s) {
+               uint8_t* ops, float* scratch, int sms, cudaStream_t s) {
     cudaFuncSetAttribute(prefill_prep_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
     cudaFuncSetAttribute(prefill_sweep_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          SW_SMEM);
-    if (prep_grid > 0)
-        prefill_prep_kernel<kBf16Out, kF32In><<<prep_grid, kThreads, PR_SMEM, s>>>(m.q, m.k, m.g, p, plan, n_max, ops);
-    const CUtensorMap& vmap = m.v;
-    prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(vmap, omap, p, plan, n_max, ops);
+    const int units = p.N * p.H;
+    const int64_t H = p.H;
+    auto prep = [&](int64_t c0, int64_t c1) {
+        const int64_t items = (c1 - c0) * H;
+        const unsigned grid = (unsigned)(items < (int64_t)sms ? items : sms);
+        if (grid > 0)
+            prefill_prep_kernel<kBf16Out, kF32In><<<grid, kThreads, PR_SMEM, s>>>(m.q, m.k, m.g, p, plan, n_max, ops,
+                                                                                  c0, c1);
+    };
+    // One long sequence whose heads would leave most SMs idle in the sweep: chunk segments, a
+    // short first one prepared on every SM, then each twice the one before, so that each is
+    // prepared by the other SMs (at the launch's 96 registers, a little slower) while the sweep
+    // runs through the previous one.
+    const bool pipelined = p.N == 1 && units * 4 <= sms && n_max >= 256;
+    if (!pipelined) {
+        prep(0, n_max);
+        prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(m.v, omap, p, plan, n_max, ops,
+                                                                                     0, INT_MAX, scratch);
+        return;
+    }
+    cudaFuncSetAttribute(prefill_pipe_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         PIPE_SMEM);
+    int64_t b[16];
+    int nb = 0;
+    b[nb++] = 0;
+    for (int64_t len = n_max / 32 > 0 ? n_max / 32 : 1; b[nb - 1] < n_max && nb < 15; len *= 2, ++nb)
+        b[nb] = b[nb - 1] + len < n_max ? b[nb - 1] + len : n_max;
+    b[nb - 1] = n_max;  // the last segment ends at the sequence's end
+    prep(b[0], b[1]);
+    for (int k = 0; k + 2 < nb; ++k)
+        prefill_pipe_kernel<kBf16Out, kF32In><<<(unsigned)sms, kSweepThreads, PIPE_SMEM, s>>>(
+            m.v, omap, m.q, m.k, m.g, p, plan, n_max, ops, scratch, units, (int)b[k], (int)b[k + 1], b[k + 1],
+            b[k + 2]);
+    prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(m.v, omap, p, plan, n_max, ops,
+                                                                                 (int)b[nb - 2], INT_MAX, scratch);
 }
 
 }  // namespace
@@ -1591,18 +1689,16 @@ kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_in, bool bf16_out, 
             return KDA_ERR_CUDA;
     }
     prefill_plan_kernel<<<1, kPlanThreads, 0, s>>>(p.cu_seqlens, p.N, p.T_tot, n_max, plan);
-    const int64_t items = n_max * p.H;
     const int sms = sm_count() > 0 ? sm_count() : 1;
-    const unsigned prep_grid = (unsigned)(items < (int64_t)sms ? items : sms);
-    const unsigned units = (unsigned)(p.N * p.H);
+    float* scratch = reinterpret_cast<float*>(ops + (size_t)n_max * (size_t)p.H * OP_BYTES);
     if (bf16_in && bf16_out)
-        launch_2p<true, false>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<true, false>(maps, omap, p, plan, n_max, ops, scratch, sms, s);
     else if (bf16_in)
-        launch_2p<false, false>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<false, false>(maps, omap, p, plan, n_max, ops, scratch, sms, s);
     else if (bf16_out)
-        launch_2p<true, true>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<true, true>(maps, omap, p, plan, n_max, ops, scratch, sms, s);
     else
-        launch_2p<false, true>(maps, omap, p, plan, n_max, ops, prep_grid, units, s);
+        launch_2p<false, true>(maps, omap, p, plan, n_max, ops, scratch, sms, s);
     return launch_status();
 }
 

@@ -356,5 +356,22 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // all but the most recently committed group
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
+// Barrier over `count` threads (a multiple of 32) on barrier `id`: lets part of a CTA
+// synchronise while other warps do something else or have exited.
+__device__ __forceinline__ void bar_named(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also returns whether any participating thread passed pred = true.
+__device__ __forceinline__ bool bar_named_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 }  // namespace umma
 }  // namespace kda

@@ -102,21 +102,6 @@ struct VLayout {
 // TMEM columns: checkpoint operand [S hi (64) | S lo (64)], then the accumulator [D_hi | D_lo]
 constexpr uint32_t TV_SA = 0, TV_D = 128, TV_COLS = 256;
 
-__device__ __forceinline__ void bar_named(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Named barrier that also returns whether any participating thread passed pred = true.
-__device__ __forceinline__ bool bar_named_or(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
 constexpr float kVFactorMax = 1.8446744e19f;  // 2^64: largest decay factor the pair tables carry
 
 template <bool kBf16>

@@ -312,3 +312,34 @@ def test_fp32_activations_bf16_state_pool(kda):
     assert worst_state(pool.float().cpu().numpy()[c["final_slot"]], s_ref) < u + TOL_STATE
     valid = c["track"] >= 0
     assert rel_l2(snap.float().cpu().numpy()[valid], snap_ref[valid]) < u + TOL_STATE
+
+
+# ---- one long sequence with few heads: the sweep runs in chunk segments, each prepared by the
+#      other SMs while the previous one is swept (segments [0, 8, 24, 56, 120, 248, 256) here)
+
+
+def test_long_sequence_pipelined_matches_oracle(kda):
+    L = 256 * 64 - 17  # 256 chunks, the last one partial
+    track = [[0, 8, 9, 24, 57, 200, 255]]  # on, beside and between segment boundaries
+    c = W.prefill_case(90, [L], 2, pool_slots=2, track=track)
+    check(c, run(kda, c))
+
+
+def test_long_sequence_pipelined_bit_exact(kda):
+    # the same sequence as one of two (the second empty) takes the unsegmented launches: the
+    # segments hand the fp32 state over exactly, so every result is bit-identical
+    L = 256 * 64 + 5
+    c = W.prefill_case(91, [L], 2, pool_slots=2, track=[[3, 64, 250]])
+    a = run(kda, c)
+    c2 = dict(c)
+    c2["N"] = 2
+    c2["cu_seqlens"] = np.array([0, L, L], np.int32)
+    c2["init_slot"] = np.array([c["init_slot"][0], -1], np.int32)
+    c2["final_slot"] = np.array([c["final_slot"][0], -1], np.int32)
+    c2["track"] = np.array([[3, 64, 250], [-1, -1, -1]], np.int32)
+    b = run(kda, c2)
+    assert a[3] == 0 and b[3] == 0
+    assert torch.equal(a[0], b[0])
+    fin = int(c["final_slot"][0])
+    assert torch.equal(a[1][fin], b[1][fin])
+    assert torch.equal(a[2][0], b[2][0])
