@@ -127,9 +127,13 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *   workspace      : optional device scratch of ws_bytes bytes.
  *                    ws_bytes >= kda_chunk_prefill_workspace_size(...) (about
  *                    2 KiB per token-head: every (chunk, head)'s prepared
- *                    operands) runs the two-phase path: all chunks' state-
- *                    independent work in parallel on every SM, then one
- *                    sequential pass per (sequence, head).  A smaller
+ *                    operands, plus 64 KiB per (sequence, head)) runs the
+ *                    two-phase path: all chunks' state-independent work in
+ *                    parallel on every SM, then one sequential pass per
+ *                    (sequence, head).  One sequence of at least 256 chunks
+ *                    whose heads number at most a quarter of the SMs runs it
+ *                    in chunk segments, each pass over a segment beside the
+ *                    preparation of the next (same results, bit for bit).  A smaller
  *                    workspace (>= 16 * ceil(N / 4) bytes) runs the single-pass
  *                    kernel with the longest sequences first; NULL runs it in
  *                    input order.  The paths agree within the stated
