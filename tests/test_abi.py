@@ -46,6 +46,19 @@ def test_status_strings_and_version(kda):
     assert kda.kda_abi_version() >= 104
 
 
+def test_prefill_workspace_size(kda):
+    # every (chunk, head)'s operand block (132 096 bytes), one fp32 state per (sequence, head) for
+    # the pipelined long-sequence path, and a plan area well under 1 MiB
+    H = 32
+    for T, N in [(0, 1), (64, 1), (41460, 8), (131072, 1), (1 << 20, 8)]:
+        n_max = (T + 63 * N) // 64
+        ws = kda.kda_chunk_prefill_workspace_size(T, N, H)
+        blocks = n_max * H * 132096 + N * H * 128 * 128 * 4
+        assert ws % 16 == 0
+        assert blocks <= ws < blocks + (1 << 20)
+    assert kda.kda_chunk_prefill_workspace_size(1000, 2, 4) <= kda.kda_chunk_prefill_workspace_size(2000, 2, 4)
+
+
 def test_workspace_sizes(kda):
     assert kda.kda_slot_copy_workspace_size(0) == 16
     assert kda.kda_slot_copy_workspace_size(4096) == 16 + 4096 // 8
