@@ -343,3 +343,10 @@ def test_long_sequence_pipelined_bit_exact(kda):
     fin = int(c["final_slot"][0])
     assert torch.equal(a[1][fin], b[1][fin])
     assert torch.equal(a[2][0], b[2][0])
+
+
+def test_long_sequence_pipelined_fp32_activations(kda):
+    # the combined launch with fp32 activations (its prep role at 96 registers)
+    L = 256 * 64 + 30
+    c = W.prefill_case(92, [L], 1, dtype="f32", pool_slots=2, track=[[0, 8, 100, 256]])
+    check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
