@@ -79,7 +79,7 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
 # once that file's sha256 no longer starts with the recorded prefix.
 PREFILL_TRAFFIC = {
     "source": "serving_kda_chunk_gb300/csrc/prefill_2p.cu",
-    "sha256_prefix": "5d5db98ee93c8f1b",
+    "sha256_prefix": "f030bc5f229e6ebc",
     "capture": "profiles/prefill_2p_prep_kernel_batched_8x2048_h16.md, "
                "profiles/prefill_2p_sweep_kernel_batched_8x2048_h16.md",
     "bytes_per_token_head": (201.975552e6 + 379.960832e6 + 553.922560e6 + 65.362432e6) / (8 * 2048 * 16),

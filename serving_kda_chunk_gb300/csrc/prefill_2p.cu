@@ -23,6 +23,14 @@
 // semantics" page, section 5: TP does not shorten that chain).  The cost is the workspace round
 // trip of the operands (about 2 KiB per token-head each way).
 //
+// One long sequence with few heads leaves most SMs idle in the sweep while the prep has long
+// finished; such a call runs in chunk segments instead, each segment's sweep beside the prep of
+// the next in one launch (the halves share no data and never wait on each other), with the state
+// handed from segment to segment through the workspace, exactly.
+//
+// Inputs may be bf16 or fp32: the prep reads fp32 q, k and the raw gate from global memory and
+// splits its products as for bf16; the sweep splits fp32 V into bf16 hi/lo tiles itself.
+//
 // Precision is the single-pass kernel's: operands that are not exact bf16 inputs are split into
 // bf16 hi + lo, products hi*hi + hi*lo + lo*hi, state fp32 in TMEM.  A chunk whose decay factors
 // leave the range of that form (a half chunk's product of 1/alpha above 2^64) is flagged by the
