@@ -89,3 +89,45 @@ def test_serving_step_replays_in_a_cuda_graph(kda):
         assert torch.equal(eager[name], graphed[name]), name
     for x, y in zip(eager["convs"], graphed["convs"]):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("shape", ["batched", "one_long_sequence"])
+def test_two_phase_prefill_replays_in_a_cuda_graph(kda, shape):
+    # the plan / prep / sweep launches (and, for one long sequence, the pipelined segment
+    # launches) capture as they are; two replays match two eager calls bit for bit
+    lengths = [300, 65, 1] if shape == "batched" else [256 * 64 + 3]
+    c = W.prefill_case(405, lengths, 2, pool_slots=4, track_per_seq=2)
+    N, H, T = c["N"], c["H"], c["T"]
+    M = c["track"].shape[1]
+    tok = [dev_tensor(c[n], "bf16") for n in ("q", "k", "v", "beta", "gate")]
+    idx = dict(cu=i32(c["cu_seqlens"]), init=i32(c["init_slot"]), fin=i32(c["final_slot"]),
+               track=i32(c["track"]))
+
+    def buffers():
+        return dict(pool=torch.from_numpy(c["pool"]).cuda(),
+                    out=torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda"),
+                    snap=torch.zeros(N, M, H, 128, 128, device="cuda"),
+                    ws=torch.empty(kda.kda_chunk_prefill_workspace_size(T, N, H), dtype=torch.uint8,
+                                   device="cuda"),
+                    st=torch.zeros(1, dtype=torch.int32, device="cuda"))
+
+    def call(b, stream):
+        kda.kda_chunk_prefill(*tok, idx["cu"], b["out"], state_pool=b["pool"], init_slot=idx["init"],
+                              final_slot=idx["fin"], track_chunk_idx=idx["track"], track_state=b["snap"],
+                              workspace=b["ws"], dev_status=b["st"], stream=stream)
+
+    eager, graphed = buffers(), buffers()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call(graphed, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    for _ in range(2):  # in place: the second call starts from the first one's final states
+        g.replay()
+        with torch.cuda.stream(stream):
+            call(eager, stream)
+    torch.cuda.synchronize()
+    assert int(eager["st"].item()) == 0 and int(graphed["st"].item()) == 0
+    for name in ("pool", "out", "snap"):
+        assert torch.equal(eager[name], graphed[name]), name
