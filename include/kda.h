@@ -85,9 +85,8 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  * q and k per head; this does it in the path instead of in a separate pass).
  * kda_spec_verify's key record still holds k as given; kda_spec_commit and
  * kda_spec_accept_commit with the same flag normalise the recorded key the
- * same way.  kda_chunk_prefill honours it on the two-phase and token-serial
- * paths (a call that would take the single-pass kernel takes the token-serial
- * one instead). */
+ * same way.  kda_chunk_prefill honours it on every path (two-phase,
+ * single-pass and token-serial). */
 #define KDA_QK_L2NORM 32u
 
 /* bits OR-ed into *dev_status by the kernels */

@@ -121,8 +121,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
     uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_trk + kTrackTc);  // [0]: MMA batches, [1]: state update
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 2);
     int* s_abort = reinterpret_cast<int*>(s_tmem + 1);  // a wait that timed out inside a phase
+    float* s_nk = reinterpret_cast<float*>(s_abort + 4);  // 64: L2 factors of the key rows
+    float* s_nq = s_nk + 64;                              // 64: of the query rows (x scale)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool l2 = (p.flags & KDA_QK_L2NORM) != 0;
+    // raw key / query element (t, ch) as the recurrence uses it (q also times scale; under
+    // KDA_QK_L2NORM each row times its L2 factor)
+    auto key_at = [&](int t, int ch) {
+        const float x = bf16_at(sm, RAW_K + t * 256 + ch * 2);
+        return l2 ? x * s_nk[t] : x;
+    };
+    auto query_at = [&](int t, int ch) {
+        const float x = bf16_at(sm, RAW_Q + t * 256 + ch * 2);
+        return l2 ? x * s_nq[t] : x * p.scale;
+    };
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int cq = warp >> 2;      // column quarter this warp takes in TMEM passes
     const int row = quarter * 32 + lane;
@@ -254,6 +267,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
             prefetch_v(j + 1);  // the other buffer's last reader was chunk j - 1
             cp_async_commit();
         }
+        if (l2) {
+            // KDA_QK_L2NORM: the factors of the key and query rows, a warp per 4 rows (first read
+            // after the channel pass's barrier)
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                const int t = 4 * warp + tt;
+                const float4 kx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + RAW_K + t * 256 + lane * 8));
+                const float4 qx = State<kStateBF16>::widen(*reinterpret_cast<const uint2*>(sm + RAW_Q + t * 256 + lane * 8));
+                float sk = f4_dot(kx, kx), sq = f4_dot(qx, qx);
+                warp_sum2(sk, sq);
+                if (lane == 0) {
+                    s_nk[t] = l2norm_factor(sk);
+                    s_nq[t] = l2norm_factor(sq) * p.scale;
+                }
+            }
+        }
 
         // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
         float al[16], iv[16];
@@ -313,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int w = 7; w >= 0; --w) {
                         const int u = g8 * 8 + w, t = 16 * tq + u;
-                        const float kk = bf16_at(sm, RAW_K + t * 256 + ci * 2);
-                        const float qq = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale;
+                        const float kk = key_at(t, ci);
+                        const float qq = query_at(t, ci);
                         lk[w] = kk * si;
                         lq[w] = qq * si;
                         r[w] = kk * sa;
@@ -350,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
                         const int u = g8 * 8 + w, t = 16 * tq + u;
-                        const float kk = bf16_at(sm, RAW_K + t * 256 + ci * 2);
-                        const float qq = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale;
+                        const float kk = key_at(t, ci);
+                        const float qq = query_at(t, ci);
                         fa *= al[u];
                         fi *= iv[u];
                         lk[w] = kk * fa;
@@ -595,8 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int w = 0; w < 8; ++w) {
                         const int u = 8 * c8 + w, t = 16 * tq + u;
                         fw *= al[u];
-                        kg[w] = bf16_at(sm, RAW_K + t * 256 + ci * 2) * fw;
-                        qg[w] = bf16_at(sm, RAW_Q + t * 256 + ci * 2) * p.scale * fw;
+                        kg[w] = key_at(t, ci) * fw;
+                        qg[w] = query_at(t, ci) * fw;
                     }
                     const int s0 = 16 * tq + 8 * c8;
                     uint4 hi, lo;
@@ -617,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int w = 7; w >= 0; --w) {
                         const int u = 8 * c8 + w, t = 16 * tq + u;
-                        kt[w] = bf16_at(sm, RAW_K + t * 256 + ci * 2) * bw;
+                        kt[w] = key_at(t, ci) * bw;
                         bw *= al[u];
                     }
                     const int s0 = 16 * tq + 8 * c8;
@@ -829,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
                     for (int q = 0; q < 32; ++q) {
                         const int i = cq * 32 + q;
                         sv[q] *= alpha[t * kD + i];
-                        d1 = fmaf(sv[q], bf16_at(sm, RAW_K + t * 256 + i * 2), d1);
+                        d1 = fmaf(sv[q], key_at(t, i), d1);
                     }
                     red[cq * 128 + c] = d1;
                     __syncthreads();
@@ -840,8 +869,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs p,
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const int i = cq * 32 + q;
-                        sv[q] = fmaf(uu, bf16_at(sm, RAW_K + t * 256 + i * 2), sv[q]);
-                        o = fmaf(sv[q], bf16_at(sm, RAW_Q + t * 256 + i * 2) * p.scale, o);
+                        sv[q] = fmaf(uu, key_at(t, i), sv[q]);
+                        o = fmaf(sv[q], query_at(t, i), o);
                     }
                     red[512 + cq * 128 + c] = o;
                     __syncthreads();
@@ -911,7 +940,7 @@ __global__ void __launch_bounds__(1024) prefill_order_kernel(const int32_t* __re
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs& p, bool bf16_in) {
-    return bf16_in && p.M <= kTrackTc && !(p.flags & KDA_QK_L2NORM);
+    return bf16_in && p.M <= kTrackTc;
 }
 
 size_t prefill_tc_workspace(int32_t N) {

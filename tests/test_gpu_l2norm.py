@@ -41,8 +41,8 @@ def _wid(c, n):
     return W.widen(c[n], "bf16")
 
 
-@pytest.mark.parametrize("two_phase", [True, False])
-def test_prefill(kda, two_phase):
+@pytest.mark.parametrize("path", ["two_phase", "single_pass", "token_serial"])
+def test_prefill(kda, path):
     c = _rescale_rows(W.prefill_case(80, [300, 1, 64, 777], 3, pool_slots=8, track_per_seq=2), 1)
     g = W.bf16_bits_to_f32(c["gate"]).copy()
     g[40:43, 1] = 40.0  # a chunk of head 1 that runs token by token
@@ -54,13 +54,13 @@ def test_prefill(kda, two_phase):
     snap = torch.full((N, M, H, 128, 128), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = None
-    if two_phase:
+    if path == "two_phase":
         ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, N, H), dtype=torch.uint8, device="cuda")
+    flags = kda.KDA_QK_L2NORM | (kda.KDA_PREFILL_RECURRENT if path == "token_serial" else 0)
     kda.kda_chunk_prefill(*(dev_tensor(c[n], "bf16") for n in ("q", "k", "v", "beta", "gate")),
                           i32(c["cu_seqlens"]), out, state_pool=pool, init_slot=i32(c["init_slot"]),
                           final_slot=i32(c["final_slot"]), track_chunk_idx=i32(c["track"]),
-                          track_state=snap, dev_status=st, workspace=ws, flags=kda.KDA_QK_L2NORM,
-                          scale=0.7)
+                          track_state=snap, dev_status=st, workspace=ws, flags=flags, scale=0.7)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     S0 = c["pool"][c["init_slot"]].astype(np.float64)
