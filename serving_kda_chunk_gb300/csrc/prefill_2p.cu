@@ -1687,6 +1687,7 @@ kda_status launch_prefill_2p(const PrefillArgs& p, bool bf16_in, bool bf16_out, 
     memset(&omap, 0, sizeof(omap));
     if (p.T_tot > 0 && bf16_out) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        if (enc == nullptr) return KDA_ERR_CUDA;
         const cuuint64_t dims[2] = {(cuuint64_t)p.H * kD, (cuuint64_t)p.T_tot};
         const cuuint64_t strides[1] = {(cuuint64_t)p.H * kD * 2};
         const cuuint32_t box[2] = {128, 64};
