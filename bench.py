@@ -829,7 +829,7 @@ def main():
         "verify_commit_graph_us": t_graph * 1e6,
         "prefill_long": {"us": t_long * 1e6, "tokens_per_s": tok_long / t_long, "bytes": b_long,
                          "hbm_frac": b_long / (hbm * 1e9) / t_long,
-                         "note": "1 x 131072 tokens, H=16: pipelined segments, each swept by 16 CTAs (one per head) while the other SMs prepare the next"},
+                         "note": "1 x 131072 tokens, H=16: the prep on every SM, then 10 chunk segments swept at once (the middle segments' state maps and offsets, the start states chained, every segment swept from its start)"},
         "slot_copy": {"us": mean["slot_copy"] * 1e6, "bytes": cp_b,
                       "hbm_frac": cp_b / (hbm * 1e9) / mean["slot_copy"]},
     }

@@ -24,9 +24,13 @@
 // trip of the operands (about 2 KiB per token-head each way).
 //
 // One long sequence with few heads leaves most SMs idle in the sweep while the prep has long
-// finished; such a call runs in chunk segments instead, each segment's sweep beside the prep of
-// the next in one launch (the halves share no data and never wait on each other), with the state
-// handed from segment to segment through the workspace, exactly.
+// finished.  Across a chunk the state map is affine, S' = M S + K~^T U~ with M = Diag(e^{G_63})
+// - K~^T W, so with few enough heads the chunks are cut into segments swept at the same time:
+// each middle segment's matrix product Phi and offset B, the segment start states chained from
+// them (S_{s+1} = Phi_s S_s + B_s), then every segment swept from its start.  With more heads
+// the segments run one after another instead, each segment's sweep beside the prep of the next
+// in one launch (the halves share no data and never wait on each other), with the state handed
+// from segment to segment through the workspace, exactly.
 //
 // Inputs may be bf16 or fp32: the prep reads fp32 q, k and the raw gate from global memory and
 // splits its products as for bf16; the sweep splits fp32 V into bf16 hi/lo tiles itself.
@@ -884,15 +888,25 @@ constexpr uint32_t TM_COLS = 512;
 constexpr int kIssuerWarp = 16;                  // after the 16 compute warps
 constexpr int kSweepThreads = kThreads + 32;
 
+// What a sweep computes over its chunk range.  Across a chunk the state map is affine,
+// S' = (Diag(e^{G_63}) - K~^T W) S + K~^T U~, so a range's end state is Phi S_in + B with
+// Phi = the range's product of those matrices and B = its end state from S_in = 0:
+//   kSweepOut  the outputs, snapshots and end state from the given start state;
+//   kSweepPhi  Phi: the state map from S = I with U~ = 0 (V read as zero); no outputs;
+//   kSweepB    B: from S = 0; no outputs.
+// (Phi is d_k x d_k and fits the d_k x d_v state's storage because d_k = d_v.)
+enum SweepMode { kSweepOut = 0, kSweepPhi = 1, kSweepB = 2 };
+
 // Unit `unit` over its chunks [j_begin, j_end) (chunk index within the sequence).  The state
-// enters from the initial slot when j_begin = 0, else from `scratch` (fp32 [unit][v][k], left by
-// the call that ran the chunks before); it leaves to the final slot when the range reaches the
-// sequence's end, else to `scratch` for the call that runs the chunks after.
+// enters from `sc_in` (fp32 [unit][v][k]) when given, else from the initial slot (kSweepOut), the
+// identity (kSweepPhi) or zero (kSweepB).  A kSweepOut range that reaches the sequence's end
+// writes the final slot; otherwise the end state goes to `sc_out` ([unit][v][k]) when given.
 template <bool kBf16Out, bool kF32In>
 __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtensorMap* omap, const PrefillArgs& p,
                                            const int32_t* __restrict__ plan, int64_t n_max,
                                            const uint8_t* __restrict__ ops, int unit, int j_begin, int j_end,
-                                           float* __restrict__ scratch) {
+                                           const float* __restrict__ sc_in, float* __restrict__ sc_out,
+                                           int mode) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -944,7 +958,10 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
     // (the call that reached the end wrote the final state)
     const int jb = j_begin, je = min(n_chunks, j_end);
     if (jb > 0 && jb >= n_chunks) return;
-    const bool state_in_scratch = jb > 0, state_to_scratch = j_end < n_chunks;
+    const bool outputs = mode == kSweepOut;  // outputs and snapshots
+    const bool zero_v = mode == kSweepPhi;   // U~ = T_b V with V read as zero
+    const bool to_pool = outputs && j_end >= n_chunks;
+    const bool to_sc = !to_pool && sc_out != nullptr;
     for (int m = tid; m < p.M; m += kSweepThreads) {
         const int jj = p.track[(size_t)n * p.M + m];
         const bool ok = jj >= -1 && jj < n_chunks;
@@ -967,7 +984,8 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
     const uint32_t mbar_a = smem_u32(s_mbar + 2), mbar_b = smem_u32(s_mbar + 3);
     const uint32_t mbar_s1 = smem_u32(s_mbar + 4), mbar_u = smem_u32(s_mbar + 5);
     uint32_t ph_s1 = 0, ph_u = 0;
-    int next_snap = next_tracked(s_trk, p.M, jb - 1);  // the next chunk with a snapshot request
+    // the next chunk with a snapshot request
+    int next_snap = outputs ? next_tracked(s_trk, p.M, jb - 1) : 0x7fffffff;
     // every thread tracks the phases in step; the waits are done by the threads that need them
     uint32_t phase = 0, phase_s = 0, phase_a = 0, phase_b = 0;
     bool pending_s = false;               // state update issued, not yet waited on
@@ -978,9 +996,10 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
     // tensor map over v, 128-byte swizzled: the MN-major MMA operand), one barrier.  fp32 V is
     // split into bf16 hi/lo tiles by the compute threads at the chunk's start instead.
     auto load_a = [&](int jj) {
-        mbar_expect_tx(mbar_a, na + (kF32In ? 0u : 16384u));
+        const bool tma_v = !kF32In && !zero_v;
+        mbar_expect_tx(mbar_a, na + (tma_v ? 16384u : 0u));
         bulk_load(sb + SW_OPS, block_of(jj), na, mbar_a);
-        if constexpr (!kF32In) {
+        if (tma_v) {
             tma_load_2d(sb + SW_V, vmap, h * kD, t0 + jj * kChunk, mbar_a);
             tma_load_2d(sb + SW_V + 8192, vmap, h * kD + 64, t0 + jj * kChunk, mbar_a);
         }
@@ -1001,7 +1020,7 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
         const uint8_t* b2 = block_of(jj);
         bulk_prefetch_l2(b2, opa_bytes(kBf16Out));
         bulk_prefetch_l2(b2 + OP_KTP, OP_BYTES - OP_KTP);
-        if constexpr (!kF32In) {
+        if (!kF32In && !zero_v) {
             tma_prefetch_2d(vmap, h * kD, t0 + jj * kChunk);
             tma_prefetch_2d(vmap, h * kD + 64, t0 + jj * kChunk);
         }
@@ -1026,21 +1045,30 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
     if (!issuer) {
         const size_t S0 = init >= 0 ? state_elem(init, H, h) + (size_t)row * kD : 0;
         const int col0 = cq * 32;
-        const float* sc = scratch + ((size_t)unit * kD + row) * kD + col0;
         float v[32];
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 4) {
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (state_in_scratch)
-                x = *reinterpret_cast<const float4*>(sc + jj);
-            else if (init >= 0)
+            if (sc_in != nullptr)
+                x = *reinterpret_cast<const float4*>(sc_in + ((size_t)unit * kD + row) * kD + col0 + jj);
+            else if (outputs && init >= 0)
                 x = state_load4(p.pool, S0 + col0 + jj, p.st);
             v[jj] = x.x;
             v[jj + 1] = x.y;
             v[jj + 2] = x.z;
             v[jj + 3] = x.w;
         }
+        if (sc_in == nullptr && mode == kSweepPhi) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = col0 + q == row ? 1.f : 0.f;
+        }
         st32(tl + TM_S + col0, v);
+        if (zero_v && !kF32In) {
+            // V stays zero: no copy ever lands in its buffer (a partial chunk's clearing writes
+            // zeros as well)
+            for (int e = tid; e < 2048; e += kThreads) st16(sm, SW_V + e * 16, make_uint4(0, 0, 0, 0));
+            fence_async_smem();
+        }
         float z[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) z[q] = 0.f;
@@ -1134,7 +1162,7 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
                         const int t = e >> 4, g8 = e & 15;
                         float x[8];
                         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-                        if (t < Lc) {
+                        if (t < Lc && !zero_v) {
                             const float4* src = reinterpret_cast<const float4*>(gv + ((size_t)(c0 + t) * H + h) * kD + 8 * g8);
                             a = __ldg(src);
                             b = __ldg(src + 1);
@@ -1313,7 +1341,7 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
             //      stores after the next chunk's barrier, fp32 straight from registers (a warp
             //      stores 32 consecutive value channels per t).  The O columns are cleared for
             //      the next MMA 3 (ordered before it by the next chunk's arrival on mbar_s1).
-            if (ok4 && !issuer) {
+            if (ok4 && !issuer && outputs) {
                 float v[16];
                 ld16(tl + TM_O + cq * 16, v);
                 if constexpr (kBf16Out) {
@@ -1332,8 +1360,15 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
                 for (int q = 0; q < 16; ++q) v[q] = 0.f;
                 st16f(tl + TM_O + cq * 16, v);
                 wait_st();
+            } else if (ok4 && !issuer) {
+                // no outputs: the O columns are only cleared for the next MMA 3
+                float z[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) z[q] = 0.f;
+                st16f(tl + TM_O + cq * 16, z);
+                wait_st();
             }
-            if constexpr (kBf16Out) {
+            if (kBf16Out && outputs) {
                 o_pending = true;
                 o_c0 = c0;
                 o_Lc = Lc;
@@ -1471,11 +1506,13 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
                     __syncthreads();
                     if (!issuer) {
                         d1 = (red[c] + red[128 + c]) + (red[256 + c] + red[384 + c]);
-                        float vt;
-                        if constexpr (kF32In)
-                            vt = __ldg(static_cast<const float*>(p.v) + ((size_t)(c0 + t) * H + h) * kD + c);
-                        else
-                            vt = bf16_at(sm, SW_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
+                        float vt = 0.f;
+                        if (!zero_v) {
+                            if constexpr (kF32In)
+                                vt = __ldg(static_cast<const float*>(p.v) + ((size_t)(c0 + t) * H + h) * kD + c);
+                            else
+                                vt = bf16_at(sm, SW_V + chunk_mn(c & ~7, t, 8192, 1024) + (c & 7) * 2);
+                        }
                         const float uu = s_beta[t] * (vt - d1);
                         float o = 0.f;
                         const float fk = s_nk[t], fq = s_nq[t];
@@ -1488,7 +1525,7 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
                         red[512 + cq * 128 + c] = o;
                     }
                     __syncthreads();
-                    if (!issuer && cq == 0)
+                    if (!issuer && cq == 0 && outputs)
                         store1<kBf16Out>(p.out, ((size_t)(c0 + t) * H + h) * kD + c,
                                          (red[512 + c] + red[640 + c]) + (red[768 + c] + red[896 + c]));
                     __syncthreads();  // red is rewritten by the next token
@@ -1530,14 +1567,14 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
         if (pending_s) mbar_wait(mbar_s, phase_s, kWaitLimit);
         if (pend_a) mbar_wait(mbar_a, phase_a, kWaitLimit);
         if (pend_b) mbar_wait(mbar_b, phase_b, kWaitLimit);
-    } else if (state_to_scratch && !issuer) {
-        float* sc = scratch + ((size_t)unit * kD + row) * kD + cq * 32;
+    } else if (to_sc && !issuer) {
+        float* sc = sc_out + ((size_t)unit * kD + row) * kD + cq * 32;
         float v[32];
         ld32(tl + TM_S + cq * 32, v);
 #pragma unroll
         for (int q4 = 0; q4 < 32; q4 += 4)
             *reinterpret_cast<float4*>(sc + q4) = make_float4(v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3]);
-    } else if (fin >= 0 && !issuer) {
+    } else if (to_pool && fin >= 0 && !issuer) {
         const size_t SD = state_elem(fin, H, h) + (size_t)row * kD;
         const int col0 = cq * 32;
         float v[32];
@@ -1558,8 +1595,10 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_sweep_kernel(const _
                                                                          PrefillArgs p, const int32_t* __restrict__ plan,
                                                                          int64_t n_max,
                                                                          const uint8_t* __restrict__ ops, int j_begin,
-                                                                         int j_end, float* __restrict__ scratch) {
-    sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, blockIdx.x, j_begin, j_end, scratch);
+                                                                         int j_end, const float* __restrict__ sc_in,
+                                                                         float* __restrict__ sc_out) {
+    sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, blockIdx.x, j_begin, j_end, sc_in, sc_out,
+                                 kSweepOut);
 }
 
 // One long sequence: the sweep over chunks [sj_begin, sj_end) on CTAs 0 .. units-1 (one per
@@ -1574,10 +1613,107 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_pipe_kernel(
     uint8_t* __restrict__ ops, float* __restrict__ scratch, int units, int sj_begin, int sj_end, int64_t pc_begin,
     int64_t pc_end) {
     if ((int)blockIdx.x < units) {
-        sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, blockIdx.x, sj_begin, sj_end, scratch);
+        sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, blockIdx.x, sj_begin, sj_end,
+                                     sj_begin > 0 ? scratch : nullptr, scratch, kSweepOut);
     } else if ((int)threadIdx.x < kThreads) {  // the prep's 512 threads; the 17th warp has no part
         prep_body<kBf16Out, kF32In>(&qmap, &kmap, &gmap, p, plan, n_max, ops, (int)blockIdx.x - units,
                                     (int)gridDim.x - units, pc_begin, pc_end);
+    }
+}
+
+// ---- one long sequence, chunk segments swept in parallel (a scan over the affine state map)
+//
+// Segments [b_0 = 0, b_1), ..., [b_{P-1}, end).  Launch 1 sweeps segment 0 from the initial
+// state (outputs included; its end state is segment 1's start) and, for every middle segment
+// s = 1 .. P-2, its Phi_s and B_s (two CTAs per head).  The combine chains the start states,
+// S_{s+1} = Phi_s S_s + B_s.  Launch 2 sweeps segments 1 .. P-1 from those starts, outputs
+// included.  Each chunk of a middle segment is swept three times, but P segments run at once.
+constexpr int kMaxSeg = 16;
+constexpr int64_t kScanMinChunks = 256;
+
+struct Segs {
+    int b[kMaxSeg + 1];
+    int P;
+};
+
+// scratch slot of one kind (0: segment start states, 1: Phi, 2: B) and segment, [unit][v][k]
+__host__ __device__ inline float* scan_slot(float* scan, int kind, int seg, int units) {
+    return scan + (size_t)(kind * kMaxSeg + seg) * (size_t)units * kD * kD;
+}
+
+template <bool kBf16Out, bool kF32In>
+__global__ void __launch_bounds__(kSweepThreads, 1) prefill_scan_kernel(
+    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, PrefillArgs p,
+    const int32_t* __restrict__ plan, int64_t n_max, const uint8_t* __restrict__ ops, Segs sg,
+    float* __restrict__ scan, int units, int second) {
+    const int bx = blockIdx.x;
+    int unit, jb, je, mode;
+    const float* sc_in = nullptr;
+    float* sc_out = nullptr;
+    if (!second) {
+        if (bx < units) {  // segment 0 from the initial state; its end state starts segment 1
+            unit = bx;
+            jb = 0;
+            je = sg.b[1];
+            sc_out = scan_slot(scan, 0, 1, units);
+            mode = kSweepOut;
+        } else {  // Phi and B of the middle segments
+            const int r = (bx - units) / units, seg = 1 + (r >> 1), kind = (r & 1) ? 2 : 1;
+            unit = (bx - units) - r * units;
+            jb = sg.b[seg];
+            je = sg.b[seg + 1];
+            sc_out = scan_slot(scan, kind, seg, units);
+            mode = kind == 1 ? kSweepPhi : kSweepB;
+        }
+    } else {  // segments 1 .. P-1 from the combined start states
+        const int seg = 1 + bx / units;
+        unit = bx - (seg - 1) * units;
+        jb = sg.b[seg];
+        je = seg + 1 == sg.P ? INT_MAX : sg.b[seg + 1];
+        sc_in = scan_slot(scan, 0, seg, units);
+        mode = kSweepOut;
+    }
+    sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, unit, jb, je, sc_in, sc_out, mode);
+}
+
+// S_{s+1} = Phi_s S_s + B_s for s = 1 .. P-2.  Stored transposed ([v][k]), with Phi stored the
+// way the sweep stores a state (phiT[k'][k] = Phi[k][k']), this is X_{s+1} = X_s phiT + bT.  A
+// block takes 8 rows v of one unit's state, a thread one column k; the rows of X stay in
+// registers and shared memory, the segments follow one another.
+constexpr int kCombineRows = 8;
+
+__global__ void __launch_bounds__(kD) prefill_scan_combine_kernel(float* __restrict__ scan, int units, int P) {
+    __shared__ float xs[kCombineRows][kD];
+    const int blocks_per_unit = kD / kCombineRows;
+    const int unit = blockIdx.x / blocks_per_unit, r0 = (blockIdx.x % blocks_per_unit) * kCombineRows;
+    const int k = threadIdx.x;
+    const size_t uo = (size_t)unit * kD * kD;
+    float x[kCombineRows];
+    const float* s1 = scan_slot(scan, 0, 1, units) + uo;
+#pragma unroll
+    for (int r = 0; r < kCombineRows; ++r) x[r] = s1[(r0 + r) * kD + k];
+    for (int seg = 1; seg + 1 < P; ++seg) {
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kCombineRows; ++r) xs[r][k] = x[r];
+        __syncthreads();
+        const float* ph = scan_slot(scan, 1, seg, units) + uo;
+        const float* bb = scan_slot(scan, 2, seg, units) + uo;
+        float acc[kCombineRows];
+#pragma unroll
+        for (int r = 0; r < kCombineRows; ++r) acc[r] = bb[(r0 + r) * kD + k];
+#pragma unroll 4
+        for (int kk = 0; kk < kD; ++kk) {
+            const float f = ph[kk * kD + k];
+#pragma unroll
+            for (int r = 0; r < kCombineRows; ++r) acc[r] = fmaf(xs[r][kk], f, acc[r]);
+        }
+        float* nx = scan_slot(scan, 0, seg + 1, units) + uo;
+#pragma unroll
+        for (int r = 0; r < kCombineRows; ++r) {
+            x[r] = acc[r];
+            nx[(r0 + r) * kD + k] = acc[r];
+        }
     }
 }
 
@@ -1592,11 +1728,17 @@ int sm_count() {
 
 bool prefill_2p_supported(const PrefillArgs& p) { return p.M <= kTrack2p && p.N <= kMaxOrderN; }
 
+// the segment scan's scratch is part of the workspace of one sequence of >= kScanMinChunks chunks
+static bool scan_room(int64_t n_max, int32_t N) { return N == 1 && n_max >= kScanMinChunks; }
+
 size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
     if (N <= 0 || N > kMaxOrderN || T_tot < 0 || H <= 0) return 0;
     const int64_t n_max = max_chunks(T_tot, N);
-    // plan, operand blocks, then one fp32 state per (sequence, head) for the pipelined path
-    return ops_offset(n_max) + (size_t)n_max * (size_t)H * OP_BYTES + (size_t)N * H * kD * kD * 4;
+    // plan, operand blocks, one fp32 state per (sequence, head) for the pipelined path, then
+    // the segment scan's start / Phi / B states
+    const size_t state = (size_t)kD * kD * 4;
+    return ops_offset(n_max) + (size_t)n_max * (size_t)H * OP_BYTES + (size_t)N * H * state +
+           (scan_room(n_max, N) ? (size_t)3 * kMaxSeg * H * state : 0);
 }
 
 namespace {
@@ -1606,6 +1748,33 @@ struct RawMaps {
 };
 
 constexpr uint32_t PIPE_SMEM = PR_SMEM > SW_SMEM ? PR_SMEM : SW_SMEM;
+
+// Segments for the scan over one sequence of n chunks and `units` heads, or false when the
+// pipelined launches are expected to be faster.  Cost in chunk-sweep times: the full prep
+// (~2.3 sweep times per (chunk, head), spread over every SM), then launch 1 and launch 2, each
+// as many waves of CTAs as it needs times the segment length; the pipelined launches cost about
+// one sweep of the whole sequence.
+bool scan_plan(int64_t n, int units, int sms, Segs& sg) {
+    if (units <= 0 || sms <= 0) return false;
+    const double prep = 2.3 * (double)n * units / sms;
+    double best = 0.9 * (double)n;  // the scan must beat the pipeline by 10 %
+    int best_p = 0;
+    for (int P = 3; P <= kMaxSeg; ++P) {
+        const int64_t len = (n + P - 1) / P;
+        const int64_t w1 = ((int64_t)units * (1 + 2 * (P - 2)) + sms - 1) / sms;
+        const int64_t w2 = ((int64_t)units * (P - 1) + sms - 1) / sms;
+        const double cost = prep + (double)(w1 + w2) * (double)len;
+        if (cost < best) {
+            best = cost;
+            best_p = P;
+        }
+    }
+    if (best_p == 0) return false;
+    sg.P = best_p;
+    for (int i = 0; i <= best_p; ++i) sg.b[i] = (int)((n * i) / best_p);
+    for (int i = best_p + 1; i <= kMaxSeg; ++i) sg.b[i] = sg.b[best_p];
+    return true;
+}
 
 template <bool kBf16Out, bool kF32In>
 void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, const int32_t* plan, int64_t n_max,
@@ -1622,6 +1791,21 @@ void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, 
             prefill_prep_kernel<kBf16Out, kF32In><<<grid, kThreads, PR_SMEM, s>>>(m.q, m.k, m.g, p, plan, n_max, ops,
                                                                                   c0, c1);
     };
+    // One long sequence with few heads: swept as P segments at once when the cost model says so
+    // (see scan_plan), else pipelined below.
+    Segs sg;
+    if (scan_room(n_max, p.N) && scan_plan(n_max, units, sms, sg)) {
+        float* scan = scratch + (size_t)p.N * p.H * kD * kD;
+        cudaFuncSetAttribute(prefill_scan_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SW_SMEM);
+        prep(0, n_max);
+        prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units + 2 * units * (sg.P - 2)), kSweepThreads, SW_SMEM,
+                                                s>>>(m.v, omap, p, plan, n_max, ops, sg, scan, units, 0);
+        prefill_scan_combine_kernel<<<(unsigned)(units * (kD / kCombineRows)), kD, 0, s>>>(scan, units, sg.P);
+        prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units * (sg.P - 1)), kSweepThreads, SW_SMEM, s>>>(
+            m.v, omap, p, plan, n_max, ops, sg, scan, units, 1);
+        return;
+    }
     // One long sequence whose heads would leave most SMs idle in the sweep: chunk segments, a
     // short first one prepared on every SM, then each twice the one before, so that each is
     // prepared by the other SMs (at the launch's 96 registers, a little slower) while the sweep
@@ -1630,7 +1814,7 @@ void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, 
     if (!pipelined) {
         prep(0, n_max);
         prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(m.v, omap, p, plan, n_max, ops,
-                                                                                     0, INT_MAX, scratch);
+                                                                                     0, INT_MAX, nullptr, nullptr);
         return;
     }
     cudaFuncSetAttribute(prefill_pipe_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1647,7 +1831,8 @@ void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, 
             m.v, omap, m.q, m.k, m.g, p, plan, n_max, ops, scratch, units, (int)b[k], (int)b[k + 1], b[k + 1],
             b[k + 2]);
     prefill_sweep_kernel<kBf16Out, kF32In><<<units, kSweepThreads, SW_SMEM, s>>>(m.v, omap, p, plan, n_max, ops,
-                                                                                 (int)b[nb - 2], INT_MAX, scratch);
+                                                                                 (int)b[nb - 2], INT_MAX, scratch,
+                                                                                 nullptr);
 }
 
 }  // namespace

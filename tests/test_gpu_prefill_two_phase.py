@@ -314,30 +314,127 @@ def test_fp32_activations_bf16_state_pool(kda):
     assert rel_l2(snap.float().cpu().numpy()[valid], snap_ref[valid]) < u + TOL_STATE
 
 
-# ---- one long sequence with few heads: the sweep runs in chunk segments, each prepared by the
-#      other SMs while the previous one is swept (segments [0, 8, 24, 56, 120, 248, 256) here)
+# ---- one long sequence with few heads.  With up to ~26 heads (on 152 SMs) the chunks are cut
+#      into segments swept at once: every middle segment's state map Phi and offset B (the sweep
+#      from S = I with V read as zero, and from S = 0), the segment start states chained from
+#      them, then every segment swept from its start (2 heads x 256 chunks: 16 segments of 16).
+#      With 27-38 heads the pipelined launches run instead (each segment's sweep beside the
+#      prep of the next: [0, 8, 24, 56, 120, 248, 256) here).
 
 
-def test_long_sequence_pipelined_matches_oracle(kda):
+def slow_decay(c, gate_shift=-8.0, beta_shift=-2.0):
+    """Shift the raw gate and raw beta so that the state remembers across segments.  With the
+    default recipe (raw gate ~ N(0,1): alpha ~ 1/2 per token) a segment's state map Phi is ~0
+    and a wrong Phi or start state would go unseen; with alpha ~ 0.9997 and beta ~ 0.12 the
+    start state still makes ~6 % of the state 16 chunks later (measured on the oracle)."""
+    c = dict(c)
+    for n, d in (("gate", gate_shift), ("beta", beta_shift)):
+        x = W.widen(c[n], c["dtype"]).astype(np.float32) + np.float32(d)
+        c[n] = W.store(x, c["dtype"])
+    return c
+
+
+def test_long_sequence_segment_scan_matches_oracle(kda):
     L = 256 * 64 - 17  # 256 chunks, the last one partial
-    track = [[0, 8, 9, 24, 57, 200, 255]]  # on, beside and between segment boundaries
-    c = W.prefill_case(90, [L], 2, pool_slots=2, track=track)
+    track = [[0, 15, 16, 17, 32, 100, 240, 255]]  # on, beside and between segment boundaries
+    c = slow_decay(W.prefill_case(90, [L], 2, pool_slots=2, track=track))
     check(c, run(kda, c))
 
 
-def test_long_sequence_pipelined_bit_exact(kda):
-    # the same sequence as one of two (the second empty) takes the unsegmented launches: the
-    # segments hand the fp32 state over exactly, so every result is bit-identical
-    L = 256 * 64 + 5
-    c = W.prefill_case(91, [L], 2, pool_slots=2, track=[[3, 64, 250]])
-    a = run(kda, c)
+def test_long_sequence_segment_scan_fast_decay(kda):
+    # the default recipe: Phi underflows towards zero, the start states come from B alone
+    L = 256 * 64 - 17
+    c = W.prefill_case(89, [L], 2, pool_slots=2, track=[[0, 16, 255]])
+    check(c, run(kda, c))
+
+
+def _as_first_of_two(c):
+    """The same single sequence followed by an empty one: N = 2 takes the unsegmented launches."""
+    L = c["lengths"][0]
     c2 = dict(c)
     c2["N"] = 2
     c2["cu_seqlens"] = np.array([0, L, L], np.int32)
     c2["init_slot"] = np.array([c["init_slot"][0], -1], np.int32)
     c2["final_slot"] = np.array([c["final_slot"][0], -1], np.int32)
-    c2["track"] = np.array([[3, 64, 250], [-1, -1, -1]], np.int32)
-    b = run(kda, c2)
+    M = c["track"].shape[1]
+    c2["track"] = np.concatenate([c["track"], np.full((1, M), -1, np.int32)])
+    return c2
+
+
+def test_long_sequence_segment_scan_close_to_unsegmented(kda):
+    # the scan re-associates the state products (Phi_s S_s + B_s), so it agrees with the
+    # unsegmented sweep to fp32 rounding rather than bit for bit
+    L = 256 * 64 + 5
+    c = slow_decay(W.prefill_case(93, [L], 3, pool_slots=2, track=[[3, 64, 250]]))
+    a = run(kda, c)
+    b = run(kda, _as_first_of_two(c))
+    assert a[3] == 0 and b[3] == 0
+    fin = int(c["final_slot"][0])
+    assert rel_l2(to_np(a[0]), to_np(b[0])) < 1e-3  # bf16 outputs: a few last-bit flips
+    assert rel_l2(a[1][fin].cpu().numpy(), b[1][fin].cpu().numpy()) < 1e-5
+    assert rel_l2(a[2][0].cpu().numpy(), b[2][0].cpu().numpy()) < 1e-5
+
+
+def test_long_sequence_segment_scan_deterministic(kda):
+    c = slow_decay(W.prefill_case(94, [256 * 64], 2, pool_slots=2, track=[[5, 130]]))
+    a = run(kda, c)
+    b = run(kda, c)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_long_sequence_segment_scan_sequence_shorter_than_rows(kda):
+    # 150 of 256 chunks' rows belong to the sequence: the segments past its end are skipped,
+    # the segment holding its end writes the final state, and rows past it stay untouched
+    L, R = 150 * 64 + 3, 256 * 64
+    c = slow_decay(W.prefill_case(95, [L], 2, pool_slots=2, track=[[0, 16, 149]]))
+    pad = W.prefill_case(96, [R - L], 2)
+    cp = dict(c)
+    for n in ("q", "k", "v", "beta", "gate"):
+        cp[n] = np.concatenate([c[n], pad[n]])
+    cp["T"] = R
+    out, pool, snap, st = run(kda, cp)
+    assert torch.isnan(out[L:].float()).all()
+    check(c, (out[:L], pool, snap, st))
+
+
+def test_long_sequence_segment_scan_strong_decay_token_path(kda):
+    # chunks on the token path inside the Phi, B and output sweeps of middle segments
+    L = 256 * 64
+    c = slow_decay(W.prefill_case(97, [L], 2, pool_slots=2, track=[[40, 41, 200]]))
+    g = W.bf16_bits_to_f32(c["gate"]).copy()
+    g[40 * 64 + 10:40 * 64 + 14] = 30.0      # chunk 40, both heads (segment 2)
+    g[41 * 64 + 3:41 * 64 + 5, 1] = 45.0     # chunk 41, head 1
+    g[200 * 64 + 60:200 * 64 + 62, 0] = 60.0  # chunk 200, head 0 (segment 12)
+    c["gate"] = W.f32_to_bf16_bits(g)
+    check(c, run(kda, c))
+
+
+def test_long_sequence_segment_scan_fp32_activations(kda):
+    L = 256 * 64 + 30
+    c = slow_decay(W.prefill_case(92, [L], 1, dtype="f32", pool_slots=2, track=[[0, 8, 100, 256]]))
+    check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
+
+
+def test_long_sequence_segment_scan_fp32_output(kda):
+    L = 256 * 64 - 40
+    c = slow_decay(W.prefill_case(98, [L], 2, pool_slots=2, track=[[1, 47, 48]]))
+    check(c, run(kda, c, out_dtype=torch.float32))
+
+
+def test_long_sequence_pipelined_matches_oracle(kda):
+    L = 256 * 64 - 17
+    track = [[0, 8, 9, 24, 57, 200, 255]]  # on, beside and between segment boundaries
+    c = slow_decay(W.prefill_case(99, [L], 32, pool_slots=2, track=track))
+    check(c, run(kda, c))
+
+
+def test_long_sequence_pipelined_bit_exact(kda):
+    # the segments hand the fp32 state over exactly, so every result is bit-identical to the
+    # unsegmented launches
+    L = 256 * 64 + 5
+    c = slow_decay(W.prefill_case(91, [L], 32, pool_slots=2, track=[[3, 64, 250]]))
+    a = run(kda, c)
+    b = run(kda, _as_first_of_two(c))
     assert a[3] == 0 and b[3] == 0
     assert torch.equal(a[0], b[0])
     fin = int(c["final_slot"][0])
@@ -348,5 +445,5 @@ def test_long_sequence_pipelined_bit_exact(kda):
 def test_long_sequence_pipelined_fp32_activations(kda):
     # the combined launch with fp32 activations (its prep role at 96 registers)
     L = 256 * 64 + 30
-    c = W.prefill_case(92, [L], 1, dtype="f32", pool_slots=2, track=[[0, 8, 100, 256]])
+    c = slow_decay(W.prefill_case(100, [L], 32, dtype="f32", pool_slots=2, track=[[0, 8, 100, 256]]))
     check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
