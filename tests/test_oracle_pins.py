@@ -187,6 +187,33 @@ def test_linear_in_initial_state_and_values():
     np.testing.assert_allclose(s_full, s_a + s_b, atol=1e-12)
 
 
+def test_span_state_map_composes_affinely():
+    # A span of tokens maps its start state affinely: S_end = Phi S_start + B, Phi the run from
+    # S = I with v = 0 (a d_k x d_k map, stored like a state when d_k = d_v), B the run from
+    # S = 0.  Chaining spans this way reproduces one run over all of them; the segment scan of
+    # the long-sequence prefill relies on exactly this.  Stored transposed ([d_v][d_k]), the
+    # chain is X_{s+1} = X_s Phi_s^T + B_s^T.
+    rng = np.random.default_rng(18)
+    T, H, d = 90, 2, 8
+    q, k, v, beta, gate = _rand_inputs(rng, T, H, d, d)
+    gate = gate - 4.0  # slow decay: the start state still matters at the end
+    S0 = rng.standard_normal((1, H, d, d))
+    _, s_ref, _, _ = oracle.prefill(q, k, v, beta, gate, [0, T], S0=S0)
+    cuts = [0, 25, 26, 61, T]  # spans of 25, 1, 35 and 29 tokens
+    eye = np.broadcast_to(np.eye(d), (1, H, d, d)).copy()
+    X = S0[0]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sl = slice(a, b)
+        _, phiT, _, _ = oracle.prefill(q[sl], k[sl], np.zeros_like(v[sl]), beta[sl], gate[sl],
+                                       [0, b - a], S0=eye)
+        _, bT, _, _ = oracle.prefill(q[sl], k[sl], v[sl], beta[sl], gate[sl], [0, b - a],
+                                     S0=np.zeros_like(S0))
+        assert np.linalg.norm(phiT[0] - eye[0]) > 1e-3  # Phi is not trivially I or 0
+        X = np.einsum("hvk,hkj->hvj", X, phiT[0]) + bT[0]
+    np.testing.assert_allclose(X, s_ref[0], rtol=0, atol=1e-12)
+    assert np.linalg.norm(s_ref[0]) > 1e-3
+
+
 def test_value_channels_are_independent():
     rng = np.random.default_rng(17)
     T, H, dk, dv = 30, 1, 8, 9
