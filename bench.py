@@ -731,6 +731,21 @@ def run_profile_case(name, reps):
             kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
                                   state_pool=pool, init_slot=sl, final_slot=sl,
                                   track_chunk_idx=tr, track_state=snap, workspace=ws)
+    elif name == "prefill_long":
+        # one sequence of 32 768 tokens (512 chunks), H = 16: the long-sequence segment scan on a
+        # reduced case (1.1 GB of workspace) so that a capture of its kernels ends quickly
+        c = W.prefill_case(13, [32768], 16, pool_slots=1, track=[[0, 64, 511]])
+        t = {n: to_dev(c[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+        pool = torch.from_numpy(c["pool"]).to(dev)
+        sl, tr, cu = i32(c["init_slot"], dev), i32(c["track"], dev), i32(c["cu_seqlens"], dev)
+        snap = torch.empty(1, 3, 16, D, D, device=dev)
+        out = torch.empty(c["T"], 16, D, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(kda.kda_chunk_prefill_workspace_size(c["T"], 1, 16), dtype=torch.uint8, device=dev)
+
+        def fn():
+            kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
+                                  state_pool=pool, init_slot=sl, final_slot=sl,
+                                  track_chunk_idx=tr, track_state=snap, workspace=ws)
     elif name == "slot_copy_small":
         # the fused copy kernel on a reduced pool (512 slots of 1 MiB states, 32 parents x 8
         # children + 64 clears: 352 MiB moved, above L2) so that a multi-pass capture holds
@@ -771,7 +786,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "prefill_single", "decode", "verify", "commit",
+    ap.add_argument("--profile", choices=["prefill", "prefill_single", "prefill_long", "decode", "verify", "commit",
                                           "conv_compact", "slot_copy", "slot_copy_small"],
                     help="run one entry point a few times (for an ncu capture) and exit")
     args = ap.parse_args()

@@ -1679,11 +1679,16 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_scan_kernel(
 // S_{s+1} = Phi_s S_s + B_s for s = 1 .. P-2.  Stored transposed ([v][k]), with Phi stored the
 // way the sweep stores a state (phiT[k'][k] = Phi[k][k']), this is X_{s+1} = X_s phiT + bT.  A
 // block takes 8 rows v of one unit's state, a thread one column k; the rows of X stay in
-// registers and shared memory, the segments follow one another.
+// registers and shared memory, the segments follow one another.  Each Phi_s (64 KiB) is staged
+// in shared memory by cp.async with all of it in flight at once: read straight from global
+// memory inside the product, its loads left the kernel waiting on latency.
 constexpr int kCombineRows = 8;
+constexpr uint32_t CB_SMEM = kD * kD * 4 + kCombineRows * kD * 4 + 1024;
 
 __global__ void __launch_bounds__(kD) prefill_scan_combine_kernel(float* __restrict__ scan, int units, int P) {
-    __shared__ float xs[kCombineRows][kD];
+    extern __shared__ uint8_t smem_raw[];
+    float* phs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
+    float* xs = phs + kD * kD;  // [kCombineRows][kD]
     const int blocks_per_unit = kD / kCombineRows;
     const int unit = blockIdx.x / blocks_per_unit, r0 = (blockIdx.x % blocks_per_unit) * kCombineRows;
     const int k = threadIdx.x;
@@ -1692,21 +1697,34 @@ __global__ void __launch_bounds__(kD) prefill_scan_combine_kernel(float* __restr
     const float* s1 = scan_slot(scan, 0, 1, units) + uo;
 #pragma unroll
     for (int r = 0; r < kCombineRows; ++r) x[r] = s1[(r0 + r) * kD + k];
+    const uint32_t phs_s = smem_u32(phs);
     for (int seg = 1; seg + 1 < P; ++seg) {
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < kCombineRows; ++r) xs[r][k] = x[r];
-        __syncthreads();
         const float* ph = scan_slot(scan, 1, seg, units) + uo;
         const float* bb = scan_slot(scan, 2, seg, units) + uo;
+        // Phi_s -> shared memory: 4096 16-byte pieces, 32 per thread, consecutive per warp
+#pragma unroll 8
+        for (int e = k; e < kD * kD / 4; e += kD) cp_async16(phs_s + (uint32_t)e * 16, ph + 4 * e, 16);
+        cp_async_commit();
         float acc[kCombineRows];
 #pragma unroll
-        for (int r = 0; r < kCombineRows; ++r) acc[r] = bb[(r0 + r) * kD + k];
-#pragma unroll 4
-        for (int kk = 0; kk < kD; ++kk) {
-            const float f = ph[kk * kD + k];
+        for (int r = 0; r < kCombineRows; ++r) {
+            acc[r] = bb[(r0 + r) * kD + k];
+            xs[r * kD + k] = x[r];
+        }
+        cp_async_wait_all();
+        __syncthreads();
+#pragma unroll 2
+        for (int kk = 0; kk < kD; kk += 4) {
+            const float f0 = phs[kk * kD + k], f1 = phs[(kk + 1) * kD + k];
+            const float f2 = phs[(kk + 2) * kD + k], f3 = phs[(kk + 3) * kD + k];
 #pragma unroll
-            for (int r = 0; r < kCombineRows; ++r) acc[r] = fmaf(xs[r][kk], f, acc[r]);
+            for (int r = 0; r < kCombineRows; ++r) {
+                const float4 xv = *reinterpret_cast<const float4*>(xs + r * kD + kk);
+                acc[r] = fmaf(xv.x, f0, acc[r]);
+                acc[r] = fmaf(xv.y, f1, acc[r]);
+                acc[r] = fmaf(xv.z, f2, acc[r]);
+                acc[r] = fmaf(xv.w, f3, acc[r]);
+            }
         }
         float* nx = scan_slot(scan, 0, seg + 1, units) + uo;
 #pragma unroll
@@ -1714,6 +1732,7 @@ __global__ void __launch_bounds__(kD) prefill_scan_combine_kernel(float* __restr
             x[r] = acc[r];
             nx[(r0 + r) * kD + k] = acc[r];
         }
+        __syncthreads();  // every thread is past its reads of phs and xs before they are rewritten
     }
 }
 
@@ -1801,7 +1820,8 @@ void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, 
         prep(0, n_max);
         prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units + 2 * units * (sg.P - 2)), kSweepThreads, SW_SMEM,
                                                 s>>>(m.v, omap, p, plan, n_max, ops, sg, scan, units, 0);
-        prefill_scan_combine_kernel<<<(unsigned)(units * (kD / kCombineRows)), kD, 0, s>>>(scan, units, sg.P);
+        cudaFuncSetAttribute(prefill_scan_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CB_SMEM);
+        prefill_scan_combine_kernel<<<(unsigned)(units * (kD / kCombineRows)), kD, CB_SMEM, s>>>(scan, units, sg.P);
         prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units * (sg.P - 1)), kSweepThreads, SW_SMEM, s>>>(
             m.v, omap, p, plan, n_max, ops, sg, scan, units, 1);
         return;
