@@ -50,6 +50,18 @@ __device__ __forceinline__ Decay decay_of(float raw, uint32_t flags) {
 
 __device__ __forceinline__ float alpha_of(float raw, uint32_t flags) { return decay_of(raw, flags).a; }
 
+// Runs body(flags) with the gate form fixed at compile time (KDA_GATE_LOG or not), so that a loop
+// of decay_of calls in the body is straight-line code: with the flag tested inside an unrolled
+// loop, each element's exponential / reciprocal chain ran after the previous one's branch.  The
+// arithmetic is decay_of's either way (the same bits).
+template <class Body>
+__device__ __forceinline__ void with_gate_form(uint32_t flags, Body&& body) {
+    if (flags & KDA_GATE_LOG)
+        body(KDA_GATE_LOG);
+    else
+        body(0u);
+}
+
 // Under KDA_QK_L2NORM a row x of q or k is used as x * l2norm_factor(sum_i x_i^2).
 constexpr float kL2NormEps = 1e-6f;
 __device__ __forceinline__ float l2norm_factor(float sum_sq) { return rsqrtf(sum_sq + kL2NormEps); }

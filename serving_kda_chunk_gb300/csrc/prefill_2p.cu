@@ -403,19 +403,18 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
         float al[16], iv[16];
         float m_big = 1.f;  // product of the factors >= 1 this quarter contributes to its half
         {
+            with_gate_form(p.flags, [&](uint32_t form) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int t = 16 * tq + u;
+                    const Decay dc = decay_of(raw_at(p.gate_raw, PR_G, t), form);
+                    al[u] = t < Lc ? dc.a : 1.f;
+                    iv[u] = t < Lc ? dc.inv : 1.f;
+                }
+            });
             float pa = 1.f, pi = 1.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const int t = 16 * tq + u;
-                const float x = raw_at(p.gate_raw, PR_G, t);
-                if (t < Lc) {
-                    const Decay dc = decay_of(x, p.flags);
-                    al[u] = dc.a;
-                    iv[u] = dc.inv;
-                } else {
-                    al[u] = 1.f;
-                    iv[u] = 1.f;
-                }
                 pa *= al[u];
                 pi *= iv[u];
                 if (tq != 0 || u > 0) m_big *= iv[u];

@@ -316,21 +316,21 @@ __global__ void __launch_bounds__(kVThreads, 2)
         {
             const uint8_t* kqg = sm + Lay::KQG;
             float kt[KC], qt[KC], at[KC], iv[KC];  // key, scaled query, alpha, 1 / alpha
+            with_gate_form(a.flags, [&](uint32_t form) {
 #pragma unroll
-            for (int t = 0; t < KC; ++t) {
-                kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
-                qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
-                if (l2) {
-                    kt[t] *= nrm[t];
-                    qt[t] *= nrm[KC + t];
+                for (int t = 0; t < KC; ++t) {
+                    kt[t] = act_at<kBf16In>(kqg, t * 128 + i);
+                    qt[t] = act_at<kBf16In>(kqg, (KC + t) * 128 + i) * a.scale;
+                    if (l2) {
+                        kt[t] *= nrm[t];
+                        qt[t] *= nrm[KC + t];
+                    }
+                    // rows past the accepted length arrived zero-filled: finite, then replaced
+                    const Decay dc = decay_of(act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i), form);
+                    at[t] = t < ql ? dc.a : 1.f;
+                    iv[t] = t < ql ? dc.inv : 1.f;
                 }
-                at[t] = iv[t] = 1.f;
-                if (t < ql) {
-                    const Decay dc = decay_of(act_at<kBf16In>(kqg, (2 * KC + t) * 128 + i), a.flags);
-                    at[t] = dc.a;
-                    iv[t] = dc.inv;
-                }
-            }
+            });
             if (warp < 4) {
                 uint16_t* bt = reinterpret_cast<uint16_t*>(sm + Lay::BT);
                 auto put = [&](int n, float val) {
