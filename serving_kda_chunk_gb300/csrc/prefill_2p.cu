@@ -427,17 +427,21 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
         // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
         if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
         if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
-        if (store_lane) bulk_wait_read_all();  // the previous item's image has left shared memory
-        if (bar_named_or(kPrepBar, kThreads, bad)) {
-            // the sweep evaluates this chunk token by token from the raw inputs
-            if (tid == 0) *reinterpret_cast<int32_t*>(blk + OP_FLAG) = 1;
-            if (has_next) prefetch(nxt, beta_bits);  // every thread is past its raw reads
-            cur = nxt;
-            continue;
-        }
-
         // ---- L = [k; q] e^{G_t - G_31}, R = k e^{G_31 - G_s}: quarters 0, 1 backward
-        //      from token 31, quarters 2, 3 forward from token 32
+        //      from token 31, quarters 2, 3 forward from token 32.  L lo goes to shared memory at
+        //      once (no image store reads its region); L hi and R, whose tiles alias the image's
+        //      W, T_b and P tiles, wait in registers until the previous item's image stores have
+        //      read those tiles, so that the wait overlaps this arithmetic.
+        uint4 lkh[2], lqh[2], rh[2], rl[2];
+        auto lr_split = [&](int g8, float(&lk)[8], float(&lq)[8], float(&r)[8]) {
+            const int tt = 16 * tq + g8 * 8;
+            uint4 lo;
+            split8p(lk, lkh[g8], lo);
+            st16(sm, PR_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
+            split8p(lq, lqh[g8], lo);
+            st16(sm, PR_L_LO + chunk_mn(64 + tt, ci, 1024, 2048), lo);
+            split8p(r, rh[g8], rl[g8]);
+        };
         if (tq < 2) {
             float sa = 1.f, si = 1.f;  // prod over (u, 31] of alpha and of 1/alpha
             if (tq == 0) {
@@ -458,17 +462,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
                     sa *= al[u];
                     si *= iv[u];
                 }
-                uint4 hi, lo;
-                const int tt = 16 * tq + g8 * 8;
-                split8p(lk, hi, lo);
-                st16(sm, PR_L_HI + chunk_mn(tt, ci, 1024, 2048), hi);
-                st16(sm, PR_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
-                split8p(lq, hi, lo);
-                st16(sm, PR_L_HI + chunk_mn(64 + tt, ci, 1024, 2048), hi);
-                st16(sm, PR_L_LO + chunk_mn(64 + tt, ci, 1024, 2048), lo);
-                split8p(r, hi, lo);
-                st16(sm, PR_R_HI + chunk_mn(tt, ci, 1024, 1024), hi);
-                st16(sm, PR_R_LO + chunk_mn(tt, ci, 1024, 1024), lo);
+                lr_split(g8, lk, lq, r);
             }
         } else {
             float fa = 1.f, fi = 1.f;  // prod over [32, t] of alpha and of 1/alpha
@@ -490,18 +484,24 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
                     lq[w8] = qq * fa;
                     r[w8] = kk * fi;
                 }
-                uint4 hi, lo;
-                const int tt = 16 * tq + g8 * 8;
-                split8p(lk, hi, lo);
-                st16(sm, PR_L_HI + chunk_mn(tt, ci, 1024, 2048), hi);
-                st16(sm, PR_L_LO + chunk_mn(tt, ci, 1024, 2048), lo);
-                split8p(lq, hi, lo);
-                st16(sm, PR_L_HI + chunk_mn(64 + tt, ci, 1024, 2048), hi);
-                st16(sm, PR_L_LO + chunk_mn(64 + tt, ci, 1024, 2048), lo);
-                split8p(r, hi, lo);
-                st16(sm, PR_R_HI + chunk_mn(tt, ci, 1024, 1024), hi);
-                st16(sm, PR_R_LO + chunk_mn(tt, ci, 1024, 1024), lo);
+                lr_split(g8, lk, lq, r);
             }
+        }
+        if (store_lane) bulk_wait_read_all();  // the previous item's image has left shared memory
+        if (bar_named_or(kPrepBar, kThreads, bad)) {
+            // the sweep evaluates this chunk token by token from the raw inputs
+            if (tid == 0) *reinterpret_cast<int32_t*>(blk + OP_FLAG) = 1;
+            if (has_next) prefetch(nxt, beta_bits);  // every thread is past its raw reads
+            cur = nxt;
+            continue;
+        }
+#pragma unroll
+        for (int g8 = 0; g8 < 2; ++g8) {
+            const int tt = 16 * tq + g8 * 8;
+            st16(sm, PR_L_HI + chunk_mn(tt, ci, 1024, 2048), lkh[g8]);
+            st16(sm, PR_L_HI + chunk_mn(64 + tt, ci, 1024, 2048), lqh[g8]);
+            st16(sm, PR_R_HI + chunk_mn(tt, ci, 1024, 1024), rh[g8]);
+            st16(sm, PR_R_LO + chunk_mn(tt, ci, 1024, 1024), rl[g8]);
         }
         fence_async_smem();
         fence_before();
