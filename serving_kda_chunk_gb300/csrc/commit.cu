@@ -209,14 +209,16 @@ __global__ void __launch_bounds__(kCommitThreads, 8) commit_kernel(
             // from t = aa - 1 down; D = exp(c_0 + g_0) = the product over the aa steps
             const int c = threadIdx.x;
             float prod = 1.f;
-            for (int t = aa - 1; t >= 0; --t) {
-                const float kv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + c] << 16)
-                                          : reinterpret_cast<const float*>(KG)[t * 2 * kD + c];
-                const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
-                                          : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
-                F[t * kD + c] = prod * (l2 ? kv * NRM[t] : kv);
-                prod *= alpha_of(gv, flags);
-            }
+            with_gate_form(flags, [&](uint32_t form) {
+                for (int t = aa - 1; t >= 0; --t) {
+                    const float kv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + c] << 16)
+                                              : reinterpret_cast<const float*>(KG)[t * 2 * kD + c];
+                    const float gv = kBf16Rec ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(KG)[t * 2 * kD + kD + c] << 16)
+                                              : reinterpret_cast<const float*>(KG)[t * 2 * kD + kD + c];
+                    F[t * kD + c] = prod * (l2 ? kv * NRM[t] : kv);
+                    prod *= alpha_of(gv, form);
+                }
+            });
             D[c] = prod;
         }
         __syncthreads();
