@@ -91,12 +91,14 @@ def test_serving_step_replays_in_a_cuda_graph(kda):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("shape", ["batched", "one_long_sequence"])
+@pytest.mark.parametrize("shape", ["batched", "one_long_sequence", "one_long_sequence_32_heads"])
 def test_two_phase_prefill_replays_in_a_cuda_graph(kda, shape):
-    # the plan / prep / sweep launches (and, for one long sequence, the pipelined segment
-    # launches) capture as they are; two replays match two eager calls bit for bit
+    # the plan / prep / sweep launches (for one long sequence with 2 heads the segment scan's
+    # launches and its combine, with 32 heads the pipelined segment launches) capture as they
+    # are; two replays match two eager calls bit for bit
     lengths = [300, 65, 1] if shape == "batched" else [256 * 64 + 3]
-    c = W.prefill_case(405, lengths, 2, pool_slots=4, track_per_seq=2)
+    H = 32 if shape == "one_long_sequence_32_heads" else 2
+    c = W.prefill_case(405, lengths, H, pool_slots=4, track_per_seq=2)
     N, H, T = c["N"], c["H"], c["T"]
     M = c["track"].shape[1]
     tok = [dev_tensor(c[n], "bf16") for n in ("q", "k", "v", "beta", "gate")]

@@ -57,7 +57,8 @@ def check(c, got, flags=0, tol_o=5e-3):
     dt = c["dtype"]
     o_ref, s_ref, snap_ref, _ = oracle.prefill(
         W.widen(c["q"], dt), W.widen(c["k"], dt), W.widen(c["v"], dt), W.widen(c["beta"], dt),
-        W.widen(c["gate"], dt), c["cu_seqlens"], S0=S0, track=c["track"], flags=flags & 3)
+        W.widen(c["gate"], dt), c["cu_seqlens"], S0=S0, track=c["track"],
+        flags=(flags & 3) | (oracle.QK_L2NORM if flags & 32 else 0))
     assert st == 0
     valid = c["track"] >= 0
     o = to_np(out)
@@ -413,6 +414,60 @@ def test_long_sequence_segment_scan_fp32_activations(kda):
     L = 256 * 64 + 30
     c = slow_decay(W.prefill_case(92, [L], 1, dtype="f32", pool_slots=2, track=[[0, 8, 100, 256]]))
     check(c, run(kda, c, out_dtype=torch.float32), tol_o=TOL_STATE)
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3])
+def test_long_sequence_segment_scan_preactivated_flags(kda, flags):
+    # the Phi and B sweeps with g given (KDA_GATE_LOG) and / or beta given (KDA_BETA_ACT), both
+    # still slow to decay
+    L = 256 * 64 - 5
+    c = slow_decay(W.prefill_case(101, [L], 2, pool_slots=2, track=[[16, 130]]))
+    if flags & 1:  # g = log alpha directly: alpha ~ 0.9995
+        g = -np.abs(W.bf16_bits_to_f32(W.prefill_case(101, [L], 2)["gate"])) * np.float32(6e-4)
+        c["gate"] = W.f32_to_bf16_bits(g.astype(np.float32))
+    if flags & 2:  # beta itself, ~0.12
+        b = 1.0 / (1.0 + np.exp(-W.bf16_bits_to_f32(c["beta"]).astype(np.float64)))
+        c["beta"] = W.f32_to_bf16_bits(b.astype(np.float32))
+    check(c, run(kda, c, flags=flags), flags=flags)
+
+
+def test_long_sequence_segment_scan_l2norm(kda):
+    # q and k rows of arbitrary length, normalised inside the kernels (KDA_QK_L2NORM)
+    L = 256 * 64 + 7
+    c = slow_decay(W.prefill_case(102, [L], 2, pool_slots=2, track=[[0, 100, 256]]))
+    rng = np.random.default_rng(3)
+    for n in ("q", "k"):
+        x = W.bf16_bits_to_f32(c[n]).reshape(c[n].shape)
+        f = rng.uniform(0.3, 4.0, x.shape[:-1] + (1,)).astype(np.float32)
+        c[n] = W.f32_to_bf16_bits((x * f).astype(np.float32)).reshape(c[n].shape)
+    check(c, run(kda, c, flags=kda.KDA_QK_L2NORM), flags=kda.KDA_QK_L2NORM)
+
+
+def test_long_sequence_segment_scan_bf16_state_pool(kda):
+    # start states, Phi and B stay fp32 in the workspace; only the final slot and the snapshots
+    # round to bf16
+    L = 256 * 64 - 70
+    c = slow_decay(W.prefill_case(103, [L], 2, pool_slots=2, track=[[0, 17, 200]]))
+    N, H, T = c["N"], c["H"], c["T"]
+    pool = torch.from_numpy(c["pool"]).cuda().to(torch.bfloat16)
+    snap = torch.zeros((N, 3, H, 128, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kda.kda_chunk_prefill_workspace_size(T, N, H), dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prefill(*(dev_tensor(c[n], "bf16") for n in ("q", "k", "v", "beta", "gate")),
+                          i32(c["cu_seqlens"]), out, state_pool=pool, init_slot=i32(c["init_slot"]),
+                          final_slot=i32(c["final_slot"]), track_chunk_idx=i32(c["track"]),
+                          track_state=snap, dev_status=st, workspace=ws, flags=kda.KDA_STATE_BF16)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    S0 = torch.from_numpy(c["pool"]).to(torch.bfloat16).float().numpy()[c["init_slot"]].astype(np.float64)
+    wid = lambda n: W.widen(c[n], "bf16")  # noqa: E731
+    o_ref, s_ref, snap_ref, _ = oracle.prefill(wid("q"), wid("k"), wid("v"), wid("beta"), wid("gate"),
+                                               c["cu_seqlens"], S0=S0, track=c["track"])
+    u = 2.0 ** -8
+    assert worst_seq_head(to_np(out), o_ref, c["cu_seqlens"]) < 5e-3
+    assert worst_state(pool.float().cpu().numpy()[c["final_slot"]], s_ref) < u + TOL_STATE
+    assert worst_state(snap.float().cpu().numpy()[0], snap_ref[0]) < u + TOL_STATE
 
 
 def test_long_sequence_segment_scan_fp32_output(kda):
