@@ -235,8 +235,8 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
     float* s_nq = s_nk + 64;                                 // 64: of the query rows (x scale)
     float* s_seg_a = s_nq + 64;                              // [4][128]: prod of alpha per token quarter
     float* s_seg_i = s_seg_a + 512;                          // [4][128]: prod of 1/alpha per quarter
-    uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_seg_i + 512);  // MMA, raw tiles
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 2);
+    uint64_t* s_mbar = reinterpret_cast<uint64_t*>(s_seg_i + 512);  // MMA, raw q / k tiles, raw gate tile
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_mbar + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -255,15 +255,17 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
     if (tid == 0) {
         mbar_init(smem_u32(s_mbar), 1);
         mbar_init(smem_u32(s_mbar + 1), 1);
+        mbar_init(smem_u32(s_mbar + 2), 1);
     }
     fence_before();
     bar_named(kPrepBar, kThreads);
     fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t mbar = smem_u32(s_mbar), mbar_raw = smem_u32(s_mbar + 1);
-    uint32_t phase = 0, phase_raw = 0;
-    bool raw_pending = false;  // a raw-tile copy issued and not yet waited on (every thread tracks it)
+    const uint32_t mbar = smem_u32(s_mbar), mbar_qk = smem_u32(s_mbar + 1), mbar_g = smem_u32(s_mbar + 2);
+    uint32_t phase = 0, phase_qk = 0, phase_g = 0;
+    // raw-tile copies issued and not yet waited on (every thread tracks them)
+    bool qk_pending = false, g_pending = false;
     bool timed_out = false;
 
     struct Item {
@@ -271,7 +273,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
         int h, c0, Lc;
     };
     const int2* cinfo = reinterpret_cast<const int2*>(reinterpret_cast<const uint8_t*>(plan) + cinfo_offset(n_max));
-    auto item_at = [&](int64_t c, int hh) {  // one 8-byte load: nothing waits on it until the prefetch
+    auto item_at = [&](int64_t c, int hh) {  // one 8-byte load
         Item it;
         it.c = c;
         it.h = hh;
@@ -283,20 +285,31 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
     // item w is (chunk w / H, head w % H); consecutive items of this CTA are ncta apart
     const int64_t step_c = ncta / H;
     const int step_h = (int)(ncta - step_c * H);
-    // raw q, k, g tiles of an item (bf16: three 128-channel x 64-token tensor-map boxes, rows
-    // past the sequence cleared once they land); its raw beta bits.  Called by every thread
-    // once every thread is past its reads of the tiles.
-    auto prefetch = [&](const Item& it, uint32_t& beta_bits) {
+    // raw tiles of an item (bf16: 128-channel x 64-token tensor-map boxes; rows past the
+    // sequence are cleared once they land).  The gate tile is read by the gate pass only, so the
+    // next item's is requested right after it; the q and k tiles are read until the K_G pass and
+    // wait for it, together with the item's raw beta bits.  Called by every thread once every
+    // thread is past its reads of the tiles concerned.
+    auto prefetch_g = [&](const Item& it) {
         if constexpr (!kF32In) {
-            // one copy per issuing thread, in three warps (a copy that lands before the expected
-            // byte count is posted only takes the count below zero while the arrival is pending)
-            if (lane == 0 && warp >= 1 && warp <= 3) {
+            if (lane == 0 && warp == 3) {
                 fence_async_smem();
-                if (warp == 1) mbar_expect_tx(mbar_raw, 3u * 16384u);
-                tma_load_2d(sb + (warp == 1 ? PR_Q : warp == 2 ? PR_K : PR_G),
-                            warp == 1 ? qmap : warp == 2 ? kmap : gmap, it.h * kD, it.c0, mbar_raw);
+                mbar_expect_tx(mbar_g, 16384u);
+                tma_load_2d(sb + PR_G, gmap, it.h * kD, it.c0, mbar_g);
             }
-            raw_pending = true;
+            g_pending = true;
+        }
+    };
+    auto prefetch_qk = [&](const Item& it, uint32_t& beta_bits) {
+        if constexpr (!kF32In) {
+            // one copy per issuing thread, in two warps (a copy that lands before the expected
+            // byte count is posted only takes the count below zero while the arrival is pending)
+            if (lane == 0 && (warp == 1 || warp == 2)) {
+                fence_async_smem();
+                if (warp == 1) mbar_expect_tx(mbar_qk, 2u * 16384u);
+                tma_load_2d(sb + (warp == 1 ? PR_Q : PR_K), warp == 1 ? qmap : kmap, it.h * kD, it.c0, mbar_qk);
+            }
+            qk_pending = true;
         }
         if (tid < 64) {
             const size_t bi = (size_t)(it.c0 + min(tid, it.Lc - 1)) * H + it.h;
@@ -309,13 +322,20 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
 
     uint32_t beta_bits = 0;
     Item cur = item_at((w_lo + cta) / H, (int)((w_lo + cta) % H));
-    // the item ncta after `it`
-    auto next_of = [&](const Item& it) {
-        int64_t c2 = it.c + step_c;
-        int h2 = it.h + step_h;
-        if (h2 >= H) {
-            h2 -= H;
-            ++c2;
+    // the item ncta after `it`, or `it` again when there is none: the choice is made on the
+    // indices, so that the 8-byte load is always in range and nothing waits on it until the
+    // item's fields are used (a choice between loaded values stalled every thread at the top of
+    // each item for the load's full latency)
+    auto next_or_same = [&](const Item& it, bool exists) {
+        int64_t c2 = it.c;
+        int h2 = it.h;
+        if (exists) {
+            c2 += step_c;
+            h2 += step_h;
+            if (h2 >= H) {
+                h2 -= H;
+                ++c2;
+            }
         }
         return item_at(c2, h2);
     };
@@ -338,25 +358,71 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
         const float x = raw_at(p.q, PR_Q, t);
         return l2 ? x * s_nq[t] : x * p.scale;
     };
-    prefetch(cur, beta_bits);
+    prefetch_g(cur);
+    prefetch_qk(cur, beta_bits);
     for (int64_t w = w_lo + cta; w < items; w += ncta) {
         const int64_t w_next = w + ncta;
         const bool has_next = w_next < items;
         const bool has_next2 = w_next + ncta < items;
-        const Item nxt = has_next ? next_of(cur) : cur;
+        const Item nxt = next_or_same(cur, has_next);
         // the item after it, for the L2 prefetch: its 8-byte load is issued here, used much later
-        const Item nxt2 = has_next2 ? next_of(nxt) : nxt;
+        const Item nxt2 = next_or_same(nxt, has_next2);
         const int Lc = cur.Lc, h = cur.h;
         uint8_t* blk = ops + ((size_t)cur.c * H + h) * OP_BYTES;
 
+        // the gate tile (a timed-out wait is decided at the gate pass's barrier; rows past the
+        // sequence are read but their decays replaced by 1)
+        bool okg = true;
         if constexpr (!kF32In) {
-            const bool okr = mbar_wait(mbar_raw, phase_raw, kWaitLimit);
-            phase_raw ^= 1;
-            raw_pending = false;
-            if (bar_named_or(kPrepBar, kThreads, !okr)) {
-                timed_out = true;
-                break;
+            okg = mbar_wait(mbar_g, phase_g, kWaitLimit);
+            phase_g ^= 1;
+            g_pending = false;
+        }
+        // beta is first read after the channel pass's barrier
+        if (tid < 64) {
+            const float braw = __uint_as_float(kF32In ? beta_bits : beta_bits << 16);
+            s_beta[tid] = tid < Lc ? beta_act(braw, p.flags) : 0.f;
+        }
+
+        // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
+        float al[16], iv[16];
+        float m_big = 1.f;  // product of the factors >= 1 this quarter contributes to its half
+        {
+            with_gate_form(p.flags, [&](uint32_t form) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int t = 16 * tq + u;
+                    const Decay dc = decay_of(raw_at(p.gate_raw, PR_G, t), form);
+                    al[u] = t < Lc ? dc.a : 1.f;
+                    iv[u] = t < Lc ? dc.inv : 1.f;
+                }
+            });
+            float pa = 1.f, pi = 1.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                pa *= al[u];
+                pi *= iv[u];
+                if (tq != 0 || u > 0) m_big *= iv[u];
             }
+            s_seg_a[tq * 128 + ci] = pa;
+            s_seg_i[tq * 128 + ci] = pi;
+        }
+        if (bar_named_or(kPrepBar, kThreads, !okg)) {
+            timed_out = true;
+            break;
+        }
+        // every gate read of this item is done: the next item's gate tile may land
+        if (has_next) prefetch_g(nxt);
+        bool bad = false;
+        // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
+        if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
+        if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
+        // the q and k tiles (a timed-out wait is decided at the barrier after the L/R arithmetic)
+        bool okqk = true;
+        if constexpr (!kF32In) {
+            okqk = mbar_wait(mbar_qk, phase_qk, kWaitLimit);
+            phase_qk ^= 1;
+            qk_pending = false;
             if (Lc < kChunk) {
                 // rows past the sequence (the next one's, or zero-filled past T_tot) -> 0, so that
                 // no other row's values (possibly non-finite) enter this chunk
@@ -366,11 +432,6 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
                 }
                 bar_named(kPrepBar, kThreads);
             }
-        }
-        // beta is first read after the channel pass's barrier
-        if (tid < 64) {
-            const float braw = __uint_as_float(kF32In ? beta_bits : beta_bits << 16);
-            s_beta[tid] = tid < Lc ? beta_act(braw, p.flags) : 0.f;
         }
         if (l2) {
             // KDA_QK_L2NORM: factors of the key and query rows, a warp per 4 rows
@@ -399,34 +460,6 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
             bar_named(kPrepBar, kThreads);
         }
 
-        // ---- channel pass: this thread's channel ci over tokens 16*tq .. 16*tq+15
-        float al[16], iv[16];
-        float m_big = 1.f;  // product of the factors >= 1 this quarter contributes to its half
-        {
-            with_gate_form(p.flags, [&](uint32_t form) {
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int t = 16 * tq + u;
-                    const Decay dc = decay_of(raw_at(p.gate_raw, PR_G, t), form);
-                    al[u] = t < Lc ? dc.a : 1.f;
-                    iv[u] = t < Lc ? dc.inv : 1.f;
-                }
-            });
-            float pa = 1.f, pi = 1.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                pa *= al[u];
-                pi *= iv[u];
-                if (tq != 0 || u > 0) m_big *= iv[u];
-            }
-            s_seg_a[tq * 128 + ci] = pa;
-            s_seg_i[tq * 128 + ci] = pi;
-        }
-        bar_named(kPrepBar, kThreads);
-        bool bad = false;
-        // largest factor a half uses: prod of 1/alpha over (0, 31] (half 0) or [32, 63] (half 1)
-        if (tq == 0) bad = !(m_big * s_seg_i[128 + ci] <= kFactorMax);
-        if (tq == 2) bad = !(m_big * s_seg_i[384 + ci] <= kFactorMax);
         // ---- L = [k; q] e^{G_t - G_31}, R = k e^{G_31 - G_s}: quarters 0, 1 backward
         //      from token 31, quarters 2, 3 forward from token 32.  L lo goes to shared memory at
         //      once (no image store reads its region); L hi and R, whose tiles alias the image's
@@ -488,10 +521,14 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
             }
         }
         if (store_lane) bulk_wait_read_all();  // the previous item's image has left shared memory
-        if (bar_named_or(kPrepBar, kThreads, bad)) {
+        if (bar_named_or(kPrepBar, kThreads, bad || !okqk)) {
+            if (bar_named_or(kPrepBar, kThreads, !okqk)) {
+                timed_out = true;
+                break;
+            }
             // the sweep evaluates this chunk token by token from the raw inputs
             if (tid == 0) *reinterpret_cast<int32_t*>(blk + OP_FLAG) = 1;
-            if (has_next) prefetch(nxt, beta_bits);  // every thread is past its raw reads
+            if (has_next) prefetch_qk(nxt, beta_bits);  // every thread is past its raw reads
             cur = nxt;
             continue;
         }
@@ -583,9 +620,9 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
                 break;
             }
         }
-        // every raw read of this item is done: the next item's tiles may land, and the one after
-        // it is pulled into L2
-        if (has_next) prefetch(nxt, beta_bits);
+        // every q / k read of this item is done: the next item's tiles may land, and the item
+        // after it is pulled into L2
+        if (has_next) prefetch_qk(nxt, beta_bits);
         if constexpr (!kF32In) {
             if (lane == 0 && warp >= 4 && warp <= 6 && has_next2)
                 tma_prefetch_2d(warp == 4 ? qmap : warp == 5 ? kmap : gmap, nxt2.h * kD, nxt2.c0);
@@ -836,8 +873,10 @@ __device__ __forceinline__ void prep_body(const CUtensorMap* qmap, const CUtenso
     if (timed_out) {
         if (tid == 0) report(p.dev_status, KDA_DEV_TIMEOUT);
         mbar_wait(mbar, phase ^ 1u, kWaitLimit);  // the phase that timed out, bounded
-        if (raw_pending) mbar_wait(mbar_raw, phase_raw, kWaitLimit);
-        mbar_wait(mbar_raw, phase_raw ^ 1u, kWaitLimit);
+        if (qk_pending) mbar_wait(mbar_qk, phase_qk, kWaitLimit);
+        mbar_wait(mbar_qk, phase_qk ^ 1u, kWaitLimit);
+        if (g_pending) mbar_wait(mbar_g, phase_g, kWaitLimit);
+        mbar_wait(mbar_g, phase_g ^ 1u, kWaitLimit);
     }
     fence_before();
     bar_named(kPrepBar, kThreads);
