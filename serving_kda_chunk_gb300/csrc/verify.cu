@@ -487,13 +487,17 @@ __global__ void __launch_bounds__(kVThreads, 2)
             }
         }
         // ---- this unit's checkpoint (every thread waits on its barrier) -> TMEM operand (all
-        //      warps, 64 columns each)
+        //      warps, 64 columns each).  A bf16 checkpoint is used where it landed: the two
+        //      64-channel boxes of 128 rows, 128-byte swizzled, are the K-major shared-memory
+        //      A operand of the MMA (its hi part, lo = 0), so it needs no conversion; it then
+        //      holds the staging buffer until the MMA has read it.
+        const bool a_in_smem = a.st == kStateBF16;
         if (raw_pend) {
             if (!mbar_wait(smem_u32(mbars), ph_raw, kVWaitLimit)) timed_out = true;
             ph_raw ^= 1u;
             raw_pend = false;
         }
-        if (ql > 0 && !timed_out) {
+        if (ql > 0 && !timed_out && !a_in_smem) {
             convert(2 * colhalf);
             convert(2 * colhalf + 1);
             wait_st();
@@ -506,24 +510,29 @@ __global__ void __launch_bounds__(kVThreads, 2)
         }
         fence_after();
         // ---- the next unit's checkpoint (RAW has been converted; requested by warp 1, so that
-        //      thread 0 goes straight to the MMAs) and token rows, then this unit's MMAs:
+        //      thread 0 goes straight to the MMAs; for a bf16 checkpoint after the MMAs have read
+        //      it, below) and token rows, then this unit's MMAs:
         //      D = S_hi [B_hi; B_lo]^T + S_lo B_hi^T
-        if (it + 1 < nu) {
-            if (meta[it + 1].y > 0) {
-                if (tid == 32) request_ckpt(it + 1);
-                raw_pend = true;
-            }
+        const bool next_ckpt = it + 1 < nu && meta[it + 1].y > 0;
+        if (next_ckpt && !a_in_smem) {
+            if (tid == 32) request_ckpt(it + 1);
+            raw_pend = true;
         }
         if (ql > 0) {
             if (tid == 0) {
                 const uint32_t id2 = idesc_bf16(128, 2 * NB, false, false, false);
                 const uint32_t id1 = idesc_bf16(128, NB, false, false, false);
                 const uint32_t b4 = sb4 + Lay::BT / 16;
+                if (a_in_smem) {
+                    // a bf16 checkpoint splits exactly into hi with lo = 0: its lo products are zero
+                    const uint32_t a4 = sb4 + Lay::RAW / 16;
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_ta(tmem + TV_D, tmem + TV_SA + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
-                // a bf16 checkpoint splits exactly into hi with lo = 0: its lo products are zero
-                if (a.st != kStateBF16) {
+                    for (int s = 0; s < 8; ++s)
+                        mma(tmem + TV_D, desc_k4(a4, 128, s), desc_k4(b4, 2 * NB, s), id2, s != 0);
+                } else {
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma_ta(tmem + TV_D, tmem + TV_SA + 8 * s, desc_k4(b4, 2 * NB, s), id2, s != 0);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
                         mma_ta(tmem + TV_D, tmem + TV_SA + 64 + 8 * s, desc_k4(b4, 2 * NB, s), id1, 1u);
@@ -546,6 +555,11 @@ __global__ void __launch_bounds__(kVThreads, 2)
             break;
         }
         fence_after();
+        // a bf16 checkpoint: the MMAs have read it, so the next one may land in its place
+        if (next_ckpt && a_in_smem) {
+            if (tid == 32) request_ckpt(it + 1);
+            raw_pend = true;
+        }
         // ---- rows (warps 0-3): triangular solve, outputs, u records
         if (warp < 4) {
             const size_t rec0 = ((size_t)r * H + h) * K;
