@@ -3,7 +3,7 @@ memory on demand (an engine whose pool allocator owns all device memory after
 start-up, or a path where cudaMalloc and the device synchronisation it may
 cause are not acceptable).  It keeps its scratch in a fixed array inside the
 library and must give exactly what kda_slot_copy gives with a caller-provided
-workspace, call after call.
+workspace, and what the oracle's slot copy gives, call after call.
 
 This file is named so that pytest collects it last."""
 import ctypes
@@ -11,6 +11,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -74,10 +75,13 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(kda):
     a = base.clone()
     b = base.clone()
     for sc in (first, second):
+        before = b.cpu().numpy()
         assert _with_workspace(kda, a, sc) == 0
         st, dev = _noalloc(kda, b, sc)
         assert st == 0 and dev == 0
         assert torch.equal(a, b)  # copies are exact: the tolerance is zero
+        (want,) = oracle.slot_copy([before], sc["clear"], sc["src"], sc["dst_offsets"], sc["dst"])
+        assert np.array_equal(b.cpu().numpy(), want)
 
 
 def test_noalloc_still_detects_overlap(kda):
