@@ -127,19 +127,20 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *                    ws_bytes >= kda_chunk_prefill_workspace_size(...) (about
  *                    2 KiB per token-head: every (chunk, head)'s prepared
  *                    operands, plus 64 KiB per (sequence, head), plus 3 MiB
- *                    per head when N = 1 with at least 256 chunks of rows)
- *                    runs the two-phase path: all chunks' state-independent
- *                    work in parallel on every SM, then one sequential pass
- *                    per (sequence, head).  One sequence of at least 256
- *                    chunks with few heads runs that pass in chunk segments:
- *                    up to ~1/6 as many heads as SMs, all segments at once
- *                    (each middle segment's linear state map and offset,
- *                    the segment start states chained from them on the GPU,
- *                    then every segment swept from its start: within fp32
- *                    rounding of the unsegmented pass, deterministic);
- *                    otherwise, up to a quarter as many heads as SMs, one
- *                    segment after another, each beside the preparation of
- *                    the next (the same results bit for bit).  A smaller
+ *                    per (sequence, head) when N <= 8 and the rows hold at
+ *                    least 256 chunks per sequence) runs the two-phase path:
+ *                    all chunks' state-independent work in parallel on every
+ *                    SM, then one sequential pass per (sequence, head).  Up
+ *                    to 8 long sequences with few (sequence, head) pairs run
+ *                    that pass in chunk segments, all at once (each middle
+ *                    segment's linear state map and offset, the segment
+ *                    start states chained from them on the GPU, then every
+ *                    segment swept from its start: within fp32 rounding of
+ *                    the unsegmented pass, deterministic), when a cost model
+ *                    expects it to pay; one sequence otherwise, with up to a
+ *                    quarter as many heads as SMs, runs its segments one
+ *                    after another, each beside the preparation of the next
+ *                    (the same results bit for bit).  A smaller
  *                    workspace (>= 16 * ceil(N / 4) bytes) runs the single-pass
  *                    kernel with the longest sequences first; NULL runs it in
  *                    input order.  The paths agree within the stated

@@ -935,16 +935,18 @@ constexpr int kSweepThreads = kThreads + 32;
 // (Phi is d_k x d_k and fits the d_k x d_v state's storage because d_k = d_v.)
 enum SweepMode { kSweepOut = 0, kSweepPhi = 1, kSweepB = 2 };
 
-// Unit `unit` over its chunks [j_begin, j_end) (chunk index within the sequence).  The state
-// enters from `sc_in` (fp32 [unit][v][k]) when given, else from the initial slot (kSweepOut), the
-// identity (kSweepPhi) or zero (kSweepB).  A kSweepOut range that reaches the sequence's end
-// writes the final slot; otherwise the end state goes to `sc_out` ([unit][v][k]) when given.
+// Unit `unit` over its chunks [j_begin, j_end) (chunk index within the sequence), or, when
+// n_seg > 0, over segment `seg` of n_seg equal parts of its sequence's chunks (the last one to
+// the end).  The state enters from `sc_in` (fp32 [unit][v][k]) when given, else from the
+// initial slot (kSweepOut), the identity (kSweepPhi) or zero (kSweepB).  A kSweepOut range that
+// reaches the sequence's end writes the final slot; otherwise the end state goes to `sc_out`
+// ([unit][v][k]) when given.
 template <bool kBf16Out, bool kF32In>
 __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtensorMap* omap, const PrefillArgs& p,
                                            const int32_t* __restrict__ plan, int64_t n_max,
                                            const uint8_t* __restrict__ ops, int unit, int j_begin, int j_end,
                                            const float* __restrict__ sc_in, float* __restrict__ sc_out,
-                                           int mode) {
+                                           int mode, int seg = 0, int n_seg = 0) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -992,13 +994,18 @@ __device__ __forceinline__ void sweep_body(const CUtensorMap* vmap, const CUtens
         if (tid == 0 && h == 0) report(p.dev_status, KDA_DEV_BAD_SLOT);
         return;
     }
-    // this call's chunks; a range that starts past the sequence's end has nothing left to do
-    // (the call that reached the end wrote the final state)
-    const int jb = j_begin, je = min(n_chunks, j_end);
-    if (jb > 0 && jb >= n_chunks) return;
+    // this call's chunks; a range that starts past the sequence's end, or a later segment of an
+    // empty sequence, has nothing left to do (the call that reached the end wrote the final state)
+    int jb = j_begin, j_last = j_end;
+    if (n_seg > 0) {  // n_chunks < 2^25 and seg < 16: the products fit in 32 bits
+        jb = n_chunks * seg / n_seg;
+        j_last = seg + 1 == n_seg ? INT_MAX : n_chunks * (seg + 1) / n_seg;
+    }
+    const int je = min(n_chunks, j_last);
+    if ((jb > 0 || seg > 0) && jb >= n_chunks) return;
     const bool outputs = mode == kSweepOut;  // outputs and snapshots
     const bool zero_v = mode == kSweepPhi;   // U~ = T_b V with V read as zero
-    const bool to_pool = outputs && j_end >= n_chunks;
+    const bool to_pool = outputs && j_last >= n_chunks;
     const bool to_sc = !to_pool && sc_out != nullptr;
     for (int m = tid; m < p.M; m += kSweepThreads) {
         const int jj = p.track[(size_t)n * p.M + m];
@@ -1659,20 +1666,19 @@ __global__ void __launch_bounds__(kSweepThreads, 1) prefill_pipe_kernel(
     }
 }
 
-// ---- one long sequence, chunk segments swept in parallel (a scan over the affine state map)
+// ---- long sequences with few heads, chunk segments swept in parallel (a scan over the affine
+//      state map)
 //
-// Segments [b_0 = 0, b_1), ..., [b_{P-1}, end).  Launch 1 sweeps segment 0 from the initial
-// state (outputs included; its end state is segment 1's start) and, for every middle segment
-// s = 1 .. P-2, its Phi_s and B_s (two CTAs per head).  The combine chains the start states,
-// S_{s+1} = Phi_s S_s + B_s.  Launch 2 sweeps segments 1 .. P-1 from those starts, outputs
-// included.  Each chunk of a middle segment is swept three times, but P segments run at once.
+// Each sequence's chunks are cut into P equal segments (the last to the end).  Launch 1 sweeps
+// segment 0 from the initial state (outputs included; its end state is segment 1's start) and,
+// for every middle segment s = 1 .. P-2, its Phi_s and B_s (two CTAs per (sequence, head)).  The
+// combine chains the start states, S_{s+1} = Phi_s S_s + B_s.  Launch 2 sweeps segments
+// 1 .. P-1 from those starts, outputs included.  Each chunk of a middle segment is swept three
+// times, but P segments run at once.  A unit's segment bounds follow its own sequence's length,
+// so sequences of different lengths (or empty ones) share the launches.
 constexpr int kMaxSeg = 16;
-constexpr int64_t kScanMinChunks = 256;
-
-struct Segs {
-    int b[kMaxSeg + 1];
-    int P;
-};
+constexpr int64_t kScanMinChunks = 256;  // per sequence, on average
+constexpr int kScanMaxN = 8;
 
 // scratch slot of one kind (0: segment start states, 1: Phi, 2: B) and segment, [unit][v][k]
 __host__ __device__ inline float* scan_slot(float* scan, int kind, int seg, int units) {
@@ -1682,36 +1688,32 @@ __host__ __device__ inline float* scan_slot(float* scan, int kind, int seg, int 
 template <bool kBf16Out, bool kF32In>
 __global__ void __launch_bounds__(kSweepThreads, 1) prefill_scan_kernel(
     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap, PrefillArgs p,
-    const int32_t* __restrict__ plan, int64_t n_max, const uint8_t* __restrict__ ops, Segs sg,
+    const int32_t* __restrict__ plan, int64_t n_max, const uint8_t* __restrict__ ops, int P,
     float* __restrict__ scan, int units, int second) {
     const int bx = blockIdx.x;
-    int unit, jb, je, mode;
+    int unit, seg, mode;
     const float* sc_in = nullptr;
     float* sc_out = nullptr;
     if (!second) {
         if (bx < units) {  // segment 0 from the initial state; its end state starts segment 1
             unit = bx;
-            jb = 0;
-            je = sg.b[1];
+            seg = 0;
             sc_out = scan_slot(scan, 0, 1, units);
             mode = kSweepOut;
         } else {  // Phi and B of the middle segments
-            const int r = (bx - units) / units, seg = 1 + (r >> 1), kind = (r & 1) ? 2 : 1;
+            const int r = (bx - units) / units, kind = (r & 1) ? 2 : 1;
+            seg = 1 + (r >> 1);
             unit = (bx - units) - r * units;
-            jb = sg.b[seg];
-            je = sg.b[seg + 1];
             sc_out = scan_slot(scan, kind, seg, units);
             mode = kind == 1 ? kSweepPhi : kSweepB;
         }
     } else {  // segments 1 .. P-1 from the combined start states
-        const int seg = 1 + bx / units;
+        seg = 1 + bx / units;
         unit = bx - (seg - 1) * units;
-        jb = sg.b[seg];
-        je = seg + 1 == sg.P ? INT_MAX : sg.b[seg + 1];
         sc_in = scan_slot(scan, 0, seg, units);
         mode = kSweepOut;
     }
-    sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, unit, jb, je, sc_in, sc_out, mode);
+    sweep_body<kBf16Out, kF32In>(&vmap, &omap, p, plan, n_max, ops, unit, 0, 0, sc_in, sc_out, mode, seg, P);
 }
 
 // S_{s+1} = Phi_s S_s + B_s for s = 1 .. P-2.  Stored transposed ([v][k]), with Phi stored the
@@ -1785,8 +1787,9 @@ int sm_count() {
 
 bool prefill_2p_supported(const PrefillArgs& p) { return p.M <= kTrack2p && p.N <= kMaxOrderN; }
 
-// the segment scan's scratch is part of the workspace of one sequence of >= kScanMinChunks chunks
-static bool scan_room(int64_t n_max, int32_t N) { return N == 1 && n_max >= kScanMinChunks; }
+// the segment scan's scratch is part of the workspace of up to kScanMaxN sequences of, on
+// average, at least kScanMinChunks chunks
+static bool scan_room(int64_t n_max, int32_t N) { return N <= kScanMaxN && n_max >= kScanMinChunks * N; }
 
 size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
     if (N <= 0 || N > kMaxOrderN || T_tot < 0 || H <= 0) return 0;
@@ -1795,7 +1798,7 @@ size_t prefill_2p_workspace(int32_t T_tot, int32_t N, int32_t H) {
     // the segment scan's start / Phi / B states
     const size_t state = (size_t)kD * kD * 4;
     return ops_offset(n_max) + (size_t)n_max * (size_t)H * OP_BYTES + (size_t)N * H * state +
-           (scan_room(n_max, N) ? (size_t)3 * kMaxSeg * H * state : 0);
+           (scan_room(n_max, N) ? (size_t)3 * kMaxSeg * N * H * state : 0);
 }
 
 namespace {
@@ -1806,15 +1809,15 @@ struct RawMaps {
 
 constexpr uint32_t PIPE_SMEM = PR_SMEM > SW_SMEM ? PR_SMEM : SW_SMEM;
 
-// Segments for the scan over one sequence of n chunks and `units` heads, or false when the
-// pipelined launches are expected to be faster.  Cost in chunk-sweep times: the full prep
-// (~2.3 sweep times per (chunk, head), spread over every SM), then launch 1 and launch 2, each
-// as many waves of CTAs as it needs times the segment length; the pipelined launches cost about
-// one sweep of the whole sequence.
-bool scan_plan(int64_t n, int units, int sms, Segs& sg) {
-    if (units <= 0 || sms <= 0) return false;
+// Segment count for the scan over sequences of about n chunks each and `units` (sequence, head)
+// pairs, or 0 when it is not expected to beat one sweep of the sequence (the pipelined launches
+// for one sequence, the plain sweep otherwise) by 10 %.  Cost in chunk-sweep times: the full
+// prep (~2.3 sweep times per (chunk, head), spread over every SM), then launch 1 and launch 2,
+// each as many waves of CTAs as it needs times the segment length.
+int scan_segments(int64_t n, int units, int sms) {
+    if (units <= 0 || sms <= 0) return 0;
     const double prep = 2.3 * (double)n * units / sms;
-    double best = 0.9 * (double)n;  // the scan must beat the pipeline by 10 %
+    double best = 0.9 * (double)n;
     int best_p = 0;
     for (int P = 3; P <= kMaxSeg; ++P) {
         const int64_t len = (n + P - 1) / P;
@@ -1826,11 +1829,7 @@ bool scan_plan(int64_t n, int units, int sms, Segs& sg) {
             best_p = P;
         }
     }
-    if (best_p == 0) return false;
-    sg.P = best_p;
-    for (int i = 0; i <= best_p; ++i) sg.b[i] = (int)((n * i) / best_p);
-    for (int i = best_p + 1; i <= kMaxSeg; ++i) sg.b[i] = sg.b[best_p];
-    return true;
+    return best_p;
 }
 
 template <bool kBf16Out, bool kF32In>
@@ -1848,20 +1847,21 @@ void launch_2p(const RawMaps& m, const CUtensorMap& omap, const PrefillArgs& p, 
             prefill_prep_kernel<kBf16Out, kF32In><<<grid, kThreads, PR_SMEM, s>>>(m.q, m.k, m.g, p, plan, n_max, ops,
                                                                                   c0, c1);
     };
-    // One long sequence with few heads: swept as P segments at once when the cost model says so
-    // (see scan_plan), else pipelined below.
-    Segs sg;
-    if (scan_room(n_max, p.N) && scan_plan(n_max, units, sms, sg)) {
+    // Long sequences with few heads: swept as P segments at once when the cost model says so
+    // (see scan_segments, with the mean sequence length), else pipelined (one sequence) or the
+    // plain sweep below.
+    const int P = scan_room(n_max, p.N) ? scan_segments(n_max / p.N, units, sms) : 0;
+    if (P > 0) {
         float* scan = scratch + (size_t)p.N * p.H * kD * kD;
         cudaFuncSetAttribute(prefill_scan_kernel<kBf16Out, kF32In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SW_SMEM);
         prep(0, n_max);
-        prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units + 2 * units * (sg.P - 2)), kSweepThreads, SW_SMEM,
-                                                s>>>(m.v, omap, p, plan, n_max, ops, sg, scan, units, 0);
+        prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units + 2 * units * (P - 2)), kSweepThreads, SW_SMEM,
+                                                s>>>(m.v, omap, p, plan, n_max, ops, P, scan, units, 0);
         cudaFuncSetAttribute(prefill_scan_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CB_SMEM);
-        prefill_scan_combine_kernel<<<(unsigned)(units * (kD / kCombineRows)), kD, CB_SMEM, s>>>(scan, units, sg.P);
-        prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units * (sg.P - 1)), kSweepThreads, SW_SMEM, s>>>(
-            m.v, omap, p, plan, n_max, ops, sg, scan, units, 1);
+        prefill_scan_combine_kernel<<<(unsigned)(units * (kD / kCombineRows)), kD, CB_SMEM, s>>>(scan, units, P);
+        prefill_scan_kernel<kBf16Out, kF32In><<<(unsigned)(units * (P - 1)), kSweepThreads, SW_SMEM, s>>>(
+            m.v, omap, p, plan, n_max, ops, P, scan, units, 1);
         return;
     }
     // One long sequence whose heads would leave most SMs idle in the sweep: chunk segments, a

@@ -48,14 +48,15 @@ def test_status_strings_and_version(kda):
 
 def test_prefill_workspace_size(kda):
     # every (chunk, head)'s operand block (132 096 bytes), one fp32 state per (sequence, head) for
-    # the pipelined long-sequence path, for one sequence of at least 256 chunks 48 more per head
-    # (the segment scan's start, Phi and B states, up to 16 segments), and a plan area well
-    # under 1 MiB
+    # the pipelined long-sequence path, for up to 8 sequences of on average at least 256 chunks
+    # 48 more per (sequence, head) (the segment scan's start, Phi and B states, up to 16
+    # segments), and a plan area well under 1 MiB
     H = 32
-    for T, N in [(0, 1), (64, 1), (41460, 8), (255 * 64, 1), (256 * 64, 1), (131072, 1), (1 << 20, 8)]:
+    for T, N in [(0, 1), (64, 1), (41460, 8), (255 * 64, 1), (256 * 64, 1), (131072, 1), (1 << 20, 8),
+                 (1 << 20, 9), (2 * 256 * 64 - 200, 2)]:
         n_max = (T + 63 * N) // 64
         ws = kda.kda_chunk_prefill_workspace_size(T, N, H)
-        scan = 48 * H * 128 * 128 * 4 if N == 1 and n_max >= 256 else 0
+        scan = 48 * N * H * 128 * 128 * 4 if N <= 8 and n_max >= 256 * N else 0
         blocks = n_max * H * 132096 + N * H * 128 * 128 * 4 + scan
         assert ws % 16 == 0
         assert blocks <= ws < blocks + (1 << 20)

@@ -476,6 +476,32 @@ def test_long_sequence_segment_scan_fp32_output(kda):
     check(c, run(kda, c, out_dtype=torch.float32))
 
 
+def test_several_long_sequences_segment_scan(kda):
+    # two sequences of different lengths, 2 heads: the scan covers both, each unit's segments
+    # cut from its own sequence's chunks
+    lengths = [256 * 64 + 5, 300 * 64 - 7]
+    c = slow_decay(W.prefill_case(104, lengths, 2, pool_slots=4, track=[[0, 100, 256], [17, 150, 299]]))
+    check(c, run(kda, c))
+
+
+def test_several_long_sequences_with_an_empty_and_a_short_one(kda):
+    # four sequences, one empty and one of two chunks: segments of the short one are mostly
+    # empty (identity maps, zero offsets), the empty one only carries its initial state to its
+    # final slot
+    lengths = [40000, 0, 30000, 70]
+    track = [[0, 300], [-1, -1], [5, 400], [0, 1]]
+    c = slow_decay(W.prefill_case(105, lengths, 2, pool_slots=6, track=track))
+    check(c, run(kda, c))
+
+
+def test_several_long_sequences_deterministic(kda):
+    lengths = [256 * 64, 280 * 64 + 1]
+    c = slow_decay(W.prefill_case(106, lengths, 2, pool_slots=4, track=[[9, 200], [3, 270]]))
+    a = run(kda, c)
+    b = run(kda, c)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
 def test_long_sequence_pipelined_matches_oracle(kda):
     L = 256 * 64 - 17
     track = [[0, 8, 9, 24, 57, 200, 255]]  # on, beside and between segment boundaries
