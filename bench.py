@@ -72,17 +72,17 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
 
 
 # DRAM traffic of one two-phase prefill call, from ncu captures of its two kernels
-# (dram__bytes_read.sum + dram__bytes_write.sum of prep and sweep: 201.97 + 379.42 and
-# 553.38 + 62.23 MB) on the `--profile prefill` case (8 x 2048 tokens, 16 heads); traffic
+# (dram__bytes_read.sum + dram__bytes_write.sum of prep and sweep: 201.94 + 379.76 and
+# 554.24 + 62.20 MB) on the `--profile prefill` case (8 x 2048 tokens, 16 heads); traffic
 # grows with the token-heads processed, so a launch is charged this much per token-head.
 # The figure belongs to the kernel source it was captured on: the line reports null traffic
 # once that file's sha256 no longer starts with the recorded prefix.
 PREFILL_TRAFFIC = {
     "source": "serving_kda_chunk_gb300/csrc/prefill_2p.cu",
-    "sha256_prefix": "de3ef993ae9d3625",
+    "sha256_prefix": "4867594909c645f8",
     "capture": "profiles/prefill_2p_prep_kernel_batched_8x2048_h16.md, "
                "profiles/prefill_2p_sweep_kernel_batched_8x2048_h16.md",
-    "bytes_per_token_head": (201.974272e6 + 379.416576e6 + 553.376000e6 + 62.227712e6) / (8 * 2048 * 16),
+    "bytes_per_token_head": (201.941760e6 + 379.763200e6 + 554.237184e6 + 62.204672e6) / (8 * 2048 * 16),
 }
 
 
