@@ -79,7 +79,7 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
 # once that file's sha256 no longer starts with the recorded prefix.
 PREFILL_TRAFFIC = {
     "source": "serving_kda_chunk_gb300/csrc/prefill_2p.cu",
-    "sha256_prefix": "4867594909c645f8",
+    "sha256_prefix": "677b46a515492a81",
     "capture": "profiles/prefill_2p_prep_kernel_batched_8x2048_h16.md, "
                "profiles/prefill_2p_sweep_kernel_batched_8x2048_h16.md",
     "bytes_per_token_head": (201.941760e6 + 379.763200e6 + 554.237184e6 + 62.204672e6) / (8 * 2048 * 16),

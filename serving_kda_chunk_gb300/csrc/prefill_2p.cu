@@ -184,8 +184,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const int32_
 // Persistent: each CTA walks (chunk, head) items blockIdx.x, + gridDim.x, ...  Per item:
 //   gate pass -> L/R -> MMA 1 ([A; P]) issued; K_G / Q_G / K~ built while it runs ->
 //   A/P extraction -> triangular solve -> T_b -> MMA 2 (W) -> W extraction -> bulk store
-// The next item's raw tiles are requested as soon as this item's are consumed, and the image
-// leaves by an asynchronous bulk store that the next item waits on only before its L/R build.
+// The next item's raw gate tile is requested right after this item's gate pass and its q / k
+// tiles after the K_G pass (each tile as soon as this item's copy is consumed); the image leaves
+// by asynchronous bulk stores that the next item waits on only before its L/R stores.
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t PR_RAW = 0;  // raw q, k, g tiles, row-major bf16 [t][128]
