@@ -502,6 +502,27 @@ def test_several_long_sequences_deterministic(kda):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_segment_scan_random_configurations(kda, seed):
+    # seeded random draws inside the scan's range: 1-4 sequences of 16-40k tokens (one of them
+    # possibly much shorter), 1-3 heads, random snapshot requests, the gate given as raw or as g
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 5))
+    lengths = [int(x) for x in rng.integers(16384, 40000, N)]
+    if N > 1 and rng.random() < 0.5:
+        lengths[int(rng.integers(0, N))] = int(rng.integers(0, 3000))
+    lengths[0] = max(lengths[0], 256 * 64 * N - sum(lengths[1:]))  # at least 256 chunks each on average
+    H = int(rng.integers(1, 4))
+    track = [[int(rng.integers(-1, (L + 63) // 64)) if L > 0 else -1 for _ in range(3)] for L in lengths]
+    c = slow_decay(W.prefill_case(200 + seed, lengths, H, pool_slots=N + 1, track=track))
+    flags = 0
+    if rng.random() < 0.5:  # the gate as g = log alpha, slow decay
+        g = -np.abs(W.bf16_bits_to_f32(W.prefill_case(200 + seed, lengths, H)["gate"])) * np.float32(6e-4)
+        c["gate"] = W.f32_to_bf16_bits(g.astype(np.float32))
+        flags = kda.KDA_GATE_LOG
+    check(c, run(kda, c, flags=flags), flags=flags)
+
+
 def test_long_sequence_pipelined_matches_oracle(kda):
     L = 256 * 64 - 17
     track = [[0, 8, 9, 24, 57, 200, 255]]  # on, beside and between segment boundaries
