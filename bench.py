@@ -774,6 +774,16 @@ def run_profile_case(name, reps):
 
         def fn():
             kda.kda_slot_copy([pool], *args, ws)
+    elif name == "verify_bf16":
+        # verify on a bf16 copy of the checkpoint pool (KDA_STATE_BF16): the checkpoint is used
+        # as the MMA's shared-memory operand where it lands
+        step = Step(dev, parts=("spec",), compact_decode_pool=True)
+        pool3 = step.pool3.to(torch.bfloat16)
+        s3 = step.spec
+
+        def fn():
+            kda.kda_spec_verify(s3["q"], s3["k"], s3["v"], s3["beta"], s3["gate"], pool3, step.ckpt3,
+                                step.rec_u, step.rec_kg, step.out3, K=7, dev_status=step.status)
     else:
         part = {"decode": "decode", "verify": "spec", "commit": "spec", "conv_compact": "spec",
                 "slot_copy": "copy"}[name]
@@ -802,7 +812,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "prefill_single", "prefill_long", "decode", "verify", "commit",
+    ap.add_argument("--profile", choices=["prefill", "prefill_single", "prefill_long", "decode", "verify", "verify_bf16", "commit",
                                           "conv_compact", "slot_copy", "slot_copy_small"],
                     help="run one entry point a few times (for an ncu capture) and exit")
     args = ap.parse_args()
