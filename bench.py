@@ -16,7 +16,9 @@ One step = one pass of every entry point over one batch of synthetic input:
                            of 1 MiB fp32 states (H=16).
 `value` is the prefill throughput in tokens/s (device time of the prefill call,
 inputs resident in HBM); the other calls are reported in microseconds per
-call.  L2 is flushed (256 MiB write) before every timed call.
+call.  L2 is flushed (256 MiB write) before every timed call.  Two long-sequence prefills
+are timed the same way outside the step and reported beside it: one sequence of 131 072
+tokens at H=16 (`prefill_long`) and four of 32 768 tokens at H=4 (`prefill_tp_slice`).
 
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 prefill workload on the host cores (the method has no runnable reference
@@ -484,6 +486,44 @@ def run_prefill_long(step, reps):
     return statistics.mean(ts), T, T * H * 1282 + n_states * H * STATE_BYTES
 
 
+def run_prefill_tp_slice(step, reps):
+    """Four sequences of 32 768 tokens at H = 4 (a tensor-parallel slice of 32 heads): 16
+    (sequence, head) units, swept as chunk segments at once.  Seeded inputs with the workload
+    recipe, initial and final states in slots, one snapshot per sequence; timed like the long
+    prefill.  Returns (mean seconds, tokens, algorithmic bytes)."""
+    import torch
+
+    c = W.tp_slice_prefill_4x32768_h4()
+    dev = step.dev
+    t = {n: to_dev(c[n], "bf16", dev) for n in ("q", "k", "v", "beta", "gate")}
+    T, H, N = c["T"], c["H"], c["N"]
+    pool = torch.from_numpy(c["pool"]).to(dev)
+    cu, sl, tr = i32(c["cu_seqlens"], dev), i32(c["init_slot"], dev), i32(c["track"], dev)
+    snap = torch.empty(N, 1, H, D, D, device=dev)
+    out = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(step.kda.kda_chunk_prefill_workspace_size(T, N, H), 16), dtype=torch.uint8, device=dev)
+
+    def call():
+        step.kda.kda_chunk_prefill(t["q"], t["k"], t["v"], t["beta"], t["gate"], cu, out,
+                                   state_pool=pool, init_slot=sl, final_slot=sl, track_chunk_idx=tr,
+                                   track_state=snap, workspace=ws, dev_status=step.status)
+
+    call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        step.flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    n_states = 2 * N + int((c["track"] >= 0).sum())  # initial + final states and snapshots
+    return statistics.mean(ts), T, T * H * 1282 + n_states * H * STATE_BYTES
+
+
 def run_e2e(step, steps, warmup):
     """Prefill through the public call with host buffers, streamed per sequence: the pinned
     H2D copies of a sequence's inputs (one stream, longest sequence first), its
@@ -838,6 +878,7 @@ def main():
     t16 = run_state_bf16(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t_graph = run_spec_graph(step, max(1, min(args.steps, 5)), min(args.warmup, 3))
     t_long, tok_long, b_long = run_prefill_long(step, 2)
+    t_tp, tok_tp, b_tp = run_prefill_tp_slice(step, 3)
 
     hbm, tc, peak_kind = load_peaks()
     mean = {k: statistics.mean(v) for k, v in times.items()}
@@ -871,6 +912,9 @@ def main():
         "prefill_long": {"us": t_long * 1e6, "tokens_per_s": tok_long / t_long, "bytes": b_long,
                          "hbm_frac": b_long / (hbm * 1e9) / t_long,
                          "note": "1 x 131072 tokens, H=16: the prep on every SM, then 10 chunk segments swept at once (the middle segments' state maps and offsets, the start states chained, every segment swept from its start)"},
+        "prefill_tp_slice": {"us": t_tp * 1e6, "tokens_per_s": tok_tp / t_tp, "bytes": b_tp,
+                             "hbm_frac": b_tp / (hbm * 1e9) / t_tp,
+                             "note": "4 x 32768 tokens, H=4 (a tensor-parallel slice of 32 heads): 16 (sequence, head) units, each swept as chunk segments at once"},
         "slot_copy": {"us": mean["slot_copy"] * 1e6, "bytes": cp_b,
                       "hbm_frac": cp_b / (hbm * 1e9) / mean["slot_copy"]},
     }

@@ -236,6 +236,12 @@ def long_prefill_131072_h16():
     return prefill_case(4, [T], 16, track=track, pool_slots=0)
 
 
+def tp_slice_prefill_4x32768_h4():
+    """4 sequences of 32768 tokens at H = 4 (a tensor-parallel slice of 32 heads), initial and
+    final states in slots, one snapshot per sequence."""
+    return prefill_case(14, [32768] * 4, 4, pool_slots=4, track_per_seq=1)
+
+
 def slot_fanout_256x8_pool4096():
     """256 parents fanned out to 8 children each, plus 512 clears, in a 4096-slot pool."""
     return slot_copy_case(4, 4096, 256, 8, 512)
