@@ -194,6 +194,25 @@ def test_long_prefill_sampled_heads(kda):
     assert worst_seq_head(to_np(out[:, heads]), o_ref, spans) < 5e-3
 
 
+def test_tp_slice_prefill_sampled_heads(kda):
+    # four 32 768-token sequences at H = 4, as the benchmark times them: every (sequence, head)
+    # is swept as chunk segments at once, starting from its slot and ending in it (with this
+    # workload's decay a segment's start state fades within a few chunks: the slow-decay scan
+    # tests of the two-phase suite are the ones that check the chained state maps)
+    c = W.tp_slice_prefill_4x32768_h4()
+    S0_all = c["pool"][c["init_slot"]].astype(np.float64)
+    out, pool, snap, st = _prefill_gpu(kda, c, c["pool"])
+    assert st == 0
+    heads = [2]
+    o_ref, s_ref, snap_ref, _ = _oracle_heads(c, heads, S0_all)
+    fin = pool.cpu().numpy()[c["final_slot"]][:, heads]
+    assert rel_l2(to_np(out[:, heads]), o_ref) < 5e-3
+    assert worst_seq_head(to_np(out[:, heads]), o_ref, c["cu_seqlens"]) < 5e-3
+    assert worst_state(fin, s_ref) < TOL_STATE
+    assert worst_state(snap.cpu().numpy()[:, :, heads], snap_ref) < TOL_STATE
+    assert not torch.isnan(snap).any()
+
+
 def test_slot_fanout_sampled(kda):
     sc = W.slot_fanout_256x8_pool4096()
     g = torch.Generator(device="cuda").manual_seed(4)
