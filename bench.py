@@ -74,17 +74,17 @@ def prefill_work(lengths, H, M, in_bytes=2, out_bytes=2):
 
 
 # DRAM traffic of one two-phase prefill call, from ncu captures of its two kernels
-# (dram__bytes_read.sum + dram__bytes_write.sum of prep and sweep: 201.94 + 379.76 and
-# 554.24 + 62.20 MB) on the `--profile prefill` case (8 x 2048 tokens, 16 heads); traffic
+# (dram__bytes_read.sum + dram__bytes_write.sum of prep and sweep: 201.94 + 379.37 and
+# 548.30 + 62.24 MB) on the `--profile prefill` case (8 x 2048 tokens, 16 heads); traffic
 # grows with the token-heads processed, so a launch is charged this much per token-head.
 # The figure belongs to the kernel source it was captured on: the line reports null traffic
 # once that file's sha256 no longer starts with the recorded prefix.
 PREFILL_TRAFFIC = {
     "source": "serving_kda_chunk_gb300/csrc/prefill_2p.cu",
-    "sha256_prefix": "677b46a515492a81",
+    "sha256_prefix": "d683cc7bea0733af",
     "capture": "profiles/prefill_2p_prep_kernel_batched_8x2048_h16.md, "
                "profiles/prefill_2p_sweep_kernel_batched_8x2048_h16.md",
-    "bytes_per_token_head": (201.941760e6 + 379.763200e6 + 554.237184e6 + 62.204672e6) / (8 * 2048 * 16),
+    "bytes_per_token_head": (201.940992e6 + 379.373312e6 + 548.301056e6 + 62.239744e6) / (8 * 2048 * 16),
 }
 
 
