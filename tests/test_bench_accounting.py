@@ -54,3 +54,23 @@ def test_peaks_fall_back_when_the_measured_file_is_absent(tmp_path, monkeypatch)
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6790.3,
                                                                "bf16_tflops": 1890.2}))
     assert bench.load_peaks() == (6790.3, 1890.2, "measured")
+
+
+def test_traffic_stamp_belongs_to_the_kernel_source():
+    # the DRAM traffic figure is charged only while the prefill source is the one it was
+    # captured on; the committed stamp must name the committed source
+    th = 41460 * 32
+    t = bench.prefill_traffic(th)
+    assert t is not None
+    assert abs(t - bench.PREFILL_TRAFFIC["bytes_per_token_head"] * th) < 1.0
+    # between the algorithmic bytes and ten times them
+    assert 1282 < bench.PREFILL_TRAFFIC["bytes_per_token_head"] < 12820
+
+
+def test_traffic_is_null_once_the_source_changes(tmp_path, monkeypatch):
+    src = tmp_path / "prefill_2p.cu"
+    src.write_text("// another kernel source\n")
+    monkeypatch.setitem(bench.PREFILL_TRAFFIC, "source", str(src))
+    assert bench.prefill_traffic(1000) is None
+    monkeypatch.setitem(bench.PREFILL_TRAFFIC, "source", str(tmp_path / "missing.cu"))
+    assert bench.prefill_traffic(1000) is None
